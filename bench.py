@@ -1,0 +1,369 @@
+#!/usr/bin/env python3
+"""Benchmark of the sm_103a fp16 GEMM (one JSON line on stdout).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--no-cpu-baseline]
+
+A step is one C = A*B of the workload (default: the square 4096^3 case, fp16
+inputs, fp32 accumulation, fp16 output) on inputs already resident in device
+memory.  Each timed step is bracketed by CUDA events on the launching stream;
+L2 is flushed (a 512 MiB write) between steps, outside the events.  `value` is
+TFLOP/s of useful 2MNK work over all ranks.  `e2e` repeats the measurement
+through the same C ABI with pinned-host inputs copied in and the result copied
+out inside the timed region.  `roofline` rates the GEMM kernel against the
+measured peak of this machine; `cpu_baseline` times the CPU oracle on a bounded
+slab of output rows.
+
+Multi-GPU: the GEMM does not need to be sharded to be measured; with torchrun
+each rank runs an independent replica of the workload on its own GPU (weak
+scaling, no collective on the data path) and rank 0 reports the aggregate.
+
+--impl reference times the CPU oracle itself, as it stands, on bounded slabs of
+the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fp16 GEMM TFLOP/s (fp32 acc) and % of GB300 roofline; HBM GB/s at small M"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "tflops": float(d["bf16_tflops"]),
+                "tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "tflops": 1900.0, "tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            if self.uuid and parts[1] != self.uuid:
+                continue
+            rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- helpers
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def cpu_oracle_rate(w, target_s: float, threads: int):
+    """Time the CPU oracle on a slab of output rows; returns (TFLOP/s, rows, seconds)."""
+    import numpy as np
+
+    import oracle
+
+    K, N = w.K, w.N
+    Bv = w.B.host_view()
+    k = np.arange(K, dtype=np.int64)
+
+    def slab(rows):
+        A_rows = np.ascontiguousarray(w.A.values_at(np.arange(rows)[:, None], k[None, :]))
+        t = time.perf_counter()
+        oracle.gemm(A_rows, Bv, threads=threads)
+        return time.perf_counter() - t
+
+    rows = 1
+    dt = slab(rows)
+    while dt < 0.5 and rows < w.M:
+        rows = min(w.M, rows * 4)
+        dt = slab(rows)
+    rate = rows / dt                              # rows per second
+    rows = int(max(1, min(w.M, rate * target_s)))
+    dt = slab(rows)
+    return 2.0 * rows * N * K / dt / 1e12, rows, dt
+
+
+# -------------------------------------------------------------- our arm
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import dense_tiled_gemm_fp16_gb300 as g
+    from dense_tiled_gemm_fp16_gb300 import ledger
+    from synth import workloads
+
+    rank, world, local = dist_env()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    w = workloads.BY_NAME[args.workload]
+    M, N, K = w.M, w.N, w.K
+    flops = ledger.flops(M, N, K)
+    nbytes = ledger.min_bytes(M, N, K)
+    peaks = load_peaks()
+    bnd = ledger.bound(M, N, K, peaks["tflops"], peaks["hbm_gbs"])
+
+    A = w.A.device_view(dev)
+    B = w.B.device_view(dev)
+    C = torch.empty((M, N), dtype=torch.float16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    plan = g.plan_for(A, B, C)
+
+    def step():
+        g.matmul(A, B, out=C, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    assert g.gemm_f16_device_status() == 0
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    uuid = f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU-") else uuid
+    clocks = ClockSampler(str(uuid) if uuid else None)
+    clocks.start()
+    time.sleep(0.3)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    wall = time.perf_counter() - t0
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    clk = clocks.stop()
+
+    total_ms = sum(ms)
+    if pg is not None:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+
+    # ---- end to end: pinned host inputs in, result out, inside the timed region
+    A_h = torch.from_numpy(np.ascontiguousarray(w.A.host_buffer())).pin_memory()
+    B_h = torch.from_numpy(np.ascontiguousarray(w.B.host_buffer())).pin_memory()
+    C_h = torch.empty((M, N), dtype=torch.float16).pin_memory()
+    A_buf = torch.empty(w.A.numel, dtype=torch.float16, device=dev)
+    B_buf = torch.empty(w.B.numel, dtype=torch.float16, device=dev)
+    A_v = A_buf.view(*w.A.buf_shape)
+    B_v = B_buf.view(*w.B.buf_shape)
+    A_v = A_v.t() if w.A.transposed else A_v
+    B_v = B_v.t() if w.B.transposed else B_v
+
+    def e2e_step():
+        A_buf.copy_(A_h, non_blocking=True)
+        B_buf.copy_(B_h, non_blocking=True)
+        g.matmul(A_v, B_v, out=C, stream=stream)
+        C_h.copy_(C, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_steps = max(3, min(args.steps, 10))
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    es.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    ee.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = es.elapsed_time(ee) / e2e_steps
+    if pg is not None:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    status = g.gemm_f16_device_status()
+
+    result = None
+    if rank == 0:
+        if bnd == "tensor":
+            achieved = flops / (ms_per_step * 1e-3) / 1e12
+            roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["tflops"],
+                    "unit": "TFLOP/s", "frac": round(achieved / peaks["tflops"], 4)}
+        else:
+            achieved = nbytes / (ms_per_step * 1e-3) / 1e9
+            roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
+        roof["traffic"] = None
+        roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json bf16 burst / copy bandwidth)"
+        roof["kernel"] = "gemm_f16_persistent"
+        cpu = None
+        if not args.no_cpu_baseline:
+            threads = os.cpu_count() or 1
+            rate, rows, dt = cpu_oracle_rate(w, args.cpu_seconds, threads)
+            cpu = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                   "sample": f"{rows} of {M} output rows x all {N} columns, K={K} ({dt:.1f} s)"}
+        result = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f16 (fp32 accumulate)",
+            "data": "synthetic (seeded SplitMix64 fill)",
+            "config": {"workload": w.name, "M": M, "N": N, "K": K,
+                       "A": f"strides {tuple(A.stride())}", "B": f"strides {tuple(B.stride())}",
+                       "distribution": w.A.kind, "l2": "flushed between steps (512 MiB write)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "plan": {k: plan[k] for k in ("swap_ab", "a_tma", "b_tma", "c_tma", "tile_n",
+                                                     "splits", "grid", "stages")}},
+            "hbm_gbs_min_traffic": round(nbytes / (ms_per_step * 1e-3) / 1e9, 1),
+            "wall_s_timed_region": round(wall, 4),
+            "clocks": clk,
+            "e2e": {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                    "ms_per_step": round(e2e_ms, 4),
+                    "h2d_bytes_per_step": int(2 * (w.A.numel + w.B.numel)),
+                    "d2h_bytes_per_step": int(2 * M * N)},
+            "gpu_launches": args.steps,
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "device_status": status,
+        }
+    if pg is not None:
+        pg.destroy_process_group()
+    return result
+
+
+# -------------------------------------------------------- reference arm
+def run_reference(args):
+    from synth import workloads
+
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    w = workloads.BY_NAME[args.workload]
+    threads = os.cpu_count() or 1
+    per_step = min(5.0, 150.0 / max(1, args.steps + args.warmup))
+    # size one slab, then time warmup + steps slabs of that size
+    _, rows, _ = cpu_oracle_rate(w, per_step, threads)
+    import numpy as np
+
+    import oracle
+    k = np.arange(w.K, dtype=np.int64)
+    A_rows = np.ascontiguousarray(w.A.values_at(np.arange(rows)[:, None], k[None, :]))
+    Bv = w.B.host_view()
+    for _ in range(args.warmup):
+        oracle.gemm(A_rows, Bv, threads=threads)
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle.gemm(A_rows, Bv, threads=threads)
+        times.append(time.perf_counter() - t)
+    sec = sum(times) / len(times)
+    value = 2.0 * rows * w.N * w.K / sec / 1e12
+    sample = f"{rows} of {w.M} output rows x all {w.N} columns, K={w.K} per step"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64 accumulate of f16 inputs (CPU oracle)",
+        "data": "synthetic (seeded SplitMix64 fill)",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="square_4096")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        log("note: fewer than 3 warm-up steps")
+    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+"""GB300-native dense tiled fp16 GEMM.
+
+Python binding of the C ABI in ``include/gemm_f16.h`` (``libgemm_f16.so``,
+built in-tree by ``build.py``).  The binding only marshals arguments: every
+step of the product runs in the library's sm_103a kernels.  If the library is
+missing, calls raise :class:`GemmF16Error`; there is no fallback.
+
+``gemm_f16`` mirrors the C entry point (device pointers as integers, element
+strides).  ``matmul`` is the torch-tensor convenience form: it reads pointers,
+strides and the current stream from the tensors and calls ``gemm_f16``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import ledger  # noqa: F401  (pure-Python cost ledger)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgemm_f16.so")
+
+STATUS = {
+    0: "GEMM_F16_OK",
+    1: "GEMM_F16_ERR_INVALID_VALUE",
+    2: "GEMM_F16_ERR_ALIAS",
+    3: "GEMM_F16_ERR_UNSUPPORTED_DEVICE",
+    4: "GEMM_F16_ERR_OUT_OF_MEMORY",
+    5: "GEMM_F16_ERR_LAUNCH",
+    6: "GEMM_F16_ERR_TIMEOUT",
+}
+OK, ERR_INVALID_VALUE, ERR_ALIAS, ERR_UNSUPPORTED_DEVICE, ERR_OUT_OF_MEMORY, ERR_LAUNCH, ERR_TIMEOUT = range(7)
+
+OPT_FORCE_GATHER = 1
+OPT_SPLITS = 2
+OPT_TILE_N = 3
+OPT_PANEL = 4
+OPT_SWAP = 5
+OPT_TIMEOUT_MS = 6
+OPT_MAX_CTAS = 7
+
+# Every symbol include/gemm_f16.h declares.
+EXPORTED = ("gemm_f16", "gemm_f16_ws", "gemm_f16_workspace_size", "gemm_f16_status_string",
+            "gemm_f16_device_status", "gemm_f16_get_plan", "gemm_f16_set_option",
+            "gemm_f16_abi_version")
+
+
+class GemmF16Error(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)}" if what else STATUS.get(status, str(status)))
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "swap_ab", "a_tma", "a_mn_major", "b_tma", "b_mn_major", "c_tma",
+        "tile_m", "tile_n", "tiles_m", "tiles_n", "splits", "kblocks", "units", "grid",
+        "stages", "smem_bytes")] + [("workspace_bytes", ctypes.c_size_t)]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib():
+    """The loaded C library (raises GemmF16Error if it was never built)."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise GemmF16Error(ERR_LAUNCH, f"{LIB_PATH} is not built (run __graft_entry__.build())")
+                L = ctypes.CDLL(LIB_PATH)
+                P, I64, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+                L.gemm_f16.argtypes = [P, I64, I64, P, I64, I64, P, I64, I64, I64, I64, P]
+                L.gemm_f16.restype = ctypes.c_int
+                L.gemm_f16_ws.argtypes = [P, I64, I64, P, I64, I64, P, I64, I64, I64, I64, P, SZ, P]
+                L.gemm_f16_ws.restype = ctypes.c_int
+                L.gemm_f16_workspace_size.argtypes = [I64, I64, I64, ctypes.POINTER(SZ)]
+                L.gemm_f16_workspace_size.restype = ctypes.c_int
+                L.gemm_f16_status_string.argtypes = [ctypes.c_int]
+                L.gemm_f16_status_string.restype = ctypes.c_char_p
+                L.gemm_f16_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.c_int]
+                L.gemm_f16_device_status.restype = ctypes.c_int
+                L.gemm_f16_get_plan.argtypes = [P, I64, I64, P, I64, I64, P, I64, I64, I64, I64,
+                                                ctypes.POINTER(Plan)]
+                L.gemm_f16_get_plan.restype = ctypes.c_int
+                L.gemm_f16_set_option.argtypes = [ctypes.c_int, I64]
+                L.gemm_f16_set_option.restype = ctypes.c_int
+                L.gemm_f16_abi_version.restype = ctypes.c_int
+                _lib = L
+    return _lib
+
+
+def _check(st: int, what: str):
+    if st != OK:
+        raise GemmF16Error(st, what)
+
+
+# ------------------------------------------------------------ C-ABI mirrors
+def gemm_f16(A: int, stride_am: int, stride_ak: int, B: int, stride_bk: int, stride_bn: int,
+             C: int, ldc: int, M: int, N: int, K: int, stream: int = 0) -> None:
+    """C = A*B on device pointers (see include/gemm_f16.h); raises on a non-OK status."""
+    _check(lib().gemm_f16(A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, M, N, K,
+                          stream or None), "gemm_f16")
+
+
+def gemm_f16_ws(A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, M, N, K,
+                workspace: int, workspace_bytes: int, stream: int = 0) -> None:
+    _check(lib().gemm_f16_ws(A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, M, N, K,
+                             workspace or None, workspace_bytes, stream or None), "gemm_f16_ws")
+
+
+def gemm_f16_workspace_size(M: int, N: int, K: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().gemm_f16_workspace_size(M, N, K, ctypes.byref(n)), "gemm_f16_workspace_size")
+    return n.value
+
+
+def gemm_f16_status_string(status: int) -> str:
+    return lib().gemm_f16_status_string(status).decode()
+
+
+def gemm_f16_device_status(reset: bool = False) -> int:
+    v = ctypes.c_int(0)
+    _check(lib().gemm_f16_device_status(ctypes.byref(v), 1 if reset else 0), "gemm_f16_device_status")
+    return v.value
+
+
+def gemm_f16_get_plan(A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, M, N, K) -> dict:
+    p = Plan()
+    _check(lib().gemm_f16_get_plan(A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, M, N, K,
+                                   ctypes.byref(p)), "gemm_f16_get_plan")
+    return p.as_dict()
+
+
+def gemm_f16_set_option(option: int, value: int) -> None:
+    _check(lib().gemm_f16_set_option(option, value), "gemm_f16_set_option")
+
+
+def gemm_f16_abi_version() -> int:
+    return lib().gemm_f16_abi_version()
+
+
+# ------------------------------------------------------------ torch helpers
+def _args(a, b, out):
+    if a.dim() != 2 or b.dim() != 2:
+        raise ValueError("expected two matrices")
+    M, K = a.shape
+    K2, N = b.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    if out.dim() != 2 or tuple(out.shape) != (M, N) or out.stride(1) != 1:
+        raise ValueError("out must be [M, N] with unit column stride")
+    return (a.data_ptr(), a.stride(0), a.stride(1), b.data_ptr(), b.stride(0), b.stride(1),
+            out.data_ptr(), out.stride(0), M, N, K)
+
+
+def matmul(a, b, out=None, stream=None):
+    """fp16 C = a @ b for CUDA torch tensors (any positive strides); returns C."""
+    import torch
+
+    if a.dtype != torch.float16 or b.dtype != torch.float16:
+        raise TypeError("gemm_f16 takes float16 tensors")
+    if not a.is_cuda or not b.is_cuda or a.device != b.device:
+        raise ValueError("inputs must share one CUDA device")
+    if out is None:
+        out = torch.empty((a.shape[0], b.shape[1]), dtype=torch.float16, device=a.device)
+    args = _args(a, b, out)
+    with torch.cuda.device(a.device):
+        s = stream if stream is not None else torch.cuda.current_stream(a.device)
+        gemm_f16(*args, stream=s.cuda_stream)
+    return out
+
+
+def plan_for(a, b, out) -> dict:
+    """The execution plan gemm_f16 would use for these torch tensors."""
+    return gemm_f16_get_plan(*_args(a, b, out))

@@ -1,0 +1,546 @@
+// Host side of the gemm_f16 C ABI: argument checks, the execution plan
+// (operand layouts, TMA eligibility, tile width, split-K, grid), tensor-map
+// encoding, the split-K workspace and the kernel launch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "gemm_f16.h"
+#include "gemm_kernel.cuh"
+
+using gemm_f16_dev::KernelParams;
+
+// Device status word, written by a kernel that gives up on a bounded wait.
+__device__ int g_gemm_f16_status = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxDynSmem = 232448;   // 227 KiB per block on sm_100-class parts
+constexpr int kSmemAlignSlack = 1024;
+
+struct DevInfo {
+    bool init = false;
+    bool supported = false;
+    int sms = 0;
+    int* status_ptr = nullptr;
+    bool smem_attr_set = false;
+};
+
+std::mutex g_mutex;
+DevInfo g_dev[kMaxDevices];
+
+struct Workspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+Workspace g_ws[kMaxDevices];
+
+std::atomic<int64_t> g_opt[8];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+PFN_cuMemGetAddressRange_v3020 g_addr_range = nullptr;
+std::once_flag g_entry_once;
+
+void load_entry_points()
+{
+    std::call_once(g_entry_once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &fn, 3020, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_addr_range = reinterpret_cast<PFN_cuMemGetAddressRange_v3020>(fn);
+        cudaGetLastError();
+    });
+}
+
+int64_t opt(int o) { return g_opt[o].load(std::memory_order_relaxed); }
+
+gemm_f16_status device_info(DevInfo** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_F16_ERR_UNSUPPORTED_DEVICE;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_F16_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lk(g_mutex);
+    DevInfo& d = g_dev[dev];
+    if (!d.init) {
+        int major = 0, minor = 0, sms = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        d.supported = (major == 10 && minor == 3);
+        d.sms = sms;
+        void* p = nullptr;
+        if (d.supported && cudaGetSymbolAddress(&p, g_gemm_f16_status) == cudaSuccess)
+            d.status_ptr = static_cast<int*>(p);
+        cudaGetLastError();
+        d.init = true;
+    }
+    *out = &d;
+    return d.supported ? GEMM_F16_OK : GEMM_F16_ERR_UNSUPPORTED_DEVICE;
+}
+
+// Span of a strided 2-D view in elements: 1 + (r-1)*s_r + (c-1)*s_c.
+bool view_extent(int64_t rows, int64_t cols, int64_t s_r, int64_t s_c, int64_t* elems)
+{
+    int64_t a, b, t;
+    if (__builtin_mul_overflow(rows - 1, s_r, &a)) return false;
+    if (__builtin_mul_overflow(cols - 1, s_c, &b)) return false;
+    if (__builtin_add_overflow(a, b, &t)) return false;
+    if (__builtin_add_overflow(t, int64_t(1), &t)) return false;
+    if (t > (INT64_MAX / 2)) return false;
+    *elems = t;
+    return true;
+}
+
+bool overlaps(uintptr_t a, int64_t a_bytes, uintptr_t b, int64_t b_bytes)
+{
+    return a < b + static_cast<uintptr_t>(b_bytes) && b < a + static_cast<uintptr_t>(a_bytes);
+}
+
+// The pointer must be device or managed memory, and [p, p+bytes) must lie
+// inside the allocation it points into.
+bool device_range_ok(const void* p, int64_t bytes)
+{
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) return false;
+    if (g_addr_range) {
+        CUdeviceptr base = 0;
+        size_t size = 0;
+        if (g_addr_range(&base, &size, reinterpret_cast<CUdeviceptr>(p)) == CUDA_SUCCESS) {
+            const uintptr_t end = static_cast<uintptr_t>(base) + size;
+            const uintptr_t q = reinterpret_cast<uintptr_t>(p);
+            if (q + static_cast<uintptr_t>(bytes) > end) return false;
+        }
+    }
+    return true;
+}
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+struct Args {
+    const void* A;
+    int64_t sam, sak;
+    const void* B;
+    int64_t sbk, sbn;
+    void* C;
+    int64_t ldc, M, N, K;
+};
+
+gemm_f16_status validate(const Args& a, bool check_memory, DevInfo** dev)
+{
+    if (!a.A || !a.B || !a.C) return GEMM_F16_ERR_INVALID_VALUE;
+    if (a.M <= 0 || a.N <= 0 || a.K <= 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (a.sam <= 0 || a.sak <= 0 || a.sbk <= 0 || a.sbn <= 0 || a.ldc < a.N) return GEMM_F16_ERR_INVALID_VALUE;
+    if ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.B) | reinterpret_cast<uintptr_t>(a.C)) & 1u)
+        return GEMM_F16_ERR_INVALID_VALUE;
+    int64_t ea, eb, ec;
+    if (!view_extent(a.M, a.K, a.sam, a.sak, &ea) || !view_extent(a.K, a.N, a.sbk, a.sbn, &eb) ||
+        !view_extent(a.M, a.N, a.ldc, 1, &ec))
+        return GEMM_F16_ERR_INVALID_VALUE;
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a.A), pb = reinterpret_cast<uintptr_t>(a.B),
+                    pc = reinterpret_cast<uintptr_t>(a.C);
+    if (overlaps(pc, 2 * ec, pa, 2 * ea) || overlaps(pc, 2 * ec, pb, 2 * eb)) return GEMM_F16_ERR_ALIAS;
+    gemm_f16_status st = device_info(dev);
+    if (st != GEMM_F16_OK) return st;
+    if (check_memory) {
+        load_entry_points();
+        if (!device_range_ok(a.A, 2 * ea) || !device_range_ok(a.B, 2 * eb) || !device_range_ok(a.C, 2 * ec))
+            return GEMM_F16_ERR_INVALID_VALUE;
+    }
+    return GEMM_F16_OK;
+}
+
+struct OperandChoice {
+    bool tma, mn;
+};
+
+// Choose how a kernel-view operand reaches shared memory.  `s_mn`, `s_k` are
+// its element strides along the MN and K dimensions, `tile_mn` the tile's MN
+// extent.  TMA needs a 16-byte-aligned base, a unit inner stride and an outer
+// pitch that is a multiple of 16 bytes.
+OperandChoice choose_operand(const void* ptr, int64_t s_mn, int64_t s_k, int64_t MN, int64_t K, int tile_mn,
+                             bool allow_tma)
+{
+    const bool aligned = (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0;
+    const int64_t lim = int64_t(1) << 40;
+    if (allow_tma && aligned && s_k == 1 && MN < (int64_t(1) << 32) && K < (int64_t(1) << 32)) {
+        const int64_t pitch = (MN == 1) ? round_up(2 * K, 16) : 2 * s_mn;
+        if (pitch % 16 == 0 && pitch >= 2 * K && pitch < lim) return {true, false};
+    }
+    if (allow_tma && aligned && s_mn == 1 && tile_mn % 64 == 0 && MN < (int64_t(1) << 32) &&
+        K < (int64_t(1) << 32)) {
+        const int64_t pitch = (K == 1) ? round_up(2 * MN, 16) : 2 * s_k;
+        if (pitch % 16 == 0 && pitch >= 2 * MN && pitch < lim) return {true, true};
+    }
+    const bool mn = (s_mn == 1 && s_k != 1 && tile_mn % 64 == 0);
+    return {false, mn};
+}
+
+bool encode_2d(CUtensorMap* tm, const void* ptr, uint64_t inner, uint64_t outer, uint64_t pitch_bytes,
+               uint32_t box_inner, uint32_t box_outer)
+{
+    if (!g_encode) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {pitch_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct Plan {
+    gemm_f16_plan pub;
+    KernelParams kp;
+    size_t ws_floats_bytes;
+};
+
+// Split-K count: only when the output tiles cannot occupy every SM.  Picks the
+// count whose units spread most evenly over the SMs, with a small penalty per
+// split for the extra partial-sum traffic, and at least 4 K blocks per split.
+int choose_splits(int64_t tiles, int kblocks, int sms)
+{
+    const int64_t forced = opt(GEMM_F16_OPT_SPLITS);
+    if (forced > 0) return static_cast<int>(std::min<int64_t>(forced, kblocks));
+    if (tiles >= sms || kblocks < 8) return 1;
+    int best = 1;
+    double best_score = -1.0;
+    const int max_s = std::min(32, kblocks / 4);
+    for (int s = 1; s <= max_s; ++s) {
+        const int64_t units = tiles * s;
+        const int64_t waves = (units + sms - 1) / sms;
+        const double eff = static_cast<double>(units) / static_cast<double>(waves * sms);
+        const double score = eff - 0.002 * s;
+        if (score > best_score + 1e-12) {
+            best_score = score;
+            best = s;
+        }
+    }
+    return best;
+}
+
+void shape_plan(int64_t M, int64_t N, int64_t K, int sms, bool* swap, int64_t* Mv, int64_t* Nv, int* BN,
+                int* tiles_m, int* tiles_n, int* kblocks, int* splits)
+{
+    const int64_t sw = opt(GEMM_F16_OPT_SWAP);
+    *swap = (sw == 2) || (sw == 0 && M <= 64 && N >= 2 * M);
+    *Mv = *swap ? N : M;
+    *Nv = *swap ? M : N;
+    int bn;
+    if (*swap) {
+        bn = static_cast<int>(round_up(*Nv, 16));
+        if (bn > 256) bn = 256;
+    } else {
+        const int64_t forced = opt(GEMM_F16_OPT_TILE_N);
+        bn = forced > 0 ? static_cast<int>(forced) : static_cast<int>(std::min<int64_t>(256, round_up(*Nv, 64)));
+    }
+    *BN = bn;
+    *tiles_m = static_cast<int>((*Mv + gemm_f16_dev::kBM - 1) / gemm_f16_dev::kBM);
+    *tiles_n = static_cast<int>((*Nv + bn - 1) / bn);
+    *kblocks = static_cast<int>((K + gemm_f16_dev::kBK - 1) / gemm_f16_dev::kBK);
+    *splits = choose_splits(static_cast<int64_t>(*tiles_m) * *tiles_n, *kblocks, sms);
+}
+
+size_t workspace_bytes_for(int64_t units, int BN, int64_t tiles, size_t* floats_bytes)
+{
+    const size_t fb = static_cast<size_t>(round_up(units * gemm_f16_dev::kBM * BN * 4, 256));
+    if (floats_bytes) *floats_bytes = fb;
+    return fb + static_cast<size_t>(round_up(tiles * 4, 256));
+}
+
+gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
+{
+    std::memset(pl, 0, sizeof(*pl));
+    KernelParams& kp = pl->kp;
+    gemm_f16_plan& pub = pl->pub;
+    bool swap;
+    int64_t Mv, Nv;
+    int BN, tiles_m, tiles_n, kblocks, splits;
+    shape_plan(a.M, a.N, a.K, dev.sms, &swap, &Mv, &Nv, &BN, &tiles_m, &tiles_n, &kblocks, &splits);
+    if (BN < 16 || BN > 256 || BN % 16 != 0) return GEMM_F16_ERR_INVALID_VALUE;
+    const int64_t tiles = static_cast<int64_t>(tiles_m) * tiles_n;
+    const int64_t units = tiles * splits;
+    if (units > INT32_MAX / 2) return GEMM_F16_ERR_INVALID_VALUE;
+
+    // Kernel view: C'[m,n] = sum_k A'[m,k] B'[k,n].
+    if (!swap) {
+        kp.A = static_cast<const __half*>(a.A), kp.a_sm = a.sam, kp.a_sk = a.sak;
+        kp.B = static_cast<const __half*>(a.B), kp.b_sk = a.sbk, kp.b_sn = a.sbn;
+        kp.C = static_cast<__half*>(a.C), kp.c_sm = a.ldc, kp.c_sn = 1;
+    } else {   // C^T = B^T A^T
+        kp.A = static_cast<const __half*>(a.B), kp.a_sm = a.sbn, kp.a_sk = a.sbk;
+        kp.B = static_cast<const __half*>(a.A), kp.b_sk = a.sak, kp.b_sn = a.sam;
+        kp.C = static_cast<__half*>(a.C), kp.c_sm = 1, kp.c_sn = a.ldc;
+    }
+    kp.M = Mv, kp.N = Nv, kp.K = a.K;
+
+    const int64_t fg = opt(GEMM_F16_OPT_FORCE_GATHER);
+    load_entry_points();
+    const bool have_tma = g_encode != nullptr;
+    OperandChoice ca = choose_operand(kp.A, kp.a_sm, kp.a_sk, Mv, a.K, gemm_f16_dev::kBM, have_tma && !(fg & 1));
+    OperandChoice cb = choose_operand(kp.B, kp.b_sn, kp.b_sk, Nv, a.K, BN, have_tma && !(fg & 2));
+    if (ca.tma) {
+        const bool ok = ca.mn ? encode_2d(&kp.tmA, kp.A, Mv, a.K, a.K == 1 ? round_up(2 * Mv, 16) : 2 * kp.a_sk, 64, 64)
+                              : encode_2d(&kp.tmA, kp.A, a.K, Mv, Mv == 1 ? round_up(2 * a.K, 16) : 2 * kp.a_sm, 64,
+                                          gemm_f16_dev::kBM);
+        if (!ok) ca = choose_operand(kp.A, kp.a_sm, kp.a_sk, Mv, a.K, gemm_f16_dev::kBM, false);
+    }
+    if (cb.tma) {
+        const bool ok = cb.mn ? encode_2d(&kp.tmB, kp.B, Nv, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk, 64, 64)
+                              : encode_2d(&kp.tmB, kp.B, a.K, Nv, Nv == 1 ? round_up(2 * a.K, 16) : 2 * kp.b_sn, 64,
+                                          static_cast<uint32_t>(BN));
+        if (!ok) cb = choose_operand(kp.B, kp.b_sn, kp.b_sk, Nv, a.K, BN, false);
+    }
+    bool c_tma = have_tma && !(fg & 4) && !swap && splits == 1 && BN % 64 == 0 &&
+                 (reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc * 2) % 16 == 0 && a.M < (int64_t(1) << 32) &&
+                 a.N < (int64_t(1) << 32) && (a.ldc * 2) < (int64_t(1) << 40);
+    if (c_tma) c_tma = encode_2d(&kp.tmC, a.C, a.N, a.M, 2 * a.ldc, 64, 32);
+
+    const uint32_t stage_b = static_cast<uint32_t>(BN) * gemm_f16_dev::kBK * 2;
+    const uint32_t stage_bytes = gemm_f16_dev::kStageABytes + stage_b;
+    const int epi = c_tma ? static_cast<int>(gemm_f16_dev::kEpiBytes) : 0;
+    int stages = (kMaxDynSmem - kSmemAlignSlack - epi - static_cast<int>(gemm_f16_dev::kBarrierBytes)) /
+                 static_cast<int>(stage_bytes);
+    stages = std::min(stages, gemm_f16_dev::kMaxStages);
+    if (stages < 2) return GEMM_F16_ERR_INVALID_VALUE;
+    const int smem = kSmemAlignSlack + stages * static_cast<int>(stage_bytes) + epi +
+                     static_cast<int>(gemm_f16_dev::kBarrierBytes);
+
+    int grid = static_cast<int>(std::min<int64_t>(units, dev.sms));
+    const int64_t cap = opt(GEMM_F16_OPT_MAX_CTAS);
+    if (cap > 0) grid = static_cast<int>(std::min<int64_t>(grid, cap));
+    const int64_t panel = opt(GEMM_F16_OPT_PANEL);
+
+    kp.status = dev.status_ptr;
+    const int64_t tmo = opt(GEMM_F16_OPT_TIMEOUT_MS);
+    kp.timeout_ns = static_cast<uint64_t>(tmo > 0 ? tmo : 1000) * 1000000ull;
+    kp.tiles_m = tiles_m, kp.tiles_n = tiles_n, kp.splits = splits, kp.kblocks = kblocks;
+    kp.num_units = static_cast<int>(units);
+    kp.panel = static_cast<int>(panel > 0 ? panel : 8);
+    kp.BN = BN, kp.stages = stages;
+    kp.a_flags = (ca.tma ? gemm_f16_dev::kOpTma : 0u) | (ca.mn ? gemm_f16_dev::kOpMnMajor : 0u);
+    kp.b_flags = (cb.tma ? gemm_f16_dev::kOpTma : 0u) | (cb.mn ? gemm_f16_dev::kOpMnMajor : 0u);
+    kp.c_tma = c_tma ? 1u : 0u;
+    // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16
+    // (bits 7-9, 10-12 = 0), A/B MN-major flags (bits 15, 16), N >> 3 (bits
+    // 17-22), M >> 4 (bits 24-28).
+    kp.idesc = (1u << 4) | ((ca.mn ? 1u : 0u) << 15) | ((cb.mn ? 1u : 0u) << 16) |
+               ((static_cast<uint32_t>(BN) >> 3) << 17) | ((static_cast<uint32_t>(gemm_f16_dev::kBM) >> 4) << 24);
+    kp.tx_bytes = (ca.tma ? gemm_f16_dev::kStageABytes : 0u) + (cb.tma ? stage_b : 0u);
+    kp.stage_b_bytes = stage_b;
+    kp.full_count = ((ca.tma || cb.tma) ? 1u : 0u) + ((!ca.tma || !cb.tma) ? 128u : 0u);
+
+    pub.swap_ab = swap;
+    pub.a_tma = ca.tma, pub.a_mn_major = ca.mn, pub.b_tma = cb.tma, pub.b_mn_major = cb.mn, pub.c_tma = c_tma;
+    pub.tile_m = gemm_f16_dev::kBM, pub.tile_n = BN, pub.tiles_m = tiles_m, pub.tiles_n = tiles_n;
+    pub.splits = splits, pub.kblocks = kblocks, pub.units = static_cast<int>(units), pub.grid = grid;
+    pub.stages = stages, pub.smem_bytes = smem;
+    pub.workspace_bytes = splits > 1 ? workspace_bytes_for(units, BN, tiles, &pl->ws_floats_bytes) : 0;
+    return GEMM_F16_OK;
+}
+
+gemm_f16_status launch(Plan& pl, DevInfo& dev, void* ws, cudaStream_t stream)
+{
+    KernelParams& kp = pl.kp;
+    if (pl.pub.splits > 1) {
+        kp.ws = static_cast<float*>(ws);
+        kp.counters = reinterpret_cast<int*>(static_cast<char*>(ws) + pl.ws_floats_bytes);
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_mutex);
+        if (!dev.smem_attr_set) {
+            if (cudaFuncSetAttribute(gemm_f16_dev::gemm_f16_persistent, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kMaxDynSmem) != cudaSuccess) {
+                cudaGetLastError();
+                return GEMM_F16_ERR_LAUNCH;
+            }
+            dev.smem_attr_set = true;
+        }
+    }
+    gemm_f16_dev::gemm_f16_persistent<<<pl.pub.grid, gemm_f16_dev::kNumThreads, pl.pub.smem_bytes, stream>>>(kp);
+    if (cudaGetLastError() != cudaSuccess) return GEMM_F16_ERR_LAUNCH;
+    return GEMM_F16_OK;
+}
+
+void* library_workspace(size_t need, cudaStream_t stream)
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(g_mutex);
+    Workspace& w = g_ws[dev];
+    if (w.bytes >= need) return w.ptr;
+    if (w.ptr) {
+        cudaDeviceSynchronize();   // earlier calls may still be using the old buffer
+        cudaFree(w.ptr);
+        w.ptr = nullptr;
+        w.bytes = 0;
+    }
+    void* p = nullptr;
+    if (cudaMalloc(&p, need) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (cudaMemsetAsync(p, 0, need, stream) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(p);
+        return nullptr;
+    }
+    w.ptr = p;
+    w.bytes = need;
+    return p;
+}
+
+gemm_f16_status run(const Args& a, void* user_ws, size_t user_ws_bytes, bool use_library_ws, cudaStream_t stream)
+{
+    DevInfo* dev = nullptr;
+    gemm_f16_status st = validate(a, true, &dev);
+    if (st != GEMM_F16_OK) return st;
+    Plan pl;
+    st = make_plan(a, *dev, &pl);
+    if (st != GEMM_F16_OK) return st;
+    void* ws = nullptr;
+    if (pl.pub.workspace_bytes > 0) {
+        if (use_library_ws) {
+            ws = library_workspace(pl.pub.workspace_bytes, stream);
+            if (!ws) return GEMM_F16_ERR_OUT_OF_MEMORY;
+        } else {
+            if (!user_ws || user_ws_bytes < pl.pub.workspace_bytes || (reinterpret_cast<uintptr_t>(user_ws) & 255u))
+                return GEMM_F16_ERR_OUT_OF_MEMORY;
+            ws = user_ws;
+        }
+    }
+    return launch(pl, *dev, ws, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_f16_status gemm_f16(const void* A, int64_t stride_am, int64_t stride_ak, const void* B, int64_t stride_bk,
+                         int64_t stride_bn, void* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                         cudaStream_t stream)
+{
+    const Args a{A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, M, N, K};
+    return run(a, nullptr, 0, true, stream);
+}
+
+gemm_f16_status gemm_f16_ws(const void* A, int64_t stride_am, int64_t stride_ak, const void* B, int64_t stride_bk,
+                            int64_t stride_bn, void* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    const Args a{A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, M, N, K};
+    return run(a, workspace, workspace_bytes, false, stream);
+}
+
+gemm_f16_status gemm_f16_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes)
+{
+    if (!bytes || M <= 0 || N <= 0 || K <= 0) return GEMM_F16_ERR_INVALID_VALUE;
+    DevInfo* dev = nullptr;
+    gemm_f16_status st = device_info(&dev);
+    if (st != GEMM_F16_OK) return st;
+    bool swap;
+    int64_t Mv, Nv;
+    int BN, tiles_m, tiles_n, kblocks, splits;
+    shape_plan(M, N, K, dev->sms, &swap, &Mv, &Nv, &BN, &tiles_m, &tiles_n, &kblocks, &splits);
+    const int64_t tiles = static_cast<int64_t>(tiles_m) * tiles_n;
+    *bytes = splits > 1 ? workspace_bytes_for(tiles * splits, BN, tiles, nullptr) : 0;
+    return GEMM_F16_OK;
+}
+
+const char* gemm_f16_status_string(int status)
+{
+    switch (status) {
+    case GEMM_F16_OK: return "GEMM_F16_OK";
+    case GEMM_F16_ERR_INVALID_VALUE: return "GEMM_F16_ERR_INVALID_VALUE";
+    case GEMM_F16_ERR_ALIAS: return "GEMM_F16_ERR_ALIAS";
+    case GEMM_F16_ERR_UNSUPPORTED_DEVICE: return "GEMM_F16_ERR_UNSUPPORTED_DEVICE";
+    case GEMM_F16_ERR_OUT_OF_MEMORY: return "GEMM_F16_ERR_OUT_OF_MEMORY";
+    case GEMM_F16_ERR_LAUNCH: return "GEMM_F16_ERR_LAUNCH";
+    case GEMM_F16_ERR_TIMEOUT: return "GEMM_F16_ERR_TIMEOUT";
+    default: return "GEMM_F16_UNKNOWN_STATUS";
+    }
+}
+
+gemm_f16_status gemm_f16_device_status(int* status, int reset)
+{
+    if (!status) return GEMM_F16_ERR_INVALID_VALUE;
+    DevInfo* dev = nullptr;
+    gemm_f16_status st = device_info(&dev);
+    if (st != GEMM_F16_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_F16_ERR_LAUNCH;
+    }
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_gemm_f16_status, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_F16_ERR_LAUNCH;
+    }
+    *status = v;
+    if (reset) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_gemm_f16_status, &zero, sizeof(int)) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_F16_ERR_LAUNCH;
+        }
+        int d = 0;
+        cudaGetDevice(&d);
+        std::lock_guard<std::mutex> lk(g_mutex);
+        if (g_ws[d].ptr && cudaMemset(g_ws[d].ptr, 0, g_ws[d].bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_F16_ERR_LAUNCH;
+        }
+    }
+    return GEMM_F16_OK;
+}
+
+gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stride_ak, const void* B,
+                                  int64_t stride_bk, int64_t stride_bn, void* C, int64_t ldc, int64_t M, int64_t N,
+                                  int64_t K, gemm_f16_plan* plan)
+{
+    if (!plan) return GEMM_F16_ERR_INVALID_VALUE;
+    const Args a{A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, M, N, K};
+    DevInfo* dev = nullptr;
+    gemm_f16_status st = validate(a, false, &dev);
+    if (st != GEMM_F16_OK) return st;
+    Plan pl;
+    st = make_plan(a, *dev, &pl);
+    if (st == GEMM_F16_OK) *plan = pl.pub;
+    return st;
+}
+
+gemm_f16_status gemm_f16_set_option(int option, int64_t value)
+{
+    if (option < 1 || option > 7 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option == GEMM_F16_OPT_FORCE_GATHER && value > 7) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option == GEMM_F16_OPT_TILE_N && value != 0 && (value % 64 != 0 || value > 256))
+        return GEMM_F16_ERR_INVALID_VALUE;
+    if (option == GEMM_F16_OPT_SWAP && value > 2) return GEMM_F16_ERR_INVALID_VALUE;
+    g_opt[option].store(value, std::memory_order_relaxed);
+    return GEMM_F16_OK;
+}
+
+int gemm_f16_abi_version(void) { return GEMM_F16_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,174 @@
+/*
+ * gemm_f16 — dense tiled fp16 matrix multiply for NVIDIA GB300 (sm_103a).
+ *
+ *   C[m, n] = fp16( sum_{k < K} A[m, k] * B[k, n] ),  0 <= m < M, 0 <= n < N
+ *
+ * with fp16 operands, fp32 accumulation and one rounding to fp16 (round to
+ * nearest even; values past the fp16 range become +-inf).
+ *
+ * The operation and its contract follow the pages this library is built from:
+ *  - the definition and the fp16-in / fp32-accumulate / fp16-out precision
+ *    points: "Triton GEMM: from one output tile to addresses, boundaries and
+ *    data reuse" (charlestar.github.io), the opening problem statement and the
+ *    paragraph on the three precision positions; TileLang tutorial ch. 14
+ *    "GEMM operators", section 1.1;
+ *  - strides in elements for both operands and an explicit output pitch: the
+ *    same Triton page, section "Shape states the meaning, stride decides the
+ *    address" (transposed views such as B = X.T are ordinary strided views);
+ *  - dimensions the tile does not divide, with the K tail zero-filled (never
+ *    wrapped modulo K) and only the M x N outputs written: section "Three
+ *    non-divisible dimensions need different boundary handling";
+ *  - 64-bit address arithmetic: section "Putting addresses and boundaries into
+ *    a short kernel";
+ *  - the argument checks (positive sizes and strides, outputs not sharing
+ *    storage with inputs): the wrapper on the same page;
+ *  - split-K with an fp32 partial-sum reduction for shapes whose output tiles
+ *    cannot fill the device: TileLang tutorial ch. 14, section 4.1.
+ *
+ * All functions are thread-safe unless stated.  No function allocates or frees
+ * the caller's memory.
+ */
+#ifndef GEMM_F16_H
+#define GEMM_F16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GEMM_F16_ABI_VERSION 1
+
+typedef enum {
+    GEMM_F16_OK = 0,
+    /* A null pointer, M/N/K <= 0, a stride <= 0, ldc < N, an fp16 pointer that
+       is not 2-byte aligned, a size whose extent overflows int64, a pointer
+       that is not device (or managed) memory of the current device, or a view
+       that runs past the end of the allocation it points into. */
+    GEMM_F16_ERR_INVALID_VALUE = 1,
+    /* The bytes C's M x N view spans overlap the bytes spanned by A or B. */
+    GEMM_F16_ERR_ALIAS = 2,
+    /* The current device is not compute capability 10.3 (GB300). */
+    GEMM_F16_ERR_UNSUPPORTED_DEVICE = 3,
+    /* The split-K workspace could not be allocated, or the caller-supplied
+       workspace is smaller than gemm_f16_workspace_size() reports. */
+    GEMM_F16_ERR_OUT_OF_MEMORY = 4,
+    /* A CUDA runtime/driver call failed while setting up or launching. */
+    GEMM_F16_ERR_LAUNCH = 5,
+    /* Reported through gemm_f16_device_status(): a kernel gave up on a bounded
+       wait (a lost pipeline arrival) and returned early; C is undefined. */
+    GEMM_F16_ERR_TIMEOUT = 6
+} gemm_f16_status;
+
+/*
+ * C = A * B on `stream` (0 = the legacy default stream).  Asynchronous: the
+ * call returns once the kernel is queued.
+ *
+ *   A        device pointer to element (0,0) of A; element (m,k) is at
+ *            A + m*stride_am + k*stride_ak (strides in ELEMENTS, fp16).
+ *   B        device pointer; element (k,n) is at B + k*stride_bk + n*stride_bn.
+ *   C        device pointer; element (m,n) is written at C + m*ldc + n.
+ *            Elements of C outside the M x N view (the pitch padding between
+ *            N and ldc) are never written.
+ *   M, N, K  sizes, all > 0.  Any value; nothing needs to be a tile multiple.
+ *
+ * Any positive strides are accepted (row-major, column-major / transposed
+ * views, pitched slices, non-unit inner strides).  Alignment is not required:
+ * operands whose base is 16-byte aligned with a unit inner stride and a
+ * 16-byte-multiple pitch go through TMA; the others through a bounds-checked
+ * gather path with identical results.
+ *
+ * Ownership: the caller owns A, B and C; they must stay valid until the work
+ * on `stream` completes.  For shapes that use split-K the library uses a
+ * per-device workspace that it allocates on first need (cudaMalloc, which
+ * synchronises the device), grows on demand and frees at process exit; split-K
+ * calls that run concurrently on different streams must use gemm_f16_ws() with
+ * separate workspaces.
+ *
+ * Errors: argument errors are returned before any device work is queued;
+ * launch errors after.  A device-side bounded-wait expiry does not show here:
+ * see gemm_f16_device_status().
+ */
+gemm_f16_status gemm_f16(const void* A, int64_t stride_am, int64_t stride_ak,
+                         const void* B, int64_t stride_bk, int64_t stride_bn,
+                         void* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                         cudaStream_t stream);
+
+/*
+ * Same as gemm_f16() with a caller-owned workspace (device memory of at least
+ * gemm_f16_workspace_size() bytes, 256-byte aligned, zero-filled before its
+ * first use; the kernels leave its counters zeroed again after each call).
+ * `workspace` may be NULL when the size query returns 0.  Calls sharing one
+ * workspace must not overlap in time on the device.
+ */
+gemm_f16_status gemm_f16_ws(const void* A, int64_t stride_am, int64_t stride_ak,
+                            const void* B, int64_t stride_bk, int64_t stride_bn,
+                            void* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes a call with these sizes needs on the current device (0 when
+ * it does not use split-K).  Depends on M, N, K and the device's SM count. */
+gemm_f16_status gemm_f16_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
+
+/* Human-readable name of a status code; never NULL. */
+const char* gemm_f16_status_string(int status);
+
+/*
+ * Read the current device's status word that kernels set on a bounded-wait
+ * expiry (GEMM_F16_OK if none since the last reset).  Synchronises the device.
+ * With reset != 0 the word is cleared and the library's split-K counters are
+ * re-zeroed (an aborted kernel may leave them non-zero).
+ */
+gemm_f16_status gemm_f16_device_status(int* status, int reset);
+
+/* How a call would be executed, for tests and profiling. */
+typedef struct {
+    int swap_ab;        /* computed as C^T = B^T A^T (small M) */
+    int a_tma, a_mn_major, b_tma, b_mn_major, c_tma;   /* kernel-view operands */
+    int tile_m, tile_n, tiles_m, tiles_n;
+    int splits, kblocks, units, grid, stages;
+    int smem_bytes;
+    size_t workspace_bytes;
+} gemm_f16_plan;
+
+/* Fill *plan for the given arguments without launching anything.  Returns the
+ * same validation status gemm_f16() would. */
+gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stride_ak,
+                                  const void* B, int64_t stride_bk, int64_t stride_bn,
+                                  void* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                  gemm_f16_plan* plan);
+
+/*
+ * Process-wide tuning and test knobs (not thread-safe with concurrent calls):
+ *   GEMM_F16_OPT_FORCE_GATHER  bit 0: A, bit 1: B, bit 2: C never use TMA
+ *   GEMM_F16_OPT_SPLITS        > 0: force this split-K count (clamped to the K blocks)
+ *   GEMM_F16_OPT_TILE_N        > 0: force the tile width (multiple of 64, <= 256)
+ *   GEMM_F16_OPT_PANEL         > 0: tile-rows per rasterisation panel (default 8)
+ *   GEMM_F16_OPT_SWAP          0 auto, 1 never swap, 2 always swap
+ *   GEMM_F16_OPT_TIMEOUT_MS    bounded-wait limit in ms (default 1000)
+ *   GEMM_F16_OPT_MAX_CTAS      > 0: cap the persistent grid
+ * A value of 0 restores the default.  Returns GEMM_F16_ERR_INVALID_VALUE for an
+ * unknown option or a value out of range.
+ */
+enum {
+    GEMM_F16_OPT_FORCE_GATHER = 1,
+    GEMM_F16_OPT_SPLITS = 2,
+    GEMM_F16_OPT_TILE_N = 3,
+    GEMM_F16_OPT_PANEL = 4,
+    GEMM_F16_OPT_SWAP = 5,
+    GEMM_F16_OPT_TIMEOUT_MS = 6,
+    GEMM_F16_OPT_MAX_CTAS = 7
+};
+gemm_f16_status gemm_f16_set_option(int option, int64_t value);
+
+/* GEMM_F16_ABI_VERSION of the loaded library. */
+int gemm_f16_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_F16_H */

@@ -1,0 +1,102 @@
+"""The C ABI without a GPU: the library loads, exports what the header declares,
+and rejects bad arguments before touching any device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dense_tiled_gemm_fp16_gb300 as g
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "gemm_f16.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gemm_f16\w*)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = g.lib()
+    names = header_functions()
+    assert set(names) == set(g.EXPORTED)
+    for n in names:
+        assert hasattr(lib, n), n
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def test_status_strings_and_version():
+    assert g.gemm_f16_abi_version() == 1
+    for code, name in g.STATUS.items():
+        assert g.gemm_f16_status_string(code) == name
+    assert g.gemm_f16_status_string(99) == "GEMM_F16_UNKNOWN_STATUS"
+
+
+# Fake, non-null, 256-byte-aligned "pointers": validation rejects these calls
+# before any CUDA call, so nothing is ever dereferenced.
+A, B, C = 1 << 20, 1 << 24, 1 << 28
+
+
+@pytest.mark.parametrize("args", [
+    (0, 4, 1, B, 4, 1, C, 4, 4, 4, 4),        # null A
+    (A, 4, 1, 0, 4, 1, C, 4, 4, 4, 4),        # null B
+    (A, 4, 1, B, 4, 1, 0, 4, 4, 4, 4),        # null C
+    (A, 4, 1, B, 4, 1, C, 4, 0, 4, 4),        # M = 0
+    (A, 4, 1, B, 4, 1, C, 4, 4, 0, 4),        # N = 0
+    (A, 4, 1, B, 4, 1, C, 4, 4, 4, 0),        # K = 0
+    (A, 0, 1, B, 4, 1, C, 4, 4, 4, 4),        # zero stride (broadcast) is outside the contract
+    (A, 4, -1, B, 4, 1, C, 4, 4, 4, 4),       # negative stride
+    (A, 4, 1, B, 4, 1, C, 3, 4, 4, 4),        # ldc < N
+    (A + 1, 4, 1, B, 4, 1, C, 4, 4, 4, 4),    # fp16 pointer not 2-byte aligned
+    (A, 1 << 62, 1, B, 4, 1, C, 4, 4, 4, 4),  # extent overflows int64
+])
+def test_invalid_arguments(args):
+    with pytest.raises(g.GemmF16Error) as e:
+        g.gemm_f16(*args)
+    assert e.value.status == g.ERR_INVALID_VALUE
+
+
+def test_alias_detected():
+    # C's 4x4 view overlaps A's view
+    with pytest.raises(g.GemmF16Error) as e:
+        g.gemm_f16(A, 4, 1, B, 4, 1, A + 8, 4, 4, 4, 4)
+    assert e.value.status == g.ERR_ALIAS
+    # C inside B's span (a transposed B spanning K*sbn)
+    with pytest.raises(g.GemmF16Error) as e:
+        g.gemm_f16(A, 4, 1, B, 1, 1000, B + 2 * 500, 4, 4, 4, 4)
+    assert e.value.status == g.ERR_ALIAS
+
+
+def test_valid_arguments_reach_the_device_check():
+    # On a host without a GB300 a well-formed call stops at the device check.
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(g.GemmF16Error) as e:
+        g.gemm_f16(A, 4, 1, B, 4, 1, C, 4, 4, 4, 4)
+    assert e.value.status == g.ERR_UNSUPPORTED_DEVICE
+
+
+def test_options_validation():
+    with pytest.raises(g.GemmF16Error):
+        g.gemm_f16_set_option(99, 1)
+    with pytest.raises(g.GemmF16Error):
+        g.gemm_f16_set_option(g.OPT_TILE_N, 100)
+    with pytest.raises(g.GemmF16Error):
+        g.gemm_f16_set_option(g.OPT_SWAP, 3)
+    with pytest.raises(g.GemmF16Error):
+        g.gemm_f16_set_option(g.OPT_SPLITS, -1)
+    g.gemm_f16_set_option(g.OPT_TILE_N, 128)
+    g.gemm_f16_set_option(g.OPT_TILE_N, 0)
+
+
+def test_package_has_no_oracle_dependency():
+    # The product never imports the oracle.
+    pkg = os.path.join(ROOT, "dense_tiled_gemm_fp16_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "gemm_oracle" not in text, f

@@ -1,0 +1,312 @@
+"""Parity of the sm_103a GEMM with the CPU oracle, through the C ABI.
+
+Every case runs the library on cuda:0 and compares with the oracle on the same
+seeded fp16 inputs: bit for bit where the inputs are integers (every fp32 sum is
+exact), within the stated tolerance otherwise.  The five configurations are
+covered at full size (whole outputs where the host can afford the oracle,
+4096 seeded samples plus a whole boundary tile where it cannot).
+"""
+import numpy as np
+import pytest
+import torch
+
+import dense_tiled_gemm_fp16_gb300 as g
+import oracle
+import synth
+from synth import workloads
+from tests.parity import assert_bits, assert_close, block_reference, oracle_threads, sampled_reference
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(autouse=True)
+def _defaults():
+    yield
+    for o in (g.OPT_FORCE_GATHER, g.OPT_SPLITS, g.OPT_TILE_N, g.OPT_PANEL, g.OPT_SWAP,
+              g.OPT_TIMEOUT_MS, g.OPT_MAX_CTAS):
+        g.gemm_f16_set_option(o, 0)
+
+
+def to_dev(x: np.ndarray):
+    return torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
+
+
+def gpu(A, B, out=None):
+    C = g.matmul(A, B, out=out)
+    torch.cuda.synchronize()
+    return C
+
+
+def host(t):
+    return t.cpu().numpy()
+
+
+# ----------------------------------------------------------------- layouts
+def make_view(values: np.ndarray, layout: str):
+    """A device fp16 view holding `values` [r, c] in the requested layout."""
+    r, c = values.shape
+    v = torch.from_numpy(np.ascontiguousarray(values))
+    if layout == "row":
+        return v.to(DEV)
+    if layout == "col":                      # transposed view of a row-major [c, r]
+        return v.t().contiguous().to(DEV).t()
+    if layout == "pitch":                    # row-major inside a wider buffer (pitch c+5)
+        buf = torch.full((r, c + 5), float("nan"), dtype=torch.float16)
+        buf[:, :c] = v
+        return buf.to(DEV)[:, :c]
+    if layout == "pitch16":                  # pitch rounded up to 16 elements (TMA-able)
+        p = (c + 15) // 16 * 16 + 16
+        buf = torch.full((r, p), float("nan"), dtype=torch.float16)
+        buf[:, :c] = v
+        return buf.to(DEV)[:, :c]
+    if layout == "offset":                   # base 2 bytes past an aligned address
+        flat = torch.full((r * c + 8,), float("nan"), dtype=torch.float16)
+        flat[1:1 + r * c] = v.reshape(-1)
+        return flat.to(DEV)[1:1 + r * c].view(r, c)
+    if layout == "strided":                  # both strides > 1
+        buf = torch.full((r * 2, c * 3), float("nan"), dtype=torch.float16)
+        buf[::2, ::3] = v
+        return buf.to(DEV)[::2, ::3]
+    raise ValueError(layout)
+
+
+LAYOUTS = ("row", "col", "pitch", "pitch16", "offset", "strided")
+
+
+# -------------------------------------------------------------- tail shape
+@pytest.mark.parametrize("w", [workloads.TAIL_ROWMAJOR_B, workloads.TAIL_TRANSPOSED_B], ids=lambda w: w.name)
+def test_tail_shape_bit_exact(w):
+    A, B = w.A.device_view(DEV), w.B.device_view(DEV)
+    assert tuple(B.stride()) == w.B.strides
+    C = gpu(A, B)
+    ref = oracle.gemm(w.A.host_view(), w.B.host_view())
+    assert_bits(host(C), ref, w.name)
+
+
+@pytest.mark.parametrize("opt,val", [(g.OPT_SWAP, 2), (g.OPT_SPLITS, 2), (g.OPT_TILE_N, 64),
+                                     (g.OPT_PANEL, 1), (g.OPT_MAX_CTAS, 1)])
+def test_tail_shape_forced_plans_bit_exact(opt, val):
+    w = workloads.TAIL_TRANSPOSED_B
+    g.gemm_f16_set_option(opt, val)
+    C = gpu(w.A.device_view(DEV), w.B.device_view(DEV))
+    assert_bits(host(C), oracle.gemm(w.A.host_view(), w.B.host_view()), f"opt {opt}={val}")
+
+
+# ------------------------------------------------------- random brute force
+CASES = []
+_rng = np.random.default_rng(1234)
+for i in range(36):
+    M, N, K = (int(x) for x in _rng.integers(1, 300, 3))
+    CASES.append((i, M, N, K, LAYOUTS[_rng.integers(0, 6)], LAYOUTS[_rng.integers(0, 6)],
+                  bool(_rng.integers(0, 2))))
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-{c[1]}x{c[2]}x{c[3]}-{c[4]}-{c[5]}-{'int' if c[6] else 'real'}")
+def test_random_shapes_and_layouts(case):
+    i, M, N, K, la, lb, integer = case
+    rng = np.random.default_rng(100 + i)
+    if integer:
+        Ah = rng.integers(-3, 4, (M, K)).astype(np.float16)
+        Bh = rng.integers(-3, 4, (K, N)).astype(np.float16)
+    else:
+        Ah = rng.uniform(-1, 1, (M, K)).astype(np.float16)
+        Bh = rng.uniform(-1, 1, (K, N)).astype(np.float16)
+    C = host(gpu(make_view(Ah, la), make_view(Bh, lb)))
+    ref = oracle.gemm(Ah, Bh)
+    if integer and K * 9 <= 2048:
+        assert_bits(C, ref, str(case))
+    else:
+        assert_close(C, ref, K, str(case))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (1, 1, 1000), (1, 700, 1), (700, 1, 1), (127, 129, 63),
+                                   (128, 256, 64), (129, 257, 65), (256, 512, 4096), (64, 64, 64),
+                                   (3, 5000, 333), (65, 300, 129), (2000, 33, 70)])
+def test_edge_sizes(M, N, K):
+    rng = np.random.default_rng(M * 7 + N * 3 + K)
+    Ah = rng.integers(-3, 4, (M, K)).astype(np.float16)
+    Bh = rng.integers(-3, 4, (K, N)).astype(np.float16)
+    C = host(gpu(to_dev(Ah), to_dev(Bh)))
+    ref = oracle.gemm(Ah, Bh, threads=oracle_threads())
+    if K * 9 <= 2048:
+        assert_bits(C, ref, f"{M}x{N}x{K}")
+    else:
+        assert_close(C, ref, K, f"{M}x{N}x{K}")
+
+
+def test_tma_and_gather_paths_agree_bit_for_bit():
+    rng = np.random.default_rng(7)
+    A = to_dev(rng.uniform(-1, 1, (520, 330)).astype(np.float16))
+    B = to_dev(rng.uniform(-1, 1, (330, 700)).astype(np.float16))
+    out = torch.empty((520, 700), dtype=torch.float16, device=DEV)
+    plan = g.plan_for(A, B, out)
+    assert plan["a_tma"] and plan["b_tma"] and plan["c_tma"] and plan["b_mn_major"]
+    C1 = host(gpu(A, B))
+    g.gemm_f16_set_option(g.OPT_FORCE_GATHER, 7)
+    plan = g.plan_for(A, B, out)
+    assert not (plan["a_tma"] or plan["b_tma"] or plan["c_tma"])
+    C2 = host(gpu(A, B))
+    assert_bits(C1, C2, "tma vs gather")
+    assert_close(C1, oracle.gemm(host(A), host(B)), 330, "vs oracle")
+
+
+def test_mn_major_a_and_k_major_b_through_tma():
+    rng = np.random.default_rng(8)
+    Ah = rng.uniform(-1, 1, (384, 256)).astype(np.float16)
+    Bh = rng.uniform(-1, 1, (256, 320)).astype(np.float16)
+    A = make_view(Ah, "col")    # M-major A
+    B = make_view(Bh, "col")    # K-major B
+    out = torch.empty((384, 320), dtype=torch.float16, device=DEV)
+    plan = g.plan_for(A, B, out)
+    assert plan["a_tma"] and plan["a_mn_major"] and plan["b_tma"] and not plan["b_mn_major"]
+    assert_close(host(gpu(A, B)), oracle.gemm(Ah, Bh), 256, "mn-major A, k-major B")
+
+
+# ------------------------------------------------------- boundary behaviour
+def test_k_tail_is_zero_filled_not_wrapped():
+    # The Triton page's K-tail example (a=[1,2,3], b=[4,5,6] -> 32; wrapping K
+    # would give 36).  The elements just past K are NaN in memory: reading any
+    # of them would poison the result.
+    a = torch.full((1, 8), float("nan"), dtype=torch.float16)
+    a[0, :3] = torch.tensor([1.0, 2.0, 3.0])
+    b = torch.full((8, 8), float("nan"), dtype=torch.float16)
+    b[:3, 0] = torch.tensor([4.0, 5.0, 6.0])
+    C = host(gpu(a.to(DEV)[:, :3], b.to(DEV)[:3, :1]))
+    assert C[0, 0] == 32.0
+    # same on the TMA path: 16-byte pitch, K = 65, NaN beyond K in every row
+    rng = np.random.default_rng(9)
+    A = torch.full((200, 72), float("nan"), dtype=torch.float16)
+    A[:, :65] = torch.from_numpy(rng.integers(-3, 4, (200, 65)).astype(np.float16))
+    B = torch.full((72, 136), float("nan"), dtype=torch.float16)
+    B[:65, :130] = torch.from_numpy(rng.integers(-3, 4, (65, 130)).astype(np.float16))
+    Av, Bv = A.to(DEV)[:, :65], B.to(DEV)[:65, :130]
+    out = torch.empty((200, 130), dtype=torch.float16, device=DEV)
+    assert g.plan_for(Av, Bv, out)["a_tma"]
+    C = host(gpu(Av, Bv))
+    assert_bits(C, oracle.gemm(A[:, :65].numpy(), B[:65, :130].numpy()), "tma k-tail")
+
+
+@pytest.mark.parametrize("force", [0, 7])
+def test_only_the_view_of_c_is_written(force):
+    g.gemm_f16_set_option(g.OPT_FORCE_GATHER, force)
+    rng = np.random.default_rng(10)
+    M, N, K, ldc = 300, 200, 96, 264
+    Ah = rng.integers(-3, 4, (M, K)).astype(np.float16)
+    Bh = rng.integers(-3, 4, (K, N)).astype(np.float16)
+    canary = np.float16(-12345.0)
+    buf = torch.full((M + 3, ldc), float(canary), dtype=torch.float16, device=DEV)
+    out = buf[:M, :N]
+    gpu(to_dev(Ah), to_dev(Bh), out=out)
+    hb = host(buf)
+    assert_bits(hb[:M, :N], oracle.gemm(Ah, Bh), "view")
+    assert np.all(hb[:M, N:] == canary) and np.all(hb[M:] == canary)
+
+
+def test_overflow_gives_inf_like_the_oracle():
+    a = torch.full((4, 64), 16.0, dtype=torch.float16, device=DEV)
+    b = torch.full((64, 4), 128.0, dtype=torch.float16, device=DEV)
+    C = host(gpu(a, b))  # 64 * 2048 = 131072 > 65504
+    assert np.all(np.isposinf(C))
+
+
+# ----------------------------------------------------------------- split-K
+def test_split_k_deterministic_and_workspace_paths():
+    rng = np.random.default_rng(11)
+    M, N, K = 16, 4096, 8192
+    Ah = rng.uniform(-1, 1, (M, K)).astype(np.float16)
+    Bh = rng.uniform(-1, 1, (K, N)).astype(np.float16)
+    A, B = to_dev(Ah), to_dev(Bh)
+    out = torch.empty((M, N), dtype=torch.float16, device=DEV)
+    plan = g.plan_for(A, B, out)
+    assert plan["swap_ab"] and plan["splits"] > 1
+    C1 = host(gpu(A, B))
+    C2 = host(gpu(A, B))
+    assert_bits(C1, C2, "split-K repeatability")
+    ref = oracle.gemm(Ah, Bh, threads=oracle_threads())
+    assert_close(C1, ref, K, "split-K vs oracle")
+    # caller-owned workspace gives the same bits
+    nbytes = g.gemm_f16_workspace_size(M, N, K)
+    assert nbytes == plan["workspace_bytes"] > 0
+    ws = torch.zeros(nbytes // 4 + 64, dtype=torch.int32, device=DEV)
+    out2 = torch.empty_like(out)
+    g.gemm_f16_ws(A.data_ptr(), K, 1, B.data_ptr(), N, 1, out2.data_ptr(), N, M, N, K,
+                  ws.data_ptr(), nbytes, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert_bits(host(out2), C1, "caller workspace")
+    # too small a workspace is refused
+    with pytest.raises(g.GemmF16Error) as e:
+        g.gemm_f16_ws(A.data_ptr(), K, 1, B.data_ptr(), N, 1, out2.data_ptr(), N, M, N, K,
+                      ws.data_ptr(), nbytes - 256, 0)
+    assert e.value.status == g.ERR_OUT_OF_MEMORY
+    # forcing no split changes the summation order only
+    g.gemm_f16_set_option(g.OPT_SPLITS, 1)
+    assert_close(host(gpu(A, B)), ref, K, "no split")
+
+
+def test_alias_and_bad_memory_rejected_on_device():
+    A = torch.zeros((64, 64), dtype=torch.float16, device=DEV)
+    B = torch.zeros((64, 64), dtype=torch.float16, device=DEV)
+    with pytest.raises(g.GemmF16Error) as e:
+        g.matmul(A, B, out=A)
+    assert e.value.status == g.ERR_ALIAS
+    # a view that runs past the end of its allocation
+    with pytest.raises(g.GemmF16Error) as e:
+        g.gemm_f16(A.data_ptr(), 1 << 20, 1, B.data_ptr(), 64, 1,
+                   torch.empty((64, 64), dtype=torch.float16, device=DEV).data_ptr(), 64, 64, 64, 64)
+    assert e.value.status == g.ERR_INVALID_VALUE
+    # host memory is refused
+    h = torch.zeros((64, 64), dtype=torch.float16)
+    with pytest.raises(g.GemmF16Error) as e:
+        g.gemm_f16(h.data_ptr(), 64, 1, B.data_ptr(), 64, 1,
+                   torch.empty((64, 64), dtype=torch.float16, device=DEV).data_ptr(), 64, 64, 64, 64)
+    assert e.value.status == g.ERR_INVALID_VALUE
+
+
+# ---------------------------------------------------- the five configurations
+def test_device_generator_matches_host():
+    for kind, seed, n in (("uniform", 2, 1 << 20), ("int3", 1, 12345)):
+        d = synth.buffer_torch(kind, seed, n, DEV).cpu().numpy()
+        assert np.array_equal(d.view(np.uint16), synth.buffer_np(kind, seed, n).view(np.uint16))
+
+
+def _run_workload(w):
+    A, B = w.A.device_view(DEV), w.B.device_view(DEV)
+    assert tuple(A.stride()) == w.A.strides and tuple(B.stride()) == w.B.strides
+    C = gpu(A, B)
+    del A, B
+    return C
+
+
+def test_decode_m16_full_output():
+    w = workloads.DECODE_16x16384x8192
+    C = host(_run_workload(w))
+    ref = oracle.gemm(w.A.host_view(), w.B.host_view(), threads=oracle_threads())
+    assert_close(C, ref, w.K, w.name)
+
+
+def test_irregular_strided_full_output():
+    w = workloads.IRREGULAR_3001x1999x4097
+    C = host(_run_workload(w))
+    ref = oracle.gemm(w.A.host_view(), w.B.host_view(), threads=oracle_threads())
+    assert_close(C, ref, w.K, w.name)
+
+
+@pytest.mark.parametrize("w", [workloads.SQUARE_4096, workloads.MOE_131072x2048x7168], ids=lambda w: w.name)
+def test_large_sampled_plus_boundary_tile(w):
+    C = _run_workload(w)
+    rng = np.random.default_rng(20260)
+    ms = rng.integers(0, w.M, 4096)
+    ns = rng.integers(0, w.N, 4096)
+    got = C[torch.from_numpy(ms).to(DEV), torch.from_numpy(ns).to(DEV)].cpu().numpy()
+    assert_close(got, sampled_reference(w, ms, ns), w.K, f"{w.name} samples")
+    out = torch.empty((1, 1), dtype=torch.float16, device=DEV)
+    bm, bn = 128, 256
+    tile = C[w.M - bm:, w.N - bn:].cpu().numpy()
+    assert_close(tile, block_reference(w, w.M - bm, w.M, w.N - bn, w.N), w.K, f"{w.name} last tile")
+    del out
+
+
+def test_no_kernel_reported_a_timeout():
+    assert g.gemm_f16_device_status(reset=True) == 0
