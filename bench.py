@@ -218,6 +218,27 @@ def run_ours(args):
     value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
 
     # ---- end to end: pinned host inputs in, result out, inside the timed region
+    if args.no_e2e:
+        e2e_ms = float("nan")
+    else:
+        e2e_ms = run_e2e(args, w, dev, stream, C, barrier, pg)
+    status = g.gemm_f16_device_status()
+    result = None
+    if rank == 0:
+        result = report(args, w, plan, peaks, bnd, flops, nbytes, ms_per_step, value, wall, clk, e2e_ms,
+                        world, status, A, B)
+    if pg is not None:
+        pg.destroy_process_group()
+    return result
+
+
+def run_e2e(args, w, dev, stream, C, barrier, pg):
+    import numpy as np
+    import torch
+
+    import dense_tiled_gemm_fp16_gb300 as g
+
+    M, N = w.M, w.N
     A_h = torch.from_numpy(np.ascontiguousarray(w.A.host_buffer())).pin_memory()
     B_h = torch.from_numpy(np.ascontiguousarray(w.B.host_buffer())).pin_memory()
     C_h = torch.empty((M, N), dtype=torch.float16).pin_memory()
@@ -250,61 +271,63 @@ def run_ours(args):
         t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         e2e_ms = float(t.item())
-    status = g.gemm_f16_device_status()
+    return e2e_ms
 
-    result = None
-    if rank == 0:
-        if bnd == "tensor":
-            achieved = flops / (ms_per_step * 1e-3) / 1e12
-            roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["tflops"],
-                    "unit": "TFLOP/s", "frac": round(achieved / peaks["tflops"], 4)}
-        else:
-            achieved = nbytes / (ms_per_step * 1e-3) / 1e9
-            roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
-        roof["traffic"] = None
-        roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json bf16 burst / copy bandwidth)"
-        roof["kernel"] = "gemm_f16_persistent"
-        cpu = None
-        if not args.no_cpu_baseline:
-            threads = os.cpu_count() or 1
-            rate, rows, dt = cpu_oracle_rate(w, args.cpu_seconds, threads)
-            cpu = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                   "sample": f"{rows} of {M} output rows x all {N} columns, K={K} ({dt:.1f} s)"}
-        result = {
-            "metric": METRIC,
-            "value": round(value, 2),
-            "unit": "TFLOP/s",
-            "n_gpus": world,
-            "steps": args.steps,
-            "warmup": args.warmup,
-            "ms_per_step": round(ms_per_step, 5),
-            "higher_is_better": True,
-            "scaling": "weak",
-            "vs_baseline": None,
-            "dtype": "f16 (fp32 accumulate)",
-            "data": "synthetic (seeded SplitMix64 fill)",
-            "config": {"workload": w.name, "M": M, "N": N, "K": K,
-                       "A": f"strides {tuple(A.stride())}", "B": f"strides {tuple(B.stride())}",
-                       "distribution": w.A.kind, "l2": "flushed between steps (512 MiB write)",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "plan": {k: plan[k] for k in ("swap_ab", "a_tma", "b_tma", "c_tma", "tile_n",
-                                                     "splits", "grid", "stages")}},
-            "hbm_gbs_min_traffic": round(nbytes / (ms_per_step * 1e-3) / 1e9, 1),
-            "wall_s_timed_region": round(wall, 4),
-            "clocks": clk,
-            "e2e": {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-                    "ms_per_step": round(e2e_ms, 4),
-                    "h2d_bytes_per_step": int(2 * (w.A.numel + w.B.numel)),
-                    "d2h_bytes_per_step": int(2 * M * N)},
-            "gpu_launches": args.steps,
-            "roofline": roof,
-            "cpu_baseline": cpu,
-            "device_status": status,
-        }
-    if pg is not None:
-        pg.destroy_process_group()
-    return result
+
+def report(args, w, plan, peaks, bnd, flops, nbytes, ms_per_step, value, wall, clk, e2e_ms, world,
+           status, A, B):
+    M, N, K = w.M, w.N, w.K
+    if bnd == "tensor":
+        achieved = flops / (ms_per_step * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["tflops"], 4)}
+    else:
+        achieved = nbytes / (ms_per_step * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    roof["traffic"] = None
+    roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json bf16 burst / copy bandwidth)"
+    roof["kernel"] = "gemm_f16_persistent"
+    cpu = None
+    if not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        rate, rows, dt = cpu_oracle_rate(w, args.cpu_seconds, threads)
+        cpu = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{rows} of {M} output rows x all {N} columns, K={K} ({dt:.1f} s)"}
+    e2e = None
+    if e2e_ms == e2e_ms:   # not NaN
+        e2e = {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+               "ms_per_step": round(e2e_ms, 4),
+               "h2d_bytes_per_step": int(2 * (w.A.numel + w.B.numel)),
+               "d2h_bytes_per_step": int(2 * M * N)}
+    return {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16 (fp32 accumulate)",
+        "data": "synthetic (seeded SplitMix64 fill)",
+        "config": {"workload": w.name, "M": M, "N": N, "K": K,
+                   "A": f"strides {tuple(A.stride())}", "B": f"strides {tuple(B.stride())}",
+                   "distribution": w.A.kind, "l2": "flushed between steps (512 MiB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "plan": {k: plan[k] for k in ("swap_ab", "a_tma", "b_tma", "c_tma", "tile_n",
+                                                 "splits", "grid", "stages")}},
+        "hbm_gbs_min_traffic": round(nbytes / (ms_per_step * 1e-3) / 1e9, 1),
+        "wall_s_timed_region": round(wall, 4),
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "device_status": status,
+    }
 
 
 # -------------------------------------------------------- reference arm
@@ -356,8 +379,19 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="square_4096")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--shape", default=None,
+                    help="M,N,K: an ad-hoc row-major uniform[-1,1] workload instead of --workload")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
+    if args.shape:
+        from synth import workloads
+        M, N, K = (int(x) for x in args.shape.split(","))
+        name = f"rowmajor_{M}x{N}x{K}"
+        workloads.BY_NAME[name] = workloads.Workload(
+            name, M, N, K, workloads.Operand(M, K, "uniform", 21), workloads.Operand(K, N, "uniform", 22),
+            "ad-hoc row-major uniform[-1,1] shape")
+        args.workload = name
     if args.warmup < 3 and args.impl == "ours":
         log("note: fewer than 3 warm-up steps")
     res = run_reference(args) if args.impl == "reference" else run_ours(args)

@@ -36,9 +36,14 @@ struct DevInfo {
 std::mutex g_mutex;
 DevInfo g_dev[kMaxDevices];
 
+// Library-owned split-K workspace: the partial sums (contents never need to be
+// initialised) and the per-tile arrival counters, which start at zero and are
+// returned to zero by the last CTA of every tile.
 struct Workspace {
-    void* ptr = nullptr;
-    size_t bytes = 0;
+    void* partials = nullptr;
+    size_t partial_bytes = 0;
+    int* counters = nullptr;
+    size_t counter_bytes = 0;
 };
 Workspace g_ws[kMaxDevices];
 
@@ -213,7 +218,8 @@ bool encode_2d(CUtensorMap* tm, const void* ptr, uint64_t inner, uint64_t outer,
 struct Plan {
     gemm_f16_plan pub;
     KernelParams kp;
-    size_t ws_floats_bytes;
+    size_t counter_bytes;   // split-K counters: align256(4 * tiles)
+    size_t partial_bytes;   // split-K partials: align256(4 * units * tile_m * tile_n)
 };
 
 // Split-K count: only when the output tiles cannot occupy every SM.  Picks the
@@ -262,11 +268,14 @@ void shape_plan(int64_t M, int64_t N, int64_t K, int sms, bool* swap, int64_t* M
     *splits = choose_splits(static_cast<int64_t>(*tiles_m) * *tiles_n, *kblocks, sms);
 }
 
-size_t workspace_bytes_for(int64_t units, int BN, int64_t tiles, size_t* floats_bytes)
+// Caller-workspace layout: [counters, align256(4*tiles)] [partials].
+size_t workspace_bytes_for(int64_t units, int BN, int64_t tiles, size_t* counter_bytes, size_t* partial_bytes)
 {
-    const size_t fb = static_cast<size_t>(round_up(units * gemm_f16_dev::kBM * BN * 4, 256));
-    if (floats_bytes) *floats_bytes = fb;
-    return fb + static_cast<size_t>(round_up(tiles * 4, 256));
+    const size_t cb = static_cast<size_t>(round_up(tiles * 4, 256));
+    const size_t pb = static_cast<size_t>(round_up(units * gemm_f16_dev::kBM * BN * 4, 256));
+    if (counter_bytes) *counter_bytes = cb;
+    if (partial_bytes) *partial_bytes = pb;
+    return cb + pb;
 }
 
 gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
@@ -356,17 +365,16 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     pub.tile_m = gemm_f16_dev::kBM, pub.tile_n = BN, pub.tiles_m = tiles_m, pub.tiles_n = tiles_n;
     pub.splits = splits, pub.kblocks = kblocks, pub.units = static_cast<int>(units), pub.grid = grid;
     pub.stages = stages, pub.smem_bytes = smem;
-    pub.workspace_bytes = splits > 1 ? workspace_bytes_for(units, BN, tiles, &pl->ws_floats_bytes) : 0;
+    pub.workspace_bytes =
+        splits > 1 ? workspace_bytes_for(units, BN, tiles, &pl->counter_bytes, &pl->partial_bytes) : 0;
     return GEMM_F16_OK;
 }
 
-gemm_f16_status launch(Plan& pl, DevInfo& dev, void* ws, cudaStream_t stream)
+gemm_f16_status launch(Plan& pl, DevInfo& dev, float* partials, int* counters, cudaStream_t stream)
 {
     KernelParams& kp = pl.kp;
-    if (pl.pub.splits > 1) {
-        kp.ws = static_cast<float*>(ws);
-        kp.counters = reinterpret_cast<int*>(static_cast<char*>(ws) + pl.ws_floats_bytes);
-    }
+    kp.ws = partials;
+    kp.counters = counters;
     {
         std::lock_guard<std::mutex> lk(g_mutex);
         if (!dev.smem_attr_set) {
@@ -383,32 +391,30 @@ gemm_f16_status launch(Plan& pl, DevInfo& dev, void* ws, cudaStream_t stream)
     return GEMM_F16_OK;
 }
 
-void* library_workspace(size_t need, cudaStream_t stream)
+// Grow one buffer of the library workspace.  Earlier calls may still use the
+// old buffer, so the device is synchronised before it is freed.
+bool grow(void** buf, size_t* have, size_t need, bool zero, cudaStream_t stream)
 {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    std::lock_guard<std::mutex> lk(g_mutex);
-    Workspace& w = g_ws[dev];
-    if (w.bytes >= need) return w.ptr;
-    if (w.ptr) {
-        cudaDeviceSynchronize();   // earlier calls may still be using the old buffer
-        cudaFree(w.ptr);
-        w.ptr = nullptr;
-        w.bytes = 0;
+    if (*have >= need) return true;
+    if (*buf) {
+        cudaDeviceSynchronize();
+        cudaFree(*buf);
+        *buf = nullptr;
+        *have = 0;
     }
     void* p = nullptr;
     if (cudaMalloc(&p, need) != cudaSuccess) {
         cudaGetLastError();
-        return nullptr;
+        return false;
     }
-    if (cudaMemsetAsync(p, 0, need, stream) != cudaSuccess) {
+    if (zero && cudaMemsetAsync(p, 0, need, stream) != cudaSuccess) {
         cudaGetLastError();
         cudaFree(p);
-        return nullptr;
+        return false;
     }
-    w.ptr = p;
-    w.bytes = need;
-    return p;
+    *buf = p;
+    *have = need;
+    return true;
 }
 
 gemm_f16_status run(const Args& a, void* user_ws, size_t user_ws_bytes, bool use_library_ws, cudaStream_t stream)
@@ -419,18 +425,35 @@ gemm_f16_status run(const Args& a, void* user_ws, size_t user_ws_bytes, bool use
     Plan pl;
     st = make_plan(a, *dev, &pl);
     if (st != GEMM_F16_OK) return st;
-    void* ws = nullptr;
-    if (pl.pub.workspace_bytes > 0) {
+    float* partials = nullptr;
+    int* counters = nullptr;
+    if (pl.pub.splits > 1) {
         if (use_library_ws) {
-            ws = library_workspace(pl.pub.workspace_bytes, stream);
-            if (!ws) return GEMM_F16_ERR_OUT_OF_MEMORY;
+            int d = 0;
+            cudaGetDevice(&d);
+            std::lock_guard<std::mutex> lk(g_mutex);
+            Workspace& w = g_ws[d];
+            void* c = w.counters;
+            if (!grow(&w.partials, &w.partial_bytes, pl.partial_bytes, false, stream) ||
+                !grow(&c, &w.counter_bytes, pl.counter_bytes, true, stream))
+                return GEMM_F16_ERR_OUT_OF_MEMORY;
+            w.counters = static_cast<int*>(c);
+            partials = static_cast<float*>(w.partials);
+            counters = w.counters;
         } else {
             if (!user_ws || user_ws_bytes < pl.pub.workspace_bytes || (reinterpret_cast<uintptr_t>(user_ws) & 255u))
                 return GEMM_F16_ERR_OUT_OF_MEMORY;
-            ws = user_ws;
+            // A caller's workspace may hold anything (another shape's partials):
+            // clear the counter block on the stream before the kernel.
+            counters = static_cast<int*>(user_ws);
+            partials = reinterpret_cast<float*>(static_cast<char*>(user_ws) + pl.counter_bytes);
+            if (cudaMemsetAsync(counters, 0, pl.counter_bytes, stream) != cudaSuccess) {
+                cudaGetLastError();
+                return GEMM_F16_ERR_LAUNCH;
+            }
         }
     }
-    return launch(pl, *dev, ws, stream);
+    return launch(pl, *dev, partials, counters, stream);
 }
 
 }  // namespace
@@ -464,7 +487,7 @@ gemm_f16_status gemm_f16_workspace_size(int64_t M, int64_t N, int64_t K, size_t*
     int BN, tiles_m, tiles_n, kblocks, splits;
     shape_plan(M, N, K, dev->sms, &swap, &Mv, &Nv, &BN, &tiles_m, &tiles_n, &kblocks, &splits);
     const int64_t tiles = static_cast<int64_t>(tiles_m) * tiles_n;
-    *bytes = splits > 1 ? workspace_bytes_for(tiles * splits, BN, tiles, nullptr) : 0;
+    *bytes = splits > 1 ? workspace_bytes_for(tiles * splits, BN, tiles, nullptr, nullptr) : 0;
     return GEMM_F16_OK;
 }
 
@@ -507,7 +530,7 @@ gemm_f16_status gemm_f16_device_status(int* status, int reset)
         int d = 0;
         cudaGetDevice(&d);
         std::lock_guard<std::mutex> lk(g_mutex);
-        if (g_ws[d].ptr && cudaMemset(g_ws[d].ptr, 0, g_ws[d].bytes) != cudaSuccess) {
+        if (g_ws[d].counters && cudaMemset(g_ws[d].counters, 0, g_ws[d].counter_bytes) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_F16_ERR_LAUNCH;
         }

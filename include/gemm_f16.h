@@ -98,11 +98,12 @@ gemm_f16_status gemm_f16(const void* A, int64_t stride_am, int64_t stride_ak,
                          cudaStream_t stream);
 
 /*
- * Same as gemm_f16() with a caller-owned workspace (device memory of at least
- * gemm_f16_workspace_size() bytes, 256-byte aligned, zero-filled before its
- * first use; the kernels leave its counters zeroed again after each call).
- * `workspace` may be NULL when the size query returns 0.  Calls sharing one
- * workspace must not overlap in time on the device.
+ * Same as gemm_f16() with a caller-owned workspace: device memory of at least
+ * gemm_f16_workspace_size() bytes, 256-byte aligned, any contents.  When the
+ * call uses split-K it first clears the workspace's counter block with
+ * cudaMemsetAsync on `stream`, then the kernel writes fp32 partial sums into
+ * the rest.  `workspace` may be NULL when the size query returns 0.  Calls
+ * sharing one workspace must not overlap in time on the device.
  */
 gemm_f16_status gemm_f16_ws(const void* A, int64_t stride_am, int64_t stride_ak,
                             const void* B, int64_t stride_bk, int64_t stride_bn,

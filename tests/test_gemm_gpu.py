@@ -138,9 +138,9 @@ def test_edge_sizes(M, N, K):
 
 def test_tma_and_gather_paths_agree_bit_for_bit():
     rng = np.random.default_rng(7)
-    A = to_dev(rng.uniform(-1, 1, (520, 330)).astype(np.float16))
-    B = to_dev(rng.uniform(-1, 1, (330, 700)).astype(np.float16))
-    out = torch.empty((520, 700), dtype=torch.float16, device=DEV)
+    A = to_dev(rng.uniform(-1, 1, (520, 336)).astype(np.float16))
+    B = to_dev(rng.uniform(-1, 1, (336, 704)).astype(np.float16))
+    out = torch.empty((520, 704), dtype=torch.float16, device=DEV)
     plan = g.plan_for(A, B, out)
     assert plan["a_tma"] and plan["b_tma"] and plan["c_tma"] and plan["b_mn_major"]
     C1 = host(gpu(A, B))
@@ -149,7 +149,7 @@ def test_tma_and_gather_paths_agree_bit_for_bit():
     assert not (plan["a_tma"] or plan["b_tma"] or plan["c_tma"])
     C2 = host(gpu(A, B))
     assert_bits(C1, C2, "tma vs gather")
-    assert_close(C1, oracle.gemm(host(A), host(B)), 330, "vs oracle")
+    assert_close(C1, oracle.gemm(host(A), host(B)), 336, "vs oracle")
 
 
 def test_mn_major_a_and_k_major_b_through_tma():
@@ -251,11 +251,20 @@ def test_alias_and_bad_memory_rejected_on_device():
     with pytest.raises(g.GemmF16Error) as e:
         g.matmul(A, B, out=A)
     assert e.value.status == g.ERR_ALIAS
-    # a view that runs past the end of its allocation
+    # a view that runs past the end of its allocation is never launched (it is
+    # refused as out of its allocation, or as overlapping C if C happens to
+    # sit in the span)
     with pytest.raises(g.GemmF16Error) as e:
         g.gemm_f16(A.data_ptr(), 1 << 20, 1, B.data_ptr(), 64, 1,
                    torch.empty((64, 64), dtype=torch.float16, device=DEV).data_ptr(), 64, 64, 64, 64)
-    assert e.value.status == g.ERR_INVALID_VALUE
+    assert e.value.status in (g.ERR_INVALID_VALUE, g.ERR_ALIAS)
+    # past the end of a 4 MiB allocation (its own segment), with C elsewhere
+    X = torch.zeros(1 << 21, dtype=torch.float16, device=DEV)
+    Cx = torch.empty((64, 64), dtype=torch.float16, device=DEV)
+    with pytest.raises(g.GemmF16Error) as e:
+        g.gemm_f16(X.data_ptr() + 2 * ((1 << 21) - 64 * 64 + 8), 64, 1, B.data_ptr(), 64, 1,
+                   Cx.data_ptr(), 64, 64, 64, 64)
+    assert e.value.status in (g.ERR_INVALID_VALUE, g.ERR_ALIAS)
     # host memory is refused
     h = torch.zeros((64, 64), dtype=torch.float16)
     with pytest.raises(g.GemmF16Error) as e:
