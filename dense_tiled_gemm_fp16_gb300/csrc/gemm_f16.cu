@@ -545,7 +545,7 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
     if (!plan) return GEMM_F16_ERR_INVALID_VALUE;
     const Args a{A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, M, N, K};
     DevInfo* dev = nullptr;
-    gemm_f16_status st = validate(a, false, &dev);
+    gemm_f16_status st = validate(a, true, &dev);
     if (st != GEMM_F16_OK) return st;
     Plan pl;
     st = make_plan(a, *dev, &pl);

@@ -245,31 +245,45 @@ def test_split_k_deterministic_and_workspace_paths():
     assert_close(host(gpu(A, B)), ref, K, "no split")
 
 
+def _segment_end(ptr):
+    """End address of the caching-allocator segment (one cudaMalloc) holding ptr."""
+    for seg in torch.cuda.memory_snapshot():
+        if seg["address"] <= ptr < seg["address"] + seg["total_size"]:
+            return seg["address"] + seg["total_size"]
+    return None
+
+
 def test_alias_and_bad_memory_rejected_on_device():
+    # Every check here goes through gemm_f16_get_plan, which validates exactly
+    # like gemm_f16 but never launches, so a view that is wrong on purpose
+    # cannot reach the GPU.
     A = torch.zeros((64, 64), dtype=torch.float16, device=DEV)
     B = torch.zeros((64, 64), dtype=torch.float16, device=DEV)
+    C = torch.empty((64, 64), dtype=torch.float16, device=DEV)
     with pytest.raises(g.GemmF16Error) as e:
         g.matmul(A, B, out=A)
     assert e.value.status == g.ERR_ALIAS
-    # a view that runs past the end of its allocation is never launched (it is
-    # refused as out of its allocation, or as overlapping C if C happens to
-    # sit in the span)
+    # the same arguments with C elsewhere are accepted
+    g.gemm_f16_get_plan(A.data_ptr(), 64, 1, B.data_ptr(), 64, 1, C.data_ptr(), 64, 64, 64, 64)
+    # A's view ends 2 bytes past the end of the cudaMalloc segment holding it
+    end = _segment_end(A.data_ptr())
+    assert end is not None
+    start = end - 2 * 64 * 64 + 2
+    start -= start % 16
+    a_ptr = start + 2 * ((end - start) // 2 - 64 * 64 + 1)
     with pytest.raises(g.GemmF16Error) as e:
-        g.gemm_f16(A.data_ptr(), 1 << 20, 1, B.data_ptr(), 64, 1,
-                   torch.empty((64, 64), dtype=torch.float16, device=DEV).data_ptr(), 64, 64, 64, 64)
+        g.gemm_f16_get_plan(a_ptr, 64, 1, B.data_ptr(), 64, 1, C.data_ptr(), 64, 64, 64, 64)
     assert e.value.status in (g.ERR_INVALID_VALUE, g.ERR_ALIAS)
-    # past the end of a 4 MiB allocation (its own segment), with C elsewhere
-    X = torch.zeros(1 << 21, dtype=torch.float16, device=DEV)
-    Cx = torch.empty((64, 64), dtype=torch.float16, device=DEV)
-    with pytest.raises(g.GemmF16Error) as e:
-        g.gemm_f16(X.data_ptr() + 2 * ((1 << 21) - 64 * 64 + 8), 64, 1, B.data_ptr(), 64, 1,
-                   Cx.data_ptr(), 64, 64, 64, 64)
-    assert e.value.status in (g.ERR_INVALID_VALUE, g.ERR_ALIAS)
+    if not (C.data_ptr() < end + 2 and a_ptr < C.data_ptr() + 2 * 64 * 64):
+        assert e.value.status == g.ERR_INVALID_VALUE
+    # the view that ends exactly at the segment end is fine
+    ok_ptr = end - 2 * 64 * 64
+    if not (ok_ptr < C.data_ptr() + 2 * 64 * 64 and C.data_ptr() < end):
+        g.gemm_f16_get_plan(ok_ptr, 64, 1, B.data_ptr(), 64, 1, C.data_ptr(), 64, 64, 64, 64)
     # host memory is refused
     h = torch.zeros((64, 64), dtype=torch.float16)
     with pytest.raises(g.GemmF16Error) as e:
-        g.gemm_f16(h.data_ptr(), 64, 1, B.data_ptr(), 64, 1,
-                   torch.empty((64, 64), dtype=torch.float16, device=DEV).data_ptr(), 64, 64, 64, 64)
+        g.gemm_f16_get_plan(h.data_ptr(), 64, 1, B.data_ptr(), 64, 1, C.data_ptr(), 64, 64, 64, 64)
     assert e.value.status == g.ERR_INVALID_VALUE
 
 
