@@ -317,6 +317,7 @@ def report(args, w, plan, peaks, bnd, flops, nbytes, ms_per_step, value, wall, c
                    "A": f"strides {tuple(A.stride())}", "B": f"strides {tuple(B.stride())}",
                    "distribution": w.A.kind, "l2": "flushed between steps (512 MiB write)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "options": args.opt,
                    "plan": {k: plan[k] for k in ("swap_ab", "a_tma", "b_tma", "c_tma", "tile_n",
                                                  "splits", "grid", "stages")}},
         "hbm_gbs_min_traffic": round(nbytes / (ms_per_step * 1e-3) / 1e9, 1),
@@ -383,7 +384,14 @@ def main():
     ap.add_argument("--shape", default=None,
                     help="M,N,K: an ad-hoc row-major uniform[-1,1] workload instead of --workload")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--opt", action="append", default=[],
+                    help="library tuning knob NAME=VALUE (force_gather, splits, tile_n, panel, swap, max_ctas)")
     args = ap.parse_args()
+    if args.opt and args.impl == "ours":
+        import dense_tiled_gemm_fp16_gb300 as g
+        for kv in args.opt:
+            k, v = kv.split("=")
+            g.gemm_f16_set_option(getattr(g, "OPT_" + k.upper()), int(v))
     if args.shape:
         from synth import workloads
         M, N, K = (int(x) for x in args.shape.split(","))

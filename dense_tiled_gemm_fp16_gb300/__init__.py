@@ -38,6 +38,7 @@ OPT_PANEL = 4
 OPT_SWAP = 5
 OPT_TIMEOUT_MS = 6
 OPT_MAX_CTAS = 7
+OPT_PAIR = 8
 
 # Every symbol include/gemm_f16.h declares.
 EXPORTED = ("gemm_f16", "gemm_f16_ws", "gemm_f16_workspace_size", "gemm_f16_status_string",
@@ -53,7 +54,7 @@ class GemmF16Error(RuntimeError):
 
 class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
-        "swap_ab", "a_tma", "a_mn_major", "b_tma", "b_mn_major", "c_tma",
+        "swap_ab", "pair", "a_tma", "a_mn_major", "b_tma", "b_mn_major", "c_tma",
         "tile_m", "tile_n", "tiles_m", "tiles_n", "splits", "kblocks", "units", "grid",
         "stages", "smem_bytes")] + [("workspace_bytes", ctypes.c_size_t)]
 

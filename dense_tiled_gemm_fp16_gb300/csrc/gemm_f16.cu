@@ -31,6 +31,8 @@ struct DevInfo {
     int sms = 0;
     int* status_ptr = nullptr;
     bool smem_attr_set = false;
+    int pair_smem = -1;       // cached max_pair_clusters() result for this smem size
+    int pair_clusters = 0;
 };
 
 std::mutex g_mutex;
@@ -47,7 +49,7 @@ struct Workspace {
 };
 Workspace g_ws[kMaxDevices];
 
-std::atomic<int64_t> g_opt[8];
+std::atomic<int64_t> g_opt[9];
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 PFN_cuMemGetAddressRange_v3020 g_addr_range = nullptr;
@@ -222,6 +224,52 @@ struct Plan {
     size_t partial_bytes;   // split-K partials: align256(4 * units * tile_m * tile_n)
 };
 
+bool set_smem_attributes(DevInfo& dev)
+{
+    std::lock_guard<std::mutex> lk(g_mutex);
+    if (dev.smem_attr_set) return true;
+    if (cudaFuncSetAttribute(gemm_f16_dev::gemm_f16_persistent<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kMaxDynSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_f16_dev::gemm_f16_persistent<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kMaxDynSmem) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    dev.smem_attr_set = true;
+    return true;
+}
+
+// How many 2-CTA clusters of the pair kernel can be resident at once (SMs are
+// paired within a GPC, so this can be less than half the SM count).
+int max_pair_clusters(DevInfo& dev, int smem)
+{
+    if (!set_smem_attributes(dev)) return 0;
+    {
+        std::lock_guard<std::mutex> lk(g_mutex);
+        if (dev.pair_smem == smem) return dev.pair_clusters;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (dev.sms / 2));
+    cfg.blockDim = dim3(gemm_f16_dev::kNumThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_f16_dev::gemm_f16_persistent<true>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    std::lock_guard<std::mutex> lk(g_mutex);
+    dev.pair_smem = smem;
+    dev.pair_clusters = n;
+    return n;
+}
+
 // Split-K count: only when the output tiles cannot occupy every SM.  Picks the
 // count whose units spread most evenly over the SMs, with a small penalty per
 // split for the extra partial-sum traffic, and at least 4 K blocks per split.
@@ -288,9 +336,6 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     int BN, tiles_m, tiles_n, kblocks, splits;
     shape_plan(a.M, a.N, a.K, dev.sms, &swap, &Mv, &Nv, &BN, &tiles_m, &tiles_n, &kblocks, &splits);
     if (BN < 16 || BN > 256 || BN % 16 != 0) return GEMM_F16_ERR_INVALID_VALUE;
-    const int64_t tiles = static_cast<int64_t>(tiles_m) * tiles_n;
-    const int64_t units = tiles * splits;
-    if (units > INT32_MAX / 2) return GEMM_F16_ERR_INVALID_VALUE;
 
     // Kernel view: C'[m,n] = sum_k A'[m,k] B'[k,n].
     if (!swap) {
@@ -309,24 +354,43 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     const bool have_tma = g_encode != nullptr;
     OperandChoice ca = choose_operand(kp.A, kp.a_sm, kp.a_sk, Mv, a.K, gemm_f16_dev::kBM, have_tma && !(fg & 1));
     OperandChoice cb = choose_operand(kp.B, kp.b_sn, kp.b_sk, Nv, a.K, BN, have_tma && !(fg & 2));
+
+    // Pair form (two CTAs per 256 x BN tile): TMA operands, no split-K, and a
+    // B half that is a whole number of 64-column swizzle atoms.
+    const int64_t pair_opt = opt(GEMM_F16_OPT_PAIR);
+    const bool pair = pair_opt == 2 && !swap && splits == 1 && ca.tma && cb.tma && (BN == 128 || BN == 256) &&
+                      Mv > gemm_f16_dev::kBM;
+    const int tile_rows = pair ? 2 * gemm_f16_dev::kBM : gemm_f16_dev::kBM;
+    const int bcols = pair ? BN / 2 : BN;   // B columns one CTA loads
+    if (pair) tiles_m = static_cast<int>((Mv + tile_rows - 1) / tile_rows);
+    const int64_t tiles = static_cast<int64_t>(tiles_m) * tiles_n;
+    const int64_t units = tiles * splits;
+    if (units > INT32_MAX / 2) return GEMM_F16_ERR_INVALID_VALUE;
+
     if (ca.tma) {
         const bool ok = ca.mn ? encode_2d(&kp.tmA, kp.A, Mv, a.K, a.K == 1 ? round_up(2 * Mv, 16) : 2 * kp.a_sk, 64, 64)
                               : encode_2d(&kp.tmA, kp.A, a.K, Mv, Mv == 1 ? round_up(2 * a.K, 16) : 2 * kp.a_sm, 64,
                                           gemm_f16_dev::kBM);
-        if (!ok) ca = choose_operand(kp.A, kp.a_sm, kp.a_sk, Mv, a.K, gemm_f16_dev::kBM, false);
+        if (!ok) {
+            if (pair) return GEMM_F16_ERR_LAUNCH;
+            ca = choose_operand(kp.A, kp.a_sm, kp.a_sk, Mv, a.K, gemm_f16_dev::kBM, false);
+        }
     }
     if (cb.tma) {
         const bool ok = cb.mn ? encode_2d(&kp.tmB, kp.B, Nv, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk, 64, 64)
                               : encode_2d(&kp.tmB, kp.B, a.K, Nv, Nv == 1 ? round_up(2 * a.K, 16) : 2 * kp.b_sn, 64,
-                                          static_cast<uint32_t>(BN));
-        if (!ok) cb = choose_operand(kp.B, kp.b_sn, kp.b_sk, Nv, a.K, BN, false);
+                                          static_cast<uint32_t>(bcols));
+        if (!ok) {
+            if (pair) return GEMM_F16_ERR_LAUNCH;
+            cb = choose_operand(kp.B, kp.b_sn, kp.b_sk, Nv, a.K, BN, false);
+        }
     }
     bool c_tma = have_tma && !(fg & 4) && !swap && splits == 1 && BN % 64 == 0 &&
                  (reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc * 2) % 16 == 0 && a.M < (int64_t(1) << 32) &&
                  a.N < (int64_t(1) << 32) && (a.ldc * 2) < (int64_t(1) << 40);
     if (c_tma) c_tma = encode_2d(&kp.tmC, a.C, a.N, a.M, 2 * a.ldc, 64, 32);
 
-    const uint32_t stage_b = static_cast<uint32_t>(BN) * gemm_f16_dev::kBK * 2;
+    const uint32_t stage_b = static_cast<uint32_t>(bcols) * gemm_f16_dev::kBK * 2;
     const uint32_t stage_bytes = gemm_f16_dev::kStageABytes + stage_b;
     const int epi = c_tma ? static_cast<int>(gemm_f16_dev::kEpiBytes) : 0;
     int stages = (kMaxDynSmem - kSmemAlignSlack - epi - static_cast<int>(gemm_f16_dev::kBarrierBytes)) /
@@ -336,9 +400,17 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     const int smem = kSmemAlignSlack + stages * static_cast<int>(stage_bytes) + epi +
                      static_cast<int>(gemm_f16_dev::kBarrierBytes);
 
-    int grid = static_cast<int>(std::min<int64_t>(units, dev.sms));
+    int grid;
     const int64_t cap = opt(GEMM_F16_OPT_MAX_CTAS);
-    if (cap > 0) grid = static_cast<int>(std::min<int64_t>(grid, cap));
+    if (pair) {
+        int64_t clusters = std::min<int64_t>(units, max_pair_clusters(const_cast<DevInfo&>(dev), smem));
+        if (cap > 0) clusters = std::min<int64_t>(clusters, std::max<int64_t>(1, cap / 2));
+        if (clusters < 1) return GEMM_F16_ERR_LAUNCH;
+        grid = static_cast<int>(2 * clusters);
+    } else {
+        grid = static_cast<int>(std::min<int64_t>(units, dev.sms));
+        if (cap > 0) grid = static_cast<int>(std::min<int64_t>(grid, cap));
+    }
     const int64_t panel = opt(GEMM_F16_OPT_PANEL);
 
     kp.status = dev.status_ptr;
@@ -353,16 +425,22 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     kp.c_tma = c_tma ? 1u : 0u;
     // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16
     // (bits 7-9, 10-12 = 0), A/B MN-major flags (bits 15, 16), N >> 3 (bits
-    // 17-22), M >> 4 (bits 24-28).
+    // 17-22), M >> 4 (bits 24-28); M is 256 for the pair form.
     kp.idesc = (1u << 4) | ((ca.mn ? 1u : 0u) << 15) | ((cb.mn ? 1u : 0u) << 16) |
-               ((static_cast<uint32_t>(BN) >> 3) << 17) | ((static_cast<uint32_t>(gemm_f16_dev::kBM) >> 4) << 24);
-    kp.tx_bytes = (ca.tma ? gemm_f16_dev::kStageABytes : 0u) + (cb.tma ? stage_b : 0u);
+               ((static_cast<uint32_t>(BN) >> 3) << 17) | ((static_cast<uint32_t>(tile_rows) >> 4) << 24);
     kp.stage_b_bytes = stage_b;
-    kp.full_count = ((ca.tma || cb.tma) ? 1u : 0u) + ((!ca.tma || !cb.tma) ? 128u : 0u);
+    if (pair) {
+        kp.tx_bytes = 2u * stage_bytes;   // both CTAs' boxes complete on the leader's barrier
+        kp.full_count = 1u;
+    } else {
+        kp.tx_bytes = (ca.tma ? gemm_f16_dev::kStageABytes : 0u) + (cb.tma ? stage_b : 0u);
+        kp.full_count = ((ca.tma || cb.tma) ? 1u : 0u) + ((!ca.tma || !cb.tma) ? 128u : 0u);
+    }
 
     pub.swap_ab = swap;
+    pub.pair = pair;
     pub.a_tma = ca.tma, pub.a_mn_major = ca.mn, pub.b_tma = cb.tma, pub.b_mn_major = cb.mn, pub.c_tma = c_tma;
-    pub.tile_m = gemm_f16_dev::kBM, pub.tile_n = BN, pub.tiles_m = tiles_m, pub.tiles_n = tiles_n;
+    pub.tile_m = tile_rows, pub.tile_n = BN, pub.tiles_m = tiles_m, pub.tiles_n = tiles_n;
     pub.splits = splits, pub.kblocks = kblocks, pub.units = static_cast<int>(units), pub.grid = grid;
     pub.stages = stages, pub.smem_bytes = smem;
     pub.workspace_bytes =
@@ -375,18 +453,28 @@ gemm_f16_status launch(Plan& pl, DevInfo& dev, float* partials, int* counters, c
     KernelParams& kp = pl.kp;
     kp.ws = partials;
     kp.counters = counters;
-    {
-        std::lock_guard<std::mutex> lk(g_mutex);
-        if (!dev.smem_attr_set) {
-            if (cudaFuncSetAttribute(gemm_f16_dev::gemm_f16_persistent, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kMaxDynSmem) != cudaSuccess) {
-                cudaGetLastError();
-                return GEMM_F16_ERR_LAUNCH;
-            }
-            dev.smem_attr_set = true;
+    if (!set_smem_attributes(dev)) return GEMM_F16_ERR_LAUNCH;
+    if (!pl.pub.pair) {
+        gemm_f16_dev::gemm_f16_persistent<false>
+            <<<pl.pub.grid, gemm_f16_dev::kNumThreads, pl.pub.smem_bytes, stream>>>(kp);
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(pl.pub.grid);
+        cfg.blockDim = dim3(gemm_f16_dev::kNumThreads);
+        cfg.dynamicSmemBytes = pl.pub.smem_bytes;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, gemm_f16_dev::gemm_f16_persistent<true>, kp) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_F16_ERR_LAUNCH;
         }
     }
-    gemm_f16_dev::gemm_f16_persistent<<<pl.pub.grid, gemm_f16_dev::kNumThreads, pl.pub.smem_bytes, stream>>>(kp);
     if (cudaGetLastError() != cudaSuccess) return GEMM_F16_ERR_LAUNCH;
     return GEMM_F16_OK;
 }
@@ -555,7 +643,8 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
 
 gemm_f16_status gemm_f16_set_option(int option, int64_t value)
 {
-    if (option < 1 || option > 7 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option < 1 || option > 8 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option == GEMM_F16_OPT_PAIR && value > 2) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_FORCE_GATHER && value > 7) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_TILE_N && value != 0 && (value % 64 != 0 || value > 256))
         return GEMM_F16_ERR_INVALID_VALUE;

@@ -1,9 +1,20 @@
 // Persistent, warp-specialised fp16 GEMM for sm_103a: C = A * B with fp16
 // operands, fp32 accumulation in tensor memory (TMEM) and fp16 output.
 //
-// One CTA per SM walks a list of work units.  A unit is one 128 x BN output
-// tile, or, in split-K mode, one K-segment of such a tile.  Roles:
+// One CTA per SM walks a list of work units.  A unit is one output tile, or,
+// in split-K mode, one K-segment of a tile.  Two forms share this source:
 //
+//   single (kPair = false)  a 128 x BN tile per CTA, cta_group::1 MMAs.  Any
+//                           operand layout (TMA or gather), split-K.
+//   pair   (kPair = true)   clusters of two CTAs; a 256 x BN tile per pair,
+//                           one cta_group::2 MMA stream issued by the leader
+//                           (rank 0).  Each CTA loads its own 128 rows of A
+//                           and its own BN/2 columns of B (no multicast), so a
+//                           CTA moves 2/3 of the single form's operand bytes
+//                           per MMA cycle and fits deeper pipelines.  TMA
+//                           operands only, no split-K.
+//
+// Roles (9 warps):
 //   warps 0-3  producers.  Operands that TMA can address are loaded by one
 //              thread with cp.async.bulk.tensor into 128-byte-swizzled shared
 //              memory (out-of-range box elements arrive as zeros).  Operands
@@ -12,7 +23,7 @@
 //              loads, written in the same swizzled layout and published to the
 //              tensor core with fence.proxy.async.  Either way the K tail is
 //              zero-filled: an index past K is never wrapped back into range.
-//   warp 4-7   epilogue.  tcgen05.ld of the fp32 accumulator (warp w reads
+//   warps 4-7  epilogue.  tcgen05.ld of the fp32 accumulator (warp w reads
 //              TMEM lanes 32*(w%4)..+31), convert to fp16, then either stage
 //              through swizzled shared memory and TMA-store (clipped to M x N)
 //              or store with per-element bounds checks.  In split-K mode the
@@ -42,7 +53,7 @@
 
 namespace gemm_f16_dev {
 
-constexpr int kBM = 128;                 // tile rows = UMMA M
+constexpr int kBM = 128;                 // rows per CTA = UMMA M of the single form
 constexpr int kBK = 64;                  // K per stage: one 128-byte swizzle row of fp16
 constexpr int kMaxStages = 16;
 constexpr int kNumThreads = 288;         // 9 warps
@@ -92,7 +103,7 @@ __device__ __forceinline__ SmemLayout smem_layout(const KernelParams& p, uint32_
 }
 
 // Barrier block: full[16], empty[16], tmem_full[2], tmem_empty[2], drain,
-// then the TMEM base address, the abort flag and a broadcast word.
+// then the TMEM base address, the abort flag and broadcast words.
 __device__ __forceinline__ uint32_t bar_full(uint32_t bars, int s) { return bars + 8u * s; }
 __device__ __forceinline__ uint32_t bar_empty(uint32_t bars, int s) { return bars + 8u * (kMaxStages + s); }
 __device__ __forceinline__ uint32_t bar_tfull(uint32_t bars, int a) { return bars + 8u * (2 * kMaxStages + a); }
@@ -136,33 +147,65 @@ __device__ __forceinline__ void raise_abort(const KernelParams& p, volatile int*
     if (p.status) atomicExch(p.status, kStatusTimeout);
 }
 
+template <bool kPair>
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const volatile int* abort, uint64_t tmo)
+{
+    return kPair ? mbar_wait_cluster(bar, parity, abort, tmo) : mbar_wait(bar, parity, abort, tmo);
+}
+
+// Bytes [sh, sh+16) of the 32-byte little-endian value w1:w0 (sh even, 2..14).
+__device__ __forceinline__ uint4 funnel16(const uint4& w0, const uint4& w1, uint32_t sh)
+{
+    const uint32_t s = (sh & 3u) * 8u;
+    uint32_t x0, x1, x2, x3, x4;
+    switch (sh >> 2) {
+    case 0: x0 = w0.x, x1 = w0.y, x2 = w0.z, x3 = w0.w, x4 = w1.x; break;
+    case 1: x0 = w0.y, x1 = w0.z, x2 = w0.w, x3 = w1.x, x4 = w1.y; break;
+    case 2: x0 = w0.z, x1 = w0.w, x2 = w1.x, x3 = w1.y, x4 = w1.z; break;
+    default: x0 = w0.w, x1 = w1.x, x2 = w1.y, x3 = w1.z, x4 = w1.w; break;
+    }
+    return make_uint4(__funnelshift_r(x0, x1, s), __funnelshift_r(x1, x2, s), __funnelshift_r(x2, x3, s),
+                      __funnelshift_r(x3, x4, s));
+}
+
+// Keep the first `nvalid` (< 8) fp16 values of a 16-byte chunk, zero the rest.
+__device__ __forceinline__ uint4 keep_first(uint4 r, int nvalid)
+{
+    const uint32_t nb = 2u * static_cast<uint32_t>(nvalid);
+    auto k = [nb](uint32_t w, uint32_t i) -> uint32_t {
+        return (4u * i + 4u <= nb) ? w : ((4u * i >= nb) ? 0u : (w & 0xFFFFu));
+    };
+    return make_uint4(k(r.x, 0), k(r.y, 1), k(r.z, 2), k(r.w, 3));
+}
+
 // Eight consecutive elements along `step`, starting at element offset `off`;
-// the first `nvalid` are loaded, the rest are zero.  Nothing outside the
-// caller's bounds is read.
+// the first `nvalid` (>= 1 unless 0) are in the caller's view, the rest are
+// returned as zero.  With a unit step the chunk is assembled from the aligned
+// 16-byte word holding its first element, plus the next word only when a valid
+// element lies in it; bytes of those words outside the view are discarded.
+// A 16-byte word that holds a valid element cannot leave that element's page,
+// so no access can fault.  Other steps load element by element.
 __device__ __forceinline__ uint4 load8(const __half* base, int64_t off, int64_t step, int nvalid)
 {
-    uint4 r = make_uint4(0u, 0u, 0u, 0u);
-    if (nvalid <= 0) return r;
+    if (nvalid <= 0) return make_uint4(0u, 0u, 0u, 0u);
     const uint16_t* q = reinterpret_cast<const uint16_t*>(base) + off;
-    if (step == 1 && nvalid >= 8) {
+    if (step == 1) {
         const uintptr_t a = reinterpret_cast<uintptr_t>(q);
-        if ((a & 15u) == 0) return ld_nc_v4(q);
-        if ((a & 3u) == 0) {
-            r.x = ld_nc_u32(q);
-            r.y = ld_nc_u32(q + 2);
-            r.z = ld_nc_u32(q + 4);
-            r.w = ld_nc_u32(q + 6);
-            return r;
+        const uint32_t sh = static_cast<uint32_t>(a & 15u);
+        const uint4 w0 = ld_nc_v4(reinterpret_cast<const void*>(a - sh));
+        uint4 r = w0;
+        if (sh != 0) {
+            uint4 w1 = make_uint4(0u, 0u, 0u, 0u);
+            if (sh + 2u * static_cast<uint32_t>(nvalid) > 16u)
+                w1 = ld_nc_v4(reinterpret_cast<const void*>(a - sh + 16));
+            r = funnel16(w0, w1, sh);
         }
+        return nvalid < 8 ? keep_first(r, nvalid) : r;
     }
     uint32_t v[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) v[e] = (e < nvalid) ? static_cast<uint32_t>(ld_nc_u16(q + e * step)) : 0u;
-    r.x = v[0] | (v[1] << 16);
-    r.y = v[2] | (v[3] << 16);
-    r.z = v[4] | (v[5] << 16);
-    r.w = v[6] | (v[7] << 16);
-    return r;
+    return make_uint4(v[0] | (v[1] << 16), v[2] | (v[3] << 16), v[4] | (v[5] << 16), v[6] | (v[7] << 16));
 }
 
 __device__ __forceinline__ int clamp8(int64_t remaining)
@@ -207,8 +250,7 @@ __device__ __forceinline__ void gather_tile(const __half* base, int64_t s_mn, in
                     step = s_mn;
                     addr[i] = dst + a * 8192 + r * 128 + ((j ^ (r & 7)) << 4);
                 }
-                v[i] = (nvalid > 0) ? load8(base, mn * s_mn + k * s_k, step, nvalid)
-                                    : make_uint4(0u, 0u, 0u, 0u);
+                v[i] = load8(base, nvalid > 0 ? mn * s_mn + k * s_k : 0, step, nvalid);
             }
         }
 #pragma unroll
@@ -222,45 +264,43 @@ __device__ __forceinline__ uint16_t half_bits(const uint32_t* h, int c)
     return static_cast<uint16_t>(h[c >> 1] >> ((c & 1) * 16));
 }
 
-// Store `cols` (<= 64) fp16 values of output row m, columns n.., with bounds
-// checks on both m and every column.
-__device__ __forceinline__ void store_row_masked(const KernelParams& p, int64_t m, int64_t n, int cols,
-                                                 const uint32_t* h)
+// Store 16 fp16 values (h[8]) of output row m, columns n..n+15, with bounds
+// checks on m and on every column.
+__device__ __forceinline__ void store_piece_masked(const KernelParams& p, int64_t m, int64_t n, const uint32_t* h)
 {
-    if (m >= p.M) return;
+    if (m >= p.M || n >= p.N) return;
     uint16_t* row = reinterpret_cast<uint16_t*>(p.C) + m * p.c_sm;
     if (p.c_sn == 1) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (8 * j < cols) {
-                const int64_t nn = n + 8 * j;
-                uint16_t* q = row + nn;
-                if (nn + 8 <= p.N && (reinterpret_cast<uintptr_t>(q) & 15u) == 0) {
-                    *reinterpret_cast<uint4*>(q) =
-                        make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
-                } else {
+        for (int j = 0; j < 2; ++j) {
+            const int64_t nn = n + 8 * j;
+            uint16_t* q = row + nn;
+            if (nn + 8 <= p.N && (reinterpret_cast<uintptr_t>(q) & 15u) == 0) {
+                *reinterpret_cast<uint4*>(q) = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+            } else {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        if (nn + e < p.N) q[e] = half_bits(h, 8 * j + e);
-                }
+                for (int e = 0; e < 8; ++e)
+                    if (nn + e < p.N) q[e] = half_bits(h, 8 * j + e);
             }
         }
     } else {
+        uint16_t* q = row + n * p.c_sn;
+        const int64_t lim = p.N - n;
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-            if (c < cols && n + c < p.N) row[(n + c) * p.c_sn] = half_bits(h, c);
+        for (int c = 0; c < 16; ++c) {
+            if (c < lim) *q = half_bits(h, c);
+            q += p.c_sn;
+        }
     }
 }
 
-// Load up to 64 accumulator columns [col0, col0+cols) of this thread's lane.
-__device__ __forceinline__ void tmem_load_group(uint32_t taddr, int cols, uint32_t* r)
+__device__ __forceinline__ void convert16(const uint32_t* r, uint32_t* h)
 {
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        if (16 * i < cols) tmem_ld_x16(taddr + 16 * i, r + 16 * i);
-    tmem_wait_ld();
+    for (int i = 0; i < 8; ++i) h[i] = pack_half2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
 }
 
+template <bool kPair>
 __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __grid_constant__ KernelParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -277,6 +317,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
     const int lane = threadIdx.x & 31;
     const bool a_tma = p.a_flags & kOpTma, b_tma = p.b_flags & kOpTma;
     const bool a_mn = p.a_flags & kOpMnMajor, b_mn = p.b_flags & kOpMnMajor;
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+    const bool leader = (rank == 0);
+    const int cid = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int ncl = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    constexpr int kTileRows = kPair ? 2 * kBM : kBM;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
@@ -285,7 +330,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar_tfull(L.bars, a), 1);
-            mbar_init(bar_tempty(L.bars, a), 4);
+            mbar_init(bar_tempty(L.bars, a), kPair ? 8 : 4);
         }
         mbar_init(bar_drain(L.bars), 1);
         *abort = 0;
@@ -296,11 +341,19 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
         if (p.c_tma) tma_prefetch_desc(&p.tmC);
     }
     if (warp == kMmaWarp) {
-        tmem_alloc(L.bars + kTmemSlotOff, kTmemCols);
-        tmem_relinquish();
+        if (kPair) {
+            tmem_alloc_pair(L.bars + kTmemSlotOff, kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(L.bars + kTmemSlotOff, kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    if (kPair)
+        cluster_sync_all();   // the peer's barriers are initialised before any remote arrival
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -313,12 +366,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
             uint32_t phase = 0;
             bool ok = true;
             int issued = 0;
-            for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+            const int bcols = kPair ? p.BN / 2 : p.BN;   // this CTA's share of the B tile
+            for (int u = cid; u < p.num_units && ok; u += ncl) {
                 const Unit w = unit_of(p, u);
-                const int64_t m0 = static_cast<int64_t>(w.m_blk) * kBM;
-                const int64_t n0 = static_cast<int64_t>(w.n_blk) * p.BN;
+                const int64_t m0 = static_cast<int64_t>(w.m_blk) * kTileRows + rank * kBM;
+                const int64_t n0 = static_cast<int64_t>(w.n_blk) * p.BN + rank * bcols;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!mbar_wait(bar_empty(L.bars, stage), phase ^ 1u, abort, p.timeout_ns)) {
+                    if (!wait_bar<kPair>(bar_empty(L.bars, stage), phase ^ 1u, abort, p.timeout_ns)) {
                         raise_abort(p, abort);
                         ok = false;
                         break;
@@ -328,25 +382,44 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                     const uint32_t fb = bar_full(L.bars, stage);
                     const int32_t k0 = kb * kBK;
                     if (t == 0 && (a_tma || b_tma)) {
-                        mbar_arrive_expect_tx(fb, p.tx_bytes);
-                        if (a_tma) {
+                        if (kPair) {
+                            // The leader expects both CTAs' bytes on its own barrier;
+                            // the peer's copies complete on the leader's barrier.
+                            if (leader) mbar_arrive_expect_tx(fb, p.tx_bytes);
+                            const uint32_t fbc = mapa_shared(fb, 0);
                             if (!a_mn) {
-                                tma_load_2d(sa, &p.tmA, k0, static_cast<int32_t>(m0), fb);
+                                tma_load_2d_pair(sa, &p.tmA, k0, static_cast<int32_t>(m0), fbc);
                             } else {
-                                tma_load_2d(sa, &p.tmA, static_cast<int32_t>(m0), k0, fb);
-                                tma_load_2d(sa + 8192, &p.tmA, static_cast<int32_t>(m0 + 64), k0, fb);
+                                tma_load_2d_pair(sa, &p.tmA, static_cast<int32_t>(m0), k0, fbc);
+                                tma_load_2d_pair(sa + 8192, &p.tmA, static_cast<int32_t>(m0 + 64), k0, fbc);
                             }
-                        }
-                        if (b_tma) {
                             if (!b_mn) {
-                                tma_load_2d(sb, &p.tmB, k0, static_cast<int32_t>(n0), fb);
+                                tma_load_2d_pair(sb, &p.tmB, k0, static_cast<int32_t>(n0), fbc);
                             } else {
-                                for (int j = 0; j < p.BN / 64; ++j)
-                                    tma_load_2d(sb + j * 8192, &p.tmB, static_cast<int32_t>(n0 + 64 * j), k0, fb);
+                                for (int j = 0; j < bcols / 64; ++j)
+                                    tma_load_2d_pair(sb + j * 8192, &p.tmB, static_cast<int32_t>(n0 + 64 * j), k0, fbc);
+                            }
+                        } else {
+                            mbar_arrive_expect_tx(fb, p.tx_bytes);
+                            if (a_tma) {
+                                if (!a_mn) {
+                                    tma_load_2d(sa, &p.tmA, k0, static_cast<int32_t>(m0), fb);
+                                } else {
+                                    tma_load_2d(sa, &p.tmA, static_cast<int32_t>(m0), k0, fb);
+                                    tma_load_2d(sa + 8192, &p.tmA, static_cast<int32_t>(m0 + 64), k0, fb);
+                                }
+                            }
+                            if (b_tma) {
+                                if (!b_mn) {
+                                    tma_load_2d(sb, &p.tmB, k0, static_cast<int32_t>(n0), fb);
+                                } else {
+                                    for (int j = 0; j < bcols / 64; ++j)
+                                        tma_load_2d(sb + j * 8192, &p.tmB, static_cast<int32_t>(n0 + 64 * j), k0, fb);
+                                }
                             }
                         }
                     }
-                    if (any_masked) {
+                    if (!kPair && any_masked) {
                         if (!a_tma)
                             gather_tile(p.A, p.a_sm, p.a_sk, p.M, p.K, m0, k0, kBM, a_mn, sa, t);
                         if (!b_tma)
@@ -361,7 +434,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                     }
                 }
             }
-            if (!ok && t == 0 && (a_tma || b_tma)) {
+            if (!ok && t == 0 && (a_tma || b_tma) && (!kPair || leader)) {
                 // Let TMA copies already in flight land before the CTA exits:
                 // wait (bounded) on the full barrier of each recently issued stage.
                 const int n = issued < p.stages ? issued : p.stages;
@@ -370,22 +443,23 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                         stage = p.stages - 1;
                         phase ^= 1u;
                     }
-                    mbar_wait(bar_full(L.bars, stage), phase, nullptr, kDrainTimeoutNs);
+                    wait_bar<kPair>(bar_full(L.bars, stage), phase, nullptr, kDrainTimeoutNs);
                 }
             }
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
             bool any = false;
-            for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+            const uint32_t b_atom_rows = 8192;   // MN-major: one 64-wide atom column over 64 K rows
+            for (int u = cid; u < p.num_units && ok; u += ncl) {
                 const Unit w = unit_of(p, u);
-                if (!mbar_wait(bar_tempty(L.bars, acc), acc_phase ^ 1u, abort, p.timeout_ns)) {
+                if (!wait_bar<kPair>(bar_tempty(L.bars, acc), acc_phase ^ 1u, abort, p.timeout_ns)) {
                     raise_abort(p, abort);
                     ok = false;
                     break;
@@ -393,7 +467,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                 tc_fence_after();
                 const uint32_t d = tmem_base + acc * kAccStride;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!mbar_wait(bar_full(L.bars, stage), phase, abort, p.timeout_ns)) {
+                    if (!wait_bar<kPair>(bar_full(L.bars, stage), phase, abort, p.timeout_ns)) {
                         raise_abort(p, abort);
                         ok = false;
                         break;
@@ -407,19 +481,29 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                         // swizzle row.  MN-major: it is 16 K rows of 128 bytes.
                         const uint64_t ad = a_mn ? umma_desc_sw128(sa + k * 2048, 8192, 1024)
                                                  : umma_desc_sw128(sa + k * 32, 16, 1024);
-                        const uint64_t bd = b_mn ? umma_desc_sw128(sb + k * 2048, 8192, 1024)
+                        const uint64_t bd = b_mn ? umma_desc_sw128(sb + k * 2048, b_atom_rows, 1024)
                                                  : umma_desc_sw128(sb + k * 32, 16, 1024);
-                        umma_f16(d, ad, bd, p.idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
+                        const uint32_t accum = (kb > w.kb0 || k > 0) ? 1u : 0u;
+                        if (kPair)
+                            umma_f16_pair(d, ad, bd, p.idesc, accum);
+                        else
+                            umma_f16(d, ad, bd, p.idesc, accum);
                     }
                     any = true;
-                    umma_commit(bar_empty(L.bars, stage));
+                    if (kPair)
+                        umma_commit_pair_mc(bar_empty(L.bars, stage), 0x3);
+                    else
+                        umma_commit(bar_empty(L.bars, stage));
                     if (++stage == p.stages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                umma_commit(bar_tfull(L.bars, acc));
+                if (kPair)
+                    umma_commit_pair_mc(bar_tfull(L.bars, acc), 0x3);
+                else
+                    umma_commit(bar_tfull(L.bars, acc));
                 if (++acc == 2) {
                     acc = 0;
                     acc_phase ^= 1u;
@@ -428,28 +512,31 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
             if (!ok && any) {
                 // Drain: wait (bounded) until every MMA issued so far has completed
                 // before the accumulator memory is released.
-                umma_commit(bar_drain(L.bars));
-                mbar_wait(bar_drain(L.bars), 0, nullptr, kDrainTimeoutNs);
+                if (kPair)
+                    umma_commit_pair_mc(bar_drain(L.bars), 0x1);
+                else
+                    umma_commit(bar_drain(L.bars));
+                wait_bar<kPair>(bar_drain(L.bars), 0, nullptr, kDrainTimeoutNs);
             }
         }
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                 // TMEM lane quarter
-        const int row = 32 * q + lane;          // row inside the tile
+        const int row = 32 * q + lane;          // row inside this CTA's 128 rows
         const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t group_count = 0;
-        const int ngroups = (p.BN + 63) / 64;
-        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+        const int npieces = p.BN / 16;          // 16 accumulator columns per piece
+        for (int u = cid; u < p.num_units; u += ncl) {
             const Unit w = unit_of(p, u);
-            const int64_t m0 = static_cast<int64_t>(w.m_blk) * kBM;
+            const int64_t m0 = static_cast<int64_t>(w.m_blk) * kTileRows + rank * kBM;
             const int64_t n0 = static_cast<int64_t>(w.n_blk) * p.BN;
             // One thread waits for the accumulator and tells the other epilogue
             // threads, so that they all leave together on an abort (the named
             // barriers below must see all 128 threads).
             if (threadIdx.x == kEpiWarp0 * 32) {
-                const bool ok = mbar_wait(bar_tfull(L.bars, acc), acc_phase, abort, p.timeout_ns);
+                const bool ok = wait_bar<kPair>(bar_tfull(L.bars, acc), acc_phase, abort, p.timeout_ns);
                 if (!ok) raise_abort(p, abort);
                 okflag[acc] = ok ? 1 : 0;
             }
@@ -457,84 +544,106 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
             if (!okflag[acc]) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + lane_off + acc * kAccStride;
+            const uint32_t tempty = kPair ? mapa_shared(bar_tempty(L.bars, acc), 0) : bar_tempty(L.bars, acc);
             if (p.splits == 1) {
-                for (int g = 0; g < ngroups; ++g) {
-                    const int cols = min(64, p.BN - 64 * g);
-                    uint32_t r[64];
-                    tmem_load_group(taddr + 64 * g, cols, r);
-                    if (g == ngroups - 1) {
+                uint32_t buf = 0;
+                for (int pc = 0; pc < npieces; pc += 2) {
+                    // two pieces (32 columns) in flight per TMEM wait
+                    const bool two = pc + 1 < npieces;
+                    uint32_t r[32];
+                    tmem_ld_x16(taddr + 16 * pc, r);
+                    if (two) tmem_ld_x16(taddr + 16 * pc + 16, r + 16);
+                    tmem_wait_ld();
+                    if (pc + 2 >= npieces) {
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(bar_tempty(L.bars, acc));
-                    }
-                    uint32_t h[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        h[i] = pack_half2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-                    if (p.c_tma) {
-                        const uint32_t buf = L.epi + (q * 2 + (group_count & 1u)) * kEpiBufBytes;
-                        if (lane == 0) bulk_wait_group_read<1>();
-                        __syncwarp();
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            st_smem_v4(buf + lane * 128 + ((j ^ (lane & 7)) << 4),
-                                       make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]));
-                        fence_proxy_async_smem();
-                        __syncwarp();
                         if (lane == 0) {
-                            tma_store_2d(&p.tmC, buf, static_cast<int32_t>(n0 + 64 * g),
-                                         static_cast<int32_t>(m0 + 32 * q));
-                            bulk_commit_group();
+                            if (kPair)
+                                mbar_arrive_cluster(tempty);
+                            else
+                                mbar_arrive(tempty);
                         }
-                        ++group_count;
-                    } else {
-                        store_row_masked(p, m0 + row, n0 + 64 * g, cols, h);
+                    }
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        if (h2 == 1 && !two) break;
+                        const int piece = pc + h2;
+                        uint32_t h[8];
+                        convert16(r + 16 * h2, h);
+                        if (p.c_tma) {
+                            const int j0 = (piece & 3) * 2;        // 16-byte chunk inside the 128-byte row
+                            if ((piece & 3) == 0) {
+                                buf = L.epi + (q * 2 + (group_count & 1u)) * kEpiBufBytes;
+                                if (lane == 0) bulk_wait_group_read<1>();
+                                __syncwarp();
+                            }
+                            st_smem_v4(buf + lane * 128 + ((j0 ^ (lane & 7)) << 4), make_uint4(h[0], h[1], h[2], h[3]));
+                            st_smem_v4(buf + lane * 128 + (((j0 + 1) ^ (lane & 7)) << 4),
+                                       make_uint4(h[4], h[5], h[6], h[7]));
+                            if ((piece & 3) == 3 || piece == npieces - 1) {
+                                fence_proxy_async_smem();
+                                __syncwarp();
+                                if (lane == 0) {
+                                    tma_store_2d(&p.tmC, buf, static_cast<int32_t>(n0 + 16 * (piece & ~3)),
+                                                 static_cast<int32_t>(m0 + 32 * q));
+                                    bulk_commit_group();
+                                }
+                                ++group_count;
+                            }
+                        } else {
+                            store_piece_masked(p, m0 + row, n0 + 16 * piece, h);
+                        }
                     }
                 }
             } else {
                 // Split-K: write this segment's fp32 partial, column-major inside
                 // the unit slot so that a warp's 32 rows form one 128-byte line.
                 float* slot = p.ws + static_cast<size_t>(u) * (kBM * p.BN);
-                for (int g = 0; g < ngroups; ++g) {
-                    const int cols = min(64, p.BN - 64 * g);
-                    uint32_t r[64];
-                    tmem_load_group(taddr + 64 * g, cols, r);
-                    if (g == ngroups - 1) {
+                for (int pc = 0; pc < npieces; ++pc) {
+                    uint32_t r[16];
+                    tmem_ld_x16(taddr + 16 * pc, r);
+                    tmem_wait_ld();
+                    if (pc == npieces - 1) {
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(bar_tempty(L.bars, acc));
+                        if (lane == 0) {
+                            if (kPair)
+                                mbar_arrive_cluster(tempty);
+                            else
+                                mbar_arrive(tempty);
+                        }
                     }
 #pragma unroll
-                    for (int c = 0; c < 64; ++c)
-                        if (c < cols) slot[(64 * g + c) * kBM + row] = __uint_as_float(r[c]);
+                    for (int c = 0; c < 16; ++c) slot[(16 * pc + c) * kBM + row] = __uint_as_float(r[c]);
                 }
-                __threadfence();
+                // Publish the partial and count this segment in: the epilogue
+                // threads' stores are ordered before the leader's release by the
+                // barrier; its acquire makes the other segments' partials visible
+                // (to all epilogue threads through the second barrier).  One
+                // device-scope atomic per unit, no per-thread fences.
                 named_bar_sync(1, 128);
                 if (threadIdx.x == kEpiWarp0 * 32) {
-                    const int old = atomicAdd(p.counters + w.tile, 1);
+                    const int old = atom_add_acq_rel_gpu(p.counters + w.tile, 1);
                     const int last = (old == p.splits - 1) ? 1 : 0;
-                    if (last) p.counters[w.tile] = 0;   // ready for the next call
+                    if (last) st_relaxed_gpu(p.counters + w.tile, 0);   // ready for the next call
                     *flag = last;
                 }
                 named_bar_sync(1, 128);
                 if (*flag) {
-                    __threadfence();
                     const float* tb = p.ws + static_cast<size_t>(w.tile) * p.splits * (kBM * p.BN);
-                    for (int g = 0; g < ngroups; ++g) {
-                        const int cols = min(64, p.BN - 64 * g);
-                        float s[64];
+                    for (int pc = 0; pc < npieces; ++pc) {
+                        float s[16];
 #pragma unroll
-                        for (int c = 0; c < 64; ++c) s[c] = 0.f;
+                        for (int c = 0; c < 16; ++c) s[c] = 0.f;
                         for (int sp = 0; sp < p.splits; ++sp) {
-                            const float* src = tb + static_cast<size_t>(sp) * (kBM * p.BN) + (64 * g) * kBM + row;
+                            const float* src = tb + static_cast<size_t>(sp) * (kBM * p.BN) + (16 * pc) * kBM + row;
 #pragma unroll
-                            for (int c = 0; c < 64; ++c)
-                                if (c < cols) s[c] += ld_cg_f32(src + c * kBM);
+                            for (int c = 0; c < 16; ++c) s[c] += ld_cg_f32(src + c * kBM);
                         }
-                        uint32_t h[32];
+                        uint32_t h[8];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) h[i] = pack_half2(s[2 * i], s[2 * i + 1]);
-                        store_row_masked(p, m0 + row, n0 + 64 * g, cols, h);
+                        for (int i = 0; i < 8; ++i) h[i] = pack_half2(s[2 * i], s[2 * i + 1]);
+                        store_piece_masked(p, m0 + row, n0 + 16 * pc, h);
                     }
                 }
             }
@@ -547,9 +656,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
     }
 
     tc_fence_before();
-    __syncthreads();
+    if (kPair)
+        cluster_sync_all();   // the leader's MMAs into this CTA's TMEM and smem are done
+    else
+        __syncthreads();
     tc_fence_after();
-    if (warp == kMmaWarp) tmem_dealloc(tmem_base, kTmemCols);
+    if (warp == kMmaWarp) {
+        if (kPair)
+            tmem_dealloc_pair(tmem_base, kTmemCols);
+        else
+            tmem_dealloc(tmem_base, kTmemCols);
+    }
 }
 
 }  // namespace gemm_f16_dev

@@ -128,6 +128,7 @@ gemm_f16_status gemm_f16_device_status(int* status, int reset);
 /* How a call would be executed, for tests and profiling. */
 typedef struct {
     int swap_ab;        /* computed as C^T = B^T A^T (small M) */
+    int pair;           /* 2-CTA clusters sharing one 256-row tile (cta_group::2) */
     int a_tma, a_mn_major, b_tma, b_mn_major, c_tma;   /* kernel-view operands */
     int tile_m, tile_n, tiles_m, tiles_n;
     int splits, kblocks, units, grid, stages;
@@ -151,6 +152,7 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
  *   GEMM_F16_OPT_SWAP          0 auto, 1 never swap, 2 always swap
  *   GEMM_F16_OPT_TIMEOUT_MS    bounded-wait limit in ms (default 1000)
  *   GEMM_F16_OPT_MAX_CTAS      > 0: cap the persistent grid
+ *   GEMM_F16_OPT_PAIR          0 default, 1 never, 2 use 2-CTA pair tiles where eligible
  * A value of 0 restores the default.  Returns GEMM_F16_ERR_INVALID_VALUE for an
  * unknown option or a value out of range.
  */
@@ -161,7 +163,8 @@ enum {
     GEMM_F16_OPT_PANEL = 4,
     GEMM_F16_OPT_SWAP = 5,
     GEMM_F16_OPT_TIMEOUT_MS = 6,
-    GEMM_F16_OPT_MAX_CTAS = 7
+    GEMM_F16_OPT_MAX_CTAS = 7,
+    GEMM_F16_OPT_PAIR = 8
 };
 gemm_f16_status gemm_f16_set_option(int option, int64_t value);
 

@@ -25,7 +25,7 @@ DEV = torch.device("cuda:0")
 def _defaults():
     yield
     for o in (g.OPT_FORCE_GATHER, g.OPT_SPLITS, g.OPT_TILE_N, g.OPT_PANEL, g.OPT_SWAP,
-              g.OPT_TIMEOUT_MS, g.OPT_MAX_CTAS):
+              g.OPT_TIMEOUT_MS, g.OPT_MAX_CTAS, g.OPT_PAIR):
         g.gemm_f16_set_option(o, 0)
 
 
@@ -162,6 +162,59 @@ def test_mn_major_a_and_k_major_b_through_tma():
     plan = g.plan_for(A, B, out)
     assert plan["a_tma"] and plan["a_mn_major"] and plan["b_tma"] and not plan["b_mn_major"]
     assert_close(host(gpu(A, B)), oracle.gemm(Ah, Bh), 256, "mn-major A, k-major B")
+
+
+# ------------------------------------------------------------ pair tiles
+PAIR_CASES = [
+    # (M, N, K, layout A, layout B, tile_n, integer inputs)
+    (512, 512, 256, "row", "row", 256, True),
+    (1000, 520, 300, "pitch16", "pitch16", 256, True),
+    (777, 384, 200, "col", "col", 128, True),       # M-major A, K-major B
+    (300, 1000, 130, "row", "col", 256, False),
+    (2048, 1024, 1024, "row", "row", 256, False),
+]
+
+
+@pytest.mark.parametrize("case", PAIR_CASES, ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}-{c[3]}-{c[4]}-bn{c[5]}")
+def test_pair_tiles_match_oracle(case):
+    M, N, K, la, lb, bn, integer = case
+    rng = np.random.default_rng(M + N + K)
+    if integer:
+        Ah = rng.integers(-3, 4, (M, K)).astype(np.float16)
+        Bh = rng.integers(-3, 4, (K, N)).astype(np.float16)
+    else:
+        Ah = rng.uniform(-1, 1, (M, K)).astype(np.float16)
+        Bh = rng.uniform(-1, 1, (K, N)).astype(np.float16)
+    A, B = make_view(Ah, la), make_view(Bh, lb)
+    out = torch.empty((M, N), dtype=torch.float16, device=DEV)
+    g.gemm_f16_set_option(g.OPT_TILE_N, bn)
+    single = host(gpu(A, B))
+    g.gemm_f16_set_option(g.OPT_PAIR, 2)
+    plan = g.plan_for(A, B, out)
+    assert plan["pair"] == 1 and plan["tile_m"] == 256 and plan["grid"] % 2 == 0, plan
+    paired = host(gpu(A, B, out=out))
+    ref = oracle.gemm(Ah, Bh, threads=oracle_threads())
+    if integer and K * 9 <= 2048:
+        assert_bits(paired, ref, f"pair {case}")
+    else:
+        assert_close(paired, ref, K, f"pair {case}")
+    assert_close(single, ref, K, f"single {case}")
+    assert g.gemm_f16_device_status() == 0
+
+
+def test_pair_tiles_many_units_per_cluster():
+    # one cluster walks every tile: exercises the TMEM double buffer and the
+    # stage ring across tiles in the pair form
+    g.gemm_f16_set_option(g.OPT_PAIR, 2)
+    g.gemm_f16_set_option(g.OPT_MAX_CTAS, 2)
+    rng = np.random.default_rng(5)
+    Ah = rng.integers(-3, 4, (1100, 192)).astype(np.float16)
+    Bh = rng.integers(-3, 4, (192, 1300)).astype(np.float16)
+    A, B = to_dev(Ah), to_dev(Bh)
+    out = torch.empty((1100, 1300), dtype=torch.float16, device=DEV)
+    plan = g.plan_for(A, B, out)
+    assert plan["pair"] == 1 and plan["grid"] == 2 and plan["units"] > 10
+    assert_bits(host(gpu(A, B, out=out)), oracle.gemm(Ah, Bh, threads=oracle_threads()), "pair, one cluster")
 
 
 # ------------------------------------------------------- boundary behaviour
