@@ -358,8 +358,8 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     // Pair form (two CTAs per 256 x BN tile): TMA operands, no split-K, and a
     // B half that is a whole number of 64-column swizzle atoms.
     const int64_t pair_opt = opt(GEMM_F16_OPT_PAIR);
-    const bool pair = pair_opt == 2 && !swap && splits == 1 && ca.tma && cb.tma && (BN == 128 || BN == 256) &&
-                      Mv > gemm_f16_dev::kBM;
+    const bool pair = pair_opt != 1 && !swap && splits == 1 && ca.tma && cb.tma &&
+                      (BN == 256 || (pair_opt == 2 && BN == 128)) && Mv > gemm_f16_dev::kBM;
     const int tile_rows = pair ? 2 * gemm_f16_dev::kBM : gemm_f16_dev::kBM;
     const int bcols = pair ? BN / 2 : BN;   // B columns one CTA loads
     if (pair) tiles_m = static_cast<int>((Mv + tile_rows - 1) / tile_rows);

@@ -178,30 +178,11 @@ __device__ __forceinline__ uint4 keep_first(uint4 r, int nvalid)
     return make_uint4(k(r.x, 0), k(r.y, 1), k(r.z, 2), k(r.w, 3));
 }
 
-// Eight consecutive elements along `step`, starting at element offset `off`;
-// the first `nvalid` (>= 1 unless 0) are in the caller's view, the rest are
-// returned as zero.  With a unit step the chunk is assembled from the aligned
-// 16-byte word holding its first element, plus the next word only when a valid
-// element lies in it; bytes of those words outside the view are discarded.
-// A 16-byte word that holds a valid element cannot leave that element's page,
-// so no access can fault.  Other steps load element by element.
-__device__ __forceinline__ uint4 load8(const __half* base, int64_t off, int64_t step, int nvalid)
+// Eight elements along a non-unit `step` from element offset `off`; the first
+// `nvalid` are loaded one by one, the rest are zero.
+__device__ __forceinline__ uint4 load8_strided(const __half* base, int64_t off, int64_t step, int nvalid)
 {
-    if (nvalid <= 0) return make_uint4(0u, 0u, 0u, 0u);
     const uint16_t* q = reinterpret_cast<const uint16_t*>(base) + off;
-    if (step == 1) {
-        const uintptr_t a = reinterpret_cast<uintptr_t>(q);
-        const uint32_t sh = static_cast<uint32_t>(a & 15u);
-        const uint4 w0 = ld_nc_v4(reinterpret_cast<const void*>(a - sh));
-        uint4 r = w0;
-        if (sh != 0) {
-            uint4 w1 = make_uint4(0u, 0u, 0u, 0u);
-            if (sh + 2u * static_cast<uint32_t>(nvalid) > 16u)
-                w1 = ld_nc_v4(reinterpret_cast<const void*>(a - sh + 16));
-            r = funnel16(w0, w1, sh);
-        }
-        return nvalid < 8 ? keep_first(r, nvalid) : r;
-    }
     uint32_t v[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) v[e] = (e < nvalid) ? static_cast<uint32_t>(ld_nc_u16(q + e * step)) : 0u;
@@ -217,6 +198,16 @@ __device__ __forceinline__ int clamp8(int64_t remaining)
 // 128B-swizzled layout the UMMA descriptor expects.  K-major: row r (128 B) at
 // r*128, its 16-byte chunk j at ((j ^ (r & 7)) << 4).  MN-major: atom column a
 // (64 MN elements) at a*8192, K row r at r*128, chunk j swizzled the same way.
+//
+// A chunk is 8 consecutive elements of the operand's contiguous dimension; the
+// first `nvalid` lie inside the view (row < extent, k < K), the rest are
+// zero-filled.  With a unit stride the chunk is assembled from the aligned
+// 16-byte word holding its first element plus, only when a valid element lies
+// in it, the next word; bytes of those words outside the view are discarded.
+// A 16-byte-aligned word that holds a valid element cannot cross that
+// element's page, so no load can fault.  Chunks are handled four at a time:
+// first every load is issued, then the words are shifted into place and
+// stored, so a thread keeps up to 8 loads in flight (more spills registers).
 __device__ __forceinline__ void gather_tile(const __half* base, int64_t s_mn, int64_t s_k,
                                             int64_t MN, int64_t K, int64_t mn0, int64_t k0,
                                             int rows_tile, bool mn_major, uint32_t dst, int t)
@@ -224,38 +215,59 @@ __device__ __forceinline__ void gather_tile(const __half* base, int64_t s_mn, in
     const int chunks = rows_tile * 8;   // 16-byte chunks in the tile
     const int iters = chunks / 128;
     const int atoms = rows_tile / 64;
-    for (int i0 = 0; i0 < iters; i0 += 8) {
-        uint4 v[8];
-        uint32_t addr[8];
+    const int64_t step = mn_major ? s_mn : s_k;
+    const uintptr_t b = reinterpret_cast<uintptr_t>(base);
+    for (int i0 = 0; i0 < iters; i0 += 4) {
+        uint4 w0[4], w1[4];
+        uint32_t addr[4], sh[4];
+        int nv[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < 4; ++i) {
+            nv[i] = 0;
             if (i0 + i < iters) {
                 const int c = t + 128 * (i0 + i);
                 const int j = c & 7;
-                int64_t mn, k, step;
-                int nvalid;
+                int64_t mn, k;
                 if (!mn_major) {
                     const int r = c >> 3;
                     mn = mn0 + r;
                     k = k0 + 8 * j;
-                    nvalid = (mn < MN) ? clamp8(K - k) : 0;
-                    step = s_k;
+                    nv[i] = (mn < MN) ? clamp8(K - k) : 0;
                     addr[i] = dst + r * 128 + ((j ^ (r & 7)) << 4);
                 } else {
                     const int a = (c >> 3) % atoms;
                     const int r = (c >> 3) / atoms;
                     mn = mn0 + 64 * a + 8 * j;
                     k = k0 + r;
-                    nvalid = (k < K) ? clamp8(MN - mn) : 0;
-                    step = s_mn;
+                    nv[i] = (k < K) ? clamp8(MN - mn) : 0;
                     addr[i] = dst + a * 8192 + r * 128 + ((j ^ (r & 7)) << 4);
                 }
-                v[i] = load8(base, nvalid > 0 ? mn * s_mn + k * s_k : 0, step, nvalid);
+                sh[i] = 0;
+                w0[i] = make_uint4(0u, 0u, 0u, 0u);
+                w1[i] = w0[i];
+                if (nv[i] > 0) {
+                    const int64_t off = mn * s_mn + k * s_k;
+                    if (step == 1) {
+                        const uintptr_t a = b + 2 * static_cast<uintptr_t>(off);
+                        sh[i] = static_cast<uint32_t>(a & 15u);
+                        const uintptr_t a0 = a - sh[i];
+                        const bool two = sh[i] != 0 && sh[i] + 2u * static_cast<uint32_t>(nv[i]) > 16u;
+                        w0[i] = ld_nc_v4(reinterpret_cast<const void*>(a0));
+                        w1[i] = ld_nc_v4(reinterpret_cast<const void*>(two ? a0 + 16 : a0));
+                    } else {
+                        w0[i] = load8_strided(base, off, step, nv[i]);
+                    }
+                }
             }
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if (i0 + i < iters) st_smem_v4(addr[i], v[i]);
+        for (int i = 0; i < 4; ++i) {
+            if (i0 + i < iters) {
+                uint4 r = (sh[i] != 0) ? funnel16(w0[i], w1[i], sh[i]) : w0[i];
+                if (nv[i] < 8) r = keep_first(r, nv[i]);
+                st_smem_v4(addr[i], r);
+            }
+        }
     }
 }
 
@@ -635,7 +647,21 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                         float s[16];
 #pragma unroll
                         for (int c = 0; c < 16; ++c) s[c] = 0.f;
-                        for (int sp = 0; sp < p.splits; ++sp) {
+                        // Segments are summed in order 0, 1, 2, ...; the loads of two
+                        // segments are issued before their adds.
+                        int sp = 0;
+                        for (; sp + 1 < p.splits; sp += 2) {
+                            const float* src = tb + static_cast<size_t>(sp) * (kBM * p.BN) + (16 * pc) * kBM + row;
+                            float x0[16], x1[16];
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) {
+                                x0[c] = ld_cg_f32(src + c * kBM);
+                                x1[c] = ld_cg_f32(src + kBM * p.BN + c * kBM);
+                            }
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) s[c] = (s[c] + x0[c]) + x1[c];
+                        }
+                        if (sp < p.splits) {
                             const float* src = tb + static_cast<size_t>(sp) * (kBM * p.BN) + (16 * pc) * kBM + row;
 #pragma unroll
                             for (int c = 0; c < 16; ++c) s[c] += ld_cg_f32(src + c * kBM);

@@ -343,26 +343,26 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo
 }
 
 // ----------------------------------------------------------- global memory
+// Read-only loads of the caller's operands.  Not volatile: the operands do not
+// change while a kernel runs, so the compiler may batch and schedule them.
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p)
 {
     uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
+    asm("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
     return v;
 }
 
 __device__ __forceinline__ uint32_t ld_nc_u32(const void* p)
 {
     uint32_t v;
-    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    asm("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
     return v;
 }
 
 __device__ __forceinline__ uint16_t ld_nc_u16(const void* p)
 {
     uint16_t v;
-    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    asm("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
     return v;
 }
 

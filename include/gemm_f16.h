@@ -152,7 +152,8 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
  *   GEMM_F16_OPT_SWAP          0 auto, 1 never swap, 2 always swap
  *   GEMM_F16_OPT_TIMEOUT_MS    bounded-wait limit in ms (default 1000)
  *   GEMM_F16_OPT_MAX_CTAS      > 0: cap the persistent grid
- *   GEMM_F16_OPT_PAIR          0 default, 1 never, 2 use 2-CTA pair tiles where eligible
+ *   GEMM_F16_OPT_PAIR          0 default (2-CTA pair tiles for 256-wide tiles of TMA
+ *                              operands without split-K), 1 never, 2 also for 128-wide tiles
  * A value of 0 restores the default.  Returns GEMM_F16_ERR_INVALID_VALUE for an
  * unknown option or a value out of range.
  */

