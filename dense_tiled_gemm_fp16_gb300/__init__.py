@@ -39,6 +39,7 @@ OPT_SWAP = 5
 OPT_TIMEOUT_MS = 6
 OPT_MAX_CTAS = 7
 OPT_PAIR = 8
+OPT_STREAMK = 9
 
 # Every symbol include/gemm_f16.h declares.
 EXPORTED = ("gemm_f16", "gemm_f16_ws", "gemm_f16_workspace_size", "gemm_f16_status_string",
@@ -56,7 +57,7 @@ class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "swap_ab", "pair", "a_tma", "a_mn_major", "b_tma", "b_mn_major", "c_tma",
         "tile_m", "tile_n", "tiles_m", "tiles_n", "splits", "kblocks", "units", "grid",
-        "stages", "smem_bytes")] + [("workspace_bytes", ctypes.c_size_t)]
+        "stages", "streamk_tiles", "smem_bytes")] + [("workspace_bytes", ctypes.c_size_t)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

@@ -49,7 +49,7 @@ struct Workspace {
 };
 Workspace g_ws[kMaxDevices];
 
-std::atomic<int64_t> g_opt[9];
+std::atomic<int64_t> g_opt[10];
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 PFN_cuMemGetAddressRange_v3020 g_addr_range = nullptr;
@@ -270,28 +270,61 @@ int max_pair_clusters(DevInfo& dev, int smem)
     return n;
 }
 
-// Split-K count: only when the output tiles cannot occupy every SM.  Picks the
-// count whose units spread most evenly over the SMs, with a small penalty per
-// split for the extra partial-sum traffic, and at least 4 K blocks per split.
-int choose_splits(int64_t tiles, int kblocks, int sms)
+// Classic split-K (every tile cut into `splits` equal K segments) runs only
+// when forced through GEMM_F16_OPT_SPLITS; otherwise the schedule below uses
+// stream-K to fill the device.
+int choose_splits(int kblocks)
 {
     const int64_t forced = opt(GEMM_F16_OPT_SPLITS);
-    if (forced > 0) return static_cast<int>(std::min<int64_t>(forced, kblocks));
-    if (tiles >= sms || kblocks < 8) return 1;
-    int best = 1;
-    double best_score = -1.0;
-    const int max_s = std::min(32, kblocks / 4);
-    for (int s = 1; s <= max_s; ++s) {
-        const int64_t units = tiles * s;
-        const int64_t waves = (units + sms - 1) / sms;
-        const double eff = static_cast<double>(units) / static_cast<double>(waves * sms);
-        const double score = eff - 0.002 * s;
-        if (score > best_score + 1e-12) {
-            best_score = score;
-            best = s;
-        }
+    return forced > 0 ? static_cast<int>(std::min<int64_t>(forced, kblocks)) : 1;
+}
+
+// How the tiles are spread over the persistent workers (CTAs, or 2-CTA
+// clusters in the pair form).  With W workers and T tiles of KB K blocks:
+//  - classic split-K (forced): T*splits equal units, round-robin;
+//  - T a multiple of W, or too little work to cut: whole tiles, round-robin;
+//  - otherwise data-parallel waves of whole tiles for all but the last
+//    1 + (T mod W)/W waves, whose K blocks are spread evenly over all W workers
+//    (stream-K; TileLang tutorial ch. 14, section 4.2), so every worker gets
+//    the same number of K blocks.  Tiles cut by a worker boundary are summed by
+//    the last of their workers to finish, in K order.
+struct Schedule {
+    int workers = 1, num_units = 0, sk_tile0 = 0, nseg_max = 0, sk_slot_base = 0;
+    int64_t sk_iters = 0;
+    int64_t partial_slots = 0;   // fp32 tile partials the workspace must hold (per CTA rank)
+};
+
+Schedule make_schedule(int64_t tiles, int kblocks, int splits, int max_workers)
+{
+    Schedule s;
+    if (splits > 1) {
+        s.num_units = static_cast<int>(tiles * splits);
+        s.workers = static_cast<int>(std::min<int64_t>(s.num_units, max_workers));
+        s.partial_slots = s.num_units;
+        return s;
     }
-    return best;
+    s.num_units = static_cast<int>(tiles);
+    s.workers = static_cast<int>(std::min<int64_t>(tiles, max_workers));
+    const int64_t W = max_workers;
+    if (opt(GEMM_F16_OPT_STREAMK) == 1 || tiles % W == 0) return s;
+    const int64_t full = tiles / W;
+    const int64_t sk_tiles = full >= 1 ? tiles % W + W : tiles;
+    const int64_t S = sk_tiles * kblocks;
+    // When the tiles alone cannot fill the device: at least 8 K blocks per
+    // worker, at most 16 workers per tile (the last one adds their partials),
+    // and more workers than tiles.
+    const int64_t w = full >= 1 ? W : std::min<int64_t>(std::min<int64_t>(W, S / 8), sk_tiles * 16);
+    if (w <= sk_tiles && full == 0) return s;
+    if (S < 4 * w) return s;
+    s.workers = static_cast<int>(w);
+    s.num_units = static_cast<int>(tiles - sk_tiles);
+    s.sk_tile0 = s.num_units;
+    s.sk_iters = S;
+    const int64_t max_range = (S + w - 1) / w;
+    s.nseg_max = static_cast<int>(max_range / kblocks + 2);
+    s.sk_slot_base = 0;
+    s.partial_slots = w * s.nseg_max;
+    return s;
 }
 
 void shape_plan(int64_t M, int64_t N, int64_t K, int sms, bool* swap, int64_t* Mv, int64_t* Nv, int* BN,
@@ -313,14 +346,17 @@ void shape_plan(int64_t M, int64_t N, int64_t K, int sms, bool* swap, int64_t* M
     *tiles_m = static_cast<int>((*Mv + gemm_f16_dev::kBM - 1) / gemm_f16_dev::kBM);
     *tiles_n = static_cast<int>((*Nv + bn - 1) / bn);
     *kblocks = static_cast<int>((K + gemm_f16_dev::kBK - 1) / gemm_f16_dev::kBK);
-    *splits = choose_splits(static_cast<int64_t>(*tiles_m) * *tiles_n, *kblocks, sms);
+    (void)sms;
+    *splits = choose_splits(*kblocks);
 }
 
-// Caller-workspace layout: [counters, align256(4*tiles)] [partials].
-size_t workspace_bytes_for(int64_t units, int BN, int64_t tiles, size_t* counter_bytes, size_t* partial_bytes)
+// Caller-workspace layout: [counters, align256(4*tiles*ranks)] [partials].
+// `ranks` is 2 for the pair form (each CTA of a pair keeps its own 128 rows).
+size_t workspace_bytes_for(int64_t slots, int BN, int64_t tiles, int ranks, size_t* counter_bytes,
+                           size_t* partial_bytes)
 {
-    const size_t cb = static_cast<size_t>(round_up(tiles * 4, 256));
-    const size_t pb = static_cast<size_t>(round_up(units * gemm_f16_dev::kBM * BN * 4, 256));
+    const size_t cb = static_cast<size_t>(round_up(tiles * ranks * 4, 256));
+    const size_t pb = static_cast<size_t>(round_up(slots * ranks * gemm_f16_dev::kBM * BN * 4, 256));
     if (counter_bytes) *counter_bytes = cb;
     if (partial_bytes) *partial_bytes = pb;
     return cb + pb;
@@ -364,8 +400,7 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     const int bcols = pair ? BN / 2 : BN;   // B columns one CTA loads
     if (pair) tiles_m = static_cast<int>((Mv + tile_rows - 1) / tile_rows);
     const int64_t tiles = static_cast<int64_t>(tiles_m) * tiles_n;
-    const int64_t units = tiles * splits;
-    if (units > INT32_MAX / 2) return GEMM_F16_ERR_INVALID_VALUE;
+    if (tiles * splits > INT32_MAX / 4 || tiles * kblocks > (int64_t(1) << 40)) return GEMM_F16_ERR_INVALID_VALUE;
 
     if (ca.tma) {
         const bool ok = ca.mn ? encode_2d(&kp.tmA, kp.A, Mv, a.K, a.K == 1 ? round_up(2 * Mv, 16) : 2 * kp.a_sk, 64, 64)
@@ -400,24 +435,25 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     const int smem = kSmemAlignSlack + stages * static_cast<int>(stage_bytes) + epi +
                      static_cast<int>(gemm_f16_dev::kBarrierBytes);
 
-    int grid;
+    // Persistent workers: CTAs, or 2-CTA clusters in the pair form.
     const int64_t cap = opt(GEMM_F16_OPT_MAX_CTAS);
-    if (pair) {
-        int64_t clusters = std::min<int64_t>(units, max_pair_clusters(const_cast<DevInfo&>(dev), smem));
-        if (cap > 0) clusters = std::min<int64_t>(clusters, std::max<int64_t>(1, cap / 2));
-        if (clusters < 1) return GEMM_F16_ERR_LAUNCH;
-        grid = static_cast<int>(2 * clusters);
-    } else {
-        grid = static_cast<int>(std::min<int64_t>(units, dev.sms));
-        if (cap > 0) grid = static_cast<int>(std::min<int64_t>(grid, cap));
-    }
+    int64_t max_workers = pair ? max_pair_clusters(const_cast<DevInfo&>(dev), smem) : dev.sms;
+    if (cap > 0) max_workers = std::min<int64_t>(max_workers, pair ? std::max<int64_t>(1, cap / 2) : cap);
+    if (max_workers < 1) return GEMM_F16_ERR_LAUNCH;
+    const Schedule sch = make_schedule(tiles, kblocks, splits, static_cast<int>(max_workers));
+    const int grid = pair ? 2 * sch.workers : sch.workers;
     const int64_t panel = opt(GEMM_F16_OPT_PANEL);
 
     kp.status = dev.status_ptr;
     const int64_t tmo = opt(GEMM_F16_OPT_TIMEOUT_MS);
     kp.timeout_ns = static_cast<uint64_t>(tmo > 0 ? tmo : 1000) * 1000000ull;
     kp.tiles_m = tiles_m, kp.tiles_n = tiles_n, kp.splits = splits, kp.kblocks = kblocks;
-    kp.num_units = static_cast<int>(units);
+    kp.num_units = sch.num_units;
+    kp.workers = sch.workers;
+    kp.sk_tile0 = sch.sk_tile0;
+    kp.sk_iters = sch.sk_iters;
+    kp.nseg_max = sch.nseg_max;
+    kp.sk_slot_base = sch.sk_slot_base;
     kp.panel = static_cast<int>(panel > 0 ? panel : 8);
     kp.BN = BN, kp.stages = stages;
     kp.a_flags = (ca.tma ? gemm_f16_dev::kOpTma : 0u) | (ca.mn ? gemm_f16_dev::kOpMnMajor : 0u);
@@ -441,10 +477,14 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     pub.pair = pair;
     pub.a_tma = ca.tma, pub.a_mn_major = ca.mn, pub.b_tma = cb.tma, pub.b_mn_major = cb.mn, pub.c_tma = c_tma;
     pub.tile_m = tile_rows, pub.tile_n = BN, pub.tiles_m = tiles_m, pub.tiles_n = tiles_n;
-    pub.splits = splits, pub.kblocks = kblocks, pub.units = static_cast<int>(units), pub.grid = grid;
+    pub.splits = splits, pub.kblocks = kblocks, pub.grid = grid;
+    pub.units = static_cast<int>(tiles * splits);
+    pub.streamk_tiles = sch.sk_iters > 0 ? static_cast<int>(tiles - sch.sk_tile0) : 0;
     pub.stages = stages, pub.smem_bytes = smem;
-    pub.workspace_bytes =
-        splits > 1 ? workspace_bytes_for(units, BN, tiles, &pl->counter_bytes, &pl->partial_bytes) : 0;
+    pub.workspace_bytes = sch.partial_slots > 0
+                              ? workspace_bytes_for(sch.partial_slots, BN, tiles, pair ? 2 : 1, &pl->counter_bytes,
+                                                    &pl->partial_bytes)
+                              : 0;
     return GEMM_F16_OK;
 }
 
@@ -515,7 +555,7 @@ gemm_f16_status run(const Args& a, void* user_ws, size_t user_ws_bytes, bool use
     if (st != GEMM_F16_OK) return st;
     float* partials = nullptr;
     int* counters = nullptr;
-    if (pl.pub.splits > 1) {
+    if (pl.pub.workspace_bytes > 0) {
         if (use_library_ws) {
             int d = 0;
             cudaGetDevice(&d);
@@ -574,8 +614,18 @@ gemm_f16_status gemm_f16_workspace_size(int64_t M, int64_t N, int64_t K, size_t*
     int64_t Mv, Nv;
     int BN, tiles_m, tiles_n, kblocks, splits;
     shape_plan(M, N, K, dev->sms, &swap, &Mv, &Nv, &BN, &tiles_m, &tiles_n, &kblocks, &splits);
-    const int64_t tiles = static_cast<int64_t>(tiles_m) * tiles_n;
-    *bytes = splits > 1 ? workspace_bytes_for(tiles * splits, BN, tiles, nullptr, nullptr) : 0;
+    // The plan also depends on the operands' layout (single or pair form), so
+    // report the larger of the two requirements.
+    size_t need = 0;
+    for (int pair = 0; pair < 2; ++pair) {
+        const int64_t rows = pair ? 2 * gemm_f16_dev::kBM : gemm_f16_dev::kBM;
+        const int64_t tiles = ((Mv + rows - 1) / rows) * tiles_n;
+        const int workers = pair ? std::max(1, dev->sms / 2) : dev->sms;
+        const Schedule s = make_schedule(tiles, kblocks, splits, workers);
+        if (s.partial_slots > 0)
+            need = std::max(need, workspace_bytes_for(s.partial_slots, BN, tiles, pair ? 2 : 1, nullptr, nullptr));
+    }
+    *bytes = need;
     return GEMM_F16_OK;
 }
 
@@ -643,7 +693,8 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
 
 gemm_f16_status gemm_f16_set_option(int option, int64_t value)
 {
-    if (option < 1 || option > 8 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option < 1 || option > 9 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option == GEMM_F16_OPT_STREAMK && value > 1) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_PAIR && value > 2) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_FORCE_GATHER && value > 7) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_TILE_N && value != 0 && (value % 64 != 0 || value > 256))

@@ -86,6 +86,16 @@ struct KernelParams {
     uint64_t timeout_ns;
     int tiles_m, tiles_n, splits, kblocks, num_units, panel, BN, stages;
     uint32_t a_flags, b_flags, c_tma, idesc, tx_bytes, stage_b_bytes, full_count;
+    // Work decomposition.  `workers` persistent CTAs (single form) or clusters
+    // (pair form).  Worker c first takes the whole-tile (or classic split-K)
+    // units c, c+workers, ... < num_units; then, if sk_iters > 0, the
+    // stream-K range [c*S/P, (c+1)*S/P) of the S = sk_iters K blocks of tiles
+    // sk_tile0 .. tiles-1, cut at tile boundaries into segments.
+    int workers;
+    int sk_tile0;
+    int64_t sk_iters;
+    int nseg_max;       // most segments one worker's stream-K range can hold
+    int sk_slot_base;   // first partial slot of the stream-K segments
 };
 
 struct SmemLayout {
@@ -115,30 +125,103 @@ constexpr uint32_t kFlagOff = kTmemSlotOff + 8;
 constexpr uint32_t kOkOff = kTmemSlotOff + 12;   // two words, indexed by accumulator
 constexpr uint64_t kDrainTimeoutNs = 10000000ull;
 
+// One unit of a worker's list: K blocks [kb0, kb1) of one output tile.  A unit
+// that covers the whole K range is stored directly (slot < 0).  Otherwise it
+// leaves an fp32 partial in workspace slot `slot`; `expected` units cover the
+// tile, and the last of them to finish adds all partials in K order.
 struct Unit {
-    int tile, m_blk, n_blk, kb0, kb1;
+    int tile, m_blk, n_blk, kb0, kb1, slot, expected;
 };
 
-// Work unit -> (tile, K segment).  Units of one tile are consecutive so that
-// the split-K partials of a tile sit next to each other.  Tiles are numbered in
-// panels of `panel` tile-rows; inside a panel the row index moves fastest, so
-// CTAs running at the same time share B columns and a few A row-blocks in L2
-// (the grouped program ordering of the Triton page; the C500 review's panel
-// rasterisation, section 10).  The ordering is only a locality hint.
-__device__ __forceinline__ Unit unit_of(const KernelParams& p, int u)
+// Tile -> (row block, column block).  Tiles are numbered in panels of `panel`
+// tile-rows; inside a panel the row index moves fastest, so CTAs running at the
+// same time share B columns and a few A row-blocks in L2 (the grouped program
+// ordering of the Triton page; the C500 review's panel rasterisation, section
+// 10).  The ordering is only a locality hint.
+__device__ __forceinline__ void tile_coords(const KernelParams& p, int tile, int& m_blk, int& n_blk)
+{
+    const int per_panel = p.panel * p.tiles_n;
+    const int panel = tile / per_panel;
+    const int r = tile - panel * per_panel;
+    const int rows = min(p.panel, p.tiles_m - panel * p.panel);
+    m_blk = panel * p.panel + r % rows;
+    n_blk = r / rows;
+}
+
+// Stream-K (TileLang tutorial ch. 14, section 4.2: split the total K
+// iterations evenly over the processors, fix up only the tiles that got cut).
+// Worker c's range starts at K block c*S/P of the stream-K tiles.
+__device__ __forceinline__ int64_t sk_start(const KernelParams& p, int c)
+{
+    return static_cast<int64_t>(c) * p.sk_iters / p.workers;
+}
+
+// The worker whose range holds stream-K block x: the largest c with
+// sk_start(c) <= x, i.e. ceil((x+1)*P/S) - 1.
+__device__ __forceinline__ int sk_worker(const KernelParams& p, int64_t x)
+{
+    const int64_t c = ((x + 1) * p.workers + p.sk_iters - 1) / p.sk_iters - 1;
+    return static_cast<int>(c < p.workers - 1 ? c : p.workers - 1);
+}
+
+__device__ __forceinline__ int classic_units(const KernelParams& p, int cid)
+{
+    return cid < p.num_units ? (p.num_units - cid + p.workers - 1) / p.workers : 0;
+}
+
+__device__ __forceinline__ int units_of_worker(const KernelParams& p, int cid)
+{
+    int n = classic_units(p, cid);
+    if (p.sk_iters > 0) {
+        const int64_t s0 = sk_start(p, cid), s1 = sk_start(p, cid + 1);
+        if (s1 > s0) n += static_cast<int>((s1 - 1) / p.kblocks - s0 / p.kblocks + 1);
+    }
+    return n;
+}
+
+// The i-th unit of worker `cid`: whole tiles or classic split-K units first
+// (u = cid, cid + P, ...; the units of one split tile are consecutive), then
+// the worker's stream-K segments in K order.
+__device__ __forceinline__ Unit unit_at(const KernelParams& p, int cid, int i)
 {
     Unit w;
-    w.tile = u / p.splits;
-    const int split = u - w.tile * p.splits;
-    const int per_panel = p.panel * p.tiles_n;
-    const int panel = w.tile / per_panel;
-    const int r = w.tile - panel * per_panel;
-    const int rows = min(p.panel, p.tiles_m - panel * p.panel);
-    w.m_blk = panel * p.panel + r % rows;
-    w.n_blk = r / rows;
-    w.kb0 = static_cast<int>(static_cast<int64_t>(split) * p.kblocks / p.splits);
-    w.kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * p.kblocks / p.splits);
+    w.slot = -1;
+    w.expected = 1;
+    const int nc = classic_units(p, cid);
+    if (i < nc) {
+        const int u = cid + i * p.workers;
+        w.tile = u / p.splits;
+        const int split = u - w.tile * p.splits;
+        w.kb0 = static_cast<int>(static_cast<int64_t>(split) * p.kblocks / p.splits);
+        w.kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * p.kblocks / p.splits);
+        if (p.splits > 1) {
+            w.slot = u;
+            w.expected = p.splits;
+        }
+    } else {
+        const int j = i - nc;
+        const int64_t s0 = sk_start(p, cid), s1 = sk_start(p, cid + 1);
+        const int64_t t0 = s0 / p.kblocks + j;
+        w.kb0 = (j == 0) ? static_cast<int>(s0 % p.kblocks) : 0;
+        w.kb1 = (t0 == (s1 - 1) / p.kblocks) ? static_cast<int>((s1 - 1) % p.kblocks) + 1 : p.kblocks;
+        w.tile = p.sk_tile0 + static_cast<int>(t0);
+        if (w.kb0 != 0 || w.kb1 != p.kblocks) {
+            w.slot = p.sk_slot_base + cid * p.nseg_max + j;
+            w.expected = sk_worker(p, t0 * p.kblocks + p.kblocks - 1) - sk_worker(p, t0 * p.kblocks) + 1;
+        }
+    }
+    tile_coords(p, w.tile, w.m_blk, w.n_blk);
     return w;
+}
+
+// Partial slot of the idx-th (in K order) unit that covers a cut tile.
+__device__ __forceinline__ int tile_slot(const KernelParams& p, int tile, int idx)
+{
+    if (tile < p.sk_tile0 || p.sk_iters == 0) return tile * p.splits + idx;
+    const int64_t t0 = tile - p.sk_tile0;
+    const int c = sk_worker(p, t0 * p.kblocks) + idx;
+    const int j = static_cast<int>(t0 - sk_start(p, c) / p.kblocks);
+    return p.sk_slot_base + c * p.nseg_max + j;
 }
 
 __device__ __forceinline__ void raise_abort(const KernelParams& p, volatile int* abort)
@@ -332,7 +415,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
     const uint32_t rank = kPair ? cluster_ctarank() : 0u;
     const bool leader = (rank == 0);
     const int cid = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-    const int ncl = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
     constexpr int kTileRows = kPair ? 2 * kBM : kBM;
 
     if (threadIdx.x == 0) {
@@ -379,8 +461,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
             bool ok = true;
             int issued = 0;
             const int bcols = kPair ? p.BN / 2 : p.BN;   // this CTA's share of the B tile
-            for (int u = cid; u < p.num_units && ok; u += ncl) {
-                const Unit w = unit_of(p, u);
+            const int nu = units_of_worker(p, cid);
+            for (int i = 0; i < nu && ok; ++i) {
+                const Unit w = unit_at(p, cid, i);
                 const int64_t m0 = static_cast<int64_t>(w.m_blk) * kTileRows + rank * kBM;
                 const int64_t n0 = static_cast<int64_t>(w.n_blk) * p.BN + rank * bcols;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -469,8 +552,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
             bool ok = true;
             bool any = false;
             const uint32_t b_atom_rows = 8192;   // MN-major: one 64-wide atom column over 64 K rows
-            for (int u = cid; u < p.num_units && ok; u += ncl) {
-                const Unit w = unit_of(p, u);
+            const int nu = units_of_worker(p, cid);
+            for (int i = 0; i < nu && ok; ++i) {
+                const Unit w = unit_at(p, cid, i);
                 if (!wait_bar<kPair>(bar_tempty(L.bars, acc), acc_phase ^ 1u, abort, p.timeout_ns)) {
                     raise_abort(p, abort);
                     ok = false;
@@ -540,8 +624,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
         uint32_t acc_phase = 0;
         uint32_t group_count = 0;
         const int npieces = p.BN / 16;          // 16 accumulator columns per piece
-        for (int u = cid; u < p.num_units; u += ncl) {
-            const Unit w = unit_of(p, u);
+        const int nu = units_of_worker(p, cid);
+        constexpr int kRanks = kPair ? 2 : 1;
+        const size_t slot_elems = static_cast<size_t>(kBM) * p.BN;   // one CTA's 128 rows of a tile
+        for (int ui = 0; ui < nu; ++ui) {
+            const Unit w = unit_at(p, cid, ui);
             const int64_t m0 = static_cast<int64_t>(w.m_blk) * kTileRows + rank * kBM;
             const int64_t n0 = static_cast<int64_t>(w.n_blk) * p.BN;
             // One thread waits for the accumulator and tells the other epilogue
@@ -557,7 +644,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
             tc_fence_after();
             const uint32_t taddr = tmem_base + lane_off + acc * kAccStride;
             const uint32_t tempty = kPair ? mapa_shared(bar_tempty(L.bars, acc), 0) : bar_tempty(L.bars, acc);
-            if (p.splits == 1) {
+            if (w.slot < 0) {
                 uint32_t buf = 0;
                 for (int pc = 0; pc < npieces; pc += 2) {
                     // two pieces (32 columns) in flight per TMEM wait
@@ -608,9 +695,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                     }
                 }
             } else {
-                // Split-K: write this segment's fp32 partial, column-major inside
-                // the unit slot so that a warp's 32 rows form one 128-byte line.
-                float* slot = p.ws + static_cast<size_t>(u) * (kBM * p.BN);
+                // A cut tile: write this segment's fp32 partial, column-major
+                // inside the slot so that a warp's 32 rows form one 128-byte line.
+                float* slot = p.ws + (static_cast<size_t>(w.slot) * kRanks + rank) * slot_elems;
                 for (int pc = 0; pc < npieces; ++pc) {
                     uint32_t r[16];
                     tmem_ld_x16(taddr + 16 * pc, r);
@@ -634,37 +721,44 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                 // (to all epilogue threads through the second barrier).  One
                 // device-scope atomic per unit, no per-thread fences.
                 named_bar_sync(1, 128);
+                int* counter = p.counters + static_cast<size_t>(w.tile) * kRanks + rank;
                 if (threadIdx.x == kEpiWarp0 * 32) {
-                    const int old = atom_add_acq_rel_gpu(p.counters + w.tile, 1);
-                    const int last = (old == p.splits - 1) ? 1 : 0;
-                    if (last) st_relaxed_gpu(p.counters + w.tile, 0);   // ready for the next call
+                    const int old = atom_add_acq_rel_gpu(counter, 1);
+                    const int last = (old == w.expected - 1) ? 1 : 0;
+                    if (last) st_relaxed_gpu(counter, 0);   // ready for the next call
                     *flag = last;
                 }
                 named_bar_sync(1, 128);
                 if (*flag) {
-                    const float* tb = p.ws + static_cast<size_t>(w.tile) * p.splits * (kBM * p.BN);
                     for (int pc = 0; pc < npieces; ++pc) {
                         float s[16];
 #pragma unroll
                         for (int c = 0; c < 16; ++c) s[c] = 0.f;
-                        // Segments are summed in order 0, 1, 2, ...; the loads of two
-                        // segments are issued before their adds.
+                        // The tile's partials are added in K order (deterministic);
+                        // the loads of two partials are issued before their adds.
                         int sp = 0;
-                        for (; sp + 1 < p.splits; sp += 2) {
-                            const float* src = tb + static_cast<size_t>(sp) * (kBM * p.BN) + (16 * pc) * kBM + row;
+                        for (; sp + 1 < w.expected; sp += 2) {
+                            const float* s0 = p.ws +
+                                              (static_cast<size_t>(tile_slot(p, w.tile, sp)) * kRanks + rank) * slot_elems +
+                                              (16 * pc) * kBM + row;
+                            const float* s1 = p.ws +
+                                              (static_cast<size_t>(tile_slot(p, w.tile, sp + 1)) * kRanks + rank) * slot_elems +
+                                              (16 * pc) * kBM + row;
                             float x0[16], x1[16];
 #pragma unroll
                             for (int c = 0; c < 16; ++c) {
-                                x0[c] = ld_cg_f32(src + c * kBM);
-                                x1[c] = ld_cg_f32(src + kBM * p.BN + c * kBM);
+                                x0[c] = ld_cg_f32(s0 + c * kBM);
+                                x1[c] = ld_cg_f32(s1 + c * kBM);
                             }
 #pragma unroll
                             for (int c = 0; c < 16; ++c) s[c] = (s[c] + x0[c]) + x1[c];
                         }
-                        if (sp < p.splits) {
-                            const float* src = tb + static_cast<size_t>(sp) * (kBM * p.BN) + (16 * pc) * kBM + row;
+                        if (sp < w.expected) {
+                            const float* s0 = p.ws +
+                                              (static_cast<size_t>(tile_slot(p, w.tile, sp)) * kRanks + rank) * slot_elems +
+                                              (16 * pc) * kBM + row;
 #pragma unroll
-                            for (int c = 0; c < 16; ++c) s[c] += ld_cg_f32(src + c * kBM);
+                            for (int c = 0; c < 16; ++c) s[c] += ld_cg_f32(s0 + c * kBM);
                         }
                         uint32_t h[8];
 #pragma unroll

@@ -111,7 +111,8 @@ gemm_f16_status gemm_f16_ws(const void* A, int64_t stride_am, int64_t stride_ak,
                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Workspace bytes a call with these sizes needs on the current device (0 when
- * it does not use split-K).  Depends on M, N, K and the device's SM count. */
+ * no tile is cut along K).  An upper bound over operand layouts; depends on
+ * M, N, K, the options and the device's SM count. */
 gemm_f16_status gemm_f16_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
 
 /* Human-readable name of a status code; never NULL. */
@@ -132,6 +133,7 @@ typedef struct {
     int a_tma, a_mn_major, b_tma, b_mn_major, c_tma;   /* kernel-view operands */
     int tile_m, tile_n, tiles_m, tiles_n;
     int splits, kblocks, units, grid, stages;
+    int streamk_tiles;  /* trailing tiles whose K blocks are spread over all workers */
     int smem_bytes;
     size_t workspace_bytes;
 } gemm_f16_plan;
@@ -146,7 +148,8 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
 /*
  * Process-wide tuning and test knobs (not thread-safe with concurrent calls):
  *   GEMM_F16_OPT_FORCE_GATHER  bit 0: A, bit 1: B, bit 2: C never use TMA
- *   GEMM_F16_OPT_SPLITS        > 0: force this split-K count (clamped to the K blocks)
+ *   GEMM_F16_OPT_SPLITS        > 0: classic split-K, every tile cut into this many K
+ *                              segments (clamped to the K blocks); replaces stream-K
  *   GEMM_F16_OPT_TILE_N        > 0: force the tile width (multiple of 64, <= 256)
  *   GEMM_F16_OPT_PANEL         > 0: tile-rows per rasterisation panel (default 8)
  *   GEMM_F16_OPT_SWAP          0 auto, 1 never swap, 2 always swap
@@ -154,6 +157,8 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
  *   GEMM_F16_OPT_MAX_CTAS      > 0: cap the persistent grid
  *   GEMM_F16_OPT_PAIR          0 default (2-CTA pair tiles for 256-wide tiles of TMA
  *                              operands without split-K), 1 never, 2 also for 128-wide tiles
+ *   GEMM_F16_OPT_STREAMK       0 default (stream-K tail when the tiles do not divide
+ *                              evenly over the SMs), 1 whole tiles only
  * A value of 0 restores the default.  Returns GEMM_F16_ERR_INVALID_VALUE for an
  * unknown option or a value out of range.
  */
@@ -165,7 +170,8 @@ enum {
     GEMM_F16_OPT_SWAP = 5,
     GEMM_F16_OPT_TIMEOUT_MS = 6,
     GEMM_F16_OPT_MAX_CTAS = 7,
-    GEMM_F16_OPT_PAIR = 8
+    GEMM_F16_OPT_PAIR = 8,
+    GEMM_F16_OPT_STREAMK = 9
 };
 gemm_f16_status gemm_f16_set_option(int option, int64_t value);
 

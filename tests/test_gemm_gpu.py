@@ -25,7 +25,7 @@ DEV = torch.device("cuda:0")
 def _defaults():
     yield
     for o in (g.OPT_FORCE_GATHER, g.OPT_SPLITS, g.OPT_TILE_N, g.OPT_PANEL, g.OPT_SWAP,
-              g.OPT_TIMEOUT_MS, g.OPT_MAX_CTAS, g.OPT_PAIR):
+              g.OPT_TIMEOUT_MS, g.OPT_MAX_CTAS, g.OPT_PAIR, g.OPT_STREAMK):
         g.gemm_f16_set_option(o, 0)
 
 
@@ -275,7 +275,7 @@ def test_split_k_deterministic_and_workspace_paths():
     A, B = to_dev(Ah), to_dev(Bh)
     out = torch.empty((M, N), dtype=torch.float16, device=DEV)
     plan = g.plan_for(A, B, out)
-    assert plan["swap_ab"] and plan["splits"] > 1
+    assert plan["swap_ab"] and plan["streamk_tiles"] > 0 and plan["workspace_bytes"] > 0
     C1 = host(gpu(A, B))
     C2 = host(gpu(A, B))
     assert_bits(C1, C2, "split-K repeatability")
@@ -283,7 +283,7 @@ def test_split_k_deterministic_and_workspace_paths():
     assert_close(C1, ref, K, "split-K vs oracle")
     # caller-owned workspace gives the same bits
     nbytes = g.gemm_f16_workspace_size(M, N, K)
-    assert nbytes == plan["workspace_bytes"] > 0
+    assert nbytes >= plan["workspace_bytes"] > 0
     ws = torch.zeros(nbytes // 4 + 64, dtype=torch.int32, device=DEV)
     out2 = torch.empty_like(out)
     g.gemm_f16_ws(A.data_ptr(), K, 1, B.data_ptr(), N, 1, out2.data_ptr(), N, M, N, K,
@@ -295,9 +295,16 @@ def test_split_k_deterministic_and_workspace_paths():
         g.gemm_f16_ws(A.data_ptr(), K, 1, B.data_ptr(), N, 1, out2.data_ptr(), N, M, N, K,
                       ws.data_ptr(), nbytes - 256, 0)
     assert e.value.status == g.ERR_OUT_OF_MEMORY
-    # forcing no split changes the summation order only
-    g.gemm_f16_set_option(g.OPT_SPLITS, 1)
+    # whole tiles only, and classic split-K, change the summation order only
+    g.gemm_f16_set_option(g.OPT_STREAMK, 1)
+    assert g.plan_for(A, B, out)["streamk_tiles"] == 0
     assert_close(host(gpu(A, B)), ref, K, "no split")
+    g.gemm_f16_set_option(g.OPT_STREAMK, 0)
+    g.gemm_f16_set_option(g.OPT_SPLITS, 4)
+    assert g.plan_for(A, B, out)["splits"] == 4
+    C3 = host(gpu(A, B))
+    assert_close(C3, ref, K, "classic split-K")
+    assert_bits(host(gpu(A, B)), C3, "classic split-K repeatability")
 
 
 def _segment_end(ptr):
@@ -306,6 +313,34 @@ def _segment_end(ptr):
         if seg["address"] <= ptr < seg["address"] + seg["total_size"]:
             return seg["address"] + seg["total_size"]
     return None
+
+
+@pytest.mark.parametrize("M,N,K,pair", [(1000, 1024, 704, 0), (1000, 1024, 704, 2), (2304, 4608, 320, 0),
+                                        (2304, 4608, 320, 2), (16, 1040, 6000, 0), (200, 56, 9000, 0)])
+def test_stream_k_bit_exact(M, N, K, pair):
+    """Tiles cut along K by the stream-K schedule are summed exactly once, in K
+    order; integer inputs make every order exact, so the result is unique."""
+    g.gemm_f16_set_option(g.OPT_PAIR, pair)
+    rng = np.random.default_rng(M + 3 * N + 7 * K)
+    hi = 3 if K * 9 <= 2048 else 1
+    Ah = rng.integers(-hi, hi + 1, (M, K)).astype(np.float16)
+    Bh = rng.integers(-hi, hi + 1, (K, N)).astype(np.float16)
+    A, B = to_dev(Ah), to_dev(Bh)
+    out = torch.empty((M, N), dtype=torch.float16, device=DEV)
+    plan = g.plan_for(A, B, out)
+    assert plan["streamk_tiles"] > 0, plan
+    if pair == 2:
+        assert plan["pair"] == 1, plan
+    got = host(gpu(A, B, out=out))
+    ref = oracle.gemm(Ah, Bh, threads=oracle_threads())
+    if np.abs(ref.astype(np.float64)).max() <= 2048:
+        assert_bits(got, ref, f"stream-K {M}x{N}x{K}")
+    else:
+        assert_close(got, ref, K, f"stream-K {M}x{N}x{K}")
+    assert_bits(host(gpu(A, B, out=out)), got, "stream-K repeatability")
+    g.gemm_f16_set_option(g.OPT_STREAMK, 1)
+    assert g.plan_for(A, B, out)["streamk_tiles"] == 0
+    assert_close(host(gpu(A, B, out=out)), ref, K, "whole tiles")
 
 
 def test_alias_and_bad_memory_rejected_on_device():
