@@ -306,7 +306,9 @@ Schedule make_schedule(int64_t tiles, int kblocks, int splits, int max_workers)
     s.num_units = static_cast<int>(tiles);
     s.workers = static_cast<int>(std::min<int64_t>(tiles, max_workers));
     const int64_t W = max_workers;
-    if (opt(GEMM_F16_OPT_STREAMK) == 1 || tiles % W == 0) return s;
+    // Stream-K is opt-in (GEMM_F16_OPT_STREAMK = 2): its fixup of cut tiles is
+    // not yet cheaper than the wave tail it removes on the measured shapes.
+    if (opt(GEMM_F16_OPT_STREAMK) != 2 || tiles % W == 0) return s;
     const int64_t full = tiles / W;
     const int64_t sk_tiles = full >= 1 ? tiles % W + W : tiles;
     const int64_t S = sk_tiles * kblocks;
@@ -694,7 +696,7 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
 gemm_f16_status gemm_f16_set_option(int option, int64_t value)
 {
     if (option < 1 || option > 9 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
-    if (option == GEMM_F16_OPT_STREAMK && value > 1) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option == GEMM_F16_OPT_STREAMK && value > 2) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_PAIR && value > 2) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_FORCE_GATHER && value > 7) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_TILE_N && value != 0 && (value % 64 != 0 || value > 256))

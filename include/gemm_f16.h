@@ -157,8 +157,8 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
  *   GEMM_F16_OPT_MAX_CTAS      > 0: cap the persistent grid
  *   GEMM_F16_OPT_PAIR          0 default (2-CTA pair tiles for 256-wide tiles of TMA
  *                              operands without split-K), 1 never, 2 also for 128-wide tiles
- *   GEMM_F16_OPT_STREAMK       0 default (stream-K tail when the tiles do not divide
- *                              evenly over the SMs), 1 whole tiles only
+ *   GEMM_F16_OPT_STREAMK       0 default / 1: whole tiles only; 2: stream-K tail when
+ *                              the tiles do not divide evenly over the SMs
  * A value of 0 restores the default.  Returns GEMM_F16_ERR_INVALID_VALUE for an
  * unknown option or a value out of range.
  */

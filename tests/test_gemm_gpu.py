@@ -274,6 +274,7 @@ def test_split_k_deterministic_and_workspace_paths():
     Bh = rng.uniform(-1, 1, (K, N)).astype(np.float16)
     A, B = to_dev(Ah), to_dev(Bh)
     out = torch.empty((M, N), dtype=torch.float16, device=DEV)
+    g.gemm_f16_set_option(g.OPT_STREAMK, 2)
     plan = g.plan_for(A, B, out)
     assert plan["swap_ab"] and plan["streamk_tiles"] > 0 and plan["workspace_bytes"] > 0
     C1 = host(gpu(A, B))
@@ -299,7 +300,7 @@ def test_split_k_deterministic_and_workspace_paths():
     g.gemm_f16_set_option(g.OPT_STREAMK, 1)
     assert g.plan_for(A, B, out)["streamk_tiles"] == 0
     assert_close(host(gpu(A, B)), ref, K, "no split")
-    g.gemm_f16_set_option(g.OPT_STREAMK, 0)
+    g.gemm_f16_set_option(g.OPT_STREAMK, 2)
     g.gemm_f16_set_option(g.OPT_SPLITS, 4)
     assert g.plan_for(A, B, out)["splits"] == 4
     C3 = host(gpu(A, B))
@@ -321,6 +322,7 @@ def test_stream_k_bit_exact(M, N, K, pair):
     """Tiles cut along K by the stream-K schedule are summed exactly once, in K
     order; integer inputs make every order exact, so the result is unique."""
     g.gemm_f16_set_option(g.OPT_PAIR, pair)
+    g.gemm_f16_set_option(g.OPT_STREAMK, 2)
     rng = np.random.default_rng(M + 3 * N + 7 * K)
     hi = 3 if K * 9 <= 2048 else 1
     Ah = rng.integers(-hi, hi + 1, (M, K)).astype(np.float16)
