@@ -44,7 +44,10 @@ OPT_STREAMK = 9
 # Every symbol include/gemm_f16.h declares.
 EXPORTED = ("gemm_f16", "gemm_f16_ws", "gemm_f16_workspace_size", "gemm_f16_status_string",
             "gemm_f16_device_status", "gemm_f16_get_plan", "gemm_f16_set_option",
-            "gemm_f16_abi_version")
+            "gemm_f16_abi_version", "gemm_f16_noalloc")
+
+# Size of the fixed device scratch array behind gemm_f16_noalloc (8 MiB).
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class GemmF16Error(RuntimeError):
@@ -93,6 +96,8 @@ def lib():
                 L.gemm_f16_set_option.argtypes = [ctypes.c_int, I64]
                 L.gemm_f16_set_option.restype = ctypes.c_int
                 L.gemm_f16_abi_version.restype = ctypes.c_int
+                L.gemm_f16_noalloc.argtypes = [P, I64, I64, P, I64, I64, P, I64, I64, I64, I64, P]
+                L.gemm_f16_noalloc.restype = ctypes.c_int
                 _lib = L
     return _lib
 
@@ -114,6 +119,15 @@ def gemm_f16_ws(A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, M, N, 
                 workspace: int, workspace_bytes: int, stream: int = 0) -> None:
     _check(lib().gemm_f16_ws(A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, M, N, K,
                              workspace or None, workspace_bytes, stream or None), "gemm_f16_ws")
+
+
+def gemm_f16_noalloc(A: int, stride_am: int, stride_ak: int, B: int, stride_bk: int, stride_bn: int,
+                     C: int, ldc: int, M: int, N: int, K: int, stream: int = 0) -> None:
+    """gemm_f16 for callers that must not allocate device memory: split-K /
+    stream-K partials go to the library's fixed 8 MiB device array instead of
+    a cudaMalloc'd workspace (see include/gemm_f16.h)."""
+    _check(lib().gemm_f16_noalloc(A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, M, N, K,
+                                  stream or None), "gemm_f16_noalloc")
 
 
 def gemm_f16_workspace_size(M: int, N: int, K: int) -> int:

@@ -586,6 +586,65 @@ gemm_f16_status run(const Args& a, void* user_ws, size_t user_ws_bytes, bool use
     return launch(pl, *dev, partials, counters, stream);
 }
 
+// ---------------------------------------------------------------------------
+// Fixed scratch for gemm_f16_noalloc(): the split-K / stream-K counters and
+// partial sums live in this file-scope device array instead of memory the
+// library allocates.  Every device that loads the library holds it (8 MiB)
+// until the process exits.  In host code `g_noalloc_scratch` is only a
+// stand-in for the symbol, never a device address: the address comes from
+// cudaGetSymbolAddress, taken once per device with that device current.
+constexpr size_t kNoAllocScratchBytes = GEMM_F16_NOALLOC_SCRATCH_BYTES;
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (nullptr if the
+// runtime could not provide it).
+void* noalloc_scratch()
+{
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(g_mutex);
+    if (!g_noalloc_ptr[d]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_noalloc_ptr[d] = p;
+    }
+    return g_noalloc_ptr[d];
+}
+
+gemm_f16_status run_noalloc(const Args& a, cudaStream_t stream)
+{
+    DevInfo* dev = nullptr;
+    gemm_f16_status st = validate(a, true, &dev);
+    if (st != GEMM_F16_OK) return st;
+    Plan pl;
+    st = make_plan(a, *dev, &pl);
+    if (st != GEMM_F16_OK) return st;
+    float* partials = nullptr;
+    int* counters = nullptr;
+    if (pl.pub.workspace_bytes > 0) {
+        if (pl.pub.workspace_bytes > kNoAllocScratchBytes) return GEMM_F16_ERR_OUT_OF_MEMORY;
+        void* s = noalloc_scratch();
+        if (!s) return GEMM_F16_ERR_LAUNCH;
+        counters = static_cast<int*>(s);
+        partials = reinterpret_cast<float*>(static_cast<char*>(s) + pl.counter_bytes);
+        // The array keeps the previous call's contents; the counters must start
+        // at zero (the partials are always written before they are read).
+        if (cudaMemsetAsync(counters, 0, pl.counter_bytes, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_F16_ERR_LAUNCH;
+        }
+    }
+    return launch(pl, *dev, partials, counters, stream);
+}
+
 }  // namespace
 
 extern "C" {
@@ -604,6 +663,14 @@ gemm_f16_status gemm_f16_ws(const void* A, int64_t stride_am, int64_t stride_ak,
 {
     const Args a{A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, M, N, K};
     return run(a, workspace, workspace_bytes, false, stream);
+}
+
+gemm_f16_status gemm_f16_noalloc(const void* A, int64_t stride_am, int64_t stride_ak, const void* B,
+                                 int64_t stride_bk, int64_t stride_bn, void* C, int64_t ldc, int64_t M, int64_t N,
+                                 int64_t K, cudaStream_t stream)
+{
+    const Args a{A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, M, N, K};
+    return run_noalloc(a, stream);
 }
 
 gemm_f16_status gemm_f16_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes)

@@ -115,6 +115,42 @@ gemm_f16_status gemm_f16_ws(const void* A, int64_t stride_am, int64_t stride_ak,
  * M, N, K, the options and the device's SM count. */
 gemm_f16_status gemm_f16_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
 
+/* Size of the fixed scratch array behind gemm_f16_noalloc(). */
+#define GEMM_F16_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+/*
+ * Same as gemm_f16(), but the library allocates nothing, ever.  (The pages
+ * this library follows have no counterpart: this entry point exists for
+ * callers, not for the method.)
+ *
+ * For callers that must not call cudaMalloc: a process that has handed all
+ * device memory to its own pool, code that runs where a device allocation is
+ * forbidden or where the device synchronisation cudaMalloc implies cannot be
+ * afforded.  gemm_f16() grows a workspace with cudaMalloc the first time a
+ * call cuts tiles along K (split-K or stream-K); this variant instead keeps
+ * those counters and partial sums in one file-scope device array of
+ * GEMM_F16_NOALLOC_SCRATCH_BYTES (8 MiB) that every device loading the library
+ * holds until the process exits.  The caller still passes A, B and C.
+ *
+ * - Set-up: the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *   first call before any stream capture on the device.
+ * - A call whose plan needs more than GEMM_F16_NOALLOC_SCRATCH_BYTES of
+ *   workspace is rejected with GEMM_F16_ERR_OUT_OF_MEMORY before anything is
+ *   queued (gemm_f16_get_plan() reports the need as workspace_bytes).
+ * - Every call on a device shares the one array and finds the previous call's
+ *   contents there: the call first clears the counter block with
+ *   cudaMemsetAsync on `stream`.  Calls that overlap on the GPU (different
+ *   streams, no ordering between them) race on the array and give undefined
+ *   results; order them.
+ * - Calls that cut no tile along K do not touch the array.
+ * Other arguments, errors and asynchrony are those of gemm_f16().
+ */
+gemm_f16_status gemm_f16_noalloc(const void* A, int64_t stride_am, int64_t stride_ak,
+                                 const void* B, int64_t stride_bk, int64_t stride_bn,
+                                 void* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                 cudaStream_t stream);
+
 /* Human-readable name of a status code; never NULL. */
 const char* gemm_f16_status_string(int status);
 

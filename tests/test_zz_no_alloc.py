@@ -1,0 +1,80 @@
+"""gemm_f16_noalloc: the entry point for callers that must not allocate.
+
+Some callers cannot call cudaMalloc (all device memory already handed to their
+own pool, or a code path where an allocation, and the device synchronisation
+it implies, is not allowed).  gemm_f16_noalloc keeps the split-K / stream-K
+partial sums in the library's fixed device array instead of a workspace it
+would allocate.  This file runs after the other test files, so a failure here
+does not hide theirs; it sets every option it needs and restores the defaults.
+"""
+import numpy as np
+import pytest
+import torch
+
+import dense_tiled_gemm_fp16_gb300 as g
+import oracle
+from tests.parity import assert_close, oracle_threads
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(autouse=True)
+def _defaults():
+    for o in (g.OPT_FORCE_GATHER, g.OPT_SPLITS, g.OPT_TILE_N, g.OPT_PANEL, g.OPT_SWAP,
+              g.OPT_TIMEOUT_MS, g.OPT_MAX_CTAS, g.OPT_PAIR, g.OPT_STREAMK):
+        g.gemm_f16_set_option(o, 0)
+    yield
+    for o in (g.OPT_STREAMK, g.OPT_SPLITS):
+        g.gemm_f16_set_option(o, 0)
+
+
+def _args(A, B, C):
+    M, K = A.shape
+    N = B.shape[1]
+    return (A.data_ptr(), A.stride(0), A.stride(1), B.data_ptr(), B.stride(0), B.stride(1),
+            C.data_ptr(), C.stride(0), M, N, K)
+
+
+@pytest.mark.parametrize("streamk,splits", [(2, 0), (0, 4)])
+def test_no_alloc_entry_matches_gemm_f16(streamk, splits):
+    torch.cuda.set_device(DEV)
+    g.gemm_f16_set_option(g.OPT_STREAMK, streamk)
+    g.gemm_f16_set_option(g.OPT_SPLITS, splits)
+    rng = np.random.default_rng(31)
+    M, N, K = 16, 4096, 8192          # small M: the plan cuts tiles along K
+    Ah = rng.uniform(-1, 1, (M, K)).astype(np.float16)
+    Bh = rng.uniform(-1, 1, (K, N)).astype(np.float16)
+    A = torch.from_numpy(Ah).to(DEV)
+    B = torch.from_numpy(Bh).to(DEV)
+    ref_out = torch.empty((M, N), dtype=torch.float16, device=DEV)
+    plan = g.gemm_f16_get_plan(*_args(A, B, ref_out))
+    assert 0 < plan["workspace_bytes"] <= g.NOALLOC_SCRATCH_BYTES, plan
+    stream = torch.cuda.current_stream(DEV).cuda_stream
+    g.gemm_f16(*_args(A, B, ref_out), stream=stream)
+    torch.cuda.synchronize(DEV)
+    expected = ref_out.cpu().numpy()
+    for call in range(2):                       # the array keeps the last call's contents
+        out = torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV)
+        g.gemm_f16_noalloc(*_args(A, B, out), stream=stream)
+        torch.cuda.synchronize(DEV)
+        got = out.cpu().numpy()
+        assert_close(got, expected, K, f"noalloc call {call} vs gemm_f16")
+    assert_close(got, oracle.gemm(Ah, Bh, threads=oracle_threads()), K, "noalloc vs oracle")
+    assert g.gemm_f16_device_status() == 0
+
+
+def test_no_alloc_rejects_a_plan_beyond_its_scratch():
+    # 128 x 4096 x 65536 with stream-K cuts 32-wide tiles over every SM; the
+    # partials need far more than 8 MiB, so the call is refused before launch.
+    g.gemm_f16_set_option(g.OPT_STREAMK, 2)
+    M, N, K = 256, 4096, 65536
+    A = torch.zeros((M, K), dtype=torch.float16, device=DEV)
+    B = torch.zeros((K, N), dtype=torch.float16, device=DEV)
+    out = torch.zeros((M, N), dtype=torch.float16, device=DEV)
+    plan = g.gemm_f16_get_plan(*_args(A, B, out))
+    assert plan["workspace_bytes"] > g.NOALLOC_SCRATCH_BYTES, plan
+    with pytest.raises(g.GemmF16Error) as e:
+        g.gemm_f16_noalloc(*_args(A, B, out))
+    assert e.value.status == g.ERR_OUT_OF_MEMORY
