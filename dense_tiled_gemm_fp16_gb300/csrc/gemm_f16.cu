@@ -49,7 +49,7 @@ struct Workspace {
 };
 Workspace g_ws[kMaxDevices];
 
-std::atomic<int64_t> g_opt[10];
+std::atomic<int64_t> g_opt[11];
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 PFN_cuMemGetAddressRange_v3020 g_addr_range = nullptr;
@@ -292,9 +292,36 @@ struct Schedule {
     int workers = 1, num_units = 0, sk_tile0 = 0, nseg_max = 0, sk_slot_base = 0;
     int64_t sk_iters = 0;
     int64_t partial_slots = 0;   // fp32 tile partials the workspace must hold (per CTA rank)
+    int tail_tile0 = INT32_MAX, tail_split = 1;
 };
 
-Schedule make_schedule(int64_t tiles, int kblocks, int splits, int max_workers)
+// Tail split: with whole tiles only, the last wave holds T mod W tiles and
+// leaves the other workers idle.  Cutting those tiles along N into s pieces
+// (each still a complete K reduction of its columns, so no partial sums) makes
+// that wave ceil(s*rem/W)/s tile-times long; take the smallest s that helps.
+// A piece keeps at least `min_bn` columns and a multiple of 64.
+void tail_split(Schedule& s, int64_t tiles, int BN, int min_bn, int64_t W)
+{
+    if (opt(GEMM_F16_OPT_TAIL_SPLIT) == 1) return;
+    const int64_t rem = tiles % W;
+    if (rem == 0) return;
+    int best = 1;
+    double best_t = 1.0;
+    for (int sp = 2; BN % sp == 0 && BN / sp >= min_bn && (BN / sp) % 64 == 0; sp *= 2) {
+        const double t = static_cast<double>((rem * sp + W - 1) / W) / sp;
+        if (t < best_t - 1e-9) {
+            best_t = t;
+            best = sp;
+        }
+    }
+    if (best == 1) return;
+    s.tail_tile0 = static_cast<int>(tiles - rem);
+    s.tail_split = best;
+    s.num_units = static_cast<int>(tiles - rem + rem * best);
+    s.workers = static_cast<int>(std::min<int64_t>(s.num_units, W));
+}
+
+Schedule make_schedule(int64_t tiles, int kblocks, int splits, int max_workers, int BN, int min_bn)
 {
     Schedule s;
     if (splits > 1) {
@@ -306,9 +333,13 @@ Schedule make_schedule(int64_t tiles, int kblocks, int splits, int max_workers)
     s.num_units = static_cast<int>(tiles);
     s.workers = static_cast<int>(std::min<int64_t>(tiles, max_workers));
     const int64_t W = max_workers;
+    if (opt(GEMM_F16_OPT_STREAMK) != 2) {
+        tail_split(s, tiles, BN, min_bn, W);
+        return s;
+    }
     // Stream-K is opt-in (GEMM_F16_OPT_STREAMK = 2): its fixup of cut tiles is
     // not yet cheaper than the wave tail it removes on the measured shapes.
-    if (opt(GEMM_F16_OPT_STREAMK) != 2 || tiles % W == 0) return s;
+    if (tiles % W == 0) return s;
     const int64_t full = tiles / W;
     const int64_t sk_tiles = full >= 1 ? tiles % W + W : tiles;
     const int64_t S = sk_tiles * kblocks;
@@ -442,7 +473,9 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     int64_t max_workers = pair ? max_pair_clusters(const_cast<DevInfo&>(dev), smem) : dev.sms;
     if (cap > 0) max_workers = std::min<int64_t>(max_workers, pair ? std::max<int64_t>(1, cap / 2) : cap);
     if (max_workers < 1) return GEMM_F16_ERR_LAUNCH;
-    const Schedule sch = make_schedule(tiles, kblocks, splits, static_cast<int>(max_workers));
+    // Narrowest tail piece: the pair form keeps >= 64 B columns per CTA; a
+    // TMA-stored C needs whole 64-column boxes.
+    const Schedule sch = make_schedule(tiles, kblocks, splits, static_cast<int>(max_workers), BN, pair ? 128 : 64);
     const int grid = pair ? 2 * sch.workers : sch.workers;
     const int64_t panel = opt(GEMM_F16_OPT_PANEL);
 
@@ -456,6 +489,8 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     kp.sk_iters = sch.sk_iters;
     kp.nseg_max = sch.nseg_max;
     kp.sk_slot_base = sch.sk_slot_base;
+    kp.tail_tile0 = sch.tail_tile0;
+    kp.tail_split = sch.tail_split;
     kp.panel = static_cast<int>(panel > 0 ? panel : 8);
     kp.BN = BN, kp.stages = stages;
     kp.a_flags = (ca.tma ? gemm_f16_dev::kOpTma : 0u) | (ca.mn ? gemm_f16_dev::kOpMnMajor : 0u);
@@ -482,6 +517,7 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     pub.splits = splits, pub.kblocks = kblocks, pub.grid = grid;
     pub.units = static_cast<int>(tiles * splits);
     pub.streamk_tiles = sch.sk_iters > 0 ? static_cast<int>(tiles - sch.sk_tile0) : 0;
+    pub.tail_split = sch.tail_split;
     pub.stages = stages, pub.smem_bytes = smem;
     pub.workspace_bytes = sch.partial_slots > 0
                               ? workspace_bytes_for(sch.partial_slots, BN, tiles, pair ? 2 : 1, &pl->counter_bytes,
@@ -690,7 +726,7 @@ gemm_f16_status gemm_f16_workspace_size(int64_t M, int64_t N, int64_t K, size_t*
         const int64_t rows = pair ? 2 * gemm_f16_dev::kBM : gemm_f16_dev::kBM;
         const int64_t tiles = ((Mv + rows - 1) / rows) * tiles_n;
         const int workers = pair ? std::max(1, dev->sms / 2) : dev->sms;
-        const Schedule s = make_schedule(tiles, kblocks, splits, workers);
+        const Schedule s = make_schedule(tiles, kblocks, splits, workers, BN, pair ? 128 : 64);
         if (s.partial_slots > 0)
             need = std::max(need, workspace_bytes_for(s.partial_slots, BN, tiles, pair ? 2 : 1, nullptr, nullptr));
     }
@@ -762,7 +798,8 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
 
 gemm_f16_status gemm_f16_set_option(int option, int64_t value)
 {
-    if (option < 1 || option > 9 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option < 1 || option > 10 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option == GEMM_F16_OPT_TAIL_SPLIT && value > 1) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_STREAMK && value > 2) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_PAIR && value > 2) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_FORCE_GATHER && value > 7) return GEMM_F16_ERR_INVALID_VALUE;

@@ -96,6 +96,11 @@ struct KernelParams {
     int64_t sk_iters;
     int nseg_max;       // most segments one worker's stream-K range can hold
     int sk_slot_base;   // first partial slot of the stream-K segments
+    // Tail split: whole tiles from tail_tile0 on are cut along N into
+    // tail_split units of BN / tail_split columns, so that a last partial wave
+    // of tiles spreads over more workers (no partial sums involved).
+    int tail_tile0;
+    int tail_split;
 };
 
 struct SmemLayout {
@@ -131,6 +136,8 @@ constexpr uint64_t kDrainTimeoutNs = 10000000ull;
 // tile, and the last of them to finish adds all partials in K order.
 struct Unit {
     int tile, m_blk, n_blk, kb0, kb1, slot, expected;
+    int bn;      // columns of this unit (BN, or BN / tail_split for a tail piece)
+    int n_off;   // first column of this unit inside its tile
 };
 
 // Tile -> (row block, column block).  Tiles are numbered in panels of `panel`
@@ -187,16 +194,27 @@ __device__ __forceinline__ Unit unit_at(const KernelParams& p, int cid, int i)
     Unit w;
     w.slot = -1;
     w.expected = 1;
+    w.bn = p.BN;
+    w.n_off = 0;
     const int nc = classic_units(p, cid);
     if (i < nc) {
         const int u = cid + i * p.workers;
-        w.tile = u / p.splits;
-        const int split = u - w.tile * p.splits;
-        w.kb0 = static_cast<int>(static_cast<int64_t>(split) * p.kblocks / p.splits);
-        w.kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * p.kblocks / p.splits);
-        if (p.splits > 1) {
-            w.slot = u;
-            w.expected = p.splits;
+        if (u >= p.tail_tile0) {
+            const int v = u - p.tail_tile0;
+            w.tile = p.tail_tile0 + v / p.tail_split;
+            w.bn = p.BN / p.tail_split;
+            w.n_off = (v % p.tail_split) * w.bn;
+            w.kb0 = 0;
+            w.kb1 = p.kblocks;
+        } else {
+            w.tile = u / p.splits;
+            const int split = u - w.tile * p.splits;
+            w.kb0 = static_cast<int>(static_cast<int64_t>(split) * p.kblocks / p.splits);
+            w.kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * p.kblocks / p.splits);
+            if (p.splits > 1) {
+                w.slot = u;
+                w.expected = p.splits;
+            }
         }
     } else {
         const int j = i - nc;
@@ -460,12 +478,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
             uint32_t phase = 0;
             bool ok = true;
             int issued = 0;
-            const int bcols = kPair ? p.BN / 2 : p.BN;   // this CTA's share of the B tile
             const int nu = units_of_worker(p, cid);
             for (int i = 0; i < nu && ok; ++i) {
                 const Unit w = unit_at(p, cid, i);
+                const int bcols = kPair ? w.bn / 2 : w.bn;   // this CTA's share of the unit's B columns
                 const int64_t m0 = static_cast<int64_t>(w.m_blk) * kTileRows + rank * kBM;
-                const int64_t n0 = static_cast<int64_t>(w.n_blk) * p.BN + rank * bcols;
+                const int64_t n0 = static_cast<int64_t>(w.n_blk) * p.BN + w.n_off + rank * bcols;
+                // Bytes one stage of this unit brings in: MN-major B comes in
+                // 64-column boxes, K-major B in one box of the full tile width.
+                const uint32_t b_bytes = b_mn ? static_cast<uint32_t>(bcols) * 128u : p.stage_b_bytes;
+                const uint32_t tx = kPair ? 2u * (kStageABytes + b_bytes)
+                                          : (a_tma ? kStageABytes : 0u) + (b_tma ? b_bytes : 0u);
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_bar<kPair>(bar_empty(L.bars, stage), phase ^ 1u, abort, p.timeout_ns)) {
                         raise_abort(p, abort);
@@ -480,7 +503,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                         if (kPair) {
                             // The leader expects both CTAs' bytes on its own barrier;
                             // the peer's copies complete on the leader's barrier.
-                            if (leader) mbar_arrive_expect_tx(fb, p.tx_bytes);
+                            if (leader) mbar_arrive_expect_tx(fb, tx);
                             const uint32_t fbc = mapa_shared(fb, 0);
                             if (!a_mn) {
                                 tma_load_2d_pair(sa, &p.tmA, k0, static_cast<int32_t>(m0), fbc);
@@ -495,7 +518,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                                     tma_load_2d_pair(sb + j * 8192, &p.tmB, static_cast<int32_t>(n0 + 64 * j), k0, fbc);
                             }
                         } else {
-                            mbar_arrive_expect_tx(fb, p.tx_bytes);
+                            mbar_arrive_expect_tx(fb, tx);
                             if (a_tma) {
                                 if (!a_mn) {
                                     tma_load_2d(sa, &p.tmA, k0, static_cast<int32_t>(m0), fb);
@@ -518,7 +541,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                         if (!a_tma)
                             gather_tile(p.A, p.a_sm, p.a_sk, p.M, p.K, m0, k0, kBM, a_mn, sa, t);
                         if (!b_tma)
-                            gather_tile(p.B, p.b_sn, p.b_sk, p.N, p.K, n0, k0, p.BN, b_mn, sb, t);
+                            gather_tile(p.B, p.b_sn, p.b_sk, p.N, p.K, n0, k0, w.bn, b_mn, sb, t);
                         fence_proxy_async_smem();
                         mbar_arrive(fb);
                     }
@@ -562,6 +585,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + acc * kAccStride;
+                // N field (bits 17-22) of the instruction descriptor: this unit's width
+                const uint32_t idesc = (p.idesc & ~(0x3Fu << 17)) | ((static_cast<uint32_t>(w.bn) >> 3) << 17);
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_bar<kPair>(bar_full(L.bars, stage), phase, abort, p.timeout_ns)) {
                         raise_abort(p, abort);
@@ -581,9 +606,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                                                  : umma_desc_sw128(sb + k * 32, 16, 1024);
                         const uint32_t accum = (kb > w.kb0 || k > 0) ? 1u : 0u;
                         if (kPair)
-                            umma_f16_pair(d, ad, bd, p.idesc, accum);
+                            umma_f16_pair(d, ad, bd, idesc, accum);
                         else
-                            umma_f16(d, ad, bd, p.idesc, accum);
+                            umma_f16(d, ad, bd, idesc, accum);
                     }
                     any = true;
                     if (kPair)
@@ -623,14 +648,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t group_count = 0;
-        const int npieces = p.BN / 16;          // 16 accumulator columns per piece
         const int nu = units_of_worker(p, cid);
         constexpr int kRanks = kPair ? 2 : 1;
         const size_t slot_elems = static_cast<size_t>(kBM) * p.BN;   // one CTA's 128 rows of a tile
         for (int ui = 0; ui < nu; ++ui) {
             const Unit w = unit_at(p, cid, ui);
             const int64_t m0 = static_cast<int64_t>(w.m_blk) * kTileRows + rank * kBM;
-            const int64_t n0 = static_cast<int64_t>(w.n_blk) * p.BN;
+            const int64_t n0 = static_cast<int64_t>(w.n_blk) * p.BN + w.n_off;
+            const int npieces = w.bn / 16;          // 16 accumulator columns per piece
             // One thread waits for the accumulator and tells the other epilogue
             // threads, so that they all leave together on an abort (the named
             // barriers below must see all 128 threads).
@@ -646,14 +671,15 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
             const uint32_t tempty = kPair ? mapa_shared(bar_tempty(L.bars, acc), 0) : bar_tempty(L.bars, acc);
             if (w.slot < 0) {
                 uint32_t buf = 0;
-                for (int pc = 0; pc < npieces; pc += 2) {
-                    // two pieces (32 columns) in flight per TMEM wait
-                    const bool two = pc + 1 < npieces;
-                    uint32_t r[32];
-                    tmem_ld_x16(taddr + 16 * pc, r);
-                    if (two) tmem_ld_x16(taddr + 16 * pc + 16, r + 16);
+                for (int pc = 0; pc < npieces; pc += 4) {
+                    // up to four pieces (64 columns) in flight per TMEM wait
+                    const int cnt = min(4, npieces - pc);
+                    uint32_t r[64];
+#pragma unroll
+                    for (int h2 = 0; h2 < 4; ++h2)
+                        if (h2 < cnt) tmem_ld_x16(taddr + 16 * (pc + h2), r + 16 * h2);
                     tmem_wait_ld();
-                    if (pc + 2 >= npieces) {
+                    if (pc + 4 >= npieces) {
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) {
@@ -664,8 +690,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                         }
                     }
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        if (h2 == 1 && !two) break;
+                    for (int h2 = 0; h2 < 4; ++h2) {
+                        if (h2 >= cnt) break;
                         const int piece = pc + h2;
                         uint32_t h[8];
                         convert16(r + 16 * h2, h);

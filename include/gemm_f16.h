@@ -170,6 +170,7 @@ typedef struct {
     int tile_m, tile_n, tiles_m, tiles_n;
     int splits, kblocks, units, grid, stages;
     int streamk_tiles;  /* trailing tiles whose K blocks are spread over all workers */
+    int tail_split;     /* trailing partial wave of tiles cut along N into this many pieces */
     int smem_bytes;
     size_t workspace_bytes;
 } gemm_f16_plan;
@@ -195,6 +196,8 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
  *                              operands without split-K), 1 never, 2 also for 128-wide tiles
  *   GEMM_F16_OPT_STREAMK       0 default / 1: whole tiles only; 2: stream-K tail when
  *                              the tiles do not divide evenly over the SMs
+ *   GEMM_F16_OPT_TAIL_SPLIT    0 default: cut the last partial wave of tiles along N
+ *                              into narrower tiles; 1 never
  * A value of 0 restores the default.  Returns GEMM_F16_ERR_INVALID_VALUE for an
  * unknown option or a value out of range.
  */
@@ -207,7 +210,8 @@ enum {
     GEMM_F16_OPT_TIMEOUT_MS = 6,
     GEMM_F16_OPT_MAX_CTAS = 7,
     GEMM_F16_OPT_PAIR = 8,
-    GEMM_F16_OPT_STREAMK = 9
+    GEMM_F16_OPT_STREAMK = 9,
+    GEMM_F16_OPT_TAIL_SPLIT = 10
 };
 gemm_f16_status gemm_f16_set_option(int option, int64_t value);
 

@@ -25,7 +25,7 @@ DEV = torch.device("cuda:0")
 def _defaults():
     yield
     for o in (g.OPT_FORCE_GATHER, g.OPT_SPLITS, g.OPT_TILE_N, g.OPT_PANEL, g.OPT_SWAP,
-              g.OPT_TIMEOUT_MS, g.OPT_MAX_CTAS, g.OPT_PAIR, g.OPT_STREAMK):
+              g.OPT_TIMEOUT_MS, g.OPT_MAX_CTAS, g.OPT_PAIR, g.OPT_STREAMK, g.OPT_TAIL_SPLIT):
         g.gemm_f16_set_option(o, 0)
 
 
@@ -306,6 +306,25 @@ def test_split_k_deterministic_and_workspace_paths():
     C3 = host(gpu(A, B))
     assert_close(C3, ref, K, "classic split-K")
     assert_bits(host(gpu(A, B)), C3, "classic split-K repeatability")
+
+
+@pytest.mark.parametrize("M,N,K,layout", [(2304, 4608, 64, "row"), (1000, 1000, 100, "pitch"),
+                                           (700, 1536, 136, "row"), (3000, 700, 72, "pitch16")])
+def test_tail_split_bit_exact(M, N, K, layout):
+    """The last partial wave of tiles is cut along N into narrower tiles; every
+    output is still one complete K reduction, so integer inputs stay exact."""
+    rng = np.random.default_rng(M + N + K)
+    Ah = rng.integers(-3, 4, (M, K)).astype(np.float16)
+    Bh = rng.integers(-3, 4, (K, N)).astype(np.float16)
+    A, B = make_view(Ah, layout), make_view(Bh, layout)
+    out = torch.empty((M, N), dtype=torch.float16, device=DEV)
+    plan = g.plan_for(A, B, out)
+    assert plan["tail_split"] > 1, plan
+    ref = oracle.gemm(Ah, Bh, threads=oracle_threads())
+    assert_bits(host(gpu(A, B, out=out)), ref, f"tail split {M}x{N}x{K}")
+    g.gemm_f16_set_option(g.OPT_TAIL_SPLIT, 1)
+    assert g.plan_for(A, B, out)["tail_split"] == 1
+    assert_bits(host(gpu(A, B, out=out)), ref, f"no tail split {M}x{N}x{K}")
 
 
 def _segment_end(ptr):
