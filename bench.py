@@ -45,6 +45,38 @@ def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
+def kernel_source_hash() -> str:
+    """First 16 hex digits of sha256 over the kernel sources (ptx, kernel, host)."""
+    import hashlib
+    csrc = os.path.join(ROOT, "dense_tiled_gemm_fp16_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ("ptx.cuh", "gemm_kernel.cuh", "gemm_f16.cu"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    or None when there is none or it was taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"gemm_f16_persistent__{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -300,7 +332,7 @@ def report(args, w, plan, peaks, bnd, flops, nbytes, ms_per_step, value, wall, c
         achieved = nbytes / (ms_per_step * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
-    roof["traffic"] = None
+    roof["traffic"] = profiled_traffic(w.name)
     roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json bf16 burst / copy bandwidth)"
     roof["kernel"] = "gemm_f16_persistent"
     cpu = None
