@@ -365,8 +365,9 @@ def report(args, w, plan, peaks, bnd, flops, nbytes, ms_per_step, value, wall, c
                    "distribution": w.A.kind, "l2": l2_note,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "options": args.opt,
-                   "plan": {k: plan[k] for k in ("swap_ab", "a_tma", "b_tma", "c_tma", "tile_n",
-                                                 "splits", "grid", "stages")}},
+                   "plan": {k: plan[k] for k in ("swap_ab", "pair", "a_tma", "b_tma", "c_tma", "tile_n",
+                                                 "splits", "streamk_tiles", "tail_split", "grid",
+                                                 "stages")}},
         "hbm_gbs_min_traffic": round(nbytes / (ms_per_step * 1e-3) / 1e9, 1),
         "wall_s_timed_region": round(wall, 4),
         "clocks": clk,

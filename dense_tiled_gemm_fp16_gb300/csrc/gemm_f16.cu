@@ -49,7 +49,7 @@ struct Workspace {
 };
 Workspace g_ws[kMaxDevices];
 
-std::atomic<int64_t> g_opt[11];
+std::atomic<int64_t> g_opt[12];
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 PFN_cuMemGetAddressRange_v3020 g_addr_range = nullptr;
@@ -217,6 +217,25 @@ bool encode_2d(CUtensorMap* tm, const void* ptr, uint64_t inner, uint64_t outer,
     return r == CUDA_SUCCESS;
 }
 
+// MN-major operand of extent MN (a multiple of 64) as a 3-D tensor: 64
+// consecutive MN elements, then K rows `pitch_bytes` apart, then MN / 64
+// atom columns 128 bytes apart.  A box of (64, 64, atoms) lands in shared
+// memory as `atoms` consecutive 64 x 64 swizzle-atom columns, the layout the
+// 2-D form builds with one copy per column.  Every element the map can reach
+// lies inside the operand's rows, so no read leaves the MN x K view.
+bool encode_3d_mn(CUtensorMap* tm, const void* ptr, uint64_t MN, uint64_t K, uint64_t pitch_bytes, uint32_t atoms)
+{
+    if (!g_encode || MN % 64 != 0) return false;
+    cuuint64_t dims[3] = {64, K, MN / 64};
+    cuuint64_t strides[2] = {pitch_bytes, 128};
+    cuuint32_t box[3] = {64, 64, atoms};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 struct Plan {
     gemm_f16_plan pub;
     KernelParams kp;
@@ -353,10 +372,17 @@ Schedule make_schedule(int64_t tiles, int kblocks, int splits, int max_workers, 
     s.num_units = static_cast<int>(tiles - sk_tiles);
     s.sk_tile0 = s.num_units;
     s.sk_iters = S;
-    const int64_t max_range = (S + w - 1) / w;
-    s.nseg_max = static_cast<int>(max_range / kblocks + 2);
+    // Partial slots are numbered per tile: stream-K tile t keeps its units'
+    // partials in slots t*nseg_max .. t*nseg_max + (units covering t) - 1.
+    auto worker_of = [&](int64_t x) {   // the worker whose range holds stream-K block x
+        return std::min<int64_t>(((x + 1) * w + S - 1) / S - 1, w - 1);
+    };
+    int64_t most = 1;
+    for (int64_t t = 0; t < sk_tiles; ++t)
+        most = std::max<int64_t>(most, worker_of(t * kblocks + kblocks - 1) - worker_of(t * kblocks) + 1);
+    s.nseg_max = static_cast<int>(most);
     s.sk_slot_base = 0;
-    s.partial_slots = w * s.nseg_max;
+    s.partial_slots = sk_tiles * most;
     return s;
 }
 
@@ -427,7 +453,7 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     // Pair form (two CTAs per 256 x BN tile): TMA operands, no split-K, and a
     // B half that is a whole number of 64-column swizzle atoms.
     const int64_t pair_opt = opt(GEMM_F16_OPT_PAIR);
-    const bool pair = pair_opt != 1 && !swap && splits == 1 && ca.tma && cb.tma &&
+    const bool pair = pair_opt != 1 && !swap && (splits == 1 || pair_opt == 2) && ca.tma && cb.tma &&
                       (BN == 256 || (pair_opt == 2 && BN == 128)) && Mv > gemm_f16_dev::kBM;
     const int tile_rows = pair ? 2 * gemm_f16_dev::kBM : gemm_f16_dev::kBM;
     const int bcols = pair ? BN / 2 : BN;   // B columns one CTA loads
@@ -435,8 +461,12 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     const int64_t tiles = static_cast<int64_t>(tiles_m) * tiles_n;
     if (tiles * splits > INT32_MAX / 4 || tiles * kblocks > (int64_t(1) << 40)) return GEMM_F16_ERR_INVALID_VALUE;
 
+    bool a_3d = false, b_3d = false;
     if (ca.tma) {
-        const bool ok = ca.mn ? encode_2d(&kp.tmA, kp.A, Mv, a.K, a.K == 1 ? round_up(2 * Mv, 16) : 2 * kp.a_sk, 64, 64)
+        a_3d = ca.mn && encode_3d_mn(&kp.tmA, kp.A, Mv, a.K, a.K == 1 ? round_up(2 * Mv, 16) : 2 * kp.a_sk,
+                                     gemm_f16_dev::kBM / 64);
+        const bool ok = a_3d ? true
+                        : ca.mn ? encode_2d(&kp.tmA, kp.A, Mv, a.K, a.K == 1 ? round_up(2 * Mv, 16) : 2 * kp.a_sk, 64, 64)
                               : encode_2d(&kp.tmA, kp.A, a.K, Mv, Mv == 1 ? round_up(2 * a.K, 16) : 2 * kp.a_sm, 64,
                                           gemm_f16_dev::kBM);
         if (!ok) {
@@ -445,7 +475,10 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
         }
     }
     if (cb.tma) {
-        const bool ok = cb.mn ? encode_2d(&kp.tmB, kp.B, Nv, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk, 64, 64)
+        b_3d = cb.mn && encode_3d_mn(&kp.tmB, kp.B, Nv, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk,
+                                     static_cast<uint32_t>(bcols / 64));
+        const bool ok = b_3d ? true
+                        : cb.mn ? encode_2d(&kp.tmB, kp.B, Nv, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk, 64, 64)
                               : encode_2d(&kp.tmB, kp.B, a.K, Nv, Nv == 1 ? round_up(2 * a.K, 16) : 2 * kp.b_sn, 64,
                                           static_cast<uint32_t>(bcols));
         if (!ok) {
@@ -460,10 +493,14 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
 
     const uint32_t stage_b = static_cast<uint32_t>(bcols) * gemm_f16_dev::kBK * 2;
     const uint32_t stage_bytes = gemm_f16_dev::kStageABytes + stage_b;
-    const int epi = c_tma ? static_cast<int>(gemm_f16_dev::kEpiBytes) : 0;
+    // The 32 KB epilogue buffer stages TMA stores of C, and is where the last
+    // unit of a tile cut along K collects the other units' partials.
+    const bool may_cut = splits > 1 || opt(GEMM_F16_OPT_STREAMK) == 2;
+    const int epi = (c_tma || may_cut) ? static_cast<int>(gemm_f16_dev::kEpiBytes) : 0;
     int stages = (kMaxDynSmem - kSmemAlignSlack - epi - static_cast<int>(gemm_f16_dev::kBarrierBytes)) /
                  static_cast<int>(stage_bytes);
     stages = std::min(stages, gemm_f16_dev::kMaxStages);
+    if (opt(GEMM_F16_OPT_MAX_STAGES) >= 2) stages = std::min<int>(stages, static_cast<int>(opt(GEMM_F16_OPT_MAX_STAGES)));
     if (stages < 2) return GEMM_F16_ERR_INVALID_VALUE;
     const int smem = kSmemAlignSlack + stages * static_cast<int>(stage_bytes) + epi +
                      static_cast<int>(gemm_f16_dev::kBarrierBytes);
@@ -493,9 +530,12 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     kp.tail_split = sch.tail_split;
     kp.panel = static_cast<int>(panel > 0 ? panel : 8);
     kp.BN = BN, kp.stages = stages;
-    kp.a_flags = (ca.tma ? gemm_f16_dev::kOpTma : 0u) | (ca.mn ? gemm_f16_dev::kOpMnMajor : 0u);
-    kp.b_flags = (cb.tma ? gemm_f16_dev::kOpTma : 0u) | (cb.mn ? gemm_f16_dev::kOpMnMajor : 0u);
+    kp.a_flags = (ca.tma ? gemm_f16_dev::kOpTma : 0u) | (ca.mn ? gemm_f16_dev::kOpMnMajor : 0u) |
+                 (a_3d ? gemm_f16_dev::kOpBox3d : 0u);
+    kp.b_flags = (cb.tma ? gemm_f16_dev::kOpTma : 0u) | (cb.mn ? gemm_f16_dev::kOpMnMajor : 0u) |
+                 (b_3d ? gemm_f16_dev::kOpBox3d : 0u);
     kp.c_tma = c_tma ? 1u : 0u;
+    kp.epi_smem = epi > 0 ? 1u : 0u;
     // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16
     // (bits 7-9, 10-12 = 0), A/B MN-major flags (bits 15, 16), N >> 3 (bits
     // 17-22), M >> 4 (bits 24-28); M is 256 for the pair form.
@@ -513,6 +553,7 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     pub.swap_ab = swap;
     pub.pair = pair;
     pub.a_tma = ca.tma, pub.a_mn_major = ca.mn, pub.b_tma = cb.tma, pub.b_mn_major = cb.mn, pub.c_tma = c_tma;
+    pub.a_box3d = a_3d && ca.tma, pub.b_box3d = b_3d && cb.tma;
     pub.tile_m = tile_rows, pub.tile_n = BN, pub.tiles_m = tiles_m, pub.tiles_n = tiles_n;
     pub.splits = splits, pub.kblocks = kblocks, pub.grid = grid;
     pub.units = static_cast<int>(tiles * splits);
@@ -798,7 +839,8 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
 
 gemm_f16_status gemm_f16_set_option(int option, int64_t value)
 {
-    if (option < 1 || option > 10 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option < 1 || option > 11 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option == GEMM_F16_OPT_MAX_STAGES && value == 1) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_TAIL_SPLIT && value > 1) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_STREAMK && value > 2) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_PAIR && value > 2) return GEMM_F16_ERR_INVALID_VALUE;

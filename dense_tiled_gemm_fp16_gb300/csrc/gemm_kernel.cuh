@@ -67,7 +67,11 @@ constexpr uint32_t kEpiBytes = 4 * 2 * kEpiBufBytes;     // 4 warps, double-buff
 constexpr uint32_t kBarrierBytes = 512;
 constexpr int kStatusTimeout = 6;
 
-enum : uint32_t { kOpTma = 1u, kOpMnMajor = 2u };
+// Operand flags.  kOpBox3d: an MN-major TMA operand whose MN extent is a
+// multiple of 64 is described as a 3-D tensor (64 MN elements, K, MN / 64
+// swizzle-atom columns), so that one copy brings every atom column of a stage
+// instead of one copy per 64-wide column.
+enum : uint32_t { kOpTma = 1u, kOpMnMajor = 2u, kOpBox3d = 4u };
 
 struct KernelParams {
     CUtensorMap tmA;   // A' (K-major: dims {K, M}; MN-major: dims {M, K})
@@ -86,6 +90,7 @@ struct KernelParams {
     uint64_t timeout_ns;
     int tiles_m, tiles_n, splits, kblocks, num_units, panel, BN, stages;
     uint32_t a_flags, b_flags, c_tma, idesc, tx_bytes, stage_b_bytes, full_count;
+    uint32_t epi_smem;   // 1: reserve the 32 KB epilogue buffer (TMA-store staging, fixup landing zone)
     // Work decomposition.  `workers` persistent CTAs (single form) or clusters
     // (pair form).  Worker c first takes the whole-tile (or classic split-K)
     // units c, c+workers, ... < num_units; then, if sk_iters > 0, the
@@ -94,7 +99,7 @@ struct KernelParams {
     int workers;
     int sk_tile0;
     int64_t sk_iters;
-    int nseg_max;       // most segments one worker's stream-K range can hold
+    int nseg_max;       // most units that cover one stream-K tile (slots per stream-K tile)
     int sk_slot_base;   // first partial slot of the stream-K segments
     // Tail split: whole tiles from tail_tile0 on are cut along N into
     // tail_split units of BN / tail_split columns, so that a last partial wave
@@ -113,18 +118,19 @@ __device__ __forceinline__ SmemLayout smem_layout(const KernelParams& p, uint32_
     s.a = base;
     s.b = s.a + p.stages * kStageABytes;
     s.epi = s.b + p.stages * p.stage_b_bytes;
-    s.bars = s.epi + (p.c_tma ? kEpiBytes : 0u);
+    s.bars = s.epi + (p.epi_smem ? kEpiBytes : 0u);
     return s;
 }
 
 // Barrier block: full[16], empty[16], tmem_full[2], tmem_empty[2], drain,
-// then the TMEM base address, the abort flag and broadcast words.
+// fixup[4], then the TMEM base address, the abort flag and broadcast words.
 __device__ __forceinline__ uint32_t bar_full(uint32_t bars, int s) { return bars + 8u * s; }
 __device__ __forceinline__ uint32_t bar_empty(uint32_t bars, int s) { return bars + 8u * (kMaxStages + s); }
 __device__ __forceinline__ uint32_t bar_tfull(uint32_t bars, int a) { return bars + 8u * (2 * kMaxStages + a); }
 __device__ __forceinline__ uint32_t bar_tempty(uint32_t bars, int a) { return bars + 8u * (2 * kMaxStages + 2 + a); }
 __device__ __forceinline__ uint32_t bar_drain(uint32_t bars) { return bars + 8u * (2 * kMaxStages + 4); }
-constexpr uint32_t kTmemSlotOff = 8u * (2 * kMaxStages + 5);
+__device__ __forceinline__ uint32_t bar_fix(uint32_t bars, int b) { return bars + 8u * (2 * kMaxStages + 5 + b); }
+constexpr uint32_t kTmemSlotOff = 8u * (2 * kMaxStages + 9);
 constexpr uint32_t kAbortOff = kTmemSlotOff + 4;
 constexpr uint32_t kFlagOff = kTmemSlotOff + 8;
 constexpr uint32_t kOkOff = kTmemSlotOff + 12;   // two words, indexed by accumulator
@@ -136,6 +142,8 @@ constexpr uint64_t kDrainTimeoutNs = 10000000ull;
 // tile, and the last of them to finish adds all partials in K order.
 struct Unit {
     int tile, m_blk, n_blk, kb0, kb1, slot, expected;
+    int seg;     // index of this unit among the units covering its tile, in K order
+    int slot0;   // slot of the tile's first unit: the idx-th (K order) one is slot0 + idx
     int bn;      // columns of this unit (BN, or BN / tail_split for a tail piece)
     int n_off;   // first column of this unit inside its tile
 };
@@ -193,7 +201,9 @@ __device__ __forceinline__ Unit unit_at(const KernelParams& p, int cid, int i)
 {
     Unit w;
     w.slot = -1;
+    w.slot0 = -1;
     w.expected = 1;
+    w.seg = 0;
     w.bn = p.BN;
     w.n_off = 0;
     const int nc = classic_units(p, cid);
@@ -212,8 +222,10 @@ __device__ __forceinline__ Unit unit_at(const KernelParams& p, int cid, int i)
             w.kb0 = static_cast<int>(static_cast<int64_t>(split) * p.kblocks / p.splits);
             w.kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * p.kblocks / p.splits);
             if (p.splits > 1) {
+                w.slot0 = w.tile * p.splits;
                 w.slot = u;
                 w.expected = p.splits;
+                w.seg = split;
             }
         }
     } else {
@@ -224,22 +236,15 @@ __device__ __forceinline__ Unit unit_at(const KernelParams& p, int cid, int i)
         w.kb1 = (t0 == (s1 - 1) / p.kblocks) ? static_cast<int>((s1 - 1) % p.kblocks) + 1 : p.kblocks;
         w.tile = p.sk_tile0 + static_cast<int>(t0);
         if (w.kb0 != 0 || w.kb1 != p.kblocks) {
-            w.slot = p.sk_slot_base + cid * p.nseg_max + j;
-            w.expected = sk_worker(p, t0 * p.kblocks + p.kblocks - 1) - sk_worker(p, t0 * p.kblocks) + 1;
+            const int first = sk_worker(p, t0 * p.kblocks);
+            w.expected = sk_worker(p, t0 * p.kblocks + p.kblocks - 1) - first + 1;
+            w.seg = cid - first;
+            w.slot0 = p.sk_slot_base + static_cast<int>(t0) * p.nseg_max;
+            w.slot = w.slot0 + w.seg;
         }
     }
     tile_coords(p, w.tile, w.m_blk, w.n_blk);
     return w;
-}
-
-// Partial slot of the idx-th (in K order) unit that covers a cut tile.
-__device__ __forceinline__ int tile_slot(const KernelParams& p, int tile, int idx)
-{
-    if (tile < p.sk_tile0 || p.sk_iters == 0) return tile * p.splits + idx;
-    const int64_t t0 = tile - p.sk_tile0;
-    const int c = sk_worker(p, t0 * p.kblocks) + idx;
-    const int j = static_cast<int>(t0 - sk_start(p, c) / p.kblocks);
-    return p.sk_slot_base + c * p.nseg_max + j;
 }
 
 __device__ __forceinline__ void raise_abort(const KernelParams& p, volatile int* abort)
@@ -413,6 +418,148 @@ __device__ __forceinline__ void convert16(const uint32_t* r, uint32_t* h)
     for (int i = 0; i < 8; ++i) h[i] = pack_half2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
 }
 
+// Epilogue of a unit whose tile is cut along K (split-K or stream-K), run by
+// the 128 epilogue threads.  This unit's fp32 sum is a partial.  The last unit
+// of the tile to finish adds all partials in K order (deterministic) and stores
+// C; the others leave their partial in the workspace.  The accumulator stays in
+// TMEM until the decision, so the last one takes its own values from TMEM.
+template <bool kPair>
+__device__ __forceinline__ void cut_tile_epilogue(const KernelParams& p, const SmemLayout& L, const Unit& w,
+                                               uint32_t taddr, uint32_t tempty, int64_t m0, int64_t n0,
+                                               volatile int* flag, volatile int* abort, uint32_t& fix_ph)
+{
+    const int lane = threadIdx.x & 31;
+    const int row = 32 * ((threadIdx.x >> 5) & 3) + lane;
+    constexpr int kRanks = kPair ? 2 : 1;
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+    const size_t slot_elems = static_cast<size_t>(kBM) * p.BN;   // one CTA's 128 rows of a tile
+    int* counter = p.counters + static_cast<size_t>(w.tile) * kRanks + rank;
+    const bool lead = threadIdx.x == kEpiWarp0 * 32;
+    // Everyone else already in?  Then this unit is last and skips its
+    // own write.  (The acquire makes their partials visible.)
+    if (lead) *flag = (ld_acquire_gpu(counter) == w.expected - 1) ? 1 : 0;
+    named_bar_sync(1, 128);
+    int last = *flag;
+    if (!last) {
+        // Partial layout [column/4][row][4] floats: a warp's 32 rows
+        // store 512 contiguous bytes per float4 store.
+        float* slot = p.ws + (static_cast<size_t>(w.slot) * kRanks + rank) * slot_elems;
+        float* dst = slot + row * 4;
+        for (int c0 = 0; c0 < w.bn; c0 += 32) {
+            const int cnt = min(2, (w.bn - c0) / 16);
+            uint32_t r[32];
+            tmem_ld_x16(taddr + c0, r);
+            if (cnt > 1) tmem_ld_x16(taddr + c0 + 16, r + 16);
+            tmem_wait_ld();
+#pragma unroll
+            for (int g4 = 0; g4 < 8; ++g4)
+                if (g4 < 4 * cnt)
+                    st_global_v4(dst + static_cast<size_t>(c0 / 4 + g4) * (kBM * 4), __uint_as_float(r[4 * g4]),
+                                 __uint_as_float(r[4 * g4 + 1]), __uint_as_float(r[4 * g4 + 2]),
+                                 __uint_as_float(r[4 * g4 + 3]));
+        }
+        // The barrier orders every thread's stores before the leader's
+        // device-scope release.
+        named_bar_sync(1, 128);
+        if (lead) *flag = (atom_add_acq_rel_gpu(counter, 1) == w.expected - 1) ? 1 : 0;
+        named_bar_sync(1, 128);
+        last = *flag;
+    }
+    if (!last) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+            if (kPair)
+                mbar_arrive_cluster(tempty);
+            else
+                mbar_arrive(tempty);
+        }
+    } else {
+        if (lead) st_relaxed_gpu(counter, 0);   // ready for the next call
+        // The other partials stream through the 32 KB epilogue buffer in
+        // 8 KB pieces (16 columns of one partial) by TMA bulk copies, four
+        // buffers deep; pieces go in (column chunk, K order).
+        if (lane == 0) bulk_wait_group_read<0>();   // TMA stores done reading it
+        named_bar_sync(1, 128);
+        const int others = w.expected - 1;
+        const int total = (w.bn / 16) * others;
+        auto issue = [&](int t) {
+            const int c = t / others, j = t - c * others;
+            const int idx = j < w.seg ? j : j + 1;   // K-order index, own one skipped
+            const size_t sl = static_cast<size_t>(w.slot0 + idx) * kRanks + rank;
+            const float* src = p.ws + sl * slot_elems + static_cast<size_t>(c) * (4 * kBM * 4);
+            const int b = t & 3;
+            fence_proxy_async_smem();   // earlier generic reads of buffer b come first
+            mbar_arrive_expect_tx(bar_fix(L.bars, b), 8192);
+            bulk_load(L.epi + b * 8192, src, 8192, bar_fix(L.bars, b));
+        };
+        if (lead)
+            for (int t0 = 0; t0 < 3 && t0 < total; ++t0) issue(t0);
+        int t = 0;
+        bool ok = true;
+        for (int c0 = 0; c0 < w.bn; c0 += 16) {
+            uint32_t own[16];
+            tmem_ld_x16(taddr + c0, own);
+            tmem_wait_ld();
+            if (c0 + 16 >= w.bn) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (kPair)
+                        mbar_arrive_cluster(tempty);
+                    else
+                        mbar_arrive(tempty);
+                }
+            }
+            float sacc[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) sacc[c] = 0.f;
+            for (int idx = 0; idx < w.expected; ++idx) {
+                if (idx == w.seg) {
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) sacc[c] += __uint_as_float(own[c]);
+                    continue;
+                }
+                const int b = t & 3;
+                // One thread keeps three pieces in flight and waits for this
+                // one; the barrier hands the data (and the verdict) over.
+                if (lead) {
+                    if (t + 3 < total) issue(t + 3);   // its buffer was freed by the last barrier
+                    const bool got = mbar_wait(bar_fix(L.bars, b), (fix_ph >> b) & 1u, abort, p.timeout_ns);
+                    if (!got) raise_abort(p, abort);
+                    *flag = got ? 1 : 0;
+                }
+                named_bar_sync(1, 128);
+                ok = *flag != 0;
+                if (!ok) break;
+                fix_ph ^= 1u << b;
+                const uint32_t src = L.epi + b * 8192 + row * 16;
+#pragma unroll
+                for (int g4 = 0; g4 < 4; ++g4) {
+                    const float4 v = ld_smem_f4(src + g4 * (kBM * 16));
+                    sacc[4 * g4] += v.x;
+                    sacc[4 * g4 + 1] += v.y;
+                    sacc[4 * g4 + 2] += v.z;
+                    sacc[4 * g4 + 3] += v.w;
+                }
+                ++t;
+                named_bar_sync(1, 128);   // buffer b free for piece t + 3
+            }
+            if (!ok) break;
+            uint32_t h[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) h[i] = pack_half2(sacc[2 * i], sacc[2 * i + 1]);
+            store_piece_masked(p, m0 + row, n0 + c0, h);
+        }
+        if (!ok && lead) {
+            // gave up on piece t: let it and the (up to three) copies issued
+            // after it land (bounded) before the CTA can exit
+            for (int u2 = t; u2 < total && u2 < t + 4; ++u2)
+                mbar_wait(bar_fix(L.bars, u2 & 3), (fix_ph >> (u2 & 3)) & 1u, nullptr, kDrainTimeoutNs);
+        }
+    }
+}
+
 template <bool kPair>
 __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __grid_constant__ KernelParams p)
 {
@@ -430,6 +577,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
     const int lane = threadIdx.x & 31;
     const bool a_tma = p.a_flags & kOpTma, b_tma = p.b_flags & kOpTma;
     const bool a_mn = p.a_flags & kOpMnMajor, b_mn = p.b_flags & kOpMnMajor;
+    const bool a_3d = p.a_flags & kOpBox3d, b_3d = p.b_flags & kOpBox3d;
     const uint32_t rank = kPair ? cluster_ctarank() : 0u;
     const bool leader = (rank == 0);
     const int cid = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
@@ -445,6 +593,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
             mbar_init(bar_tempty(L.bars, a), kPair ? 8 : 4);
         }
         mbar_init(bar_drain(L.bars), 1);
+        for (int b = 0; b < 4; ++b) mbar_init(bar_fix(L.bars, b), 1);
         *abort = 0;
         *flag = 0;
         fence_mbarrier_init();
@@ -485,8 +634,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                 const int64_t m0 = static_cast<int64_t>(w.m_blk) * kTileRows + rank * kBM;
                 const int64_t n0 = static_cast<int64_t>(w.n_blk) * p.BN + w.n_off + rank * bcols;
                 // Bytes one stage of this unit brings in: MN-major B comes in
-                // 64-column boxes, K-major B in one box of the full tile width.
-                const uint32_t b_bytes = b_mn ? static_cast<uint32_t>(bcols) * 128u : p.stage_b_bytes;
+                // 64-column boxes (or one 3-D box of the full stage width),
+                // K-major B in one box of the full tile width.
+                const uint32_t b_bytes = (b_mn && !b_3d) ? static_cast<uint32_t>(bcols) * 128u : p.stage_b_bytes;
                 const uint32_t tx = kPair ? 2u * (kStageABytes + b_bytes)
                                           : (a_tma ? kStageABytes : 0u) + (b_tma ? b_bytes : 0u);
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -507,12 +657,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                             const uint32_t fbc = mapa_shared(fb, 0);
                             if (!a_mn) {
                                 tma_load_2d_pair(sa, &p.tmA, k0, static_cast<int32_t>(m0), fbc);
+                            } else if (a_3d) {
+                                tma_load_3d_pair(sa, &p.tmA, 0, k0, static_cast<int32_t>(m0 >> 6), fbc);
                             } else {
                                 tma_load_2d_pair(sa, &p.tmA, static_cast<int32_t>(m0), k0, fbc);
                                 tma_load_2d_pair(sa + 8192, &p.tmA, static_cast<int32_t>(m0 + 64), k0, fbc);
                             }
                             if (!b_mn) {
                                 tma_load_2d_pair(sb, &p.tmB, k0, static_cast<int32_t>(n0), fbc);
+                            } else if (b_3d) {
+                                tma_load_3d_pair(sb, &p.tmB, 0, k0, static_cast<int32_t>(n0 >> 6), fbc);
                             } else {
                                 for (int j = 0; j < bcols / 64; ++j)
                                     tma_load_2d_pair(sb + j * 8192, &p.tmB, static_cast<int32_t>(n0 + 64 * j), k0, fbc);
@@ -522,6 +676,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                             if (a_tma) {
                                 if (!a_mn) {
                                     tma_load_2d(sa, &p.tmA, k0, static_cast<int32_t>(m0), fb);
+                                } else if (a_3d) {
+                                    tma_load_3d(sa, &p.tmA, 0, k0, static_cast<int32_t>(m0 >> 6), fb);
                                 } else {
                                     tma_load_2d(sa, &p.tmA, static_cast<int32_t>(m0), k0, fb);
                                     tma_load_2d(sa + 8192, &p.tmA, static_cast<int32_t>(m0 + 64), k0, fb);
@@ -530,6 +686,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                             if (b_tma) {
                                 if (!b_mn) {
                                     tma_load_2d(sb, &p.tmB, k0, static_cast<int32_t>(n0), fb);
+                                } else if (b_3d) {
+                                    tma_load_3d(sb, &p.tmB, 0, k0, static_cast<int32_t>(n0 >> 6), fb);
                                 } else {
                                     for (int j = 0; j < bcols / 64; ++j)
                                         tma_load_2d(sb + j * 8192, &p.tmB, static_cast<int32_t>(n0 + 64 * j), k0, fb);
@@ -648,9 +806,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t group_count = 0;
+        uint32_t fix_ph = 0u;   // bit b: parity of the next phase of fixup barrier b (b < 4)
         const int nu = units_of_worker(p, cid);
-        constexpr int kRanks = kPair ? 2 : 1;
-        const size_t slot_elems = static_cast<size_t>(kBM) * p.BN;   // one CTA's 128 rows of a tile
         for (int ui = 0; ui < nu; ++ui) {
             const Unit w = unit_at(p, cid, ui);
             const int64_t m0 = static_cast<int64_t>(w.m_blk) * kTileRows + rank * kBM;
@@ -721,77 +878,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                     }
                 }
             } else {
-                // A cut tile: write this segment's fp32 partial, column-major
-                // inside the slot so that a warp's 32 rows form one 128-byte line.
-                float* slot = p.ws + (static_cast<size_t>(w.slot) * kRanks + rank) * slot_elems;
-                for (int pc = 0; pc < npieces; ++pc) {
-                    uint32_t r[16];
-                    tmem_ld_x16(taddr + 16 * pc, r);
-                    tmem_wait_ld();
-                    if (pc == npieces - 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) {
-                            if (kPair)
-                                mbar_arrive_cluster(tempty);
-                            else
-                                mbar_arrive(tempty);
-                        }
-                    }
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) slot[(16 * pc + c) * kBM + row] = __uint_as_float(r[c]);
-                }
-                // Publish the partial and count this segment in: the epilogue
-                // threads' stores are ordered before the leader's release by the
-                // barrier; its acquire makes the other segments' partials visible
-                // (to all epilogue threads through the second barrier).  One
-                // device-scope atomic per unit, no per-thread fences.
-                named_bar_sync(1, 128);
-                int* counter = p.counters + static_cast<size_t>(w.tile) * kRanks + rank;
-                if (threadIdx.x == kEpiWarp0 * 32) {
-                    const int old = atom_add_acq_rel_gpu(counter, 1);
-                    const int last = (old == w.expected - 1) ? 1 : 0;
-                    if (last) st_relaxed_gpu(counter, 0);   // ready for the next call
-                    *flag = last;
-                }
-                named_bar_sync(1, 128);
-                if (*flag) {
-                    for (int pc = 0; pc < npieces; ++pc) {
-                        float s[16];
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) s[c] = 0.f;
-                        // The tile's partials are added in K order (deterministic);
-                        // the loads of two partials are issued before their adds.
-                        int sp = 0;
-                        for (; sp + 1 < w.expected; sp += 2) {
-                            const float* s0 = p.ws +
-                                              (static_cast<size_t>(tile_slot(p, w.tile, sp)) * kRanks + rank) * slot_elems +
-                                              (16 * pc) * kBM + row;
-                            const float* s1 = p.ws +
-                                              (static_cast<size_t>(tile_slot(p, w.tile, sp + 1)) * kRanks + rank) * slot_elems +
-                                              (16 * pc) * kBM + row;
-                            float x0[16], x1[16];
-#pragma unroll
-                            for (int c = 0; c < 16; ++c) {
-                                x0[c] = ld_cg_f32(s0 + c * kBM);
-                                x1[c] = ld_cg_f32(s1 + c * kBM);
-                            }
-#pragma unroll
-                            for (int c = 0; c < 16; ++c) s[c] = (s[c] + x0[c]) + x1[c];
-                        }
-                        if (sp < w.expected) {
-                            const float* s0 = p.ws +
-                                              (static_cast<size_t>(tile_slot(p, w.tile, sp)) * kRanks + rank) * slot_elems +
-                                              (16 * pc) * kBM + row;
-#pragma unroll
-                            for (int c = 0; c < 16; ++c) s[c] += ld_cg_f32(s0 + c * kBM);
-                        }
-                        uint32_t h[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) h[i] = pack_half2(s[2 * i], s[2 * i + 1]);
-                        store_piece_masked(p, m0 + row, n0 + 16 * pc, h);
-                    }
-                }
+                cut_tile_epilogue<kPair>(p, L, w, taddr, tempty, m0, n0, flag, abort, fix_ph);
             }
             if (++acc == 2) {
                 acc = 0;

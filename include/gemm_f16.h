@@ -173,6 +173,7 @@ typedef struct {
     int tail_split;     /* trailing partial wave of tiles cut along N into this many pieces */
     int smem_bytes;
     size_t workspace_bytes;
+    int a_box3d, b_box3d;   /* MN-major TMA operand read as one 3-D box per stage */
 } gemm_f16_plan;
 
 /* Fill *plan for the given arguments without launching anything.  Returns the
@@ -198,6 +199,8 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
  *                              the tiles do not divide evenly over the SMs
  *   GEMM_F16_OPT_TAIL_SPLIT    0 default: cut the last partial wave of tiles along N
  *                              into narrower tiles; 1 never
+ *   GEMM_F16_OPT_MAX_STAGES    >= 2: cap the pipeline depth (default: as many stages
+ *                              as shared memory holds, at most 16)
  * A value of 0 restores the default.  Returns GEMM_F16_ERR_INVALID_VALUE for an
  * unknown option or a value out of range.
  */
@@ -211,7 +214,8 @@ enum {
     GEMM_F16_OPT_MAX_CTAS = 7,
     GEMM_F16_OPT_PAIR = 8,
     GEMM_F16_OPT_STREAMK = 9,
-    GEMM_F16_OPT_TAIL_SPLIT = 10
+    GEMM_F16_OPT_TAIL_SPLIT = 10,
+    GEMM_F16_OPT_MAX_STAGES = 11
 };
 gemm_f16_status gemm_f16_set_option(int option, int64_t value);
 

@@ -25,7 +25,7 @@ DEV = torch.device("cuda:0")
 def _defaults():
     yield
     for o in (g.OPT_FORCE_GATHER, g.OPT_SPLITS, g.OPT_TILE_N, g.OPT_PANEL, g.OPT_SWAP,
-              g.OPT_TIMEOUT_MS, g.OPT_MAX_CTAS, g.OPT_PAIR, g.OPT_STREAMK, g.OPT_TAIL_SPLIT):
+              g.OPT_TIMEOUT_MS, g.OPT_MAX_CTAS, g.OPT_PAIR, g.OPT_STREAMK, g.OPT_TAIL_SPLIT, g.OPT_MAX_STAGES):
         g.gemm_f16_set_option(o, 0)
 
 
@@ -162,6 +162,35 @@ def test_mn_major_a_and_k_major_b_through_tma():
     plan = g.plan_for(A, B, out)
     assert plan["a_tma"] and plan["a_mn_major"] and plan["b_tma"] and not plan["b_mn_major"]
     assert_close(host(gpu(A, B)), oracle.gemm(Ah, Bh), 256, "mn-major A, k-major B")
+
+
+# MN-major TMA operands whose MN extent is a multiple of 64 are read with one
+# 3-D box per stage (all swizzle-atom columns at once); the others with one 2-D
+# box per atom column.  Atom columns past the edge of the view must come in as
+# zeros, never as the neighbouring elements of memory.
+BOX_CASES = [
+    # (M, N, K, layout A, layout B, pair option, expected a_box3d, b_box3d)
+    (300, 320, 200, "row", "row", 0, 0, 1),       # pair; last tile holds one valid atom column
+    (384, 136, 200, "col", "row", 0, 1, 0),       # M-major A in 3-D; N % 64 != 0 keeps B in 2-D
+    (200, 576, 216, "row", "row", 1, 0, 1),       # single CTA, four atom columns per box
+    (640, 512, 96, "col", "row", 0, 1, 1),        # pair; both operands in 3-D
+    (32, 1024, 200, "row", "row", 0, 1, 0),       # swapped: B^T is the M-major kernel A
+]
+
+
+@pytest.mark.parametrize("case", BOX_CASES, ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}-{c[3]}-{c[4]}-pair{c[5]}")
+def test_mn_major_box_forms_bit_exact(case):
+    M, N, K, la, lb, pair, a3, b3 = case
+    rng = np.random.default_rng(M * 7 + N + K)
+    Ah = rng.integers(-3, 4, (M, K)).astype(np.float16)
+    Bh = rng.integers(-3, 4, (K, N)).astype(np.float16)
+    A, B = make_view(Ah, la), make_view(Bh, lb)
+    out = torch.empty((M, N), dtype=torch.float16, device=DEV)
+    g.gemm_f16_set_option(g.OPT_PAIR, pair)
+    plan = g.plan_for(A, B, out)
+    assert (plan["a_box3d"], plan["b_box3d"]) == (a3, b3), plan
+    assert_bits(host(gpu(A, B, out=out)), oracle.gemm(Ah, Bh, threads=oracle_threads()), f"boxes {case}")
+    assert g.gemm_f16_device_status() == 0
 
 
 # ------------------------------------------------------------ pair tiles
