@@ -59,6 +59,13 @@ constexpr int kMaxStages = 16;
 constexpr int kNumThreads = 288;         // 9 warps
 constexpr int kEpiWarp0 = 4;
 constexpr int kMmaWarp = 8;
+// Threads that wait on barriers for long stretches sit on SM sub-partitions
+// other than the MMA issuer's (warp 8 shares sub-partition 0 with warps 0
+// and 4): the TMA-issuing producer thread is lane 0 of warp 1 (when no operand
+// is gathered) and the epilogue thread that waits for accumulators is lane 0
+// of warp 5.
+constexpr int kTmaThread = 32;
+constexpr int kEpiLead = (kEpiWarp0 + 1) * 32;
 constexpr uint32_t kTmemCols = 512;      // two accumulators of up to 256 columns
 constexpr uint32_t kAccStride = 256;
 constexpr uint32_t kStageABytes = kBM * kBK * 2;        // 16 KiB
@@ -434,7 +441,7 @@ __device__ __forceinline__ void cut_tile_epilogue(const KernelParams& p, const S
     const uint32_t rank = kPair ? cluster_ctarank() : 0u;
     const size_t slot_elems = static_cast<size_t>(kBM) * p.BN;   // one CTA's 128 rows of a tile
     int* counter = p.counters + static_cast<size_t>(w.tile) * kRanks + rank;
-    const bool lead = threadIdx.x == kEpiWarp0 * 32;
+    const bool lead = threadIdx.x == kEpiLead;
     // Everyone else already in?  Then this unit is last and skips its
     // own write.  (The acquire makes their partials visible.)
     if (lead) *flag = (ld_acquire_gpu(counter) == w.expected - 1) ? 1 : 0;
@@ -622,7 +629,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
         // ------------------------------------------------------------ producers
         const int t = threadIdx.x;
         const bool any_masked = !a_tma || !b_tma;
-        if (t == 0 || any_masked) {
+        const int tiss = any_masked ? 0 : kTmaThread;   // the thread that issues TMA copies
+        if (t == tiss || any_masked) {
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -649,7 +657,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                     const uint32_t sb = L.b + stage * p.stage_b_bytes;
                     const uint32_t fb = bar_full(L.bars, stage);
                     const int32_t k0 = kb * kBK;
-                    if (t == 0 && (a_tma || b_tma)) {
+                    if (t == tiss && (a_tma || b_tma)) {
                         if (kPair) {
                             // The leader expects both CTAs' bytes on its own barrier;
                             // the peer's copies complete on the leader's barrier.
@@ -710,7 +718,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                     }
                 }
             }
-            if (!ok && t == 0 && (a_tma || b_tma) && (!kPair || leader)) {
+            if (!ok && t == tiss && (a_tma || b_tma) && (!kPair || leader)) {
                 // Let TMA copies already in flight land before the CTA exits:
                 // wait (bounded) on the full barrier of each recently issued stage.
                 const int n = issued < p.stages ? issued : p.stages;
@@ -816,7 +824,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
             // One thread waits for the accumulator and tells the other epilogue
             // threads, so that they all leave together on an abort (the named
             // barriers below must see all 128 threads).
-            if (threadIdx.x == kEpiWarp0 * 32) {
+            if (threadIdx.x == kEpiLead) {
                 const bool ok = wait_bar<kPair>(bar_tfull(L.bars, acc), acc_phase, abort, p.timeout_ns);
                 if (!ok) raise_abort(p, abort);
                 okflag[acc] = ok ? 1 : 0;

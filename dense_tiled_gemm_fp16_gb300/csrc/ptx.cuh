@@ -45,15 +45,22 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// A waiting thread is suspended by the hardware until the phase completes or
+// this many nanoseconds pass.  Without the hint try_wait returns at once and
+// the wait loop spins, taking issue slots from the warps that share the SM
+// sub-partition (the MMA issuer among them): measured on 8192^3, the hint
+// cut the cycles per K block by a fifth.
+constexpr uint32_t kSuspendHintNs = 200000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return ok != 0;
 }
@@ -65,13 +72,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    uint32_t it = 0;
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((++it & 31u) == 0) {
-            if (abort && *abort) return false;
-            if (globaltimer_ns() - t0 > timeout_ns) return false;
-        }
+        if (mbar_try_wait(bar, parity)) return true;   // suspends for up to kSuspendHintNs
+        if (abort && *abort) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
     }
 }
 
@@ -106,10 +110,10 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return ok != 0;
 }
@@ -121,13 +125,10 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
 {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    uint32_t it = 0;
     while (true) {
         if (mbar_try_wait_cluster(bar, parity)) return true;
-        if ((++it & 31u) == 0) {
-            if (abort && *abort) return false;
-            if (globaltimer_ns() - t0 > timeout_ns) return false;
-        }
+        if (abort && *abort) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
     }
 }
 
