@@ -42,6 +42,7 @@ OPT_PAIR = 8
 OPT_STREAMK = 9
 OPT_TAIL_SPLIT = 10
 OPT_MAX_STAGES = 11
+OPT_MULTICAST = 12
 
 # Every symbol include/gemm_f16.h declares.
 EXPORTED = ("gemm_f16", "gemm_f16_ws", "gemm_f16_workspace_size", "gemm_f16_status_string",
@@ -63,7 +64,7 @@ class Plan(ctypes.Structure):
         "swap_ab", "pair", "a_tma", "a_mn_major", "b_tma", "b_mn_major", "c_tma",
         "tile_m", "tile_n", "tiles_m", "tiles_n", "splits", "kblocks", "units", "grid",
         "stages", "streamk_tiles", "tail_split", "smem_bytes")] + [("workspace_bytes", ctypes.c_size_t)] + [
-        (n, ctypes.c_int) for n in ("a_box3d", "b_box3d")]
+        (n, ctypes.c_int) for n in ("a_box3d", "b_box3d", "cluster_ctas")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

@@ -31,8 +31,10 @@ struct DevInfo {
     int sms = 0;
     int* status_ptr = nullptr;
     bool smem_attr_set = false;
-    int pair_smem = -1;       // cached max_pair_clusters() result for this smem size
+    int pair_smem = -1;       // cached max_clusters() results for this smem size
     int pair_clusters = 0;
+    int quad_smem = -1;
+    int quad_clusters = 0;
 };
 
 std::mutex g_mutex;
@@ -49,7 +51,7 @@ struct Workspace {
 };
 Workspace g_ws[kMaxDevices];
 
-std::atomic<int64_t> g_opt[12];
+std::atomic<int64_t> g_opt[13];
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 PFN_cuMemGetAddressRange_v3020 g_addr_range = nullptr;
@@ -247,10 +249,12 @@ bool set_smem_attributes(DevInfo& dev)
 {
     std::lock_guard<std::mutex> lk(g_mutex);
     if (dev.smem_attr_set) return true;
-    if (cudaFuncSetAttribute(gemm_f16_dev::gemm_f16_persistent<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kMaxDynSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(gemm_f16_dev::gemm_f16_persistent<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kMaxDynSmem) != cudaSuccess) {
+    if (cudaFuncSetAttribute(gemm_f16_dev::gemm_f16_persistent<false, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_f16_dev::gemm_f16_persistent<true, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_f16_dev::gemm_f16_persistent<true, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
@@ -258,34 +262,43 @@ bool set_smem_attributes(DevInfo& dev)
     return true;
 }
 
-// How many 2-CTA clusters of the pair kernel can be resident at once (SMs are
-// paired within a GPC, so this can be less than half the SM count).
-int max_pair_clusters(DevInfo& dev, int smem)
+// How many clusters of `size` CTAs (2: pair form, 4: four-CTA multicast form)
+// can be resident at once.  Clusters must fit inside a GPC, so this can be less
+// than the SM count divided by the size.
+int max_clusters(DevInfo& dev, int smem, int size)
 {
     if (!set_smem_attributes(dev)) return 0;
     {
         std::lock_guard<std::mutex> lk(g_mutex);
-        if (dev.pair_smem == smem) return dev.pair_clusters;
+        if (size == 2 && dev.pair_smem == smem) return dev.pair_clusters;
+        if (size == 4 && dev.quad_smem == smem) return dev.quad_clusters;
     }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = size;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(2 * (dev.sms / 2));
+    cfg.gridDim = dim3(size * (dev.sms / size));
     cfg.blockDim = dim3(gemm_f16_dev::kNumThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_f16_dev::gemm_f16_persistent<true>, &cfg) != cudaSuccess) {
+    const cudaError_t e = size == 4 ? cudaOccupancyMaxActiveClusters(&n, gemm_f16_dev::gemm_f16_persistent<true, true>, &cfg)
+                                    : cudaOccupancyMaxActiveClusters(&n, gemm_f16_dev::gemm_f16_persistent<true, false>, &cfg);
+    if (e != cudaSuccess) {
         cudaGetLastError();
         n = 0;
     }
     std::lock_guard<std::mutex> lk(g_mutex);
-    dev.pair_smem = smem;
-    dev.pair_clusters = n;
+    if (size == 4) {
+        dev.quad_smem = smem;
+        dev.quad_clusters = n;
+    } else {
+        dev.pair_smem = smem;
+        dev.pair_clusters = n;
+    }
     return n;
 }
 
@@ -340,7 +353,7 @@ void tail_split(Schedule& s, int64_t tiles, int BN, int min_bn, int64_t W)
     s.workers = static_cast<int>(std::min<int64_t>(s.num_units, W));
 }
 
-Schedule make_schedule(int64_t tiles, int kblocks, int splits, int max_workers, int BN, int min_bn)
+Schedule make_schedule(int64_t tiles, int kblocks, int splits, int max_workers, int BN, int min_bn, bool streamk)
 {
     Schedule s;
     if (splits > 1) {
@@ -352,12 +365,10 @@ Schedule make_schedule(int64_t tiles, int kblocks, int splits, int max_workers, 
     s.num_units = static_cast<int>(tiles);
     s.workers = static_cast<int>(std::min<int64_t>(tiles, max_workers));
     const int64_t W = max_workers;
-    if (opt(GEMM_F16_OPT_STREAMK) != 2) {
+    if (!streamk) {
         tail_split(s, tiles, BN, min_bn, W);
         return s;
     }
-    // Stream-K is opt-in (GEMM_F16_OPT_STREAMK = 2): its fixup of cut tiles is
-    // not yet cheaper than the wave tail it removes on the measured shapes.
     if (tiles % W == 0) return s;
     const int64_t full = tiles / W;
     const int64_t sk_tiles = full >= 1 ? tiles % W + W : tiles;
@@ -460,6 +471,10 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     if (pair) tiles_m = static_cast<int>((Mv + tile_rows - 1) / tile_rows);
     const int64_t tiles = static_cast<int64_t>(tiles_m) * tiles_n;
     if (tiles * splits > INT32_MAX / 4 || tiles * kblocks > (int64_t(1) << 40)) return GEMM_F16_ERR_INVALID_VALUE;
+    // Four-CTA multicast form: two pairs on vertically adjacent tiles share each
+    // B tile (whole tiles only: no K cut, no tail split).
+    const int64_t mc_opt = opt(GEMM_F16_OPT_MULTICAST);
+    bool quad = pair && mc_opt == 2 && BN == 256 && splits == 1 && opt(GEMM_F16_OPT_STREAMK) != 2 && tiles_m >= 2;
 
     bool a_3d = false, b_3d = false;
     if (ca.tma) {
@@ -474,14 +489,19 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
             ca = choose_operand(kp.A, kp.a_sm, kp.a_sk, Mv, a.K, gemm_f16_dev::kBM, false);
         }
     }
-    if (cb.tma) {
+    // B's box: a CTA's whole share of the tile's columns, or in the four-CTA form
+    // the 64-column quarter it multicasts.
+    auto encode_b = [&](bool quarter) {
+        const int cols = quarter ? bcols / 2 : bcols;
         b_3d = cb.mn && encode_3d_mn(&kp.tmB, kp.B, Nv, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk,
-                                     static_cast<uint32_t>(bcols / 64));
-        const bool ok = b_3d ? true
-                        : cb.mn ? encode_2d(&kp.tmB, kp.B, Nv, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk, 64, 64)
-                              : encode_2d(&kp.tmB, kp.B, a.K, Nv, Nv == 1 ? round_up(2 * a.K, 16) : 2 * kp.b_sn, 64,
-                                          static_cast<uint32_t>(bcols));
-        if (!ok) {
+                                     static_cast<uint32_t>(cols / 64));
+        return b_3d ? true
+               : cb.mn ? encode_2d(&kp.tmB, kp.B, Nv, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk, 64, 64)
+                       : encode_2d(&kp.tmB, kp.B, a.K, Nv, Nv == 1 ? round_up(2 * a.K, 16) : 2 * kp.b_sn, 64,
+                                   static_cast<uint32_t>(cols));
+    };
+    if (cb.tma) {
+        if (!encode_b(quad)) {
             if (pair) return GEMM_F16_ERR_LAUNCH;
             cb = choose_operand(kp.B, kp.b_sn, kp.b_sk, Nv, a.K, BN, false);
         }
@@ -495,7 +515,12 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     const uint32_t stage_bytes = gemm_f16_dev::kStageABytes + stage_b;
     // The 32 KB epilogue buffer stages TMA stores of C, and is where the last
     // unit of a tile cut along K collects the other units' partials.
-    const bool may_cut = splits > 1 || opt(GEMM_F16_OPT_STREAMK) == 2;
+    // Stream-K: forced by GEMM_F16_OPT_STREAMK = 2, and the default when an
+    // operand is gathered (gathered tiles are slow, so balancing the last wave
+    // pays for the fixup); otherwise the last partial wave is split along N.
+    const int64_t sk_opt = opt(GEMM_F16_OPT_STREAMK);
+    const bool use_sk = splits == 1 && !quad && (sk_opt == 2 || (sk_opt == 0 && (!ca.tma || !cb.tma)));
+    const bool may_cut = splits > 1 || use_sk;
     const int epi = (c_tma || may_cut) ? static_cast<int>(gemm_f16_dev::kEpiBytes) : 0;
     int stages = (kMaxDynSmem - kSmemAlignSlack - epi - static_cast<int>(gemm_f16_dev::kBarrierBytes)) /
                  static_cast<int>(stage_bytes);
@@ -505,21 +530,35 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     const int smem = kSmemAlignSlack + stages * static_cast<int>(stage_bytes) + epi +
                      static_cast<int>(gemm_f16_dev::kBarrierBytes);
 
-    // Persistent workers: CTAs, or 2-CTA clusters in the pair form.
+    // Persistent workers: CTAs, or clusters (of 2 CTAs in the pair form, of 4 in
+    // the four-CTA form).
     const int64_t cap = opt(GEMM_F16_OPT_MAX_CTAS);
-    int64_t max_workers = pair ? max_pair_clusters(const_cast<DevInfo&>(dev), smem) : dev.sms;
-    if (cap > 0) max_workers = std::min<int64_t>(max_workers, pair ? std::max<int64_t>(1, cap / 2) : cap);
+    int64_t max_workers = dev.sms;
+    if (quad) {
+        max_workers = max_clusters(const_cast<DevInfo&>(dev), smem, 4);
+        if (max_workers < 1) {   // no four-CTA cluster fits: plain pairs
+            quad = false;
+            if (!encode_b(false)) return GEMM_F16_ERR_LAUNCH;
+        }
+    }
+    const int cluster_ctas = quad ? 4 : (pair ? 2 : 1);
+    if (pair && !quad) max_workers = max_clusters(const_cast<DevInfo&>(dev), smem, 2);
+    if (cap > 0) max_workers = std::min<int64_t>(max_workers, std::max<int64_t>(1, cap / cluster_ctas));
     if (max_workers < 1) return GEMM_F16_ERR_LAUNCH;
+    // Units of the four-CTA form cover two tile rows.
+    const int unit_rows = quad ? (tiles_m + 1) / 2 : tiles_m;
+    const int64_t unit_tiles = static_cast<int64_t>(unit_rows) * tiles_n;
     // Narrowest tail piece: the pair form keeps >= 64 B columns per CTA; a
-    // TMA-stored C needs whole 64-column boxes.
-    const Schedule sch = make_schedule(tiles, kblocks, splits, static_cast<int>(max_workers), BN, pair ? 128 : 64);
-    const int grid = pair ? 2 * sch.workers : sch.workers;
+    // TMA-stored C needs whole 64-column boxes; the four-CTA form never cuts.
+    const Schedule sch = make_schedule(unit_tiles, kblocks, splits, static_cast<int>(max_workers), BN,
+                                       quad ? 2 * BN : (pair ? 128 : 64), use_sk);
+    const int grid = cluster_ctas * sch.workers;
     const int64_t panel = opt(GEMM_F16_OPT_PANEL);
 
     kp.status = dev.status_ptr;
     const int64_t tmo = opt(GEMM_F16_OPT_TIMEOUT_MS);
     kp.timeout_ns = static_cast<uint64_t>(tmo > 0 ? tmo : 1000) * 1000000ull;
-    kp.tiles_m = tiles_m, kp.tiles_n = tiles_n, kp.splits = splits, kp.kblocks = kblocks;
+    kp.tiles_m = unit_rows, kp.tiles_n = tiles_n, kp.splits = splits, kp.kblocks = kblocks;
     kp.num_units = sch.num_units;
     kp.workers = sch.workers;
     kp.sk_tile0 = sch.sk_tile0;
@@ -528,6 +567,16 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     kp.sk_slot_base = sch.sk_slot_base;
     kp.tail_tile0 = sch.tail_tile0;
     kp.tail_split = sch.tail_split;
+    if (cb.tma && sch.tail_split > 1 && !(cb.mn && !b_3d)) {
+        // Tail pieces read B through a box of their own width (the 2-D N-major
+        // form already reads one 64-column box per atom column).
+        const int piece = bcols / sch.tail_split;
+        const bool ok = b_3d ? encode_3d_mn(&kp.tmB2, kp.B, Nv, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk,
+                                            static_cast<uint32_t>(piece / 64))
+                             : encode_2d(&kp.tmB2, kp.B, a.K, Nv, Nv == 1 ? round_up(2 * a.K, 16) : 2 * kp.b_sn, 64,
+                                         static_cast<uint32_t>(piece));
+        if (!ok) return GEMM_F16_ERR_LAUNCH;
+    }
     kp.panel = static_cast<int>(panel > 0 ? panel : 8);
     kp.BN = BN, kp.stages = stages;
     kp.a_flags = (ca.tma ? gemm_f16_dev::kOpTma : 0u) | (ca.mn ? gemm_f16_dev::kOpMnMajor : 0u) |
@@ -547,16 +596,18 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
         kp.full_count = 1u;
     } else {
         kp.tx_bytes = (ca.tma ? gemm_f16_dev::kStageABytes : 0u) + (cb.tma ? stage_b : 0u);
-        kp.full_count = ((ca.tma || cb.tma) ? 1u : 0u) + ((!ca.tma || !cb.tma) ? 128u : 0u);
+        kp.full_count = ((ca.tma || cb.tma) ? 1u : 0u) +
+                        ((!ca.tma || !cb.tma) ? static_cast<uint32_t>(gemm_f16_dev::kProducerThreads) : 0u);
     }
 
     pub.swap_ab = swap;
     pub.pair = pair;
+    pub.cluster_ctas = cluster_ctas;
     pub.a_tma = ca.tma, pub.a_mn_major = ca.mn, pub.b_tma = cb.tma, pub.b_mn_major = cb.mn, pub.c_tma = c_tma;
     pub.a_box3d = a_3d && ca.tma, pub.b_box3d = b_3d && cb.tma;
     pub.tile_m = tile_rows, pub.tile_n = BN, pub.tiles_m = tiles_m, pub.tiles_n = tiles_n;
     pub.splits = splits, pub.kblocks = kblocks, pub.grid = grid;
-    pub.units = static_cast<int>(tiles * splits);
+    pub.units = static_cast<int>(quad ? unit_tiles : tiles * splits);
     pub.streamk_tiles = sch.sk_iters > 0 ? static_cast<int>(tiles - sch.sk_tile0) : 0;
     pub.tail_split = sch.tail_split;
     pub.stages = stages, pub.smem_bytes = smem;
@@ -574,13 +625,13 @@ gemm_f16_status launch(Plan& pl, DevInfo& dev, float* partials, int* counters, c
     kp.counters = counters;
     if (!set_smem_attributes(dev)) return GEMM_F16_ERR_LAUNCH;
     if (!pl.pub.pair) {
-        gemm_f16_dev::gemm_f16_persistent<false>
+        gemm_f16_dev::gemm_f16_persistent<false, false>
             <<<pl.pub.grid, gemm_f16_dev::kNumThreads, pl.pub.smem_bytes, stream>>>(kp);
     } else {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.x = pl.pub.cluster_ctas;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.gridDim = dim3(pl.pub.grid);
@@ -589,7 +640,10 @@ gemm_f16_status launch(Plan& pl, DevInfo& dev, float* partials, int* counters, c
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, gemm_f16_dev::gemm_f16_persistent<true>, kp) != cudaSuccess) {
+        const cudaError_t e = pl.pub.cluster_ctas == 4
+                                  ? cudaLaunchKernelEx(&cfg, gemm_f16_dev::gemm_f16_persistent<true, true>, kp)
+                                  : cudaLaunchKernelEx(&cfg, gemm_f16_dev::gemm_f16_persistent<true, false>, kp);
+        if (e != cudaSuccess) {
             cudaGetLastError();
             return GEMM_F16_ERR_LAUNCH;
         }
@@ -767,7 +821,10 @@ gemm_f16_status gemm_f16_workspace_size(int64_t M, int64_t N, int64_t K, size_t*
         const int64_t rows = pair ? 2 * gemm_f16_dev::kBM : gemm_f16_dev::kBM;
         const int64_t tiles = ((Mv + rows - 1) / rows) * tiles_n;
         const int workers = pair ? std::max(1, dev->sms / 2) : dev->sms;
-        const Schedule s = make_schedule(tiles, kblocks, splits, workers, BN, pair ? 128 : 64);
+        // the single form may gather an operand, which turns stream-K on by default
+        const int64_t sk = opt(GEMM_F16_OPT_STREAMK);
+        const bool streamk = splits == 1 && (sk == 2 || (sk == 0 && !pair));
+        const Schedule s = make_schedule(tiles, kblocks, splits, workers, BN, pair ? 128 : 64, streamk);
         if (s.partial_slots > 0)
             need = std::max(need, workspace_bytes_for(s.partial_slots, BN, tiles, pair ? 2 : 1, nullptr, nullptr));
     }
@@ -839,7 +896,8 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
 
 gemm_f16_status gemm_f16_set_option(int option, int64_t value)
 {
-    if (option < 1 || option > 11 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option < 1 || option > 12 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option == GEMM_F16_OPT_MULTICAST && value > 2) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_MAX_STAGES && value == 1) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_TAIL_SPLIT && value > 1) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_STREAMK && value > 2) return GEMM_F16_ERR_INVALID_VALUE;

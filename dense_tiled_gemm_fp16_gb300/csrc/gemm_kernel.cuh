@@ -14,12 +14,12 @@
 //                           per MMA cycle and fits deeper pipelines.  TMA
 //                           operands only, no split-K.
 //
-// Roles (9 warps):
-//   warps 0-3  producers.  Operands that TMA can address are loaded by one
+// Roles (8 warps; 256 threads leave each thread up to 255 registers):
+//   warps 0-2  producers.  Operands that TMA can address are loaded by one
 //              thread with cp.async.bulk.tensor into 128-byte-swizzled shared
 //              memory (out-of-range box elements arrive as zeros).  Operands
 //              TMA cannot address (unaligned base or pitch, non-unit inner
-//              stride) are gathered by all 128 threads with bounds-checked
+//              stride) are gathered by all 96 threads with bounds-checked
 //              loads, written in the same swizzled layout and published to the
 //              tensor core with fence.proxy.async.  Either way the K tail is
 //              zero-filled: an index past K is never wrapped back into range.
@@ -29,7 +29,7 @@
 //              or store with per-element bounds checks.  In split-K mode the
 //              fp32 partial goes to a workspace and the last CTA to finish a
 //              tile sums the partials in split order (deterministic).
-//   warp 8     TMEM allocation and the MMA issuer (one thread): 4 x
+//   warp 3     TMEM allocation and the MMA issuer (one thread): 4 x
 //              tcgen05.mma (K = 16 each) per 64-wide K block into one of two
 //              TMEM accumulators, so the epilogue of a tile overlaps the main
 //              loop of the next.
@@ -56,14 +56,15 @@ namespace gemm_f16_dev {
 constexpr int kBM = 128;                 // rows per CTA = UMMA M of the single form
 constexpr int kBK = 64;                  // K per stage: one 128-byte swizzle row of fp16
 constexpr int kMaxStages = 16;
-constexpr int kNumThreads = 288;         // 9 warps
+constexpr int kNumThreads = 256;         // 8 warps
+constexpr int kProducerThreads = 96;     // warps 0-2
 constexpr int kEpiWarp0 = 4;
-constexpr int kMmaWarp = 8;
+constexpr int kMmaWarp = 3;
 // Threads that wait on barriers for long stretches sit on SM sub-partitions
-// other than the MMA issuer's (warp 8 shares sub-partition 0 with warps 0
-// and 4): the TMA-issuing producer thread is lane 0 of warp 1 (when no operand
-// is gathered) and the epilogue thread that waits for accumulators is lane 0
-// of warp 5.
+// other than the MMA issuer's (warp 3, sub-partition 3, shared only with the
+// epilogue warp 7): the TMA-issuing producer thread is lane 0 of warp 1 (when
+// no operand is gathered) and the epilogue thread that waits for accumulators
+// is lane 0 of warp 5.
 constexpr int kTmaThread = 32;
 constexpr int kEpiLead = (kEpiWarp0 + 1) * 32;
 constexpr uint32_t kTmemCols = 512;      // two accumulators of up to 256 columns
@@ -83,6 +84,7 @@ enum : uint32_t { kOpTma = 1u, kOpMnMajor = 2u, kOpBox3d = 4u };
 struct KernelParams {
     CUtensorMap tmA;   // A' (K-major: dims {K, M}; MN-major: dims {M, K})
     CUtensorMap tmB;   // B' (K-major: dims {K, N}; MN-major: dims {N, K})
+    CUtensorMap tmB2;  // B' with the box of a tail piece (tail_split > 1): as narrow as the piece
     CUtensorMap tmC;   // C  (dims {N, M}, box 64 x 32)
     const __half* A;   // A'[m,k] = A[m*a_sm + k*a_sk]
     int64_t a_sm, a_sk;
@@ -130,14 +132,14 @@ __device__ __forceinline__ SmemLayout smem_layout(const KernelParams& p, uint32_
 }
 
 // Barrier block: full[16], empty[16], tmem_full[2], tmem_empty[2], drain,
-// fixup[4], then the TMEM base address, the abort flag and broadcast words.
+// fixup, then the TMEM base address, the abort flag and broadcast words.
 __device__ __forceinline__ uint32_t bar_full(uint32_t bars, int s) { return bars + 8u * s; }
 __device__ __forceinline__ uint32_t bar_empty(uint32_t bars, int s) { return bars + 8u * (kMaxStages + s); }
 __device__ __forceinline__ uint32_t bar_tfull(uint32_t bars, int a) { return bars + 8u * (2 * kMaxStages + a); }
 __device__ __forceinline__ uint32_t bar_tempty(uint32_t bars, int a) { return bars + 8u * (2 * kMaxStages + 2 + a); }
 __device__ __forceinline__ uint32_t bar_drain(uint32_t bars) { return bars + 8u * (2 * kMaxStages + 4); }
-__device__ __forceinline__ uint32_t bar_fix(uint32_t bars, int b) { return bars + 8u * (2 * kMaxStages + 5 + b); }
-constexpr uint32_t kTmemSlotOff = 8u * (2 * kMaxStages + 9);
+__device__ __forceinline__ uint32_t bar_fix(uint32_t bars) { return bars + 8u * (2 * kMaxStages + 5); }
+constexpr uint32_t kTmemSlotOff = 8u * (2 * kMaxStages + 6);
 constexpr uint32_t kAbortOff = kTmemSlotOff + 4;
 constexpr uint32_t kFlagOff = kTmemSlotOff + 8;
 constexpr uint32_t kOkOff = kTmemSlotOff + 12;   // two words, indexed by accumulator
@@ -307,6 +309,10 @@ __device__ __forceinline__ int clamp8(int64_t remaining)
     return remaining >= 8 ? 8 : (remaining <= 0 ? 0 : static_cast<int>(remaining));
 }
 
+// Chunks each producer thread keeps in flight while gathering with a non-unit
+// stride (unit-stride operands go row by row, below).
+constexpr int kGatherBatch = 4;
+
 // Gather one operand tile (rows = MN extent `rows_tile`, 64 K columns) into the
 // 128B-swizzled layout the UMMA descriptor expects.  K-major: row r (128 B) at
 // r*128, its 16-byte chunk j at ((j ^ (r & 7)) << 4).  MN-major: atom column a
@@ -321,24 +327,102 @@ __device__ __forceinline__ int clamp8(int64_t remaining)
 // element's page, so no load can fault.  Chunks are handled four at a time:
 // first every load is issued, then the words are shifted into place and
 // stored, so a thread keeps up to 8 loads in flight (more spills registers).
+// Unit-stride operands, row by row: each thread fills whole 128-byte rows of
+// the swizzled tile (64 consecutive elements of the contiguous dimension: a
+// K-major row, or one K row of an MN-major atom column).  The row's elements
+// start at any 2-byte-aligned address; the thread loads the aligned 16-byte
+// words that hold valid elements (at most 9, the same rule as above, so no
+// load can fault), then funnel-shifts them into the row's 8 chunks.  One
+// address computation per row instead of per chunk, and two rows in flight.
+__device__ __forceinline__ int clamp64(int64_t remaining)
+{
+    return remaining >= 64 ? 64 : (remaining <= 0 ? 0 : static_cast<int>(remaining));
+}
+
+__device__ __forceinline__ void gather_rows_unit(const __half* base, int64_t s_mn, int64_t s_k, int64_t MN,
+                                                 int64_t K, int64_t mn0, int64_t k0, int rows_tile, bool mn_major,
+                                                 uint32_t dst, int t)
+{
+    const int nrows = rows_tile;   // K-major: MN rows; MN-major: (rows_tile / 64) atoms x 64 K rows
+    const uintptr_t b = reinterpret_cast<uintptr_t>(base);
+    for (int r0 = t; r0 < nrows; r0 += 2 * kProducerThreads) {
+        uint4 wv[2][9];
+        uint32_t sh[2], rowaddr[2];
+        int nv[2], rk[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int rr = r0 + q * kProducerThreads;
+            nv[q] = 0;
+            sh[q] = 0;
+            rk[q] = 0;
+            rowaddr[q] = 0;
+            if (rr < nrows) {
+                int64_t off;
+                if (!mn_major) {
+                    const int64_t mn = mn0 + rr;
+                    nv[q] = (mn < MN) ? clamp64(K - k0) : 0;
+                    off = mn * s_mn + k0;   // s_k == 1
+                    rk[q] = rr;
+                    rowaddr[q] = dst + rr * 128;
+                } else {
+                    const int a = rr >> 6, r = rr & 63;   // atom column a, K row r
+                    const int64_t k = k0 + r, mn = mn0 + 64 * a;
+                    nv[q] = (k < K) ? clamp64(MN - mn) : 0;
+                    off = k * s_k + mn;   // s_mn == 1
+                    rk[q] = r;
+                    rowaddr[q] = dst + a * 8192 + r * 128;
+                }
+                if (nv[q] > 0) {
+                    const uintptr_t addr = b + 2 * static_cast<uintptr_t>(off);
+                    sh[q] = static_cast<uint32_t>(addr & 15u);
+                    const uintptr_t a0 = addr - sh[q];
+                    const int nw = static_cast<int>((sh[q] + 2u * static_cast<uint32_t>(nv[q]) + 15u) / 16u);
+#pragma unroll
+                    for (int i = 0; i < 9; ++i)
+                        wv[q][i] = (i < nw) ? ld_nc_v4(reinterpret_cast<const void*>(a0 + 16u * i))
+                                            : make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            if (r0 + q * kProducerThreads >= nrows) break;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                uint4 c = make_uint4(0u, 0u, 0u, 0u);
+                const int cv = clamp8(nv[q] - 8 * j);
+                if (cv > 0) {
+                    c = (sh[q] != 0) ? funnel16(wv[q][j], wv[q][j + 1], sh[q]) : wv[q][j];
+                    if (cv < 8) c = keep_first(c, cv);
+                }
+                st_smem_v4(rowaddr[q] + ((j ^ (rk[q] & 7)) << 4), c);
+            }
+        }
+    }
+}
+
 __device__ __forceinline__ void gather_tile(const __half* base, int64_t s_mn, int64_t s_k,
                                             int64_t MN, int64_t K, int64_t mn0, int64_t k0,
                                             int rows_tile, bool mn_major, uint32_t dst, int t)
 {
+    if ((mn_major ? s_mn : s_k) == 1) {
+        gather_rows_unit(base, s_mn, s_k, MN, K, mn0, k0, rows_tile, mn_major, dst, t);
+        return;
+    }
     const int chunks = rows_tile * 8;   // 16-byte chunks in the tile
-    const int iters = chunks / 128;
+    const int iters = (chunks + kProducerThreads - 1) / kProducerThreads;
     const int atoms = rows_tile / 64;
     const int64_t step = mn_major ? s_mn : s_k;
     const uintptr_t b = reinterpret_cast<uintptr_t>(base);
-    for (int i0 = 0; i0 < iters; i0 += 4) {
-        uint4 w0[4], w1[4];
-        uint32_t addr[4], sh[4];
-        int nv[4];
+    for (int i0 = 0; i0 < iters; i0 += kGatherBatch) {
+        uint4 w0[kGatherBatch], w1[kGatherBatch];
+        uint32_t addr[kGatherBatch], sh[kGatherBatch];
+        int nv[kGatherBatch];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < kGatherBatch; ++i) {
             nv[i] = 0;
-            if (i0 + i < iters) {
-                const int c = t + 128 * (i0 + i);
+            const int c = t + kProducerThreads * (i0 + i);
+            if (i0 + i < iters && c < chunks) {
                 const int j = c & 7;
                 int64_t mn, k;
                 if (!mn_major) {
@@ -374,8 +458,8 @@ __device__ __forceinline__ void gather_tile(const __half* base, int64_t s_mn, in
             }
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (i0 + i < iters) {
+        for (int i = 0; i < kGatherBatch; ++i) {
+            if (i0 + i < iters && t + kProducerThreads * (i0 + i) < chunks) {
                 uint4 r = (sh[i] != 0) ? funnel16(w0[i], w1[i], sh[i]) : w0[i];
                 if (nv[i] < 8) r = keep_first(r, nv[i]);
                 st_smem_v4(addr[i], r);
@@ -425,6 +509,16 @@ __device__ __forceinline__ void convert16(const uint32_t* r, uint32_t* h)
     for (int i = 0; i < 8; ++i) h[i] = pack_half2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
 }
 
+// sacc[i] += the fp32 accumulator column taddr + i of this thread's lane.
+__device__ __forceinline__ void add_tmem16(uint32_t taddr, float* sacc)
+{
+    uint32_t v[16];
+    tmem_ld_x16(taddr, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sacc[i] += __uint_as_float(v[i]);
+}
+
 // Epilogue of a unit whose tile is cut along K (split-K or stream-K), run by
 // the 128 epilogue threads.  This unit's fp32 sum is a partial.  The last unit
 // of the tile to finish adds all partials in K order (deterministic) and stores
@@ -433,12 +527,13 @@ __device__ __forceinline__ void convert16(const uint32_t* r, uint32_t* h)
 template <bool kPair>
 __device__ __forceinline__ void cut_tile_epilogue(const KernelParams& p, const SmemLayout& L, const Unit& w,
                                                uint32_t taddr, uint32_t tempty, int64_t m0, int64_t n0,
-                                               volatile int* flag, volatile int* abort, uint32_t& fix_ph)
+                                               volatile int* flag, volatile int* abort, uint32_t& fix_ph,
+                                               bool last_unit)
 {
     const int lane = threadIdx.x & 31;
     const int row = 32 * ((threadIdx.x >> 5) & 3) + lane;
     constexpr int kRanks = kPair ? 2 : 1;
-    const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+    const uint32_t rank = kPair ? (cluster_ctarank() & 1u) : 0u;
     const size_t slot_elems = static_cast<size_t>(kBM) * p.BN;   // one CTA's 128 rows of a tile
     int* counter = p.counters + static_cast<size_t>(w.tile) * kRanks + rank;
     const bool lead = threadIdx.x == kEpiLead;
@@ -483,91 +578,200 @@ __device__ __forceinline__ void cut_tile_epilogue(const KernelParams& p, const S
         }
     } else {
         if (lead) st_relaxed_gpu(counter, 0);   // ready for the next call
-        // The other partials stream through the 32 KB epilogue buffer in
-        // 8 KB pieces (16 columns of one partial) by TMA bulk copies, four
-        // buffers deep; pieces go in (column chunk, K order).
-        if (lane == 0) bulk_wait_group_read<0>();   // TMA stores done reading it
-        named_bar_sync(1, 128);
+        // The other partials come into shared memory by TMA bulk copies of 8 KB
+        // pieces (16 columns of one partial), in batches of as many pieces as the
+        // landing zone holds, all copies of a batch in flight at once and one
+        // wait per batch.  The zone is the 32 KB epilogue buffer, or, for the
+        // worker's last unit, the whole stage area: that unit's accumulator is
+        // full, so every pipeline stage has been consumed.
         const int others = w.expected - 1;
-        const int total = (w.bn / 16) * others;
-        auto issue = [&](int t) {
-            const int c = t / others, j = t - c * others;
-            const int idx = j < w.seg ? j : j + 1;   // K-order index, own one skipped
-            const size_t sl = static_cast<size_t>(w.slot0 + idx) * kRanks + rank;
-            const float* src = p.ws + sl * slot_elems + static_cast<size_t>(c) * (4 * kBM * 4);
-            const int b = t & 3;
-            fence_proxy_async_smem();   // earlier generic reads of buffer b come first
-            mbar_arrive_expect_tx(bar_fix(L.bars, b), 8192);
-            bulk_load(L.epi + b * 8192, src, 8192, bar_fix(L.bars, b));
-        };
-        if (lead)
-            for (int t0 = 0; t0 < 3 && t0 < total; ++t0) issue(t0);
-        int t = 0;
-        bool ok = true;
-        for (int c0 = 0; c0 < w.bn; c0 += 16) {
-            uint32_t own[16];
-            tmem_ld_x16(taddr + c0, own);
-            tmem_wait_ld();
-            if (c0 + 16 >= w.bn) {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    if (kPair)
-                        mbar_arrive_cluster(tempty);
-                    else
-                        mbar_arrive(tempty);
-                }
-            }
-            float sacc[16];
-#pragma unroll
-            for (int c = 0; c < 16; ++c) sacc[c] = 0.f;
-            for (int idx = 0; idx < w.expected; ++idx) {
-                if (idx == w.seg) {
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) sacc[c] += __uint_as_float(own[c]);
-                    continue;
-                }
-                const int b = t & 3;
-                // One thread keeps three pieces in flight and waits for this
-                // one; the barrier hands the data (and the verdict) over.
+        if (lane == 0) bulk_wait_group_read<0>();   // TMA stores of C done reading the epilogue buffer
+        named_bar_sync(1, 128);
+        const uint32_t zone = last_unit ? L.a : L.epi;
+        const int cap = static_cast<int>(last_unit ? (L.epi - L.a) / 8192u : kEpiBytes / 8192u);
+        const int chunks = w.bn / 16;
+        if (others <= 3) {
+            // Common case (stream-K and split-K up to four ways): whole chunks per
+            // batch, four chunks (64 columns) per TMEM wait, and when the
+            // epilogue buffer is free (last unit) and C takes TMA stores, the
+            // result goes out through swizzled staging and TMA stores like a
+            // whole tile's.
+            int per = cap / others;
+            if (per >= 4) per &= ~3;
+            const bool stage_c = last_unit && p.c_tma;
+            const int q = (threadIdx.x >> 5) & 3;
+            uint32_t gc = 0;   // TMA-store groups this warp issued
+            for (int b0 = 0; b0 < chunks; b0 += per) {
+                const int nch = min(per, chunks - b0);
                 if (lead) {
-                    if (t + 3 < total) issue(t + 3);   // its buffer was freed by the last barrier
-                    const bool got = mbar_wait(bar_fix(L.bars, b), (fix_ph >> b) & 1u, abort, p.timeout_ns);
-                    if (!got) raise_abort(p, abort);
+                    fence_proxy_async_smem();   // the previous batch's generic reads come first
+                    const uint32_t fb = bar_fix(L.bars);
+                    mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nch * others) * 8192u);
+                    for (int c = 0; c < nch; ++c)
+                        for (int j = 0; j < others; ++j) {
+                            const int idx = j < w.seg ? j : j + 1;   // K-order index, own one skipped
+                            const size_t sl = static_cast<size_t>(w.slot0 + idx) * kRanks + rank;
+                            const float* src =
+                                p.ws + sl * slot_elems + static_cast<size_t>(b0 + c) * (4 * kBM * 4);
+                            bulk_load(zone + static_cast<uint32_t>(c * others + j) * 8192u, src, 8192, fb);
+                        }
+                    const bool got = mbar_wait(fb, fix_ph & 1u, abort, p.timeout_ns);
+                    if (!got) {
+                        raise_abort(p, abort);
+                        mbar_wait(fb, fix_ph & 1u, nullptr, kDrainTimeoutNs);   // let the copies land
+                    }
                     *flag = got ? 1 : 0;
                 }
+                fix_ph ^= 1u;
                 named_bar_sync(1, 128);
-                ok = *flag != 0;
-                if (!ok) break;
-                fix_ph ^= 1u << b;
-                const uint32_t src = L.epi + b * 8192 + row * 16;
+                if (*flag == 0) break;
+                for (int g0 = 0; g0 < nch; g0 += 4) {
+                    const int gn = min(4, nch - g0);
+                    uint32_t buf = 0;
+                    if (stage_c) {
+                        buf = L.epi + (q * 2 + (gc & 1u)) * kEpiBufBytes;
+                        if (lane == 0) bulk_wait_group_read<1>();
+                        __syncwarp();
+                    }
+                    for (int s0 = 0; s0 < gn; s0 += 2) {   // two chunks (32 columns) per TMEM wait
+                        const int sn = min(2, gn - s0);
+                        uint32_t r[32];   // this unit's own sums for the two chunks
+                        tmem_ld_x16(taddr + (b0 + g0 + s0) * 16, r);
+                        if (sn > 1) tmem_ld_x16(taddr + (b0 + g0 + s0 + 1) * 16, r + 16);
+                        tmem_wait_ld();
 #pragma unroll
-                for (int g4 = 0; g4 < 4; ++g4) {
-                    const float4 v = ld_smem_f4(src + g4 * (kBM * 16));
-                    sacc[4 * g4] += v.x;
-                    sacc[4 * g4 + 1] += v.y;
-                    sacc[4 * g4 + 2] += v.z;
-                    sacc[4 * g4 + 3] += v.w;
+                        for (int h1 = 0; h1 < 2; ++h1) {
+                            if (h1 >= sn) break;
+                            const int c = g0 + s0 + h1;
+                            float acc[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+                            for (int j = 0; j < others; ++j) {   // K order, own sum at position seg
+                                if (j == w.seg) {
+#pragma unroll
+                                    for (int i = 0; i < 16; ++i) acc[i] += __uint_as_float(r[16 * h1 + i]);
+                                }
+                                const uint32_t src =
+                                    zone + static_cast<uint32_t>(c * others + j) * 8192u + row * 16;
+#pragma unroll
+                                for (int g4 = 0; g4 < 4; ++g4) {
+                                    const float4 v = ld_smem_f4(src + g4 * (kBM * 16));
+                                    acc[4 * g4] += v.x;
+                                    acc[4 * g4 + 1] += v.y;
+                                    acc[4 * g4 + 2] += v.z;
+                                    acc[4 * g4 + 3] += v.w;
+                                }
+                            }
+                            if (w.seg == others) {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) acc[i] += __uint_as_float(r[16 * h1 + i]);
+                            }
+                            uint32_t h[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) h[i] = pack_half2(acc[2 * i], acc[2 * i + 1]);
+                            if (stage_c) {
+                                const int j0 = (s0 + h1) * 2;   // 16-byte chunk inside the 128-byte row
+                                st_smem_v4(buf + lane * 128 + ((j0 ^ (lane & 7)) << 4),
+                                           make_uint4(h[0], h[1], h[2], h[3]));
+                                st_smem_v4(buf + lane * 128 + (((j0 + 1) ^ (lane & 7)) << 4),
+                                           make_uint4(h[4], h[5], h[6], h[7]));
+                            } else {
+                                store_piece_masked(p, m0 + row, n0 + (b0 + c) * 16, h);
+                            }
+                        }
+                    }
+                    if (stage_c) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (m0 + 32 * q < p.M)
+                                tma_store_2d(&p.tmC, buf, static_cast<int32_t>(n0 + 16 * (b0 + g0)),
+                                             static_cast<int32_t>(m0 + 32 * q));
+                            bulk_commit_group();
+                        }
+                        ++gc;
+                    }
                 }
-                ++t;
-                named_bar_sync(1, 128);   // buffer b free for piece t + 3
+                named_bar_sync(1, 128);   // the zone is free for the next batch
             }
-            if (!ok) break;
-            uint32_t h[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) h[i] = pack_half2(sacc[2 * i], sacc[2 * i + 1]);
-            store_piece_masked(p, m0 + row, n0 + c0, h);
+            if (stage_c && lane == 0) bulk_wait_group_read<0>();   // staging free for the caller's next unit
+        } else {
+            // Pieces are numbered t = chunk * others + j (j-th other partial of the
+            // chunk in K order); a batch holds up to `cap` of them.  Each thread keeps
+            // the running sum of the current chunk across batches, adds its own sum
+            // (from TMEM) at its K position, and stores the chunk after its last piece.
+            const int total = chunks * others;
+            float sacc[16];
+            for (int t0 = 0; t0 < total; t0 += cap) {
+                const int nb = min(cap, total - t0);
+                if (lead) {
+                    fence_proxy_async_smem();   // the previous batch's generic reads come first
+                    const uint32_t fb = bar_fix(L.bars);
+                    mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nb) * 8192u);
+                    for (int u = 0; u < nb; ++u) {
+                        const int t = t0 + u, c = t / others, j = t - c * others;
+                        const int idx = j < w.seg ? j : j + 1;   // K-order index, own one skipped
+                        const size_t sl = static_cast<size_t>(w.slot0 + idx) * kRanks + rank;
+                        const float* src = p.ws + sl * slot_elems + static_cast<size_t>(c) * (4 * kBM * 4);
+                        bulk_load(zone + static_cast<uint32_t>(u) * 8192u, src, 8192, fb);
+                    }
+                    const bool got = mbar_wait(fb, fix_ph & 1u, abort, p.timeout_ns);
+                    if (!got) {
+                        raise_abort(p, abort);
+                        mbar_wait(fb, fix_ph & 1u, nullptr, kDrainTimeoutNs);   // let the copies land
+                    }
+                    *flag = got ? 1 : 0;
+                }
+                fix_ph ^= 1u;
+                named_bar_sync(1, 128);
+                if (*flag == 0) break;
+                for (int u = 0; u < nb; ++u) {
+                    const int t = t0 + u, c = t / others, j = t - c * others;
+                    if (j == 0) {
+    #pragma unroll
+                        for (int i = 0; i < 16; ++i) sacc[i] = 0.f;
+                    }
+                    // own sum (K index seg) goes before the piece with K index seg + 1;
+                    // seg and j are uniform, so the TMEM load is warp-wide
+                    if (j == w.seg) add_tmem16(taddr + c * 16, sacc);
+                    const uint32_t src = zone + static_cast<uint32_t>(u) * 8192u + row * 16;
+    #pragma unroll
+                    for (int g4 = 0; g4 < 4; ++g4) {
+                        const float4 v = ld_smem_f4(src + g4 * (kBM * 16));
+                        sacc[4 * g4] += v.x;
+                        sacc[4 * g4 + 1] += v.y;
+                        sacc[4 * g4 + 2] += v.z;
+                        sacc[4 * g4 + 3] += v.w;
+                    }
+                    if (j == others - 1) {
+                        if (w.seg == others) add_tmem16(taddr + c * 16, sacc);   // own sum is the last in K order
+                        uint32_t h[8];
+    #pragma unroll
+                        for (int i = 0; i < 8; ++i) h[i] = pack_half2(sacc[2 * i], sacc[2 * i + 1]);
+                        store_piece_masked(p, m0 + row, n0 + c * 16, h);
+                    }
+                }
+                named_bar_sync(1, 128);   // the zone is free for the next batch
+            }
         }
-        if (!ok && lead) {
-            // gave up on piece t: let it and the (up to three) copies issued
-            // after it land (bounded) before the CTA can exit
-            for (int u2 = t; u2 < total && u2 < t + 4; ++u2)
-                mbar_wait(bar_fix(L.bars, u2 & 3), (fix_ph >> (u2 & 3)) & 1u, nullptr, kDrainTimeoutNs);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+            if (kPair)
+                mbar_arrive_cluster(tempty);
+            else
+                mbar_arrive(tempty);
         }
     }
 }
 
-template <bool kPair>
+// kQuad (with kPair): clusters of four CTAs, two pairs on vertically adjacent
+// 256-row tiles with the same B columns.  Cluster ranks 0,1 form pair 0 and
+// 2,3 pair 1.  Each CTA loads its own 128 A rows and one 64-column quarter of
+// the pair's B columns, multicast to the CTA with the same pair rank in both
+// pairs, so B is read from L2 once per cluster instead of once per pair.  The
+// stage's empty barrier then waits for both pairs' MMAs (count 2).
+template <bool kPair, bool kQuad>
 __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __grid_constant__ KernelParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -585,27 +789,34 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
     const bool a_tma = p.a_flags & kOpTma, b_tma = p.b_flags & kOpTma;
     const bool a_mn = p.a_flags & kOpMnMajor, b_mn = p.b_flags & kOpMnMajor;
     const bool a_3d = p.a_flags & kOpBox3d, b_3d = p.b_flags & kOpBox3d;
-    const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+    static_assert(kPair || !kQuad, "the four-CTA form is built on pairs");
+    const uint32_t crank = kPair ? cluster_ctarank() : 0u;   // rank in the cluster
+    const uint32_t rank = crank & 1u;                         // rank in the pair
+    const uint32_t pp = kQuad ? (crank >> 1) : 0u;            // pair index in the cluster
+    const uint32_t lead_rank = crank & ~1u;                   // cluster rank of this pair's leader
     const bool leader = (rank == 0);
-    const int cid = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int cid = static_cast<int>(blockIdx.x >> (kQuad ? 2 : (kPair ? 1 : 0)));
     constexpr int kTileRows = kPair ? 2 * kBM : kBM;
+    // Tile rows handled per unit by the cluster (two pair tiles in the four-CTA form).
+    constexpr int kUnitRows = kQuad ? 2 * kTileRows : kTileRows;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(bar_full(L.bars, s), p.full_count);
-            mbar_init(bar_empty(L.bars, s), 1);
+            mbar_init(bar_empty(L.bars, s), kQuad ? 2 : 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar_tfull(L.bars, a), 1);
             mbar_init(bar_tempty(L.bars, a), kPair ? 8 : 4);
         }
         mbar_init(bar_drain(L.bars), 1);
-        for (int b = 0; b < 4; ++b) mbar_init(bar_fix(L.bars, b), 1);
+        mbar_init(bar_fix(L.bars), 1);
         *abort = 0;
         *flag = 0;
         fence_mbarrier_init();
         if (a_tma) tma_prefetch_desc(&p.tmA);
         if (b_tma) tma_prefetch_desc(&p.tmB);
+        if (b_tma && p.tail_split > 1) tma_prefetch_desc(&p.tmB2);
         if (p.c_tma) tma_prefetch_desc(&p.tmC);
     }
     if (warp == kMmaWarp) {
@@ -625,7 +836,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp < 4) {
+    if (warp < kMmaWarp) {
         // ------------------------------------------------------------ producers
         const int t = threadIdx.x;
         const bool any_masked = !a_tma || !b_tma;
@@ -639,12 +850,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
             for (int i = 0; i < nu && ok; ++i) {
                 const Unit w = unit_at(p, cid, i);
                 const int bcols = kPair ? w.bn / 2 : w.bn;   // this CTA's share of the unit's B columns
-                const int64_t m0 = static_cast<int64_t>(w.m_blk) * kTileRows + rank * kBM;
+                const int64_t m0 = static_cast<int64_t>(w.m_blk) * kUnitRows + pp * kTileRows + rank * kBM;
                 const int64_t n0 = static_cast<int64_t>(w.n_blk) * p.BN + w.n_off + rank * bcols;
                 // Bytes one stage of this unit brings in: MN-major B comes in
                 // 64-column boxes (or one 3-D box of the full stage width),
-                // K-major B in one box of the full tile width.
-                const uint32_t b_bytes = (b_mn && !b_3d) ? static_cast<uint32_t>(bcols) * 128u : p.stage_b_bytes;
+                // K-major B in one box of the full tile width.  A tail piece
+                // narrower than the tile reads B through tmB2, whose box is the
+                // piece's width, so it brings only its own columns.
+                const bool narrow = w.bn < p.BN;
+                const CUtensorMap* tmb = narrow ? &p.tmB2 : &p.tmB;
+                const uint32_t b_bytes =
+                    ((b_mn && !b_3d) || narrow) ? static_cast<uint32_t>(bcols) * 128u : p.stage_b_bytes;
                 const uint32_t tx = kPair ? 2u * (kStageABytes + b_bytes)
                                           : (a_tma ? kStageABytes : 0u) + (b_tma ? b_bytes : 0u);
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -662,7 +878,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                             // The leader expects both CTAs' bytes on its own barrier;
                             // the peer's copies complete on the leader's barrier.
                             if (leader) mbar_arrive_expect_tx(fb, tx);
-                            const uint32_t fbc = mapa_shared(fb, 0);
+                            const uint32_t fbc = mapa_shared(fb, lead_rank);
                             if (!a_mn) {
                                 tma_load_2d_pair(sa, &p.tmA, k0, static_cast<int32_t>(m0), fbc);
                             } else if (a_3d) {
@@ -671,10 +887,22 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                                 tma_load_2d_pair(sa, &p.tmA, static_cast<int32_t>(m0), k0, fbc);
                                 tma_load_2d_pair(sa + 8192, &p.tmA, static_cast<int32_t>(m0 + 64), k0, fbc);
                             }
-                            if (!b_mn) {
-                                tma_load_2d_pair(sb, &p.tmB, k0, static_cast<int32_t>(n0), fbc);
+                            if (kQuad) {
+                                // This CTA's quarter: B columns n0 + 64*pp .. +64 of its pair
+                                // rank's half, into both pairs' CTAs of that rank.
+                                const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (2u + rank)));
+                                const int32_t nq = static_cast<int32_t>(n0 + 64 * pp);
+                                const uint32_t sq = sb + pp * 8192u;
+                                if (!b_mn)
+                                    tma_load_2d_pair_mc(sq, &p.tmB, k0, nq, fbc, mask);
+                                else if (b_3d)
+                                    tma_load_3d_pair_mc(sq, &p.tmB, 0, k0, nq >> 6, fbc, mask);
+                                else
+                                    tma_load_2d_pair_mc(sq, &p.tmB, nq, k0, fbc, mask);
+                            } else if (!b_mn) {
+                                tma_load_2d_pair(sb, tmb, k0, static_cast<int32_t>(n0), fbc);
                             } else if (b_3d) {
-                                tma_load_3d_pair(sb, &p.tmB, 0, k0, static_cast<int32_t>(n0 >> 6), fbc);
+                                tma_load_3d_pair(sb, tmb, 0, k0, static_cast<int32_t>(n0 >> 6), fbc);
                             } else {
                                 for (int j = 0; j < bcols / 64; ++j)
                                     tma_load_2d_pair(sb + j * 8192, &p.tmB, static_cast<int32_t>(n0 + 64 * j), k0, fbc);
@@ -693,9 +921,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                             }
                             if (b_tma) {
                                 if (!b_mn) {
-                                    tma_load_2d(sb, &p.tmB, k0, static_cast<int32_t>(n0), fb);
+                                    tma_load_2d(sb, tmb, k0, static_cast<int32_t>(n0), fb);
                                 } else if (b_3d) {
-                                    tma_load_3d(sb, &p.tmB, 0, k0, static_cast<int32_t>(n0 >> 6), fb);
+                                    tma_load_3d(sb, tmb, 0, k0, static_cast<int32_t>(n0 >> 6), fb);
                                 } else {
                                     for (int j = 0; j < bcols / 64; ++j)
                                         tma_load_2d(sb + j * 8192, &p.tmB, static_cast<int32_t>(n0 + 64 * j), k0, fb);
@@ -778,7 +1006,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                     }
                     any = true;
                     if (kPair)
-                        umma_commit_pair_mc(bar_empty(L.bars, stage), 0x3);
+                        umma_commit_pair_mc(bar_empty(L.bars, stage), kQuad ? 0xF : 0x3);
                     else
                         umma_commit(bar_empty(L.bars, stage));
                     if (++stage == p.stages) {
@@ -788,7 +1016,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                 }
                 if (!ok) break;
                 if (kPair)
-                    umma_commit_pair_mc(bar_tfull(L.bars, acc), 0x3);
+                    umma_commit_pair_mc(bar_tfull(L.bars, acc), static_cast<uint16_t>(0x3u << crank));
                 else
                     umma_commit(bar_tfull(L.bars, acc));
                 if (++acc == 2) {
@@ -800,7 +1028,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                 // Drain: wait (bounded) until every MMA issued so far has completed
                 // before the accumulator memory is released.
                 if (kPair)
-                    umma_commit_pair_mc(bar_drain(L.bars), 0x1);
+                    umma_commit_pair_mc(bar_drain(L.bars), static_cast<uint16_t>(0x1u << crank));
                 else
                     umma_commit(bar_drain(L.bars));
                 wait_bar<kPair>(bar_drain(L.bars), 0, nullptr, kDrainTimeoutNs);
@@ -814,11 +1042,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t group_count = 0;
-        uint32_t fix_ph = 0u;   // bit b: parity of the next phase of fixup barrier b (b < 4)
+        uint32_t fix_ph = 0u;   // bit 0: parity of the next phase of the fixup barrier
         const int nu = units_of_worker(p, cid);
         for (int ui = 0; ui < nu; ++ui) {
             const Unit w = unit_at(p, cid, ui);
-            const int64_t m0 = static_cast<int64_t>(w.m_blk) * kTileRows + rank * kBM;
+            const int64_t m0 = static_cast<int64_t>(w.m_blk) * kUnitRows + pp * kTileRows + rank * kBM;
             const int64_t n0 = static_cast<int64_t>(w.n_blk) * p.BN + w.n_off;
             const int npieces = w.bn / 16;          // 16 accumulator columns per piece
             // One thread waits for the accumulator and tells the other epilogue
@@ -833,7 +1061,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
             if (!okflag[acc]) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + lane_off + acc * kAccStride;
-            const uint32_t tempty = kPair ? mapa_shared(bar_tempty(L.bars, acc), 0) : bar_tempty(L.bars, acc);
+            const uint32_t tempty = kPair ? mapa_shared(bar_tempty(L.bars, acc), lead_rank) : bar_tempty(L.bars, acc);
             if (w.slot < 0) {
                 uint32_t buf = 0;
                 for (int pc = 0; pc < npieces; pc += 4) {
@@ -874,8 +1102,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                                 fence_proxy_async_smem();
                                 __syncwarp();
                                 if (lane == 0) {
-                                    tma_store_2d(&p.tmC, buf, static_cast<int32_t>(n0 + 16 * (piece & ~3)),
-                                                 static_cast<int32_t>(m0 + 32 * q));
+                                    // (a box wholly below row M, e.g. the second pair tile of a
+                                    // four-CTA unit on the last row, is not stored)
+                                    if (m0 + 32 * q < p.M)
+                                        tma_store_2d(&p.tmC, buf, static_cast<int32_t>(n0 + 16 * (piece & ~3)),
+                                                     static_cast<int32_t>(m0 + 32 * q));
                                     bulk_commit_group();
                                 }
                                 ++group_count;
@@ -886,7 +1117,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                     }
                 }
             } else {
-                cut_tile_epilogue<kPair>(p, L, w, taddr, tempty, m0, n0, flag, abort, fix_ph);
+                cut_tile_epilogue<kPair>(p, L, w, taddr, tempty, m0, n0, flag, abort, fix_ph, ui == nu - 1);
             }
             if (++acc == 2) {
                 acc = 0;

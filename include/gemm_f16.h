@@ -174,6 +174,7 @@ typedef struct {
     int smem_bytes;
     size_t workspace_bytes;
     int a_box3d, b_box3d;   /* MN-major TMA operand read as one 3-D box per stage */
+    int cluster_ctas;       /* CTAs per cluster: 1, 2 (pair form) or 4 (two pairs sharing B by multicast) */
 } gemm_f16_plan;
 
 /* Fill *plan for the given arguments without launching anything.  Returns the
@@ -195,12 +196,16 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
  *   GEMM_F16_OPT_MAX_CTAS      > 0: cap the persistent grid
  *   GEMM_F16_OPT_PAIR          0 default (2-CTA pair tiles for 256-wide tiles of TMA
  *                              operands without split-K), 1 never, 2 also for 128-wide tiles
- *   GEMM_F16_OPT_STREAMK       0 default / 1: whole tiles only; 2: stream-K tail when
- *                              the tiles do not divide evenly over the SMs
+ *   GEMM_F16_OPT_STREAMK       0 default: stream-K tail when an operand is gathered (not
+ *                              TMA-addressable), whole tiles otherwise; 1: whole tiles only;
+ *                              2: stream-K tail whenever the tiles do not divide evenly
  *   GEMM_F16_OPT_TAIL_SPLIT    0 default: cut the last partial wave of tiles along N
  *                              into narrower tiles; 1 never
  *   GEMM_F16_OPT_MAX_STAGES    >= 2: cap the pipeline depth (default: as many stages
  *                              as shared memory holds, at most 16)
+ *   GEMM_F16_OPT_MULTICAST     0 default / 1: pairs load their own B; 2: clusters of four
+ *                              CTAs (two pairs on adjacent 256-row tiles) read each B tile
+ *                              once and multicast it (whole 256x256 tiles only)
  * A value of 0 restores the default.  Returns GEMM_F16_ERR_INVALID_VALUE for an
  * unknown option or a value out of range.
  */
@@ -215,7 +220,8 @@ enum {
     GEMM_F16_OPT_PAIR = 8,
     GEMM_F16_OPT_STREAMK = 9,
     GEMM_F16_OPT_TAIL_SPLIT = 10,
-    GEMM_F16_OPT_MAX_STAGES = 11
+    GEMM_F16_OPT_MAX_STAGES = 11,
+    GEMM_F16_OPT_MULTICAST = 12
 };
 gemm_f16_status gemm_f16_set_option(int option, int64_t value);
 

@@ -25,7 +25,7 @@ DEV = torch.device("cuda:0")
 def _defaults():
     yield
     for o in (g.OPT_FORCE_GATHER, g.OPT_SPLITS, g.OPT_TILE_N, g.OPT_PANEL, g.OPT_SWAP,
-              g.OPT_TIMEOUT_MS, g.OPT_MAX_CTAS, g.OPT_PAIR, g.OPT_STREAMK, g.OPT_TAIL_SPLIT, g.OPT_MAX_STAGES):
+              g.OPT_TIMEOUT_MS, g.OPT_MAX_CTAS, g.OPT_PAIR, g.OPT_STREAMK, g.OPT_TAIL_SPLIT, g.OPT_MAX_STAGES, g.OPT_MULTICAST):
         g.gemm_f16_set_option(o, 0)
 
 
@@ -248,6 +248,57 @@ def test_pair_tiles_many_units_per_cluster():
     assert_bits(host(gpu(A, B, out=out)), oracle.gemm(Ah, Bh, threads=oracle_threads()), "pair, one cluster")
 
 
+# ------------------------------------------------ four-CTA multicast form
+# Clusters of four CTAs: two pairs on vertically adjacent 256-row tiles, each
+# CTA loading a 64-column quarter of B that TMA multicasts to both pairs.
+QUAD_CASES = [
+    # (M, N, K, layout A, layout B, integer inputs)
+    (1000, 520, 200, "row", "row", True),      # B N-major, N % 64 != 0: 2-D quarter boxes
+    (700, 512, 216, "row", "row", True),       # 3 tile rows: the last unit's second pair is below M
+    (1024, 640, 200, "row", "col", True),      # K-major B: 64-row quarter boxes
+    (776, 384, 136, "col", "row", True),       # M-major A, 3-D quarter boxes of B
+    (2048, 1024, 1024, "row", "row", False),
+]
+
+
+@pytest.mark.parametrize("case", QUAD_CASES, ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}-{c[3]}-{c[4]}")
+def test_four_cta_multicast_matches_oracle(case):
+    M, N, K, la, lb, integer = case
+    rng = np.random.default_rng(M * 3 + N + K)
+    if integer:
+        Ah = rng.integers(-3, 4, (M, K)).astype(np.float16)
+        Bh = rng.integers(-3, 4, (K, N)).astype(np.float16)
+    else:
+        Ah = rng.uniform(-1, 1, (M, K)).astype(np.float16)
+        Bh = rng.uniform(-1, 1, (K, N)).astype(np.float16)
+    A, B = make_view(Ah, la), make_view(Bh, lb)
+    out = torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV)
+    g.gemm_f16_set_option(g.OPT_MULTICAST, 2)
+    plan = g.plan_for(A, B, out)
+    assert plan["cluster_ctas"] == 4 and plan["grid"] % 4 == 0, plan
+    got = host(gpu(A, B, out=out))
+    ref = oracle.gemm(Ah, Bh, threads=oracle_threads())
+    if integer:
+        assert_bits(got, ref, f"four-CTA {case}")
+    else:
+        assert_close(got, ref, K, f"four-CTA {case}")
+    assert g.gemm_f16_device_status() == 0
+
+
+def test_four_cta_one_cluster_walks_every_unit():
+    g.gemm_f16_set_option(g.OPT_MULTICAST, 2)
+    g.gemm_f16_set_option(g.OPT_MAX_CTAS, 4)
+    rng = np.random.default_rng(11)
+    Ah = rng.integers(-3, 4, (1300, 128)).astype(np.float16)
+    Bh = rng.integers(-3, 4, (128, 1280)).astype(np.float16)
+    A, B = to_dev(Ah), to_dev(Bh)
+    out = torch.empty((1300, 1280), dtype=torch.float16, device=DEV)
+    plan = g.plan_for(A, B, out)
+    assert plan["cluster_ctas"] == 4 and plan["grid"] == 4 and plan["units"] == 15, plan
+    assert_bits(host(gpu(A, B, out=out)), oracle.gemm(Ah, Bh, threads=oracle_threads()), "four-CTA, one cluster")
+    assert g.gemm_f16_device_status() == 0
+
+
 # ------------------------------------------------------- boundary behaviour
 def test_k_tail_is_zero_filled_not_wrapped():
     # The Triton page's K-tail example (a=[1,2,3], b=[4,5,6] -> 32; wrapping K
@@ -347,6 +398,7 @@ def test_tail_split_bit_exact(M, N, K, layout):
     Bh = rng.integers(-3, 4, (K, N)).astype(np.float16)
     A, B = make_view(Ah, layout), make_view(Bh, layout)
     out = torch.empty((M, N), dtype=torch.float16, device=DEV)
+    g.gemm_f16_set_option(g.OPT_STREAMK, 1)   # whole tiles (gathered operands default to stream-K)
     plan = g.plan_for(A, B, out)
     assert plan["tail_split"] > 1, plan
     ref = oracle.gemm(Ah, Bh, threads=oracle_threads())
@@ -354,6 +406,21 @@ def test_tail_split_bit_exact(M, N, K, layout):
     g.gemm_f16_set_option(g.OPT_TAIL_SPLIT, 1)
     assert g.plan_for(A, B, out)["tail_split"] == 1
     assert_bits(host(gpu(A, B, out=out)), ref, f"no tail split {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K,layout", [(1000, 1000, 1000, "pitch"), (3001, 1999, 200, "offset")])
+def test_gathered_operands_default_to_stream_k(M, N, K, layout):
+    """Gathered (non-TMA) operands make tiles slow, so by default the last
+    partial wave is balanced by stream-K; integer inputs stay bit-exact."""
+    rng = np.random.default_rng(M + 5 * N + K)
+    Ah = rng.integers(-3, 4, (M, K)).astype(np.float16)
+    Bh = rng.integers(-3, 4, (K, N)).astype(np.float16)
+    A, B = make_view(Ah, layout), make_view(Bh, layout)
+    out = torch.empty((M, N), dtype=torch.float16, device=DEV)
+    plan = g.plan_for(A, B, out)
+    assert not (plan["a_tma"] and plan["b_tma"]) and plan["streamk_tiles"] > 0, plan
+    assert_bits(host(gpu(A, B, out=out)), oracle.gemm(Ah, Bh, threads=oracle_threads()), f"gathered {M}x{N}x{K}")
+    assert g.gemm_f16_device_status() == 0
 
 
 def _segment_end(ptr):

@@ -23,7 +23,7 @@ DEV = torch.device("cuda:0")
 @pytest.fixture(autouse=True)
 def _defaults():
     for o in (g.OPT_FORCE_GATHER, g.OPT_SPLITS, g.OPT_TILE_N, g.OPT_PANEL, g.OPT_SWAP,
-              g.OPT_TIMEOUT_MS, g.OPT_MAX_CTAS, g.OPT_PAIR, g.OPT_STREAMK, g.OPT_TAIL_SPLIT, g.OPT_MAX_STAGES):
+              g.OPT_TIMEOUT_MS, g.OPT_MAX_CTAS, g.OPT_PAIR, g.OPT_STREAMK, g.OPT_TAIL_SPLIT, g.OPT_MAX_STAGES, g.OPT_MULTICAST):
         g.gemm_f16_set_option(o, 0)
     yield
     for o in (g.OPT_STREAMK, g.OPT_SPLITS):
