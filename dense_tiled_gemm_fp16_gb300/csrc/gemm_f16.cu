@@ -526,7 +526,8 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
                  static_cast<int>(stage_bytes);
     stages = std::min(stages, gemm_f16_dev::kMaxStages);
     if (opt(GEMM_F16_OPT_MAX_STAGES) >= 2) stages = std::min<int>(stages, static_cast<int>(opt(GEMM_F16_OPT_MAX_STAGES)));
-    if (stages < 2) return GEMM_F16_ERR_INVALID_VALUE;
+    stages -= stages % gemm_f16_dev::kSlots;   // whole barrier phases of kSlots slots
+    if (stages < gemm_f16_dev::kSlots) return GEMM_F16_ERR_INVALID_VALUE;
     const int smem = kSmemAlignSlack + stages * static_cast<int>(stage_bytes) + epi +
                      static_cast<int>(gemm_f16_dev::kBarrierBytes);
 

@@ -56,6 +56,10 @@ namespace gemm_f16_dev {
 constexpr int kBM = 128;                 // rows per CTA = UMMA M of the single form
 constexpr int kBK = 64;                  // K per stage: one 128-byte swizzle row of fp16
 constexpr int kMaxStages = 16;
+// K blocks (shared-memory slots of 64 K) per pipeline barrier phase: the MMA
+// issuer waits once and commits once per kSlots * 4 MMAs, which halves the
+// per-K-block cost of the barrier round trip (it cannot overlap the issue).
+constexpr int kSlots = 2;
 constexpr int kNumThreads = 256;         // 8 warps
 constexpr int kProducerThreads = 96;     // warps 0-2
 constexpr int kEpiWarp0 = 4;
@@ -633,6 +637,49 @@ __device__ __forceinline__ void cut_tile_epilogue(const KernelParams& p, const S
                         if (lane == 0) bulk_wait_group_read<1>();
                         __syncwarp();
                     }
+                    if (others == 1 && gn == 4) {
+                        // One other partial (the usual stream-K cut): four chunks per
+                        // TMEM wait, every shared-memory load issued before the adds.
+                        uint32_t r[64];
+#pragma unroll
+                        for (int h2 = 0; h2 < 4; ++h2) tmem_ld_x16(taddr + (b0 + g0 + h2) * 16, r + 16 * h2);
+                        tmem_wait_ld();
+                        const bool own_first = w.seg == 0;
+#pragma unroll
+                        for (int hp = 0; hp < 4; hp += 2) {   // shared-memory loads two chunks at a time
+                            float4 v[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                v[e] = ld_smem_f4(zone + static_cast<uint32_t>(g0 + hp + (e >> 2)) * 8192u + row * 16 +
+                                                  (e & 3) * (kBM * 16));
+#pragma unroll
+                            for (int h1 = 0; h1 < 2; ++h1) {
+                                const int h2 = hp + h1;
+                                uint32_t h[8];
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    const float o0 = __uint_as_float(r[16 * h2 + 2 * i]);
+                                    const float o1 = __uint_as_float(r[16 * h2 + 2 * i + 1]);
+                                    const float4& q4 = v[4 * h1 + (i >> 1)];
+                                    const float p0 = (i & 1) ? q4.z : q4.x;
+                                    const float p1 = (i & 1) ? q4.w : q4.y;
+                                    // K order: 0 + first + second, exactly as in the general loop
+                                    const float s0v = own_first ? (0.f + o0) + p0 : (0.f + p0) + o0;
+                                    const float s1v = own_first ? (0.f + o1) + p1 : (0.f + p1) + o1;
+                                    h[i] = pack_half2(s0v, s1v);
+                                }
+                                if (stage_c) {
+                                    const int j0 = h2 * 2;
+                                    st_smem_v4(buf + lane * 128 + ((j0 ^ (lane & 7)) << 4),
+                                               make_uint4(h[0], h[1], h[2], h[3]));
+                                    st_smem_v4(buf + lane * 128 + (((j0 + 1) ^ (lane & 7)) << 4),
+                                               make_uint4(h[4], h[5], h[6], h[7]));
+                                } else {
+                                    store_piece_masked(p, m0 + row, n0 + (b0 + g0 + h2) * 16, h);
+                                }
+                            }
+                        }
+                    } else
                     for (int s0 = 0; s0 < gn; s0 += 2) {   // two chunks (32 columns) per TMEM wait
                         const int sn = min(2, gn - s0);
                         uint32_t r[32];   // this unit's own sums for the two chunks
@@ -799,6 +846,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
     constexpr int kTileRows = kPair ? 2 * kBM : kBM;
     // Tile rows handled per unit by the cluster (two pair tiles in the four-CTA form).
     constexpr int kUnitRows = kQuad ? 2 * kTileRows : kTileRows;
+    const int nps = p.stages / kSlots;   // barrier phases in the slot ring
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
@@ -863,21 +911,25 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                     ((b_mn && !b_3d) || narrow) ? static_cast<uint32_t>(bcols) * 128u : p.stage_b_bytes;
                 const uint32_t tx = kPair ? 2u * (kStageABytes + b_bytes)
                                           : (a_tma ? kStageABytes : 0u) + (b_tma ? b_bytes : 0u);
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                for (int kb = w.kb0; kb < w.kb1; kb += kSlots) {
+                    const int nk = min(kSlots, w.kb1 - kb);   // K blocks in this barrier phase
                     if (!wait_bar<kPair>(bar_empty(L.bars, stage), phase ^ 1u, abort, p.timeout_ns)) {
                         raise_abort(p, abort);
                         ok = false;
                         break;
                     }
-                    const uint32_t sa = L.a + stage * kStageABytes;
-                    const uint32_t sb = L.b + stage * p.stage_b_bytes;
                     const uint32_t fb = bar_full(L.bars, stage);
-                    const int32_t k0 = kb * kBK;
+                    // The leader (pair form) expects both CTAs' bytes of every slot of
+                    // the phase on its own barrier; the peer's copies complete there.
+                    if (t == tiss && (a_tma || b_tma) && (!kPair || leader))
+                        mbar_arrive_expect_tx(fb, tx * static_cast<uint32_t>(nk));
+                    for (int h = 0; h < nk; ++h) {
+                    const int slot = stage * kSlots + h;
+                    const uint32_t sa = L.a + slot * kStageABytes;
+                    const uint32_t sb = L.b + slot * p.stage_b_bytes;
+                    const int32_t k0 = (kb + h) * kBK;
                     if (t == tiss && (a_tma || b_tma)) {
                         if (kPair) {
-                            // The leader expects both CTAs' bytes on its own barrier;
-                            // the peer's copies complete on the leader's barrier.
-                            if (leader) mbar_arrive_expect_tx(fb, tx);
                             const uint32_t fbc = mapa_shared(fb, lead_rank);
                             if (!a_mn) {
                                 tma_load_2d_pair(sa, &p.tmA, k0, static_cast<int32_t>(m0), fbc);
@@ -908,7 +960,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                                     tma_load_2d_pair(sb + j * 8192, &p.tmB, static_cast<int32_t>(n0 + 64 * j), k0, fbc);
                             }
                         } else {
-                            mbar_arrive_expect_tx(fb, tx);
                             if (a_tma) {
                                 if (!a_mn) {
                                     tma_load_2d(sa, &p.tmA, k0, static_cast<int32_t>(m0), fb);
@@ -936,11 +987,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                             gather_tile(p.A, p.a_sm, p.a_sk, p.M, p.K, m0, k0, kBM, a_mn, sa, t);
                         if (!b_tma)
                             gather_tile(p.B, p.b_sn, p.b_sk, p.N, p.K, n0, k0, w.bn, b_mn, sb, t);
+                    }
+                    }
+                    if (!kPair && any_masked) {
                         fence_proxy_async_smem();
                         mbar_arrive(fb);
                     }
                     ++issued;
-                    if (++stage == p.stages) {
+                    if (++stage == nps) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -948,11 +1002,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
             }
             if (!ok && t == tiss && (a_tma || b_tma) && (!kPair || leader)) {
                 // Let TMA copies already in flight land before the CTA exits:
-                // wait (bounded) on the full barrier of each recently issued stage.
-                const int n = issued < p.stages ? issued : p.stages;
+                // wait (bounded) on the full barrier of each recently issued phase.
+                const int n = issued < nps ? issued : nps;
                 for (int i = 0; i < n; ++i) {
                     if (--stage < 0) {
-                        stage = p.stages - 1;
+                        stage = nps - 1;
                         phase ^= 1u;
                     }
                     wait_bar<kPair>(bar_full(L.bars, stage), phase, nullptr, kDrainTimeoutNs);
@@ -981,35 +1035,39 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                 const uint32_t d = tmem_base + acc * kAccStride;
                 // N field (bits 17-22) of the instruction descriptor: this unit's width
                 const uint32_t idesc = (p.idesc & ~(0x3Fu << 17)) | ((static_cast<uint32_t>(w.bn) >> 3) << 17);
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                for (int kb = w.kb0; kb < w.kb1; kb += kSlots) {
+                    const int nk = min(kSlots, w.kb1 - kb);   // K blocks in this barrier phase
                     if (!wait_bar<kPair>(bar_full(L.bars, stage), phase, abort, p.timeout_ns)) {
                         raise_abort(p, abort);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = L.a + stage * kStageABytes;
-                    const uint32_t sb = L.b + stage * p.stage_b_bytes;
+                    for (int h = 0; h < nk; ++h) {
+                        const int slot = stage * kSlots + h;
+                        const uint32_t sa = L.a + slot * kStageABytes;
+                        const uint32_t sb = L.b + slot * p.stage_b_bytes;
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k) {
-                        // K-major: the 16-wide K step is 32 bytes inside the
-                        // swizzle row.  MN-major: it is 16 K rows of 128 bytes.
-                        const uint64_t ad = a_mn ? umma_desc_sw128(sa + k * 2048, 8192, 1024)
-                                                 : umma_desc_sw128(sa + k * 32, 16, 1024);
-                        const uint64_t bd = b_mn ? umma_desc_sw128(sb + k * 2048, b_atom_rows, 1024)
-                                                 : umma_desc_sw128(sb + k * 32, 16, 1024);
-                        const uint32_t accum = (kb > w.kb0 || k > 0) ? 1u : 0u;
-                        if (kPair)
-                            umma_f16_pair(d, ad, bd, idesc, accum);
-                        else
-                            umma_f16(d, ad, bd, idesc, accum);
+                        for (int k = 0; k < kBK / 16; ++k) {
+                            // K-major: the 16-wide K step is 32 bytes inside the
+                            // swizzle row.  MN-major: it is 16 K rows of 128 bytes.
+                            const uint64_t ad = a_mn ? umma_desc_sw128(sa + k * 2048, 8192, 1024)
+                                                     : umma_desc_sw128(sa + k * 32, 16, 1024);
+                            const uint64_t bd = b_mn ? umma_desc_sw128(sb + k * 2048, b_atom_rows, 1024)
+                                                     : umma_desc_sw128(sb + k * 32, 16, 1024);
+                            const uint32_t accum = (kb + h > w.kb0 || k > 0) ? 1u : 0u;
+                            if (kPair)
+                                umma_f16_pair(d, ad, bd, idesc, accum);
+                            else
+                                umma_f16(d, ad, bd, idesc, accum);
+                        }
                     }
                     any = true;
                     if (kPair)
                         umma_commit_pair_mc(bar_empty(L.bars, stage), kQuad ? 0xF : 0x3);
                     else
                         umma_commit(bar_empty(L.bars, stage));
-                    if (++stage == p.stages) {
+                    if (++stage == nps) {
                         stage = 0;
                         phase ^= 1u;
                     }

@@ -201,8 +201,9 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
  *                              2: stream-K tail whenever the tiles do not divide evenly
  *   GEMM_F16_OPT_TAIL_SPLIT    0 default: cut the last partial wave of tiles along N
  *                              into narrower tiles; 1 never
- *   GEMM_F16_OPT_MAX_STAGES    >= 2: cap the pipeline depth (default: as many stages
- *                              as shared memory holds, at most 16)
+ *   GEMM_F16_OPT_MAX_STAGES    >= 2: cap the pipeline depth in 64-wide K slots, rounded
+ *                              down to an even count (default: as many as shared memory
+ *                              holds, at most 16)
  *   GEMM_F16_OPT_MULTICAST     0 default / 1: pairs load their own B; 2: clusters of four
  *                              CTAs (two pairs on adjacent 256-row tiles) read each B tile
  *                              once and multicast it (whole 256x256 tiles only)
