@@ -47,7 +47,10 @@ OPT_MULTICAST = 12
 # Every symbol include/gemm_f16.h declares.
 EXPORTED = ("gemm_f16", "gemm_f16_ws", "gemm_f16_workspace_size", "gemm_f16_status_string",
             "gemm_f16_device_status", "gemm_f16_get_plan", "gemm_f16_set_option",
-            "gemm_f16_abi_version", "gemm_f16_noalloc")
+            "gemm_f16_abi_version", "gemm_f16_noalloc", "gemm_f16_batched", "gemm_f16_grouped")
+
+# Most groups of one gemm_f16_grouped call.
+MAX_GROUPS = 64
 
 # Size of the fixed device scratch array behind gemm_f16_noalloc (8 MiB).
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -102,6 +105,12 @@ def lib():
                 L.gemm_f16_abi_version.restype = ctypes.c_int
                 L.gemm_f16_noalloc.argtypes = [P, I64, I64, P, I64, I64, P, I64, I64, I64, I64, P]
                 L.gemm_f16_noalloc.restype = ctypes.c_int
+                L.gemm_f16_batched.argtypes = [P, I64, I64, I64, P, I64, I64, I64, P, I64, I64, I64, I64, I64,
+                                               I64, P]
+                L.gemm_f16_batched.restype = ctypes.c_int
+                L.gemm_f16_grouped.argtypes = [P, I64, I64, P, I64, I64, I64, P, I64, ctypes.POINTER(I64), I64,
+                                               I64, I64, P]
+                L.gemm_f16_grouped.restype = ctypes.c_int
                 _lib = L
     return _lib
 
@@ -132,6 +141,23 @@ def gemm_f16_noalloc(A: int, stride_am: int, stride_ak: int, B: int, stride_bk: 
     a cudaMalloc'd workspace (see include/gemm_f16.h)."""
     _check(lib().gemm_f16_noalloc(A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, M, N, K,
                                   stream or None), "gemm_f16_noalloc")
+
+
+def gemm_f16_batched(A: int, stride_ab: int, stride_am: int, stride_ak: int, B: int, stride_bb: int,
+                     stride_bk: int, stride_bn: int, C: int, stride_cb: int, ldc: int, M: int, N: int, K: int,
+                     batch: int, stream: int = 0) -> None:
+    """`batch` problems C_b = A_b * B_b of one shape (see include/gemm_f16.h)."""
+    _check(lib().gemm_f16_batched(A, stride_ab, stride_am, stride_ak, B, stride_bb, stride_bk, stride_bn, C,
+                                  stride_cb, ldc, M, N, K, batch, stream or None), "gemm_f16_batched")
+
+
+def gemm_f16_grouped(A: int, stride_am: int, stride_ak: int, B: int, stride_bg: int, stride_bk: int,
+                     stride_bn: int, C: int, ldc: int, group_rows, N: int, K: int, stream: int = 0) -> None:
+    """Grouped problems sharing K and N: group g owns group_rows[g] consecutive rows
+    of A and C and multiplies them by B + g*stride_bg (see include/gemm_f16.h)."""
+    rows = (ctypes.c_int64 * len(group_rows))(*[int(r) for r in group_rows])
+    _check(lib().gemm_f16_grouped(A, stride_am, stride_ak, B, stride_bg, stride_bk, stride_bn, C, ldc, rows,
+                                  len(group_rows), N, K, stream or None), "gemm_f16_grouped")
 
 
 def gemm_f16_workspace_size(M: int, N: int, K: int) -> int:
@@ -193,6 +219,46 @@ def matmul(a, b, out=None, stream=None):
     with torch.cuda.device(a.device):
         s = stream if stream is not None else torch.cuda.current_stream(a.device)
         gemm_f16(*args, stream=s.cuda_stream)
+    return out
+
+
+def bmm(a, b, out=None, stream=None):
+    """fp16 C[i] = a[i] @ b[i] for 3-D CUDA torch tensors (a batch dimension of
+    stride 0 shares that operand); returns C."""
+    import torch
+
+    if a.dim() != 3 or b.dim() != 3 or a.shape[0] != b.shape[0] or a.shape[2] != b.shape[1]:
+        raise ValueError("bmm takes [batch, M, K] and [batch, K, N]")
+    if out is None:
+        out = torch.empty((a.shape[0], a.shape[1], b.shape[2]), dtype=torch.float16, device=a.device)
+    if out.stride(2) != 1:
+        raise ValueError("out must have a unit column stride")
+    with torch.cuda.device(a.device):
+        s = stream if stream is not None else torch.cuda.current_stream(a.device)
+        gemm_f16_batched(a.data_ptr(), a.stride(0), a.stride(1), a.stride(2), b.data_ptr(), b.stride(0),
+                         b.stride(1), b.stride(2), out.data_ptr(), out.stride(0), out.stride(1), a.shape[1],
+                         b.shape[2], a.shape[2], a.shape[0], stream=s.cuda_stream)
+    return out
+
+
+def grouped_mm(a, b, group_rows, out=None, stream=None):
+    """fp16 grouped product: rows of `a` [sum(group_rows), K] in consecutive groups,
+    group g times b[g] ([G, K, N]); returns C [sum(group_rows), N]."""
+    import torch
+
+    if a.dim() != 2 or b.dim() != 3 or b.shape[0] != len(group_rows) or a.shape[1] != b.shape[1]:
+        raise ValueError("grouped_mm takes [rows, K], [G, K, N] and G row counts")
+    if sum(int(r) for r in group_rows) != a.shape[0]:
+        raise ValueError("group_rows must add up to a's rows")
+    if out is None:
+        out = torch.empty((a.shape[0], b.shape[2]), dtype=torch.float16, device=a.device)
+    if out.stride(1) != 1:
+        raise ValueError("out must have a unit column stride")
+    with torch.cuda.device(a.device):
+        s = stream if stream is not None else torch.cuda.current_stream(a.device)
+        gemm_f16_grouped(a.data_ptr(), a.stride(0), a.stride(1), b.data_ptr(), b.stride(0), b.stride(1),
+                         b.stride(2), out.data_ptr(), out.stride(0), group_rows, b.shape[2], a.shape[1],
+                         stream=s.cuda_stream)
     return out
 
 

@@ -13,6 +13,7 @@
 
 #include "gemm_f16.h"
 #include "gemm_kernel.cuh"
+static_assert(GEMM_F16_MAX_GROUPS == gemm_f16_dev::kMaxGroups, "the header and the kernel agree on the group limit");
 
 using gemm_f16_dev::KernelParams;
 
@@ -153,7 +154,24 @@ struct Args {
     int64_t sbk, sbn;
     void* C;
     int64_t ldc, M, N, K;
+    // Batched (batch > 1, no group table): problem b at element offsets
+    // b*sab, b*sbb, b*scb.  Grouped (rows != nullptr): `batch` groups, group g
+    // owning rows rows[g] of the concatenated A and C (M is their sum) and
+    // problem g of B at offset g*sbb.
+    int64_t batch = 1;
+    int64_t sab = 0, sbb = 0, scb = 0;
+    const int64_t* rows = nullptr;
 };
+
+// Elements spanned by `n` copies of a view of `e` elements placed `stride`
+// apart (false on overflow).
+bool batch_extent(int64_t e, int64_t n, int64_t stride, int64_t* total)
+{
+    int64_t t;
+    if (__builtin_mul_overflow(n - 1, stride, &t) || __builtin_add_overflow(t, e, &t) || t > INT64_MAX / 2) return false;
+    *total = t;
+    return true;
+}
 
 gemm_f16_status validate(const Args& a, bool check_memory, DevInfo** dev)
 {
@@ -162,10 +180,22 @@ gemm_f16_status validate(const Args& a, bool check_memory, DevInfo** dev)
     if (a.sam <= 0 || a.sak <= 0 || a.sbk <= 0 || a.sbn <= 0 || a.ldc < a.N) return GEMM_F16_ERR_INVALID_VALUE;
     if ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.B) | reinterpret_cast<uintptr_t>(a.C)) & 1u)
         return GEMM_F16_ERR_INVALID_VALUE;
+    if (a.batch < 1 || a.sab < 0 || a.sbb < 0 || a.scb < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (a.rows && a.batch > gemm_f16_dev::kMaxGroups) return GEMM_F16_ERR_INVALID_VALUE;
     int64_t ea, eb, ec;
     if (!view_extent(a.M, a.K, a.sam, a.sak, &ea) || !view_extent(a.K, a.N, a.sbk, a.sbn, &eb) ||
         !view_extent(a.M, a.N, a.ldc, 1, &ec))
         return GEMM_F16_ERR_INVALID_VALUE;
+    if (a.batch > 1) {
+        // B (and, batched, A and C) repeat per problem.  The problems' outputs must
+        // not overlap: a C stride below one view's span is refused.
+        if (!batch_extent(eb, a.batch, a.sbb, &eb)) return GEMM_F16_ERR_INVALID_VALUE;
+        if (!a.rows) {
+            if (a.scb < ec) return GEMM_F16_ERR_INVALID_VALUE;
+            if (!batch_extent(ea, a.batch, a.sab, &ea) || !batch_extent(ec, a.batch, a.scb, &ec))
+                return GEMM_F16_ERR_INVALID_VALUE;
+        }
+    }
     const uintptr_t pa = reinterpret_cast<uintptr_t>(a.A), pb = reinterpret_cast<uintptr_t>(a.B),
                     pc = reinterpret_cast<uintptr_t>(a.C);
     if (overlaps(pc, 2 * ec, pa, 2 * ea) || overlaps(pc, 2 * ec, pb, 2 * eb)) return GEMM_F16_ERR_ALIAS;
@@ -205,15 +235,18 @@ OperandChoice choose_operand(const void* ptr, int64_t s_mn, int64_t s_k, int64_t
     return {false, mn};
 }
 
+// `nb` > 0 adds a trailing batch dimension of nb problems `bstride_bytes` apart
+// (the box takes one problem).
 bool encode_2d(CUtensorMap* tm, const void* ptr, uint64_t inner, uint64_t outer, uint64_t pitch_bytes,
-               uint32_t box_inner, uint32_t box_outer)
+               uint32_t box_inner, uint32_t box_outer, uint64_t nb = 0, uint64_t bstride_bytes = 0)
 {
     if (!g_encode) return false;
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {pitch_bytes};
-    cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+    cuuint64_t dims[3] = {inner, outer, nb};
+    cuuint64_t strides[2] = {pitch_bytes, bstride_bytes};
+    cuuint32_t box[3] = {box_inner, box_outer, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, nb > 0 ? 3 : 2, const_cast<void*>(ptr), dims, strides,
+                          box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -225,14 +258,16 @@ bool encode_2d(CUtensorMap* tm, const void* ptr, uint64_t inner, uint64_t outer,
 // memory as `atoms` consecutive 64 x 64 swizzle-atom columns, the layout the
 // 2-D form builds with one copy per column.  Every element the map can reach
 // lies inside the operand's rows, so no read leaves the MN x K view.
-bool encode_3d_mn(CUtensorMap* tm, const void* ptr, uint64_t MN, uint64_t K, uint64_t pitch_bytes, uint32_t atoms)
+bool encode_3d_mn(CUtensorMap* tm, const void* ptr, uint64_t MN, uint64_t K, uint64_t pitch_bytes, uint32_t atoms,
+                  uint64_t nb = 0, uint64_t bstride_bytes = 0)
 {
     if (!g_encode || MN % 64 != 0) return false;
-    cuuint64_t dims[3] = {64, K, MN / 64};
-    cuuint64_t strides[2] = {pitch_bytes, 128};
-    cuuint32_t box[3] = {64, 64, atoms};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+    cuuint64_t dims[4] = {64, K, MN / 64, nb};
+    cuuint64_t strides[3] = {pitch_bytes, 128, bstride_bytes};
+    cuuint32_t box[4] = {64, 64, atoms, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, nb > 0 ? 4 : 3, const_cast<void*>(ptr), dims, strides,
+                          box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -249,12 +284,16 @@ bool set_smem_attributes(DevInfo& dev)
 {
     std::lock_guard<std::mutex> lk(g_mutex);
     if (dev.smem_attr_set) return true;
-    if (cudaFuncSetAttribute(gemm_f16_dev::gemm_f16_persistent<false, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(gemm_f16_dev::gemm_f16_persistent<true, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(gemm_f16_dev::gemm_f16_persistent<true, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) != cudaSuccess) {
+    using namespace gemm_f16_dev;
+    const void* kernels[] = {reinterpret_cast<const void*>(gemm_f16_persistent<false, false, false>),
+                             reinterpret_cast<const void*>(gemm_f16_persistent<true, false, false>),
+                             reinterpret_cast<const void*>(gemm_f16_persistent<true, true, false>),
+                             reinterpret_cast<const void*>(gemm_f16_persistent<false, false, true>),
+                             reinterpret_cast<const void*>(gemm_f16_persistent<true, false, true>)};
+    bool ok = true;
+    for (const void* k : kernels)
+        ok = ok && cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) == cudaSuccess;
+    if (!ok) {
         cudaGetLastError();
         return false;
     }
@@ -285,8 +324,9 @@ int max_clusters(DevInfo& dev, int smem, int size)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    const cudaError_t e = size == 4 ? cudaOccupancyMaxActiveClusters(&n, gemm_f16_dev::gemm_f16_persistent<true, true>, &cfg)
-                                    : cudaOccupancyMaxActiveClusters(&n, gemm_f16_dev::gemm_f16_persistent<true, false>, &cfg);
+    const cudaError_t e =
+        size == 4 ? cudaOccupancyMaxActiveClusters(&n, gemm_f16_dev::gemm_f16_persistent<true, true, false>, &cfg)
+                  : cudaOccupancyMaxActiveClusters(&n, gemm_f16_dev::gemm_f16_persistent<true, false, false>, &cfg);
     if (e != cudaSuccess) {
         cudaGetLastError();
         n = 0;
@@ -397,11 +437,11 @@ Schedule make_schedule(int64_t tiles, int kblocks, int splits, int max_workers, 
     return s;
 }
 
-void shape_plan(int64_t M, int64_t N, int64_t K, int sms, bool* swap, int64_t* Mv, int64_t* Nv, int* BN,
-                int* tiles_m, int* tiles_n, int* kblocks, int* splits)
+void shape_plan(int64_t M, int64_t N, int64_t K, int sms, bool allow_swap, bool* swap, int64_t* Mv, int64_t* Nv,
+                int* BN, int* tiles_m, int* tiles_n, int* kblocks, int* splits)
 {
     const int64_t sw = opt(GEMM_F16_OPT_SWAP);
-    *swap = (sw == 2) || (sw == 0 && M <= 64 && N >= 2 * M);
+    *swap = allow_swap && ((sw == 2) || (sw == 0 && M <= 64 && N >= 2 * M));
     *Mv = *swap ? N : M;
     *Nv = *swap ? M : N;
     int bn;
@@ -440,7 +480,10 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     bool swap;
     int64_t Mv, Nv;
     int BN, tiles_m, tiles_n, kblocks, splits;
-    shape_plan(a.M, a.N, a.K, dev.sms, &swap, &Mv, &Nv, &BN, &tiles_m, &tiles_n, &kblocks, &splits);
+    const bool grouped = a.rows != nullptr;
+    const bool batched = !grouped && a.batch > 1;
+    // (groups differ in M, so the swapped form, which tiles over M as N, is not used)
+    shape_plan(a.M, a.N, a.K, dev.sms, !grouped, &swap, &Mv, &Nv, &BN, &tiles_m, &tiles_n, &kblocks, &splits);
     if (BN < 16 || BN > 256 || BN % 16 != 0) return GEMM_F16_ERR_INVALID_VALUE;
 
     // Kernel view: C'[m,n] = sum_k A'[m,k] B'[k,n].
@@ -454,12 +497,28 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
         kp.C = static_cast<__half*>(a.C), kp.c_sm = 1, kp.c_sn = a.ldc;
     }
     kp.M = Mv, kp.N = Nv, kp.K = a.K;
+    // Batch strides of the kernel view; an operand shared by every problem
+    // (stride 0) needs no batch dimension.
+    int64_t a_bs = 0, b_bs = 0, c_bs = 0;
+    if (batched) {
+        a_bs = swap ? a.sbb : a.sab;
+        b_bs = swap ? a.sab : a.sbb;
+        c_bs = a.scb;
+    } else if (grouped) {
+        b_bs = a.sbb;
+    }
+    const bool a_bd = batched && a_bs > 0;
+    const bool b_bd = (batched || grouped) && a.batch > 1 && b_bs > 0;
+    const bool c_bd = batched;
+    auto bs_ok = [](int64_t bs) { return (2 * bs) % 16 == 0 && 2 * bs < (int64_t(1) << 40); };   // TMA stride rules
 
     const int64_t fg = opt(GEMM_F16_OPT_FORCE_GATHER);
     load_entry_points();
     const bool have_tma = g_encode != nullptr;
-    OperandChoice ca = choose_operand(kp.A, kp.a_sm, kp.a_sk, Mv, a.K, gemm_f16_dev::kBM, have_tma && !(fg & 1));
-    OperandChoice cb = choose_operand(kp.B, kp.b_sn, kp.b_sk, Nv, a.K, BN, have_tma && !(fg & 2));
+    OperandChoice ca = choose_operand(kp.A, kp.a_sm, kp.a_sk, Mv, a.K, gemm_f16_dev::kBM,
+                                      have_tma && !(fg & 1) && (!a_bd || bs_ok(a_bs)));
+    OperandChoice cb = choose_operand(kp.B, kp.b_sn, kp.b_sk, Nv, a.K, BN,
+                                      have_tma && !(fg & 2) && (!b_bd || bs_ok(b_bs)));
 
     // Pair form (two CTAs per 256 x BN tile): TMA operands, no split-K, and a
     // B half that is a whole number of 64-column swizzle atoms.
@@ -469,21 +528,44 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     const int tile_rows = pair ? 2 * gemm_f16_dev::kBM : gemm_f16_dev::kBM;
     const int bcols = pair ? BN / 2 : BN;   // B columns one CTA loads
     if (pair) tiles_m = static_cast<int>((Mv + tile_rows - 1) / tile_rows);
-    const int64_t tiles = static_cast<int64_t>(tiles_m) * tiles_n;
+    int64_t tiles = static_cast<int64_t>(tiles_m) * tiles_n * (batched ? a.batch : 1);
+    if (grouped) {   // per group: ceil(rows / tile_rows) tile rows; tiles numbered group by group
+        int64_t t0 = 0, row0 = 0;
+        for (int64_t g = 0; g < a.batch; ++g) {
+            const int64_t tm = (a.rows[g] + tile_rows - 1) / tile_rows;
+            if (t0 > INT32_MAX / 4) return GEMM_F16_ERR_INVALID_VALUE;
+            kp.g_tile0[g] = static_cast<int>(t0);
+            kp.g_tm[g] = static_cast<int>(tm);
+            kp.g_row0[g] = row0;
+            kp.g_rows[g] = a.rows[g];
+            t0 += tm * tiles_n;
+            row0 += a.rows[g];
+        }
+        kp.g_tile0[a.batch] = static_cast<int>(t0);
+        tiles = t0;
+    }
     if (tiles * splits > INT32_MAX / 4 || tiles * kblocks > (int64_t(1) << 40)) return GEMM_F16_ERR_INVALID_VALUE;
+    kp.gmode = grouped ? 2 : (batched ? 1 : 0);
+    kp.groups = static_cast<int>(a.batch);
+    kp.a_bs = a_bs, kp.b_bs = b_bs, kp.c_bs = c_bs;
     // Four-CTA multicast form: two pairs on vertically adjacent tiles share each
     // B tile (whole tiles only: no K cut, no tail split).
     const int64_t mc_opt = opt(GEMM_F16_OPT_MULTICAST);
-    bool quad = pair && mc_opt == 2 && BN == 256 && splits == 1 && opt(GEMM_F16_OPT_STREAMK) != 2 && tiles_m >= 2;
+    bool quad = pair && mc_opt == 2 && BN == 256 && splits == 1 && opt(GEMM_F16_OPT_STREAMK) != 2 && tiles_m >= 2 &&
+                !batched && !grouped;
 
     bool a_3d = false, b_3d = false;
+    // trailing batch dimensions (0: none)
+    const uint64_t nb_a = a_bd ? a.batch : 0, bst_a = a_bd ? 2 * a_bs : 0;
+    const uint64_t nb_b = b_bd ? a.batch : 0, bst_b = b_bd ? 2 * b_bs : 0;
     if (ca.tma) {
         a_3d = ca.mn && encode_3d_mn(&kp.tmA, kp.A, Mv, a.K, a.K == 1 ? round_up(2 * Mv, 16) : 2 * kp.a_sk,
-                                     gemm_f16_dev::kBM / 64);
+                                     gemm_f16_dev::kBM / 64, nb_a, bst_a);
         const bool ok = a_3d ? true
-                        : ca.mn ? encode_2d(&kp.tmA, kp.A, Mv, a.K, a.K == 1 ? round_up(2 * Mv, 16) : 2 * kp.a_sk, 64, 64)
+                        : ca.mn ? encode_2d(&kp.tmA, kp.A, Mv, a.K, a.K == 1 ? round_up(2 * Mv, 16) : 2 * kp.a_sk, 64, 64,
+                                            nb_a, bst_a)
                               : encode_2d(&kp.tmA, kp.A, a.K, Mv, Mv == 1 ? round_up(2 * a.K, 16) : 2 * kp.a_sm, 64,
-                                          gemm_f16_dev::kBM);
+                                          gemm_f16_dev::kBM, nb_a, bst_a);
         if (!ok) {
             if (pair) return GEMM_F16_ERR_LAUNCH;
             ca = choose_operand(kp.A, kp.a_sm, kp.a_sk, Mv, a.K, gemm_f16_dev::kBM, false);
@@ -494,11 +576,12 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     auto encode_b = [&](bool quarter) {
         const int cols = quarter ? bcols / 2 : bcols;
         b_3d = cb.mn && encode_3d_mn(&kp.tmB, kp.B, Nv, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk,
-                                     static_cast<uint32_t>(cols / 64));
+                                     static_cast<uint32_t>(cols / 64), nb_b, bst_b);
         return b_3d ? true
-               : cb.mn ? encode_2d(&kp.tmB, kp.B, Nv, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk, 64, 64)
+               : cb.mn ? encode_2d(&kp.tmB, kp.B, Nv, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk, 64, 64,
+                                   nb_b, bst_b)
                        : encode_2d(&kp.tmB, kp.B, a.K, Nv, Nv == 1 ? round_up(2 * a.K, 16) : 2 * kp.b_sn, 64,
-                                   static_cast<uint32_t>(cols));
+                                   static_cast<uint32_t>(cols), nb_b, bst_b);
     };
     if (cb.tma) {
         if (!encode_b(quad)) {
@@ -506,10 +589,17 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
             cb = choose_operand(kp.B, kp.b_sn, kp.b_sk, Nv, a.K, BN, false);
         }
     }
-    bool c_tma = have_tma && !(fg & 4) && !swap && splits == 1 && BN % 64 == 0 &&
+    // TMA stores write whole 16-byte chunks at the N edge, so a C row whose
+    // width is not a multiple of 8 elements would get its pitch padding
+    // overwritten: such a C goes through the masked stores.
+    bool c_tma = have_tma && !(fg & 4) && !swap && splits == 1 && BN % 64 == 0 && a.N % 8 == 0 &&
                  (reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc * 2) % 16 == 0 && a.M < (int64_t(1) << 32) &&
-                 a.N < (int64_t(1) << 32) && (a.ldc * 2) < (int64_t(1) << 40);
-    if (c_tma) c_tma = encode_2d(&kp.tmC, a.C, a.N, a.M, 2 * a.ldc, 64, 32);
+                 a.N < (int64_t(1) << 32) && (a.ldc * 2) < (int64_t(1) << 40) && (!c_bd || bs_ok(c_bs));
+    if (c_tma)
+        c_tma = encode_2d(&kp.tmC, a.C, a.N, a.M, 2 * a.ldc, 64, 32, c_bd ? a.batch : 0, c_bd ? 2 * c_bs : 0);
+    kp.a_bdim = (ca.tma && a_bd) ? 1u : 0u;
+    kp.b_bdim = (cb.tma && b_bd) ? 1u : 0u;
+    kp.c_bdim = (c_tma && c_bd) ? 1u : 0u;
 
     const uint32_t stage_b = static_cast<uint32_t>(bcols) * gemm_f16_dev::kBK * 2;
     const uint32_t stage_bytes = gemm_f16_dev::kStageABytes + stage_b;
@@ -548,7 +638,7 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     if (max_workers < 1) return GEMM_F16_ERR_LAUNCH;
     // Units of the four-CTA form cover two tile rows.
     const int unit_rows = quad ? (tiles_m + 1) / 2 : tiles_m;
-    const int64_t unit_tiles = static_cast<int64_t>(unit_rows) * tiles_n;
+    const int64_t unit_tiles = quad ? static_cast<int64_t>(unit_rows) * tiles_n : tiles;
     // Narrowest tail piece: the pair form keeps >= 64 B columns per CTA; a
     // TMA-stored C needs whole 64-column boxes; the four-CTA form never cuts.
     const Schedule sch = make_schedule(unit_tiles, kblocks, splits, static_cast<int>(max_workers), BN,
@@ -573,9 +663,9 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
         // form already reads one 64-column box per atom column).
         const int piece = bcols / sch.tail_split;
         const bool ok = b_3d ? encode_3d_mn(&kp.tmB2, kp.B, Nv, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk,
-                                            static_cast<uint32_t>(piece / 64))
+                                            static_cast<uint32_t>(piece / 64), nb_b, bst_b)
                              : encode_2d(&kp.tmB2, kp.B, a.K, Nv, Nv == 1 ? round_up(2 * a.K, 16) : 2 * kp.b_sn, 64,
-                                         static_cast<uint32_t>(piece));
+                                         static_cast<uint32_t>(piece), nb_b, bst_b);
         if (!ok) return GEMM_F16_ERR_LAUNCH;
     }
     kp.panel = static_cast<int>(panel > 0 ? panel : 8);
@@ -624,10 +714,16 @@ gemm_f16_status launch(Plan& pl, DevInfo& dev, float* partials, int* counters, c
     KernelParams& kp = pl.kp;
     kp.ws = partials;
     kp.counters = counters;
+    if (pl.pub.grid == 0) return GEMM_F16_OK;   // no tile (every group empty)
     if (!set_smem_attributes(dev)) return GEMM_F16_ERR_LAUNCH;
+    const bool multi = kp.gmode != 0;
     if (!pl.pub.pair) {
-        gemm_f16_dev::gemm_f16_persistent<false, false>
-            <<<pl.pub.grid, gemm_f16_dev::kNumThreads, pl.pub.smem_bytes, stream>>>(kp);
+        if (multi)
+            gemm_f16_dev::gemm_f16_persistent<false, false, true>
+                <<<pl.pub.grid, gemm_f16_dev::kNumThreads, pl.pub.smem_bytes, stream>>>(kp);
+        else
+            gemm_f16_dev::gemm_f16_persistent<false, false, false>
+                <<<pl.pub.grid, gemm_f16_dev::kNumThreads, pl.pub.smem_bytes, stream>>>(kp);
     } else {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
@@ -641,9 +737,10 @@ gemm_f16_status launch(Plan& pl, DevInfo& dev, float* partials, int* counters, c
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        const cudaError_t e = pl.pub.cluster_ctas == 4
-                                  ? cudaLaunchKernelEx(&cfg, gemm_f16_dev::gemm_f16_persistent<true, true>, kp)
-                                  : cudaLaunchKernelEx(&cfg, gemm_f16_dev::gemm_f16_persistent<true, false>, kp);
+        const cudaError_t e =
+            pl.pub.cluster_ctas == 4 ? cudaLaunchKernelEx(&cfg, gemm_f16_dev::gemm_f16_persistent<true, true, false>, kp)
+            : multi                  ? cudaLaunchKernelEx(&cfg, gemm_f16_dev::gemm_f16_persistent<true, false, true>, kp)
+                                     : cudaLaunchKernelEx(&cfg, gemm_f16_dev::gemm_f16_persistent<true, false, false>, kp);
         if (e != cudaSuccess) {
             cudaGetLastError();
             return GEMM_F16_ERR_LAUNCH;
@@ -805,6 +902,35 @@ gemm_f16_status gemm_f16_noalloc(const void* A, int64_t stride_am, int64_t strid
     return run_noalloc(a, stream);
 }
 
+gemm_f16_status gemm_f16_batched(const void* A, int64_t stride_ab, int64_t stride_am, int64_t stride_ak,
+                                 const void* B, int64_t stride_bb, int64_t stride_bk, int64_t stride_bn, void* C,
+                                 int64_t stride_cb, int64_t ldc, int64_t M, int64_t N, int64_t K, int64_t batch,
+                                 cudaStream_t stream)
+{
+    Args a{A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, M, N, K};
+    a.batch = batch;
+    a.sab = stride_ab, a.sbb = stride_bb, a.scb = stride_cb;
+    return run(a, nullptr, 0, true, stream);
+}
+
+gemm_f16_status gemm_f16_grouped(const void* A, int64_t stride_am, int64_t stride_ak, const void* B,
+                                 int64_t stride_bg, int64_t stride_bk, int64_t stride_bn, void* C, int64_t ldc,
+                                 const int64_t* group_rows, int64_t groups, int64_t N, int64_t K,
+                                 cudaStream_t stream)
+{
+    if (!group_rows || groups < 1 || groups > gemm_f16_dev::kMaxGroups) return GEMM_F16_ERR_INVALID_VALUE;
+    int64_t total = 0;
+    for (int64_t g = 0; g < groups; ++g) {
+        if (group_rows[g] < 0 || __builtin_add_overflow(total, group_rows[g], &total)) return GEMM_F16_ERR_INVALID_VALUE;
+    }
+    if (total == 0) return (A && B && C && N > 0 && K > 0) ? GEMM_F16_OK : GEMM_F16_ERR_INVALID_VALUE;
+    Args a{A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, total, N, K};
+    a.batch = groups;
+    a.sbb = stride_bg;
+    a.rows = group_rows;
+    return run(a, nullptr, 0, true, stream);
+}
+
 gemm_f16_status gemm_f16_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes)
 {
     if (!bytes || M <= 0 || N <= 0 || K <= 0) return GEMM_F16_ERR_INVALID_VALUE;
@@ -814,7 +940,7 @@ gemm_f16_status gemm_f16_workspace_size(int64_t M, int64_t N, int64_t K, size_t*
     bool swap;
     int64_t Mv, Nv;
     int BN, tiles_m, tiles_n, kblocks, splits;
-    shape_plan(M, N, K, dev->sms, &swap, &Mv, &Nv, &BN, &tiles_m, &tiles_n, &kblocks, &splits);
+    shape_plan(M, N, K, dev->sms, true, &swap, &Mv, &Nv, &BN, &tiles_m, &tiles_n, &kblocks, &splits);
     // The plan also depends on the operands' layout (single or pair form), so
     // report the larger of the two requirements.
     size_t need = 0;

@@ -60,6 +60,7 @@ constexpr int kMaxStages = 16;
 // issuer waits once and commits once per kSlots * 4 MMAs, which halves the
 // per-K-block cost of the barrier round trip (it cannot overlap the issue).
 constexpr int kSlots = 2;
+constexpr int kMaxGroups = 64;   // groups of one grouped launch (GEMM_F16_MAX_GROUPS)
 constexpr int kNumThreads = 256;         // 8 warps
 constexpr int kProducerThreads = 96;     // warps 0-2
 constexpr int kEpiWarp0 = 4;
@@ -119,6 +120,22 @@ struct KernelParams {
     // of tiles spreads over more workers (no partial sums involved).
     int tail_tile0;
     int tail_split;
+    // Several problems in one launch (TileLang tutorial ch. 14, sections 4.3
+    // and 4.4).  gmode 0: one GEMM.  1: `groups` batches of the same shape,
+    // batch b at element offsets b*a_bs, b*b_bs, b*c_bs (a stride of 0 shares
+    // the operand); tiles are numbered batch by batch.  2: grouped: G GEMMs
+    // that share K and N, group g owning rows g_row0[g] .. + g_rows[g] of the
+    // concatenated A' and C and batch g of B'; its tiles start at g_tile0[g]
+    // and span g_tm[g] tile rows.  An operand whose tensor map carries a
+    // trailing batch dimension (x_bdim) takes the batch or group index as that
+    // coordinate.
+    int gmode, groups;
+    uint32_t a_bdim, b_bdim, c_bdim;
+    int64_t a_bs, b_bs, c_bs;
+    int g_tile0[kMaxGroups + 1];
+    int g_tm[kMaxGroups];
+    int64_t g_row0[kMaxGroups];
+    int64_t g_rows[kMaxGroups];
 };
 
 struct SmemLayout {
@@ -155,6 +172,7 @@ constexpr uint64_t kDrainTimeoutNs = 10000000ull;
 // tile, and the last of them to finish adds all partials in K order.
 struct Unit {
     int tile, m_blk, n_blk, kb0, kb1, slot, expected;
+    int g;       // batch or group of the tile
     int seg;     // index of this unit among the units covering its tile, in K order
     int slot0;   // slot of the tile's first unit: the idx-th (K order) one is slot0 + idx
     int bn;      // columns of this unit (BN, or BN / tail_split for a tail piece)
@@ -166,12 +184,25 @@ struct Unit {
 // same time share B columns and a few A row-blocks in L2 (the grouped program
 // ordering of the Triton page; the C500 review's panel rasterisation, section
 // 10).  The ordering is only a locality hint.
-__device__ __forceinline__ void tile_coords(const KernelParams& p, int tile, int& m_blk, int& n_blk)
+template <bool kMulti>
+__device__ __forceinline__ void tile_coords(const KernelParams& p, int tile, int& g, int& m_blk, int& n_blk)
 {
+    int t = tile, tm = p.tiles_m;
+    g = 0;
+    if (!kMulti) {
+    } else if (p.gmode == 1) {   // batches of tiles_m x tiles_n tiles
+        const int per = p.tiles_m * p.tiles_n;
+        g = tile / per;
+        t = tile - g * per;
+    } else if (p.gmode == 2) {   // groups of g_tm[g] x tiles_n tiles
+        while (g + 1 < p.groups && tile >= p.g_tile0[g + 1]) ++g;
+        t = tile - p.g_tile0[g];
+        tm = p.g_tm[g];
+    }
     const int per_panel = p.panel * p.tiles_n;
-    const int panel = tile / per_panel;
-    const int r = tile - panel * per_panel;
-    const int rows = min(p.panel, p.tiles_m - panel * p.panel);
+    const int panel = t / per_panel;
+    const int r = t - panel * per_panel;
+    const int rows = min(p.panel, tm - panel * p.panel);
     m_blk = panel * p.panel + r % rows;
     n_blk = r / rows;
 }
@@ -210,6 +241,7 @@ __device__ __forceinline__ int units_of_worker(const KernelParams& p, int cid)
 // The i-th unit of worker `cid`: whole tiles or classic split-K units first
 // (u = cid, cid + P, ...; the units of one split tile are consecutive), then
 // the worker's stream-K segments in K order.
+template <bool kMulti>
 __device__ __forceinline__ Unit unit_at(const KernelParams& p, int cid, int i)
 {
     Unit w;
@@ -256,8 +288,130 @@ __device__ __forceinline__ Unit unit_at(const KernelParams& p, int cid, int i)
             w.slot = w.slot0 + w.seg;
         }
     }
-    tile_coords(p, w.tile, w.m_blk, w.n_blk);
+    tile_coords<kMulti>(p, w.tile, w.g, w.m_blk, w.n_blk);
     return w;
+}
+
+// Where one unit's problem lives: the A'/C row of its row 0 (groups are
+// concatenated along rows), the first row past its problem, the trailing
+// (batch) coordinates of the three tensor maps, and the bases the gather and
+// masked paths index from.
+struct UnitGeom {
+    int64_t a_row, row_lim;
+    int32_t az, bz, cz;
+    const __half* A;
+    const __half* B;
+    __half* C;
+};
+
+template <bool kMulti>
+__device__ __forceinline__ UnitGeom unit_geom(const KernelParams& p, const Unit& w)
+{
+    UnitGeom u;
+    const int64_t g = w.g;
+    u.a_row = 0;
+    u.row_lim = p.M;
+    u.az = u.bz = u.cz = 0;
+    u.A = p.A;
+    u.B = p.B;
+    u.C = p.C;
+    if (!kMulti) {
+    } else if (p.gmode == 1) {
+        u.az = u.bz = u.cz = w.g;
+        u.A = p.A + g * p.a_bs;
+        u.B = p.B + g * p.b_bs;
+        u.C = p.C + g * p.c_bs;
+    } else if (p.gmode == 2) {
+        u.a_row = p.g_row0[w.g];
+        u.row_lim = p.g_row0[w.g] + p.g_rows[w.g];
+        u.bz = w.g;
+        u.B = p.B + g * p.b_bs;
+    }
+    return u;
+}
+
+// TMA loads of one slot, single or pair form, with the map's trailing batch
+// coordinate z when it has one.
+template <bool kPair>
+__device__ __forceinline__ void tma2(uint32_t d, const void* m, int32_t x, int32_t y, uint32_t bar)
+{
+    if (kPair)
+        tma_load_2d_pair(d, m, x, y, bar);
+    else
+        tma_load_2d(d, m, x, y, bar);
+}
+template <bool kPair>
+__device__ __forceinline__ void tma3(uint32_t d, const void* m, int32_t x, int32_t y, int32_t z, uint32_t bar)
+{
+    if (kPair)
+        tma_load_3d_pair(d, m, x, y, z, bar);
+    else
+        tma_load_3d(d, m, x, y, z, bar);
+}
+template <bool kPair>
+__device__ __forceinline__ void tma4(uint32_t d, const void* m, int32_t x, int32_t y, int32_t z, int32_t v,
+                                     uint32_t bar)
+{
+    if (kPair)
+        tma_load_4d_pair(d, m, x, y, z, v, bar);
+    else
+        tma_load_4d(d, m, x, y, z, v, bar);
+}
+
+// A' rows row .. row+127 of one 64-wide K slot: K-major one box (k, row);
+// MN-major one 3-D box (0, k, row/64) or two 2-D boxes (row, k) and (row+64, k).
+template <bool kPair>
+__device__ __forceinline__ void load_a_slot(const KernelParams& p, uint32_t sa, int32_t k0, int64_t row, int32_t z,
+                                            bool a_mn, bool a_3d, bool bd, uint32_t bar)
+{
+    const int32_t r = static_cast<int32_t>(row);
+    if (!a_mn) {
+        if (bd)
+            tma3<kPair>(sa, &p.tmA, k0, r, z, bar);
+        else
+            tma2<kPair>(sa, &p.tmA, k0, r, bar);
+    } else if (a_3d) {
+        if (bd)
+            tma4<kPair>(sa, &p.tmA, 0, k0, r >> 6, z, bar);
+        else
+            tma3<kPair>(sa, &p.tmA, 0, k0, r >> 6, bar);
+    } else {
+        for (int j = 0; j < 2; ++j) {
+            if (bd)
+                tma3<kPair>(sa + j * 8192, &p.tmA, r + 64 * j, k0, z, bar);
+            else
+                tma2<kPair>(sa + j * 8192, &p.tmA, r + 64 * j, k0, bar);
+        }
+    }
+}
+
+// B' columns col .. col+bcols-1 of one slot: K-major one box (k, col) of the
+// map's width; MN-major one 3-D box (0, k, col/64) or one 2-D box (col, k) per
+// 64 columns.
+template <bool kPair>
+__device__ __forceinline__ void load_b_slot(const KernelParams& p, const CUtensorMap* tmb, uint32_t sb, int32_t k0,
+                                            int64_t col, int32_t z, int bcols, bool b_mn, bool b_3d, bool bd,
+                                            uint32_t bar)
+{
+    const int32_t c = static_cast<int32_t>(col);
+    if (!b_mn) {
+        if (bd)
+            tma3<kPair>(sb, tmb, k0, c, z, bar);
+        else
+            tma2<kPair>(sb, tmb, k0, c, bar);
+    } else if (b_3d) {
+        if (bd)
+            tma4<kPair>(sb, tmb, 0, k0, c >> 6, z, bar);
+        else
+            tma3<kPair>(sb, tmb, 0, k0, c >> 6, bar);
+    } else {
+        for (int j = 0; j < bcols / 64; ++j) {
+            if (bd)
+                tma3<kPair>(sb + j * 8192, &p.tmB, c + 64 * j, k0, z, bar);
+            else
+                tma2<kPair>(sb + j * 8192, &p.tmB, c + 64 * j, k0, bar);
+        }
+    }
 }
 
 __device__ __forceinline__ void raise_abort(const KernelParams& p, volatile int* abort)
@@ -479,10 +633,11 @@ __device__ __forceinline__ uint16_t half_bits(const uint32_t* h, int c)
 
 // Store 16 fp16 values (h[8]) of output row m, columns n..n+15, with bounds
 // checks on m and on every column.
-__device__ __forceinline__ void store_piece_masked(const KernelParams& p, int64_t m, int64_t n, const uint32_t* h)
+__device__ __forceinline__ void store_piece_masked(const KernelParams& p, __half* C, int64_t m_lim, int64_t m, int64_t n,
+                                                   const uint32_t* h)
 {
-    if (m >= p.M || n >= p.N) return;
-    uint16_t* row = reinterpret_cast<uint16_t*>(p.C) + m * p.c_sm;
+    if (m >= m_lim || n >= p.N) return;
+    uint16_t* row = reinterpret_cast<uint16_t*>(C) + m * p.c_sm;
     if (p.c_sn == 1) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -528,9 +683,9 @@ __device__ __forceinline__ void add_tmem16(uint32_t taddr, float* sacc)
 // of the tile to finish adds all partials in K order (deterministic) and stores
 // C; the others leave their partial in the workspace.  The accumulator stays in
 // TMEM until the decision, so the last one takes its own values from TMEM.
-template <bool kPair>
+template <bool kPair, bool kMulti>
 __device__ __forceinline__ void cut_tile_epilogue(const KernelParams& p, const SmemLayout& L, const Unit& w,
-                                               uint32_t taddr, uint32_t tempty, int64_t m0, int64_t n0,
+                                               const UnitGeom& ug, uint32_t taddr, uint32_t tempty, int64_t m0, int64_t n0,
                                                volatile int* flag, volatile int* abort, uint32_t& fix_ph,
                                                bool last_unit)
 {
@@ -602,7 +757,8 @@ __device__ __forceinline__ void cut_tile_epilogue(const KernelParams& p, const S
             // whole tile's.
             int per = cap / others;
             if (per >= 4) per &= ~3;
-            const bool stage_c = last_unit && p.c_tma;
+            const int64_t crow = ug.a_row + m0 + 32 * ((threadIdx.x >> 5) & 3);   // this warp's first C row
+            const bool stage_c = last_unit && p.c_tma && (!kMulti || p.gmode != 2 || crow + 32 <= ug.row_lim);
             const int q = (threadIdx.x >> 5) & 3;
             uint32_t gc = 0;   // TMA-store groups this warp issued
             for (int b0 = 0; b0 < chunks; b0 += per) {
@@ -675,7 +831,8 @@ __device__ __forceinline__ void cut_tile_epilogue(const KernelParams& p, const S
                                     st_smem_v4(buf + lane * 128 + (((j0 + 1) ^ (lane & 7)) << 4),
                                                make_uint4(h[4], h[5], h[6], h[7]));
                                 } else {
-                                    store_piece_masked(p, m0 + row, n0 + (b0 + g0 + h2) * 16, h);
+                                    store_piece_masked(p, ug.C, ug.row_lim, ug.a_row + m0 + row, n0 + (b0 + g0 + h2) * 16,
+                                                       h);
                                 }
                             }
                         }
@@ -723,7 +880,7 @@ __device__ __forceinline__ void cut_tile_epilogue(const KernelParams& p, const S
                                 st_smem_v4(buf + lane * 128 + (((j0 + 1) ^ (lane & 7)) << 4),
                                            make_uint4(h[4], h[5], h[6], h[7]));
                             } else {
-                                store_piece_masked(p, m0 + row, n0 + (b0 + c) * 16, h);
+                                store_piece_masked(p, ug.C, ug.row_lim, ug.a_row + m0 + row, n0 + (b0 + c) * 16, h);
                             }
                         }
                     }
@@ -731,9 +888,13 @@ __device__ __forceinline__ void cut_tile_epilogue(const KernelParams& p, const S
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            if (m0 + 32 * q < p.M)
-                                tma_store_2d(&p.tmC, buf, static_cast<int32_t>(n0 + 16 * (b0 + g0)),
-                                             static_cast<int32_t>(m0 + 32 * q));
+                            if (crow < ug.row_lim) {
+                                const int32_t xn = static_cast<int32_t>(n0 + 16 * (b0 + g0));
+                                if (kMulti && p.c_bdim)
+                                    tma_store_3d(&p.tmC, buf, xn, static_cast<int32_t>(crow), ug.cz);
+                                else
+                                    tma_store_2d(&p.tmC, buf, xn, static_cast<int32_t>(crow));
+                            }
                             bulk_commit_group();
                         }
                         ++gc;
@@ -795,7 +956,7 @@ __device__ __forceinline__ void cut_tile_epilogue(const KernelParams& p, const S
                         uint32_t h[8];
     #pragma unroll
                         for (int i = 0; i < 8; ++i) h[i] = pack_half2(sacc[2 * i], sacc[2 * i + 1]);
-                        store_piece_masked(p, m0 + row, n0 + c * 16, h);
+                        store_piece_masked(p, ug.C, ug.row_lim, ug.a_row + m0 + row, n0 + c * 16, h);
                     }
                 }
                 named_bar_sync(1, 128);   // the zone is free for the next batch
@@ -818,7 +979,9 @@ __device__ __forceinline__ void cut_tile_epilogue(const KernelParams& p, const S
 // the pair's B columns, multicast to the CTA with the same pair rank in both
 // pairs, so B is read from L2 once per cluster instead of once per pair.  The
 // stage's empty barrier then waits for both pairs' MMAs (count 2).
-template <bool kPair, bool kQuad>
+// kMulti: batched or grouped launches (gmode != 0); the one-GEMM launch is
+// compiled without that geometry.
+template <bool kPair, bool kQuad, bool kMulti>
 __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __grid_constant__ KernelParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -836,6 +999,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
     const bool a_tma = p.a_flags & kOpTma, b_tma = p.b_flags & kOpTma;
     const bool a_mn = p.a_flags & kOpMnMajor, b_mn = p.b_flags & kOpMnMajor;
     const bool a_3d = p.a_flags & kOpBox3d, b_3d = p.b_flags & kOpBox3d;
+    const bool a_bd = kMulti && p.a_bdim != 0, b_bd = kMulti && p.b_bdim != 0;   // maps with a trailing batch dimension
     static_assert(kPair || !kQuad, "the four-CTA form is built on pairs");
     const uint32_t crank = kPair ? cluster_ctarank() : 0u;   // rank in the cluster
     const uint32_t rank = crank & 1u;                         // rank in the pair
@@ -896,10 +1060,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
             int issued = 0;
             const int nu = units_of_worker(p, cid);
             for (int i = 0; i < nu && ok; ++i) {
-                const Unit w = unit_at(p, cid, i);
+                const Unit w = unit_at<kMulti>(p, cid, i);
+                const UnitGeom ug = unit_geom<kMulti>(p, w);
                 const int bcols = kPair ? w.bn / 2 : w.bn;   // this CTA's share of the unit's B columns
                 const int64_t m0 = static_cast<int64_t>(w.m_blk) * kUnitRows + pp * kTileRows + rank * kBM;
                 const int64_t n0 = static_cast<int64_t>(w.n_blk) * p.BN + w.n_off + rank * bcols;
+                const int64_t arow = ug.a_row + m0;   // A' row of the slot boxes (rows of a group are concatenated)
                 // Bytes one stage of this unit brings in: MN-major B comes in
                 // 64-column boxes (or one 3-D box of the full stage width),
                 // K-major B in one box of the full tile width.  A tail piece
@@ -931,14 +1097,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                     if (t == tiss && (a_tma || b_tma)) {
                         if (kPair) {
                             const uint32_t fbc = mapa_shared(fb, lead_rank);
-                            if (!a_mn) {
-                                tma_load_2d_pair(sa, &p.tmA, k0, static_cast<int32_t>(m0), fbc);
-                            } else if (a_3d) {
-                                tma_load_3d_pair(sa, &p.tmA, 0, k0, static_cast<int32_t>(m0 >> 6), fbc);
-                            } else {
-                                tma_load_2d_pair(sa, &p.tmA, static_cast<int32_t>(m0), k0, fbc);
-                                tma_load_2d_pair(sa + 8192, &p.tmA, static_cast<int32_t>(m0 + 64), k0, fbc);
-                            }
+                            load_a_slot<true>(p, sa, k0, arow, ug.az, a_mn, a_3d, a_bd, fbc);
                             if (kQuad) {
                                 // This CTA's quarter: B columns n0 + 64*pp .. +64 of its pair
                                 // rank's half, into both pairs' CTAs of that rank.
@@ -951,42 +1110,19 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                                     tma_load_3d_pair_mc(sq, &p.tmB, 0, k0, nq >> 6, fbc, mask);
                                 else
                                     tma_load_2d_pair_mc(sq, &p.tmB, nq, k0, fbc, mask);
-                            } else if (!b_mn) {
-                                tma_load_2d_pair(sb, tmb, k0, static_cast<int32_t>(n0), fbc);
-                            } else if (b_3d) {
-                                tma_load_3d_pair(sb, tmb, 0, k0, static_cast<int32_t>(n0 >> 6), fbc);
                             } else {
-                                for (int j = 0; j < bcols / 64; ++j)
-                                    tma_load_2d_pair(sb + j * 8192, &p.tmB, static_cast<int32_t>(n0 + 64 * j), k0, fbc);
+                                load_b_slot<true>(p, tmb, sb, k0, n0, ug.bz, bcols, b_mn, b_3d, b_bd, fbc);
                             }
                         } else {
-                            if (a_tma) {
-                                if (!a_mn) {
-                                    tma_load_2d(sa, &p.tmA, k0, static_cast<int32_t>(m0), fb);
-                                } else if (a_3d) {
-                                    tma_load_3d(sa, &p.tmA, 0, k0, static_cast<int32_t>(m0 >> 6), fb);
-                                } else {
-                                    tma_load_2d(sa, &p.tmA, static_cast<int32_t>(m0), k0, fb);
-                                    tma_load_2d(sa + 8192, &p.tmA, static_cast<int32_t>(m0 + 64), k0, fb);
-                                }
-                            }
-                            if (b_tma) {
-                                if (!b_mn) {
-                                    tma_load_2d(sb, tmb, k0, static_cast<int32_t>(n0), fb);
-                                } else if (b_3d) {
-                                    tma_load_3d(sb, tmb, 0, k0, static_cast<int32_t>(n0 >> 6), fb);
-                                } else {
-                                    for (int j = 0; j < bcols / 64; ++j)
-                                        tma_load_2d(sb + j * 8192, &p.tmB, static_cast<int32_t>(n0 + 64 * j), k0, fb);
-                                }
-                            }
+                            if (a_tma) load_a_slot<false>(p, sa, k0, arow, ug.az, a_mn, a_3d, a_bd, fb);
+                            if (b_tma) load_b_slot<false>(p, tmb, sb, k0, n0, ug.bz, bcols, b_mn, b_3d, b_bd, fb);
                         }
                     }
                     if (!kPair && any_masked) {
                         if (!a_tma)
-                            gather_tile(p.A, p.a_sm, p.a_sk, p.M, p.K, m0, k0, kBM, a_mn, sa, t);
+                            gather_tile(ug.A, p.a_sm, p.a_sk, ug.row_lim, p.K, ug.a_row + m0, k0, kBM, a_mn, sa, t);
                         if (!b_tma)
-                            gather_tile(p.B, p.b_sn, p.b_sk, p.N, p.K, n0, k0, w.bn, b_mn, sb, t);
+                            gather_tile(ug.B, p.b_sn, p.b_sk, p.N, p.K, n0, k0, w.bn, b_mn, sb, t);
                     }
                     }
                     if (!kPair && any_masked) {
@@ -1025,7 +1161,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
             const uint32_t b_atom_rows = 8192;   // MN-major: one 64-wide atom column over 64 K rows
             const int nu = units_of_worker(p, cid);
             for (int i = 0; i < nu && ok; ++i) {
-                const Unit w = unit_at(p, cid, i);
+                const Unit w = unit_at<kMulti>(p, cid, i);
                 if (!wait_bar<kPair>(bar_tempty(L.bars, acc), acc_phase ^ 1u, abort, p.timeout_ns)) {
                     raise_abort(p, abort);
                     ok = false;
@@ -1103,7 +1239,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
         uint32_t fix_ph = 0u;   // bit 0: parity of the next phase of the fixup barrier
         const int nu = units_of_worker(p, cid);
         for (int ui = 0; ui < nu; ++ui) {
-            const Unit w = unit_at(p, cid, ui);
+            const Unit w = unit_at<kMulti>(p, cid, ui);
             const int64_t m0 = static_cast<int64_t>(w.m_blk) * kUnitRows + pp * kTileRows + rank * kBM;
             const int64_t n0 = static_cast<int64_t>(w.n_blk) * p.BN + w.n_off;
             const int npieces = w.bn / 16;          // 16 accumulator columns per piece
@@ -1120,6 +1256,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
             tc_fence_after();
             const uint32_t taddr = tmem_base + lane_off + acc * kAccStride;
             const uint32_t tempty = kPair ? mapa_shared(bar_tempty(L.bars, acc), lead_rank) : bar_tempty(L.bars, acc);
+            const UnitGeom ug = unit_geom<kMulti>(p, w);
+            // this warp's first row of C, and whether its 32-row boxes go out by TMA
+            // store: clipped at the problem's M by the map, except that a box of a
+            // group must not spill into the next group's rows
+            const int64_t crow = ug.a_row + m0 + 32 * q;
+            const bool ctma = p.c_tma && (!kMulti || p.gmode != 2 || crow + 32 <= ug.row_lim);
             if (w.slot < 0) {
                 uint32_t buf = 0;
                 for (int pc = 0; pc < npieces; pc += 4) {
@@ -1146,7 +1288,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                         const int piece = pc + h2;
                         uint32_t h[8];
                         convert16(r + 16 * h2, h);
-                        if (p.c_tma) {
+                        if (ctma) {
                             const int j0 = (piece & 3) * 2;        // 16-byte chunk inside the 128-byte row
                             if ((piece & 3) == 0) {
                                 buf = L.epi + (q * 2 + (group_count & 1u)) * kEpiBufBytes;
@@ -1162,20 +1304,24 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                                 if (lane == 0) {
                                     // (a box wholly below row M, e.g. the second pair tile of a
                                     // four-CTA unit on the last row, is not stored)
-                                    if (m0 + 32 * q < p.M)
-                                        tma_store_2d(&p.tmC, buf, static_cast<int32_t>(n0 + 16 * (piece & ~3)),
-                                                     static_cast<int32_t>(m0 + 32 * q));
+                                    if (crow < ug.row_lim) {
+                                        const int32_t xn = static_cast<int32_t>(n0 + 16 * (piece & ~3));
+                                        if (kMulti && p.c_bdim)
+                                            tma_store_3d(&p.tmC, buf, xn, static_cast<int32_t>(crow), ug.cz);
+                                        else
+                                            tma_store_2d(&p.tmC, buf, xn, static_cast<int32_t>(crow));
+                                    }
                                     bulk_commit_group();
                                 }
                                 ++group_count;
                             }
                         } else {
-                            store_piece_masked(p, m0 + row, n0 + 16 * piece, h);
+                            store_piece_masked(p, ug.C, ug.row_lim, ug.a_row + m0 + row, n0 + 16 * piece, h);
                         }
                     }
                 }
             } else {
-                cut_tile_epilogue<kPair>(p, L, w, taddr, tempty, m0, n0, flag, abort, fix_ph, ui == nu - 1);
+                cut_tile_epilogue<kPair, kMulti>(p, L, w, ug, taddr, tempty, m0, n0, flag, abort, fix_ph, ui == nu - 1);
             }
             if (++acc == 2) {
                 acc = 0;

@@ -203,6 +203,27 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap,
         : "memory");
 }
 
+// Four-dimensional boxes (a batch dimension after a 3-D box), single and pair form.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                            int32_t w, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                                 int32_t w, uint32_t bar_cluster)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar_cluster)
+        : "memory");
+}
+
 // Pair form with cluster multicast: the box lands at the same shared-memory
 // offset in every CTA of `cta_mask`, and the transaction bytes are signalled on
 // the barrier at `bar_cluster`'s offset in the leader CTA of each destination's
@@ -244,6 +265,14 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
                      reinterpret_cast<uint64_t>(tmap)),
                  "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int32_t x, int32_t y, int32_t z)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y), "r"(z), "r"(src)
                  : "memory");
 }
 

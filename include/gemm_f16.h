@@ -115,6 +115,56 @@ gemm_f16_status gemm_f16_ws(const void* A, int64_t stride_am, int64_t stride_ak,
  * M, N, K, the options and the device's SM count. */
 gemm_f16_status gemm_f16_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
 
+/*
+ * Batched GEMM: `batch` problems of the same shape in one launch,
+ *
+ *   C_b[m, n] = fp16( sum_k A_b[m, k] * B_b[k, n] ),  0 <= b < batch,
+ *
+ * with A_b at A + b*stride_ab, B_b at B + b*stride_bb, C_b at C + b*stride_cb
+ * (element offsets; inside a problem the addressing of gemm_f16()).  Follows
+ * the TileLang tutorial ch. 14 "GEMM operators", section 4.4 (batched GEMM:
+ * identical shapes, the (batch, m-tile, n-tile) space flattened into one tile
+ * space).  A stride of 0 for A or B shares that operand across the batch
+ * (e.g. one weight matrix); stride_cb must be at least the span of one C view,
+ * so the problems' outputs do not overlap.  batch >= 1.
+ * Operands whose batch stride is a multiple of 16 bytes keep the TMA path;
+ * others are gathered.  Precision, tails, workspace, errors and asynchrony are
+ * those of gemm_f16().
+ */
+gemm_f16_status gemm_f16_batched(const void* A, int64_t stride_ab, int64_t stride_am, int64_t stride_ak,
+                                 const void* B, int64_t stride_bb, int64_t stride_bk, int64_t stride_bn,
+                                 void* C, int64_t stride_cb, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                 int64_t batch, cudaStream_t stream);
+
+/* Most groups of one gemm_f16_grouped() call. */
+#define GEMM_F16_MAX_GROUPS 64
+
+/*
+ * Grouped GEMM (the MoE expert layer): `groups` problems that share K and N
+ * and differ in M.  Group g owns group_rows[g] consecutive rows of A and C
+ * (the groups' rows concatenated in group order, starting at row 0) and
+ * multiplies them by its own B_g at B + g*stride_bg:
+ *
+ *   C[r, n] = fp16( sum_k A[r, k] * B_g[k, n] )   for row r of group g.
+ *
+ * Follows the TileLang tutorial ch. 14 "GEMM operators", section 4.3 (grouped
+ * GEMM: concatenated A and C with a per-group offset table, the scheduler
+ * walking every group's tiles in one launch); the offset table is built here
+ * from group_rows.
+ *
+ *   group_rows  HOST array of `groups` row counts (>= 0; empty groups allowed).
+ *   groups      1 .. GEMM_F16_MAX_GROUPS.
+ *   stride_bg   element distance between consecutive groups' B (0 shares one B).
+ *   A, C        addressed as in gemm_f16() with M = sum of group_rows.
+ * A tile never mixes groups: rows past a group's end are computed from the
+ * next group's A rows but never stored.  With every group empty the call does
+ * nothing and returns GEMM_F16_OK.  Other behaviour is that of gemm_f16().
+ */
+gemm_f16_status gemm_f16_grouped(const void* A, int64_t stride_am, int64_t stride_ak,
+                                 const void* B, int64_t stride_bg, int64_t stride_bk, int64_t stride_bn,
+                                 void* C, int64_t ldc, const int64_t* group_rows, int64_t groups,
+                                 int64_t N, int64_t K, cudaStream_t stream);
+
 /* Size of the fixed scratch array behind gemm_f16_noalloc(). */
 #define GEMM_F16_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 

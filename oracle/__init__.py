@@ -140,6 +140,43 @@ def gemm(A: np.ndarray, B: np.ndarray, threads: int = 1) -> np.ndarray:
     return C.view(np.float16)
 
 
+def gemm_batched(A: np.ndarray, B: np.ndarray, threads: int = 1) -> np.ndarray:
+    """Batched GEMM, C[b] = A[b] @ B[b] for 3-D float16 views [batch, M, K] and
+    [batch, K, N] (any strides, a batch stride of 0 included).
+
+    TileLang tutorial ch. 14 "GEMM operators", section 4.4 (batched GEMM: the
+    same GEMM on every batch index).  Each problem is ``gemm`` as it stands.
+    """
+    if A.ndim != 3 or B.ndim != 3 or A.shape[0] != B.shape[0] or A.shape[2] != B.shape[1]:
+        raise ValueError("shape mismatch")
+    C = np.zeros((A.shape[0], A.shape[1], B.shape[2]), dtype=np.float16)
+    for b in range(A.shape[0]):
+        C[b] = gemm(A[b], B[b], threads)
+    return C
+
+
+def gemm_grouped(A: np.ndarray, B: np.ndarray, group_rows, threads: int = 1) -> np.ndarray:
+    """Grouped GEMM: the rows of A [sum(group_rows), K] form consecutive groups and
+    group g's rows are multiplied by B[g] ([G, K, N]); returns C [sum, N].
+
+    TileLang tutorial ch. 14 "GEMM operators", section 4.3 (grouped GEMM: G
+    GEMMs sharing K and N, the experts' rows concatenated and located through
+    an offset table).  Each group is ``gemm`` as it stands; empty groups give
+    no rows.
+    """
+    if A.ndim != 2 or B.ndim != 3 or B.shape[0] != len(group_rows) or A.shape[1] != B.shape[1]:
+        raise ValueError("shape mismatch")
+    if sum(int(r) for r in group_rows) != A.shape[0]:
+        raise ValueError("group rows do not add up to A's rows")
+    C = np.zeros((A.shape[0], B.shape[2]), dtype=np.float16)
+    r0 = 0
+    for g, rows in enumerate(int(r) for r in group_rows):
+        if rows:
+            C[r0:r0 + rows] = gemm(A[r0:r0 + rows], B[g], threads)
+        r0 += rows
+    return C
+
+
 def _base_of(v: np.ndarray):
     item = v.itemsize
     if any(s % item for s in v.strides) or any(s <= 0 for s in v.strides):

@@ -339,6 +339,21 @@ def test_only_the_view_of_c_is_written(force):
     assert np.all(hb[:M, N:] == canary) and np.all(hb[M:] == canary)
 
 
+@pytest.mark.parametrize("N,ldc", [(130, 136), (70, 80), (200, 208)])
+def test_pitch_padding_untouched_when_n_is_not_a_multiple_of_8(N, ldc):
+    # A TMA-aligned pitch but a row width that ends inside a 16-byte chunk: the
+    # padding after column N keeps its NaN.
+    rng = np.random.default_rng(N + ldc)
+    M, K = 300, 96
+    Ah = rng.integers(-3, 4, (M, K)).astype(np.float16)
+    Bh = rng.integers(-3, 4, (K, N)).astype(np.float16)
+    buf = torch.full((M, ldc), float("nan"), dtype=torch.float16, device=DEV)
+    gpu(to_dev(Ah), to_dev(Bh), out=buf[:, :N])
+    host_buf = buf.cpu().numpy()
+    assert_bits(host_buf[:, :N], oracle.gemm(Ah, Bh), f"N={N}, ldc={ldc}")
+    assert np.isnan(host_buf[:, N:]).all()
+
+
 def test_overflow_gives_inf_like_the_oracle():
     a = torch.full((4, 64), 16.0, dtype=torch.float16, device=DEV)
     b = torch.full((64, 4), 128.0, dtype=torch.float16, device=DEV)

@@ -251,3 +251,73 @@ def test_openmp_rows_do_not_change_results():
     B = rng.uniform(-1, 1, (300, 50)).astype(np.float16)
     assert np.array_equal(oracle.gemm(A, B, threads=1).view(np.uint16),
                           oracle.gemm(A, B, threads=4).view(np.uint16))
+
+
+# ------------------------------------------------- batched and grouped GEMM
+# TileLang tutorial ch. 14 "GEMM operators", sections 4.3 (grouped) and 4.4
+# (batched).  Pinned against numpy's float64 einsum (a library routine) then
+# numpy's rounding, per problem, and against closed forms that a wrong batch
+# index or group offset would break.
+def _ref_batched(A, B):
+    return np.einsum("bmk,bkn->bmn", A.astype(np.float64), B.astype(np.float64)).astype(np.float16)
+
+
+def test_batched_matches_einsum_per_problem():
+    rng = np.random.default_rng(21)
+    for _ in range(8):
+        nb, M, N, K = (int(x) for x in rng.integers(1, 24, 4))
+        A = rng.uniform(-1, 1, (nb, M, K)).astype(np.float16)
+        B = rng.uniform(-1, 1, (nb, K, N)).astype(np.float16)
+        C = oracle.gemm_batched(A, B)
+        assert np.array_equal(C.view(np.uint16), _ref_batched(A, B).view(np.uint16))
+    # a B shared by every problem (batch stride 0) and transposed A views
+    A = rng.uniform(-1, 1, (5, 9, 13)).astype(np.float16)
+    B1 = rng.uniform(-1, 1, (13, 7)).astype(np.float16)
+    Bs = np.broadcast_to(B1, (5, 13, 7))
+    At = np.ascontiguousarray(A.transpose(0, 2, 1)).transpose(0, 2, 1)
+    C = oracle.gemm_batched(At, Bs)
+    assert np.array_equal(C.view(np.uint16), _ref_batched(A, np.broadcast_to(B1, (5, 13, 7))).view(np.uint16))
+
+
+def test_batched_problems_are_independent():
+    # permuting the batch permutes the results: a wrong batch index (reading
+    # problem b+1's B, say) fails this
+    rng = np.random.default_rng(22)
+    A = rng.integers(-3, 4, (6, 11, 17)).astype(np.float16)
+    B = rng.integers(-3, 4, (6, 17, 5)).astype(np.float16)
+    perm = rng.permutation(6)
+    C = oracle.gemm_batched(A, B)
+    assert np.array_equal(oracle.gemm_batched(A[perm], B[perm]), C[perm])
+    for b in range(6):
+        assert np.array_equal(C[b].astype(np.int64), _exact_int_product(A[b].astype(np.int64), B[b].astype(np.int64)))
+
+
+def test_grouped_matches_per_group_products():
+    rng = np.random.default_rng(23)
+    rows = [0, 7, 1, 0, 13, 4]
+    G, N, K = len(rows), 9, 15
+    A = rng.uniform(-1, 1, (sum(rows), K)).astype(np.float16)
+    B = rng.uniform(-1, 1, (G, K, N)).astype(np.float16)
+    C = oracle.gemm_grouped(A, B, rows)
+    r0 = 0
+    for g, r in enumerate(rows):
+        ref = (A[r0:r0 + r].astype(np.float64) @ B[g].astype(np.float64)).astype(np.float16)
+        assert np.array_equal(C[r0:r0 + r].view(np.uint16), ref.view(np.uint16))
+        r0 += r
+
+
+def test_grouped_closed_forms():
+    rng = np.random.default_rng(24)
+    A = rng.integers(-3, 4, (20, 8)).astype(np.float16)
+    B = rng.integers(-3, 4, (8, 6)).astype(np.float16)
+    # one group is the plain product; every group sharing one B is too
+    assert np.array_equal(oracle.gemm_grouped(A, B[None], [20]), oracle.gemm(A, B))
+    assert np.array_equal(oracle.gemm_grouped(A, np.stack([B] * 4), [3, 0, 12, 5]), oracle.gemm(A, B))
+    # group g scaled by g+1 shows which rows each group owns (an off-by-one
+    # group offset fails this)
+    rows = [3, 0, 12, 5]
+    Bg = np.stack([B * (g + 1) for g in range(4)]).astype(np.float16)
+    C = oracle.gemm_grouped(A, Bg, rows).astype(np.int64)
+    base = oracle.gemm(A, B).astype(np.int64)
+    scale = np.repeat(np.arange(1, 5), rows)[:, None]
+    assert np.array_equal(C, base * scale)
