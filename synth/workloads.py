@@ -114,3 +114,63 @@ MOE_131072x2048x7168 = Workload(
 ALL = [TAIL_ROWMAJOR_B, TAIL_TRANSPOSED_B, SQUARE_4096, DECODE_16x16384x8192,
        IRREGULAR_3001x1999x4097, MOE_131072x2048x7168]
 BY_NAME = {w.name: w for w in ALL}
+
+
+# ------------------------------------------------ several problems per launch
+def group_rows_for(total: int, groups: int, seed: int) -> tuple:
+    """Synthetic per-expert row counts standing in for routing: expert g gets a
+    share proportional to 1.5 + v_g (v_g a seeded uniform[-1,1) draw, so shares
+    differ by up to 5x); the rounding remainder goes to the last expert."""
+    v = values_np("uniform", seed, np.arange(groups, dtype=np.uint64)).astype(np.float64)
+    w = 1.5 + v
+    rows = [int(total * x / w.sum()) for x in w[:-1]]
+    rows.append(total - sum(rows))
+    return tuple(rows)
+
+
+@dataclass(frozen=True)
+class MultiWorkload:
+    """Several problems in one launch.  kind "batched": `count` problems of
+    M x N x K, A stacked as count*M rows of K, B as count*K rows of N.  kind
+    "grouped": `count` groups sharing N and K, A the M = sum(group_rows) rows,
+    B stacked as count*K rows of N (group g's B in rows g*K ..)."""
+    name: str
+    kind: str
+    M: int
+    N: int
+    K: int
+    count: int
+    A: Operand
+    B: Operand
+    description: str = ""
+    group_rows: tuple = ()
+
+    @property
+    def flops(self) -> float:
+        problems = self.count if self.kind == "batched" else 1
+        return 2.0 * problems * self.M * self.N * self.K
+
+    @property
+    def c_rows(self) -> int:
+        return self.count * self.M if self.kind == "batched" else self.M
+
+    def first_problem(self) -> Workload:
+        """Problem (or group) 0 as a one-GEMM workload over the same values: the
+        stacked operands' first rows are the first problem's."""
+        m0 = self.M if self.kind == "batched" else self.group_rows[0]
+        return Workload(self.name + "[0]", m0, self.N, self.K, _op(m0, self.K, self.A.kind, self.A.seed),
+                        _op(self.K, self.N, self.B.kind, self.B.seed), "first problem")
+
+
+BATCHED_32x1024 = MultiWorkload(
+    "batched_32x1024x1024x1024", "batched", 1024, 1024, 1024, 32,
+    _op(32 * 1024, 1024, "uniform", 12), _op(32 * 1024, 1024, "uniform", 13),
+    "batched: 32 problems of 1024^3, contiguous row-major")
+GROUPED_MOE = MultiWorkload(
+    "grouped_moe_g8_131072x2048x7168", "grouped", 131072, 2048, 7168, 8,
+    _op(131072, 7168, "uniform", 14), _op(8 * 7168, 2048, "uniform", 15),
+    "grouped MoE layer: 131072 routed rows over 8 experts (seeded shares), each expert's [7168,2048] B",
+    group_rows_for(131072, 8, 16))
+
+MULTI = [BATCHED_32x1024, GROUPED_MOE]
+BY_NAME.update({w.name: w for w in MULTI})

@@ -10,6 +10,7 @@ import torch
 
 import dense_tiled_gemm_fp16_gb300 as g
 import oracle
+from synth import workloads
 from tests.parity import assert_bits, assert_close, oracle_threads
 
 pytestmark = pytest.mark.gpu
@@ -186,3 +187,57 @@ def test_grouped_all_empty_does_nothing():
                        [0, 0, 0], 64, 64)
     torch.cuda.synchronize()
     assert C.numel() == 0 and g.gemm_f16_device_status() == 0
+
+
+# ------------------------------------------------------- full-size workloads
+def _launch_as_bench(w, A, B, C):
+    """The call bench.py times for a multi-problem workload."""
+    M, N, K, n = w.M, w.N, w.K, w.count
+    if w.kind == "batched":
+        g.gemm_f16_batched(A.data_ptr(), M * K, K, 1, B.data_ptr(), K * N, N, 1, C.data_ptr(), M * N, N,
+                           M, N, K, n)
+    else:
+        g.gemm_f16_grouped(A.data_ptr(), K, 1, B.data_ptr(), K * N, N, 1, C.data_ptr(), N, list(w.group_rows),
+                           N, K)
+
+
+def _problem_of_rows(w, rows):
+    """Problem (batched) or group (grouped) index of each stacked output row."""
+    if w.kind == "batched":
+        return rows // w.M
+    ends = np.cumsum(w.group_rows)
+    return np.searchsorted(ends, rows, side="right")
+
+
+@pytest.mark.parametrize("w", workloads.MULTI, ids=lambda w: w.name)
+def test_full_size_workload_sampled(w):
+    """Sampled outputs of the bench's batched / grouped workloads at full size,
+    plus the first and last row of every problem, against the oracle's dot
+    products over the regenerated rows of A and columns of B."""
+    A, B = w.A.device_view(DEV), w.B.device_view(DEV)
+    C = torch.full((w.c_rows, w.N), float("nan"), dtype=torch.float16, device=DEV)
+    _launch_as_bench(w, A, B, C)
+    torch.cuda.synchronize()
+    del A, B
+    assert not torch.isnan(C).any(), "an output element was not written"
+    K = w.K
+    if w.kind == "batched":
+        starts = np.arange(w.count, dtype=np.int64) * w.M
+        ends = starts + w.M
+    else:
+        ends = np.cumsum(np.asarray(w.group_rows, dtype=np.int64))
+        starts = ends - np.asarray(w.group_rows, dtype=np.int64)
+    rng = np.random.default_rng(20261)
+    edge = np.concatenate([starts, ends - 1])
+    rows = np.concatenate([rng.integers(0, w.c_rows, 2048), edge])
+    cols = np.concatenate([rng.integers(0, w.N, 2048), rng.integers(0, w.N, edge.size)])
+    cols[-4:] = w.N - 1
+    prob = _problem_of_rows(w, rows)
+    k = np.arange(K, dtype=np.int64)
+    A_rows = w.A.values_at(rows[:, None], k[None, :])                    # [S, K]
+    B_cols = w.B.values_at(prob[:, None] * K + k[None, :], cols[:, None])  # [S, K]
+    idx = np.arange(rows.size, dtype=np.int64) * K
+    ref, _ = oracle.dots(A_rows.reshape(-1), idx, 1, B_cols.reshape(-1), idx, 1, K, threads=oracle_threads())
+    got = C[torch.from_numpy(rows).to(DEV), torch.from_numpy(cols).to(DEV)].cpu().numpy()
+    assert_close(got, ref, K, f"{w.name} samples")
+    assert g.gemm_f16_device_status() == 0
