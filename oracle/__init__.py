@@ -11,6 +11,10 @@ pure-Python restatement of the output-tiled loop used to pin the pages' worked
 examples (logical read counts, the ragged-tail program counts, the K-tail
 counter-example).
 
+``gemm_fused`` (with its grouped and batched forms) adds the fused output
+stage: bias, activation and the gate/up product, evaluated in double on the
+unrounded sums from ``gemm_exact`` and rounded once.
+
 Every function here is pinned by ``tests/test_oracle_pins.py``; none is
 "parity unpinned".
 """
@@ -56,6 +60,9 @@ def _load():
             lib.oracle_gemm_f16.argtypes = [P, I64, I64, P, I64, I64, P, I64, I64, I64, I64,
                                             ctypes.c_int]
             lib.oracle_gemm_f16.restype = None
+            lib.oracle_gemm_f64.argtypes = [P, I64, I64, P, I64, I64, P, I64, I64, I64, I64,
+                                            ctypes.c_int]
+            lib.oracle_gemm_f64.restype = None
             lib.oracle_dot_f16.argtypes = [P, P, I64, P, P, I64, I64, I64, P, P, ctypes.c_int]
             lib.oracle_dot_f16.restype = None
             lib.oracle_half_to_double_n.argtypes = [P, P, I64]
@@ -175,6 +182,142 @@ def gemm_grouped(A: np.ndarray, B: np.ndarray, group_rows, threads: int = 1) -> 
             C[r0:r0 + rows] = gemm(A[r0:r0 + rows], B[g], threads)
         r0 += rows
     return C
+
+
+def gemm_exact(A: np.ndarray, B: np.ndarray, threads: int = 1) -> np.ndarray:
+    """The unrounded double sums of ``gemm``: S = A @ B as float64 [M, N]."""
+    if A.ndim != 2 or B.ndim != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError("shape mismatch")
+    M, K = A.shape
+    N = B.shape[1]
+    a_base, (s_am, s_ak) = _base_of(_u16(A))
+    b_base, (s_bk, s_bn) = _base_of(_u16(B))
+    S = np.zeros((M, N), dtype=np.float64)
+    _load().oracle_gemm_f64(a_base, s_am, s_ak, b_base, s_bk, s_bn, S.ctypes.data, N, M, N, K, int(threads))
+    return S
+
+
+# ---------------------------------------------------------------- fused epilogue
+# The pages name the fusions without fixing their arithmetic: the TileLang
+# tutorial's comparison checklist (ch. 14, section 6.3, item 4) and the AI-infra
+# page's section 05 list bias and activation fused into the GEMM's output stage;
+# the C500 review (section 17.3) lists a gate/up GEMM that fuses the two
+# projections and one that adds the activation and the multiply.  Read plainly:
+#   out = act(A @ B + bias)                                 (bias broadcast along rows)
+#   out = act(A @ B_gate + bias_gate) * (A @ B_up + bias_up)  (gate/up)
+# with act one of identity, ReLU, SiLU (x * logistic(x)) and GELU in its exact
+# form x * Phi(x) (Phi the standard normal CDF).  All of it is evaluated here in
+# double on the unrounded sums and rounded to fp16 once.
+ACTIVATIONS = ("none", "relu", "silu", "gelu")
+
+
+def _erfc(x: np.ndarray) -> np.ndarray:
+    import math
+
+    return np.vectorize(math.erfc, otypes=[np.float64])(x)
+
+
+def activation(x, act: str) -> np.ndarray:
+    """act(x) in double.  relu(x) = 0 for x < 0 and x otherwise; silu(x) =
+    x / (1 + exp(-x)); gelu(x) = x * Phi(x) with Phi(x) = erfc(-x / sqrt(2)) / 2,
+    the same as x/2 * (1 + erf(x / sqrt(2))) but without the cancellation in
+    the far negative tail."""
+    x = np.asarray(x, dtype=np.float64)
+    if act == "none":
+        return x.copy()
+    if act == "relu":
+        return np.where(x < 0, 0.0, x)
+    if act == "silu":
+        with np.errstate(over="ignore"):
+            return x / (1.0 + np.exp(-x))
+    if act == "gelu":
+        return x * (0.5 * _erfc(-x / np.sqrt(2.0)))
+    raise ValueError(f"unknown activation {act!r}")
+
+
+def _bias_row(bias, N):
+    if bias is None:
+        return np.zeros(N, dtype=np.float64)
+    b = half_to_double(np.ascontiguousarray(np.asarray(bias, dtype=np.float16)))
+    if b.shape != (N,):
+        raise ValueError("bias must hold N values")
+    return b
+
+
+def gemm_fused(A: np.ndarray, B: np.ndarray, B_up: np.ndarray | None = None, bias=None, bias_up=None,
+               act: str = "none", threads: int = 1, parts: bool = False):
+    """fp16 act(A @ B + bias), or with ``B_up`` the gate/up form
+    act(A @ B + bias) * (A @ B_up + bias_up); one rounding to fp16 at the end.
+
+    With ``parts`` also returns the double pre-activation gate g = A @ B + bias
+    and up u = A @ B_up + bias_up (None without B_up), for error bounds.
+    """
+    if act not in ACTIVATIONS:
+        raise ValueError(f"unknown activation {act!r}")
+    if bias_up is not None and B_up is None:
+        raise ValueError("bias_up needs B_up")
+    N = B.shape[1]
+    g = gemm_exact(A, B, threads) + _bias_row(bias, N)[None, :]
+    out = activation(g, act)
+    u = None
+    if B_up is not None:
+        if B_up.shape != B.shape:
+            raise ValueError("B_up must have B's shape")
+        u = gemm_exact(A, B_up, threads) + _bias_row(bias_up, N)[None, :]
+        out = out * u
+    C = double_to_half(out)
+    return (C, g, u) if parts else C
+
+
+def gemm_fused_grouped(A: np.ndarray, B: np.ndarray, group_rows, B_up=None, bias=None, bias_up=None,
+                       act: str = "none", threads: int = 1, parts: bool = False):
+    """``gemm_fused`` per group of a grouped problem (see ``gemm_grouped``):
+    group g uses B[g], B_up[g] and the bias rows bias[g], bias_up[g] ([G, N]);
+    a bias of shape [N] is shared by every group."""
+    G, K, N = B.shape
+    if sum(int(r) for r in group_rows) != A.shape[0] or len(group_rows) != G:
+        raise ValueError("group rows do not match")
+    C = np.zeros((A.shape[0], N), dtype=np.float16)
+    gs = np.zeros((A.shape[0], N))
+    us = np.zeros((A.shape[0], N)) if B_up is not None else None
+
+    def pick(b, g):
+        if b is None:
+            return None
+        b = np.asarray(b)
+        return b[g] if b.ndim == 2 else b
+
+    r0 = 0
+    for g, rows in enumerate(int(r) for r in group_rows):
+        if rows:
+            c, gg, uu = gemm_fused(A[r0:r0 + rows], B[g], None if B_up is None else B_up[g], pick(bias, g),
+                                   pick(bias_up, g), act, threads, parts=True)
+            C[r0:r0 + rows] = c
+            gs[r0:r0 + rows] = gg
+            if us is not None:
+                us[r0:r0 + rows] = uu
+        r0 += rows
+    return (C, gs, us) if parts else C
+
+
+def gemm_fused_batched(A: np.ndarray, B: np.ndarray, B_up=None, bias=None, bias_up=None, act: str = "none",
+                       threads: int = 1, parts: bool = False):
+    """``gemm_fused`` per problem of a batch ([batch, M, K] @ [batch, K, N]); a
+    bias [batch, N] per problem or [N] shared."""
+    nb, M, _ = A.shape
+    N = B.shape[2]
+    C = np.zeros((nb, M, N), dtype=np.float16)
+    gs = np.zeros((nb, M, N))
+    us = np.zeros((nb, M, N)) if B_up is not None else None
+    for b in range(nb):
+        pb = None if bias is None else (np.asarray(bias)[b] if np.ndim(bias) == 2 else bias)
+        pu = None if bias_up is None else (np.asarray(bias_up)[b] if np.ndim(bias_up) == 2 else bias_up)
+        c, gg, uu = gemm_fused(A[b], B[b], None if B_up is None else B_up[b], pb, pu, act, threads, parts=True)
+        C[b] = c
+        gs[b] = gg
+        if us is not None:
+            us[b] = uu
+    return (C, gs, us) if parts else C
 
 
 def _base_of(v: np.ndarray):

@@ -119,6 +119,29 @@ void oracle_gemm_f16(const uint16_t *A, int64_t s_am, int64_t s_ak,
 }
 
 /*
+ * The same sums left unrounded: S[m*lds + n] = sum_{k<K} A[..] * B[..] in
+ * double, k = 0..K-1.  The fused-epilogue oracle applies its bias, activation
+ * and gate product to these before its single rounding to fp16.
+ */
+void oracle_gemm_f64(const uint16_t *A, int64_t s_am, int64_t s_ak,
+                     const uint16_t *B, int64_t s_bk, int64_t s_bn,
+                     double *S, int64_t lds,
+                     int64_t M, int64_t N, int64_t K, int threads)
+{
+    ensure_table();
+    if (threads < 1) threads = 1;
+#pragma omp parallel for num_threads(threads) schedule(dynamic, 1)
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += g_dec[A[m * s_am + k * s_ak]] * g_dec[B[k * s_bk + n * s_bn]];
+            S[m * lds + n] = acc;
+        }
+    }
+}
+
+/*
  * Sampled form of the same definition, for outputs too many to compute whole:
  * out[i] = fp16( sum_k A[a_off[i] + k*s_ak] * B[b_off[i] + k*s_bk] ), where
  * a_off[i] = m_i*s_am (start of row m_i of A) and b_off[i] = n_i*s_bn (start of

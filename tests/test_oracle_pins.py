@@ -321,3 +321,113 @@ def test_grouped_closed_forms():
     base = oracle.gemm(A, B).astype(np.int64)
     scale = np.repeat(np.arange(1, 5), rows)[:, None]
     assert np.array_equal(C, base * scale)
+
+
+# ------------------------------------------------------------- fused epilogue
+# Bias + activation in the output stage and the gate/up product (TileLang
+# tutorial ch. 14, section 6.3, item 4; AI-infra page, section 05; C500 review,
+# section 17.3).  Pinned to textbook function values, library routines other
+# than the ones the oracle calls, exact identities and a hand-worked example.
+def test_exact_sums_round_to_the_plain_oracle():
+    rng = np.random.default_rng(50)
+    A, B = h(rng.uniform(-1, 1, (37, 150))), h(rng.uniform(-1, 1, (150, 29)))
+    S = oracle.gemm_exact(A, B)
+    assert np.array_equal(oracle.double_to_half(S).view(np.uint16), oracle.gemm(A, B).view(np.uint16))
+    # integer inputs: the sums are the exact integer products
+    Ai, Bi = rng.integers(-3, 4, (20, 31)), rng.integers(-3, 4, (31, 17))
+    assert np.array_equal(oracle.gemm_exact(h(Ai), h(Bi)), (Ai @ Bi).astype(np.float64))
+
+
+@pytest.mark.parametrize("act,table,form", [("gelu", "phi", "x*F"), ("silu", "sigma", "x*F")])
+def test_activations_at_textbook_points(act, table, form):
+    d = golden("fused_epilogue.json")
+    for xs, F in d[table].items():
+        x = float(xs)
+        assert abs(oracle.activation(x, act) - x * F) <= 1e-15 * max(1.0, abs(x)), (act, x)
+    assert oracle.activation(0.0, act) == 0.0
+
+
+def test_activations_match_independent_library_routines():
+    special = pytest.importorskip("scipy.special")
+    x = np.concatenate([np.linspace(-30, 30, 4001), [-1e-6, 1e-6, 0.0]])
+    silu = oracle.activation(x, "silu")
+    assert np.allclose(silu, x * special.expit(x), rtol=1e-13, atol=1e-300)
+    gelu = oracle.activation(x, "gelu")
+    assert np.allclose(gelu, x * special.ndtr(x), rtol=1e-12, atol=1e-290)
+    assert np.array_equal(oracle.activation(x, "relu"), np.maximum(x, 0.0))
+    assert np.array_equal(oracle.activation(x, "none"), x)
+
+
+@pytest.mark.parametrize("act", ["relu", "silu", "gelu"])
+def test_activation_odd_part_is_identity(act):
+    # relu, silu and gelu all satisfy f(x) - f(-x) = x (sigma(x) + sigma(-x) = 1,
+    # Phi(x) + Phi(-x) = 1): a wrong sign or a dropped factor breaks it
+    x = np.linspace(-12, 12, 2401)
+    d = oracle.activation(x, act) - oracle.activation(-x, act)
+    assert np.allclose(d, x, rtol=0, atol=1e-13 * 12)
+
+
+def test_fused_without_epilogue_is_the_plain_gemm():
+    rng = np.random.default_rng(51)
+    A, B = h(rng.uniform(-1, 1, (45, 300))), h(rng.uniform(-1, 1, (300, 70)))
+    assert np.array_equal(oracle.gemm_fused(A, B).view(np.uint16), oracle.gemm(A, B).view(np.uint16))
+
+
+def test_bias_runs_along_columns():
+    # A = I: C = act(B + bias[None, :]) elementwise; a bias indexed by row
+    # (or added twice) gives other values since M != N and the entries differ
+    rng = np.random.default_rng(52)
+    B = rng.integers(-4, 5, (3, 5))
+    bias = np.array([1, -2, 3, 0, -1])
+    C = oracle.gemm_fused(h(np.eye(3)), h(B), bias=h(bias))
+    assert np.array_equal(C.astype(np.int64), B + bias[None, :])
+    C = oracle.gemm_fused(h(np.eye(3)), h(B), bias=h(bias), act="relu")
+    assert np.array_equal(C.astype(np.int64), np.where(B + bias < 0, 0, B + bias))
+
+
+def test_gated_hand_worked_example():
+    d = golden("fused_epilogue.json")
+    C, g, u = oracle.gemm_fused(h(d["A"]), h(d["B_gate"]), h(d["B_up"]), h(d["bias_gate"]), h(d["bias_up"]),
+                                act="relu", parts=True)
+    assert np.array_equal(g, np.array(d["gate_pre"], dtype=np.float64))
+    assert np.array_equal(u, np.array(d["up"], dtype=np.float64))
+    assert np.array_equal(C.astype(np.float64), np.array(d["out_relu"], dtype=np.float64))
+
+
+@pytest.mark.parametrize("act", ["none", "relu", "silu", "gelu"])
+def test_gate_by_constant_up_scales_the_plain_form(act):
+    # B_up = 0 and bias_up = 1: the product is the non-gated result, bit for bit;
+    # bias_up = 2 doubles it exactly (a power of two, far from overflow)
+    rng = np.random.default_rng(53)
+    A, B = h(rng.uniform(-1, 1, (30, 64))), h(rng.uniform(-1, 1, (64, 40)))
+    bias = h(rng.uniform(-1, 1, 40))
+    plain = oracle.gemm_fused(A, B, bias=bias, act=act)
+    zero = np.zeros_like(B)
+    one = oracle.gemm_fused(A, B, zero, bias, h(np.ones(40)), act=act)
+    two = oracle.gemm_fused(A, B, zero, bias, h(np.full(40, 2.0)), act=act)
+    assert np.array_equal(one.view(np.uint16), plain.view(np.uint16))
+    # exact where the doubled value stays normal; a subnormal result is rounded
+    # on a fixed grid of 2^-24, so there it may differ by one step
+    p64, t64 = plain.astype(np.float64), two.astype(np.float64)
+    normal = np.abs(p64) >= 2.0 ** -14
+    assert np.array_equal(t64[normal], 2 * p64[normal])
+    assert np.all(np.abs(t64[~normal] - 2 * p64[~normal]) <= 2.0 ** -24)
+
+
+def test_fused_grouped_and_batched_compose_per_problem():
+    rng = np.random.default_rng(54)
+    rows = [7, 0, 12, 1]
+    A = h(rng.uniform(-1, 1, (sum(rows), 24)))
+    B, Bu = h(rng.uniform(-1, 1, (4, 24, 16))), h(rng.uniform(-1, 1, (4, 24, 16)))
+    bias = h(rng.uniform(-1, 1, (4, 16)))
+    C = oracle.gemm_fused_grouped(A, B, rows, Bu, bias, None, "silu")
+    r0 = 0
+    for g, r in enumerate(rows):
+        ref = oracle.gemm_fused(A[r0:r0 + r], B[g], Bu[g], bias[g], None, "silu")
+        assert np.array_equal(C[r0:r0 + r].view(np.uint16), ref.view(np.uint16))
+        r0 += r
+    A3 = h(rng.uniform(-1, 1, (3, 9, 24)))
+    C3 = oracle.gemm_fused_batched(A3, B[:3], None, bias[0], None, "gelu")
+    for b in range(3):
+        ref = oracle.gemm_fused(A3[b], B[b], bias=bias[0], act="gelu")
+        assert np.array_equal(C3[b].view(np.uint16), ref.view(np.uint16))
