@@ -147,31 +147,47 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
-def cpu_oracle_rate(w, target_s: float, threads: int):
-    """Time the CPU oracle on a slab of output rows; returns (TFLOP/s, rows, seconds)."""
+def oracle_slab(w, rows: int, threads: int, fused=None):
+    """(callable, FLOPs): the CPU oracle on the first `rows` output rows of the
+    one-GEMM workload `w`; `fused` = (up projection operand or None, act) runs
+    the fused output stage's oracle instead."""
     import numpy as np
 
     import oracle
 
-    K, N = w.K, w.N
+    k = np.arange(w.K, dtype=np.int64)
+    A_rows = np.ascontiguousarray(w.A.values_at(np.arange(rows)[:, None], k[None, :]))
     Bv = w.B.host_view()
-    k = np.arange(K, dtype=np.int64)
+    flops = 2.0 * rows * w.N * w.K
+    if fused is None:
+        return (lambda: oracle.gemm(A_rows, Bv, threads=threads)), flops
+    up, act = fused
+    if up is None:
+        return (lambda: oracle.gemm_fused(A_rows, Bv, act=act, threads=threads)), flops
+    Uv = up.host_view()
+    return (lambda: oracle.gemm_fused(A_rows, Bv, Uv, act=act, threads=threads)), 2 * flops
 
-    def slab(rows):
-        A_rows = np.ascontiguousarray(w.A.values_at(np.arange(rows)[:, None], k[None, :]))
+
+def cpu_oracle_rate(w, target_s: float, threads: int, fused=None):
+    """Time the CPU oracle on a slab of output rows (repeated when the whole
+    problem takes less than the target); returns (TFLOP/s, rows, seconds, reps)."""
+    def slab(rows, reps=1):
+        run, flops = oracle_slab(w, rows, threads, fused)
         t = time.perf_counter()
-        oracle.gemm(A_rows, Bv, threads=threads)
-        return time.perf_counter() - t
+        for _ in range(reps):
+            run()
+        return time.perf_counter() - t, flops * reps
 
     rows = 1
-    dt = slab(rows)
+    dt, _ = slab(rows)
     while dt < 0.5 and rows < w.M:
         rows = min(w.M, rows * 4)
-        dt = slab(rows)
+        dt, _ = slab(rows)
     rate = rows / dt                              # rows per second
     rows = int(max(1, min(w.M, rate * target_s)))
-    dt = slab(rows)
-    return 2.0 * rows * N * K / dt / 1e12, rows, dt
+    reps = max(1, min(100, int(target_s * rate / rows))) if rows == w.M else 1
+    dt, flops = slab(rows, reps)
+    return flops / dt / 1e12, rows, dt, reps
 
 
 # -------------------------------------------------------------- our arm
@@ -291,33 +307,50 @@ def run_ours_multi(args, w, dev, barrier, pg, rank, world):
 
     M, N, K, n = w.M, w.N, w.K, w.count
     flops = w.flops
+    fused = w.B_up is not None or w.act != "none"
+    nB = 2 if w.B_up is not None else 1   # projections read per problem
     if w.kind == "batched":
-        nbytes = 2.0 * n * (M * K + K * N + M * N)
+        nbytes = 2.0 * n * (M * K + nB * K * N + M * N)
     else:
-        nbytes = 2.0 * (M * K + n * K * N + M * N)
+        nbytes = 2.0 * (M * K + nB * n * K * N + M * N)
     peaks = load_peaks()
     bnd = "tensor" if flops / nbytes * peaks["hbm_gbs"] * 1e9 > peaks["tflops"] * 1e12 else "hbm"
     A = w.A.device_view(dev)
     B = w.B.device_view(dev)
+    U = w.B_up.device_view(dev) if w.B_up is not None else None
     C = torch.empty((w.c_rows, N), dtype=torch.float16, device=dev)
-    in_bytes = 2 * (w.A.numel + w.B.numel)
+    in_bytes = 2 * (w.A.numel + w.B.numel + (w.B_up.numel if w.B_up is not None else 0))
     flush_needed = in_bytes <= L2_BYTES
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if flush_needed else None
     l2_note = ("flushed between steps (512 MiB write)" if flush_needed else
                f"not flushed: inputs ({in_bytes / 1e6:.0f} MB) exceed L2 ({L2_BYTES / 1e6:.0f} MB)")
     stream = torch.cuda.current_stream(dev)
     handle = stream.cuda_stream
-    if w.kind == "batched":
+    act = g.ACTIVATIONS[w.act]
+    up = U.data_ptr() if U is not None else 0
+    if w.kind == "batched" and not fused:
         call = (A.data_ptr(), M * K, K, 1, B.data_ptr(), K * N, N, 1, C.data_ptr(), M * N, N, M, N, K, n)
 
         def step():
             g.gemm_f16_batched(*call, stream=handle)
-    else:
+    elif w.kind == "batched":
+        call = (A.data_ptr(), M * K, K, 1, B.data_ptr(), K * N, N, 1, up, 0, 0, 0, act, C.data_ptr(), M * N, N,
+                M, N, K, n)
+
+        def step():
+            g.gemm_f16_batched_fused(*call, stream=handle)
+    elif not fused:
         rows = list(w.group_rows)
         call = (A.data_ptr(), K, 1, B.data_ptr(), K * N, N, 1, C.data_ptr(), N, rows, N, K)
 
         def step():
             g.gemm_f16_grouped(*call, stream=handle)
+    else:
+        rows = list(w.group_rows)
+        call = (A.data_ptr(), K, 1, B.data_ptr(), K * N, N, 1, up, 0, 0, 0, act, C.data_ptr(), N, rows, N, K)
+
+        def step():
+            g.gemm_f16_grouped_fused(*call, stream=handle)
 
     for _ in range(args.warmup):
         if flush is not None:
@@ -363,21 +396,38 @@ def run_ours_multi(args, w, dev, barrier, pg, rank, world):
         C_h = torch.empty(tuple(C.shape), dtype=torch.float16).pin_memory()
         A_buf = torch.empty(w.A.numel, dtype=torch.float16, device=dev)
         B_buf = torch.empty(w.B.numel, dtype=torch.float16, device=dev)
+        U_h = U_buf = U3 = None
+        if w.B_up is not None:
+            U_h = torch.from_numpy(np.ascontiguousarray(w.B_up.host_buffer())).pin_memory()
+            U_buf = torch.empty(w.B_up.numel, dtype=torch.float16, device=dev)
+            U3 = U_buf.view(n, K, N)
+        B3 = B_buf.view(n, K, N)
+
+        def copy_in():
+            A_buf.copy_(A_h, non_blocking=True)
+            B_buf.copy_(B_h, non_blocking=True)
+            if U_h is not None:
+                U_buf.copy_(U_h, non_blocking=True)
+
         if w.kind == "batched":
-            A3, B3, C3 = A_buf.view(n, M, K), B_buf.view(n, K, N), C.view(n, M, N)
+            A3, C3 = A_buf.view(n, M, K), C.view(n, M, N)
 
             def e2e_step():
-                A_buf.copy_(A_h, non_blocking=True)
-                B_buf.copy_(B_h, non_blocking=True)
-                g.bmm(A3, B3, out=C3, stream=stream)
+                copy_in()
+                if fused:
+                    g.fused_mm(A3, B3, act=w.act, b_up=U3, out=C3, stream=stream)
+                else:
+                    g.bmm(A3, B3, out=C3, stream=stream)
                 C_h.copy_(C, non_blocking=True)
         else:
-            A2, B3 = A_buf.view(M, K), B_buf.view(n, K, N)
+            A2 = A_buf.view(M, K)
 
             def e2e_step():
-                A_buf.copy_(A_h, non_blocking=True)
-                B_buf.copy_(B_h, non_blocking=True)
-                g.grouped_mm(A2, B3, list(w.group_rows), out=C, stream=stream)
+                copy_in()
+                if fused:
+                    g.grouped_fused_mm(A2, B3, list(w.group_rows), act=w.act, b_up=U3, out=C, stream=stream)
+                else:
+                    g.grouped_mm(A2, B3, list(w.group_rows), out=C, stream=stream)
                 C_h.copy_(C, non_blocking=True)
         for _ in range(max(1, args.warmup)):
             e2e_step()
@@ -414,10 +464,14 @@ def run_ours_multi(args, w, dev, barrier, pg, rank, world):
     if not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
         first = w.first_problem()
-        rate, r, dt = cpu_oracle_rate(first, args.cpu_seconds, threads)
+        fused = (w.first_up(), w.act) if (w.B_up is not None or w.act != "none") else None
+        rate, r, dt, reps = cpu_oracle_rate(first, args.cpu_seconds, threads, fused)
+        what = "fused-stage oracle" if fused else "oracle"
         cpu = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": f"{r} of {first.M} output rows of problem 0 x all {N} columns, K={K} ({dt:.1f} s)"}
+               "sample": f"{what}: {r} of {first.M} output rows of problem 0 x all {N} columns, K={K}"
+                         f"{f', {reps} times' if reps > 1 else ''} ({dt:.1f} s)"}
     config = {"workload": w.name, "kind": w.kind, "M": M, "N": N, "K": K, "problems": n,
+              "fused_stage": ({"act": w.act, "gate_up": w.B_up is not None} if fused else None),
               "distribution": w.A.kind, "l2": l2_note,
               "parallelism": f"replicas x{world}" if world > 1 else "single GPU", "options": args.opt}
     if w.kind == "grouped":
@@ -492,7 +546,7 @@ def report(args, w, plan, peaks, bnd, flops, nbytes, ms_per_step, value, wall, c
     cpu = None
     if not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
-        rate, rows, dt = cpu_oracle_rate(w, args.cpu_seconds, threads)
+        rate, rows, dt, _ = cpu_oracle_rate(w, args.cpu_seconds, threads)
         cpu = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"{rows} of {M} output rows x all {N} columns, K={K} ({dt:.1f} s)"}
     e2e = None
@@ -541,28 +595,27 @@ def run_reference(args):
     if rank != 0:
         return None
     w = workloads.BY_NAME[args.workload]
+    fused = None
     if isinstance(w, workloads.MultiWorkload):   # the oracle on problem 0, at the same rate unit
+        if w.B_up is not None or w.act != "none":
+            fused = (w.first_up(), w.act)
         w = w.first_problem()
     threads = os.cpu_count() or 1
     per_step = min(5.0, 150.0 / max(1, args.steps + args.warmup))
     # size one slab, then time warmup + steps slabs of that size
-    _, rows, _ = cpu_oracle_rate(w, per_step, threads)
-    import numpy as np
-
-    import oracle
-    k = np.arange(w.K, dtype=np.int64)
-    A_rows = np.ascontiguousarray(w.A.values_at(np.arange(rows)[:, None], k[None, :]))
-    Bv = w.B.host_view()
+    _, rows, _, _ = cpu_oracle_rate(w, per_step, threads, fused)
+    run, flops = oracle_slab(w, rows, threads, fused)
     for _ in range(args.warmup):
-        oracle.gemm(A_rows, Bv, threads=threads)
+        run()
     times = []
     for _ in range(args.steps):
         t = time.perf_counter()
-        oracle.gemm(A_rows, Bv, threads=threads)
+        run()
         times.append(time.perf_counter() - t)
     sec = sum(times) / len(times)
-    value = 2.0 * rows * w.N * w.K / sec / 1e12
-    sample = f"{rows} of {w.M} output rows x all {w.N} columns, K={w.K} per step"
+    value = flops / sec / 1e12
+    sample = (f"{'fused-stage oracle: ' if fused else ''}{rows} of {w.M} output rows x all {w.N} columns, "
+              f"K={w.K} per step")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,

@@ -44,10 +44,15 @@ OPT_TAIL_SPLIT = 10
 OPT_MAX_STAGES = 11
 OPT_MULTICAST = 12
 
+# Activations of the fused output stage (gemm_f16_fused and friends).
+ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU = range(4)
+ACTIVATIONS = {"none": ACT_NONE, "relu": ACT_RELU, "silu": ACT_SILU, "gelu": ACT_GELU}
+
 # Every symbol include/gemm_f16.h declares.
 EXPORTED = ("gemm_f16", "gemm_f16_ws", "gemm_f16_workspace_size", "gemm_f16_status_string",
             "gemm_f16_device_status", "gemm_f16_get_plan", "gemm_f16_set_option",
-            "gemm_f16_abi_version", "gemm_f16_noalloc", "gemm_f16_batched", "gemm_f16_grouped")
+            "gemm_f16_abi_version", "gemm_f16_noalloc", "gemm_f16_batched", "gemm_f16_grouped",
+            "gemm_f16_fused", "gemm_f16_batched_fused", "gemm_f16_grouped_fused", "gemm_f16_fused_get_plan")
 
 # Most groups of one gemm_f16_grouped call.
 MAX_GROUPS = 64
@@ -67,7 +72,7 @@ class Plan(ctypes.Structure):
         "swap_ab", "pair", "a_tma", "a_mn_major", "b_tma", "b_mn_major", "c_tma",
         "tile_m", "tile_n", "tiles_m", "tiles_n", "splits", "kblocks", "units", "grid",
         "stages", "streamk_tiles", "tail_split", "smem_bytes")] + [("workspace_bytes", ctypes.c_size_t)] + [
-        (n, ctypes.c_int) for n in ("a_box3d", "b_box3d", "cluster_ctas")]
+        (n, ctypes.c_int) for n in ("a_box3d", "b_box3d", "cluster_ctas", "fused", "gated")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -111,6 +116,18 @@ def lib():
                 L.gemm_f16_grouped.argtypes = [P, I64, I64, P, I64, I64, I64, P, I64, ctypes.POINTER(I64), I64,
                                                I64, I64, P]
                 L.gemm_f16_grouped.restype = ctypes.c_int
+                I = ctypes.c_int
+                L.gemm_f16_fused.argtypes = [P, I64, I64, P, I64, I64, P, P, P, I, P, I64, I64, I64, I64, P]
+                L.gemm_f16_fused.restype = ctypes.c_int
+                L.gemm_f16_batched_fused.argtypes = [P, I64, I64, I64, P, I64, I64, I64, P, P, P, I64, I, P, I64,
+                                                     I64, I64, I64, I64, I64, P]
+                L.gemm_f16_batched_fused.restype = ctypes.c_int
+                L.gemm_f16_grouped_fused.argtypes = [P, I64, I64, P, I64, I64, I64, P, P, P, I64, I, P, I64,
+                                                     ctypes.POINTER(I64), I64, I64, I64, P]
+                L.gemm_f16_grouped_fused.restype = ctypes.c_int
+                L.gemm_f16_fused_get_plan.argtypes = [P, I64, I64, P, I64, I64, P, P, P, I, P, I64, I64, I64, I64,
+                                                      ctypes.POINTER(Plan)]
+                L.gemm_f16_fused_get_plan.restype = ctypes.c_int
                 _lib = L
     return _lib
 
@@ -158,6 +175,45 @@ def gemm_f16_grouped(A: int, stride_am: int, stride_ak: int, B: int, stride_bg: 
     rows = (ctypes.c_int64 * len(group_rows))(*[int(r) for r in group_rows])
     _check(lib().gemm_f16_grouped(A, stride_am, stride_ak, B, stride_bg, stride_bk, stride_bn, C, ldc, rows,
                                   len(group_rows), N, K, stream or None), "gemm_f16_grouped")
+
+
+def gemm_f16_fused(A: int, stride_am: int, stride_ak: int, B: int, stride_bk: int, stride_bn: int, B_up: int,
+                   bias: int, bias_up: int, act: int, C: int, ldc: int, M: int, N: int, K: int,
+                   stream: int = 0) -> None:
+    """C = act(A*B + bias), or with B_up (read with B's strides) the gate/up form
+    act(A*B + bias) * (A*B_up + bias_up); 0 for an absent B_up / bias (see
+    include/gemm_f16.h)."""
+    _check(lib().gemm_f16_fused(A, stride_am, stride_ak, B, stride_bk, stride_bn, B_up or None, bias or None,
+                                bias_up or None, act, C, ldc, M, N, K, stream or None), "gemm_f16_fused")
+
+
+def gemm_f16_batched_fused(A: int, stride_ab: int, stride_am: int, stride_ak: int, B: int, stride_bb: int,
+                           stride_bk: int, stride_bn: int, B_up: int, bias: int, bias_up: int, stride_bias: int,
+                           act: int, C: int, stride_cb: int, ldc: int, M: int, N: int, K: int, batch: int,
+                           stream: int = 0) -> None:
+    """gemm_f16_batched with the fused output stage (see include/gemm_f16.h)."""
+    _check(lib().gemm_f16_batched_fused(A, stride_ab, stride_am, stride_ak, B, stride_bb, stride_bk, stride_bn,
+                                        B_up or None, bias or None, bias_up or None, stride_bias, act, C,
+                                        stride_cb, ldc, M, N, K, batch, stream or None), "gemm_f16_batched_fused")
+
+
+def gemm_f16_grouped_fused(A: int, stride_am: int, stride_ak: int, B: int, stride_bg: int, stride_bk: int,
+                           stride_bn: int, B_up: int, bias: int, bias_up: int, stride_bias: int, act: int, C: int,
+                           ldc: int, group_rows, N: int, K: int, stream: int = 0) -> None:
+    """gemm_f16_grouped with the fused output stage (see include/gemm_f16.h)."""
+    rows = (ctypes.c_int64 * len(group_rows))(*[int(r) for r in group_rows])
+    _check(lib().gemm_f16_grouped_fused(A, stride_am, stride_ak, B, stride_bg, stride_bk, stride_bn, B_up or None,
+                                        bias or None, bias_up or None, stride_bias, act, C, ldc, rows,
+                                        len(group_rows), N, K, stream or None), "gemm_f16_grouped_fused")
+
+
+def gemm_f16_fused_get_plan(A, stride_am, stride_ak, B, stride_bk, stride_bn, B_up, bias, bias_up, act, C, ldc, M,
+                            N, K) -> dict:
+    p = Plan()
+    _check(lib().gemm_f16_fused_get_plan(A, stride_am, stride_ak, B, stride_bk, stride_bn, B_up or None,
+                                         bias or None, bias_up or None, act, C, ldc, M, N, K, ctypes.byref(p)),
+           "gemm_f16_fused_get_plan")
+    return p.as_dict()
 
 
 def gemm_f16_workspace_size(M: int, N: int, K: int) -> int:
@@ -260,6 +316,108 @@ def grouped_mm(a, b, group_rows, out=None, stream=None):
                          b.stride(2), out.data_ptr(), out.stride(0), group_rows, b.shape[2], a.shape[1],
                          stream=s.cuda_stream)
     return out
+
+
+def _act(act) -> int:
+    if isinstance(act, str):
+        if act not in ACTIVATIONS:
+            raise ValueError(f"unknown activation {act!r}")
+        return ACTIVATIONS[act]
+    return int(act)
+
+
+def _epilogue_args(b, b_up, bias, bias_up, problems: int, n: int):
+    """(B_up pointer, bias pointer, bias_up pointer, bias stride) for the fused
+    entry points; a bias is [n] (shared) or [problems, n] with a unit last stride."""
+    import torch
+
+    if b_up is not None:
+        if b_up.shape != b.shape or b_up.stride() != b.stride() or b_up.dtype != torch.float16:
+            raise ValueError("b_up must be float16 with b's shape and strides")
+    if bias_up is not None and b_up is None:
+        raise ValueError("bias_up needs b_up")
+    strides = []
+    ptrs = []
+    for v in (bias, bias_up):
+        if v is None:
+            ptrs.append(0)
+            continue
+        if v.dtype != torch.float16 or v.shape[-1] != n or v.stride(-1) != 1 or v.dim() not in (1, 2):
+            raise ValueError("a bias is float16 [N] or [problems, N] with unit stride")
+        if v.dim() == 2:
+            if v.shape[0] != problems:
+                raise ValueError("a 2-D bias has one row per problem")
+            strides.append(v.stride(0))
+        else:
+            strides.append(0)
+        ptrs.append(v.data_ptr())
+    if len(set(strides)) > 1:
+        raise ValueError("bias and bias_up must share one layout")
+    return (b_up.data_ptr() if b_up is not None else 0), ptrs[0], ptrs[1], (strides[0] if strides else 0)
+
+
+def fused_mm(a, b, bias=None, act="none", b_up=None, bias_up=None, out=None, stream=None):
+    """fp16 act(a @ b + bias), or with b_up the gate/up form
+    act(a @ b + bias) * (a @ b_up + bias_up), for 2-D or batched 3-D CUDA
+    tensors; returns C."""
+    import torch
+
+    if a.dim() != b.dim() or a.dim() not in (2, 3):
+        raise ValueError("fused_mm takes two matrices or two batches of matrices")
+    code = _act(act)
+    if a.dim() == 2:
+        if out is None:
+            out = torch.empty((a.shape[0], b.shape[1]), dtype=torch.float16, device=a.device)
+        args = _args(a, b, out)
+        bu, bp, bup, _ = _epilogue_args(b, b_up, bias, bias_up, 1, b.shape[1])
+        with torch.cuda.device(a.device):
+            s = stream if stream is not None else torch.cuda.current_stream(a.device)
+            gemm_f16_fused(*args[:6], bu, bp, bup, code, *args[6:], stream=s.cuda_stream)
+        return out
+    if a.shape[0] != b.shape[0] or a.shape[2] != b.shape[1]:
+        raise ValueError("fused_mm takes [batch, M, K] and [batch, K, N]")
+    if out is None:
+        out = torch.empty((a.shape[0], a.shape[1], b.shape[2]), dtype=torch.float16, device=a.device)
+    if out.stride(2) != 1:
+        raise ValueError("out must have a unit column stride")
+    bu, bp, bup, sbias = _epilogue_args(b, b_up, bias, bias_up, a.shape[0], b.shape[2])
+    with torch.cuda.device(a.device):
+        s = stream if stream is not None else torch.cuda.current_stream(a.device)
+        gemm_f16_batched_fused(a.data_ptr(), a.stride(0), a.stride(1), a.stride(2), b.data_ptr(), b.stride(0),
+                               b.stride(1), b.stride(2), bu, bp, bup, sbias, code, out.data_ptr(), out.stride(0),
+                               out.stride(1), a.shape[1], b.shape[2], a.shape[2], a.shape[0],
+                               stream=s.cuda_stream)
+    return out
+
+
+def grouped_fused_mm(a, b, group_rows, bias=None, act="none", b_up=None, bias_up=None, out=None, stream=None):
+    """grouped_mm with the fused output stage: group g's rows become
+    act(a_g @ b[g] + bias[g]) (times a_g @ b_up[g] + bias_up[g] with b_up); a
+    bias is [N] (shared) or [G, N]."""
+    import torch
+
+    if a.dim() != 2 or b.dim() != 3 or b.shape[0] != len(group_rows) or a.shape[1] != b.shape[1]:
+        raise ValueError("grouped_fused_mm takes [rows, K], [G, K, N] and G row counts")
+    if sum(int(r) for r in group_rows) != a.shape[0]:
+        raise ValueError("group_rows must add up to a's rows")
+    if out is None:
+        out = torch.empty((a.shape[0], b.shape[2]), dtype=torch.float16, device=a.device)
+    if out.stride(1) != 1:
+        raise ValueError("out must have a unit column stride")
+    bu, bp, bup, sbias = _epilogue_args(b, b_up, bias, bias_up, b.shape[0], b.shape[2])
+    with torch.cuda.device(a.device):
+        s = stream if stream is not None else torch.cuda.current_stream(a.device)
+        gemm_f16_grouped_fused(a.data_ptr(), a.stride(0), a.stride(1), b.data_ptr(), b.stride(0), b.stride(1),
+                               b.stride(2), bu, bp, bup, sbias, _act(act), out.data_ptr(), out.stride(0), group_rows,
+                               b.shape[2], a.shape[1], stream=s.cuda_stream)
+    return out
+
+
+def fused_plan_for(a, b, out, bias=None, act="none", b_up=None, bias_up=None) -> dict:
+    """The execution plan fused_mm would use for these 2-D torch tensors."""
+    args = _args(a, b, out)
+    bu, bp, bup, _ = _epilogue_args(b, b_up, bias, bias_up, 1, b.shape[1])
+    return gemm_f16_fused_get_plan(*args[:6], bu, bp, bup, _act(act), *args[6:])
 
 
 def plan_for(a, b, out) -> dict:

@@ -161,6 +161,16 @@ struct Args {
     int64_t batch = 1;
     int64_t sab = 0, sbb = 0, scb = 0;
     const int64_t* rows = nullptr;
+    // Fused output stage (`fused`): C = act(A*B + bias), or with Bu (the up
+    // projection, read with B's strides and batch stride) the gate/up form
+    // act(A*B + bias) * (A*Bu + bias_up).  Bias vectors are fp16, N long,
+    // problem (group) b's at element offset b*sbias.
+    bool fused = false;
+    const void* Bu = nullptr;
+    const void* bias = nullptr;
+    const void* bias_up = nullptr;
+    int64_t sbias = 0;
+    int act = 0;
 };
 
 // Elements spanned by `n` copies of a view of `e` elements placed `stride`
@@ -199,11 +209,29 @@ gemm_f16_status validate(const Args& a, bool check_memory, DevInfo** dev)
     const uintptr_t pa = reinterpret_cast<uintptr_t>(a.A), pb = reinterpret_cast<uintptr_t>(a.B),
                     pc = reinterpret_cast<uintptr_t>(a.C);
     if (overlaps(pc, 2 * ec, pa, 2 * ea) || overlaps(pc, 2 * ec, pb, 2 * eb)) return GEMM_F16_ERR_ALIAS;
+    // Fused stage: the up projection spans what B spans; a bias vector N
+    // elements per problem.  None of them may overlap C.
+    int64_t ebias = a.N;
+    if (a.fused) {
+        if (a.act < GEMM_F16_ACT_NONE || a.act > GEMM_F16_ACT_GELU || a.sbias < 0) return GEMM_F16_ERR_INVALID_VALUE;
+        if (a.bias_up && !a.Bu) return GEMM_F16_ERR_INVALID_VALUE;
+        if ((reinterpret_cast<uintptr_t>(a.Bu) | reinterpret_cast<uintptr_t>(a.bias) |
+             reinterpret_cast<uintptr_t>(a.bias_up)) & 1u)
+            return GEMM_F16_ERR_INVALID_VALUE;
+        if (a.batch > 1 && !batch_extent(ebias, a.batch, a.sbias, &ebias)) return GEMM_F16_ERR_INVALID_VALUE;
+        if ((a.Bu && overlaps(pc, 2 * ec, reinterpret_cast<uintptr_t>(a.Bu), 2 * eb)) ||
+            (a.bias && overlaps(pc, 2 * ec, reinterpret_cast<uintptr_t>(a.bias), 2 * ebias)) ||
+            (a.bias_up && overlaps(pc, 2 * ec, reinterpret_cast<uintptr_t>(a.bias_up), 2 * ebias)))
+            return GEMM_F16_ERR_ALIAS;
+    }
     gemm_f16_status st = device_info(dev);
     if (st != GEMM_F16_OK) return st;
     if (check_memory) {
         load_entry_points();
         if (!device_range_ok(a.A, 2 * ea) || !device_range_ok(a.B, 2 * eb) || !device_range_ok(a.C, 2 * ec))
+            return GEMM_F16_ERR_INVALID_VALUE;
+        if (a.fused && ((a.Bu && !device_range_ok(a.Bu, 2 * eb)) || (a.bias && !device_range_ok(a.bias, 2 * ebias)) ||
+                        (a.bias_up && !device_range_ok(a.bias_up, 2 * ebias))))
             return GEMM_F16_ERR_INVALID_VALUE;
     }
     return GEMM_F16_OK;
@@ -275,6 +303,7 @@ bool encode_3d_mn(CUtensorMap* tm, const void* ptr, uint64_t MN, uint64_t K, uin
 
 struct Plan {
     gemm_f16_plan pub;
+    bool fused;   // launch the kernels with the fused output stage
     KernelParams kp;
     size_t counter_bytes;   // split-K counters: align256(4 * tiles)
     size_t partial_bytes;   // split-K partials: align256(4 * units * tile_m * tile_n)
@@ -289,7 +318,9 @@ bool set_smem_attributes(DevInfo& dev)
                              reinterpret_cast<const void*>(gemm_f16_persistent<true, false, false>),
                              reinterpret_cast<const void*>(gemm_f16_persistent<true, true, false>),
                              reinterpret_cast<const void*>(gemm_f16_persistent<false, false, true>),
-                             reinterpret_cast<const void*>(gemm_f16_persistent<true, false, true>)};
+                             reinterpret_cast<const void*>(gemm_f16_persistent<true, false, true>),
+                             reinterpret_cast<const void*>(gemm_f16_persistent<false, false, true, true>),
+                             reinterpret_cast<const void*>(gemm_f16_persistent<true, false, true, true>)};
     bool ok = true;
     for (const void* k : kernels)
         ok = ok && cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) == cudaSuccess;
@@ -482,8 +513,22 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     int BN, tiles_m, tiles_n, kblocks, splits;
     const bool grouped = a.rows != nullptr;
     const bool batched = !grouped && a.batch > 1;
-    // (groups differ in M, so the swapped form, which tiles over M as N, is not used)
-    shape_plan(a.M, a.N, a.K, dev.sms, !grouped, &swap, &Mv, &Nv, &BN, &tiles_m, &tiles_n, &kblocks, &splits);
+    const bool gated = a.fused && a.Bu != nullptr;
+    // (groups differ in M, so the swapped form, which tiles over M as N, is not
+    // used; nor for the gate/up form, whose two products share the MMA's N)
+    shape_plan(a.M, a.N, a.K, dev.sms, !grouped && !gated, &swap, &Mv, &Nv, &BN, &tiles_m, &tiles_n, &kblocks,
+               &splits);
+    // Gate/up: tiles of `out` output columns whose accumulator holds 2*out
+    // columns (gate then up); whole tiles only.
+    int out_cols = BN;
+    if (gated) {
+        const int64_t forced = opt(GEMM_F16_OPT_TILE_N);
+        out_cols = forced > 0 ? static_cast<int>(std::min<int64_t>(forced, 128))
+                              : static_cast<int>(std::min<int64_t>(128, round_up(a.N, 64)));
+        BN = 2 * out_cols;
+        tiles_n = static_cast<int>((a.N + out_cols - 1) / out_cols);
+        splits = 1;
+    }
     if (BN < 16 || BN > 256 || BN % 16 != 0) return GEMM_F16_ERR_INVALID_VALUE;
 
     // Kernel view: C'[m,n] = sum_k A'[m,k] B'[k,n].
@@ -517,8 +562,15 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     const bool have_tma = g_encode != nullptr;
     OperandChoice ca = choose_operand(kp.A, kp.a_sm, kp.a_sk, Mv, a.K, gemm_f16_dev::kBM,
                                       have_tma && !(fg & 1) && (!a_bd || bs_ok(a_bs)));
-    OperandChoice cb = choose_operand(kp.B, kp.b_sn, kp.b_sk, Nv, a.K, BN,
+    OperandChoice cb = choose_operand(kp.B, kp.b_sn, kp.b_sk, Nv, a.K, gated ? out_cols : BN,
                                       have_tma && !(fg & 2) && (!b_bd || bs_ok(b_bs)));
+    if (gated) {
+        // both projections take the same path (same strides; only the bases differ)
+        kp.Bu = static_cast<const __half*>(a.Bu);
+        const OperandChoice cu = choose_operand(kp.Bu, kp.b_sn, kp.b_sk, Nv, a.K, out_cols,
+                                                have_tma && !(fg & 2) && (!b_bd || bs_ok(b_bs)));
+        if (cu.tma != cb.tma || cu.mn != cb.mn) cb = choose_operand(kp.B, kp.b_sn, kp.b_sk, Nv, a.K, out_cols, false);
+    }
 
     // Pair form (two CTAs per 256 x BN tile): TMA operands, no split-K, and a
     // B half that is a whole number of 64-column swizzle atoms.
@@ -552,7 +604,7 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     // B tile (whole tiles only: no K cut, no tail split).
     const int64_t mc_opt = opt(GEMM_F16_OPT_MULTICAST);
     bool quad = pair && mc_opt == 2 && BN == 256 && splits == 1 && opt(GEMM_F16_OPT_STREAMK) != 2 && tiles_m >= 2 &&
-                !batched && !grouped;
+                !batched && !grouped && !a.fused;
 
     bool a_3d = false, b_3d = false;
     // trailing batch dimensions (0: none)
@@ -573,26 +625,30 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     }
     // B's box: a CTA's whole share of the tile's columns, or in the four-CTA form
     // the 64-column quarter it multicasts.
+    // The gate/up form reads boxes of its output width from both projections.
     auto encode_b = [&](bool quarter) {
-        const int cols = quarter ? bcols / 2 : bcols;
-        b_3d = cb.mn && encode_3d_mn(&kp.tmB, kp.B, Nv, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk,
-                                     static_cast<uint32_t>(cols / 64), nb_b, bst_b);
-        return b_3d ? true
-               : cb.mn ? encode_2d(&kp.tmB, kp.B, Nv, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk, 64, 64,
-                                   nb_b, bst_b)
-                       : encode_2d(&kp.tmB, kp.B, a.K, Nv, Nv == 1 ? round_up(2 * a.K, 16) : 2 * kp.b_sn, 64,
-                                   static_cast<uint32_t>(cols), nb_b, bst_b);
+        const int cols = gated ? out_cols : (quarter ? bcols / 2 : bcols);
+        auto enc = [&](CUtensorMap* tm, const __half* ptr) {
+            b_3d = cb.mn && encode_3d_mn(tm, ptr, Nv, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk,
+                                         static_cast<uint32_t>(cols / 64), nb_b, bst_b);
+            return b_3d ? true
+                   : cb.mn ? encode_2d(tm, ptr, Nv, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk, 64, 64, nb_b,
+                                       bst_b)
+                           : encode_2d(tm, ptr, a.K, Nv, Nv == 1 ? round_up(2 * a.K, 16) : 2 * kp.b_sn, 64,
+                                       static_cast<uint32_t>(cols), nb_b, bst_b);
+        };
+        return enc(&kp.tmB, kp.B) && (!gated || enc(&kp.tmBu, kp.Bu));
     };
     if (cb.tma) {
         if (!encode_b(quad)) {
             if (pair) return GEMM_F16_ERR_LAUNCH;
-            cb = choose_operand(kp.B, kp.b_sn, kp.b_sk, Nv, a.K, BN, false);
+            cb = choose_operand(kp.B, kp.b_sn, kp.b_sk, Nv, a.K, gated ? out_cols : BN, false);
         }
     }
     // TMA stores write whole 16-byte chunks at the N edge, so a C row whose
     // width is not a multiple of 8 elements would get its pitch padding
     // overwritten: such a C goes through the masked stores.
-    bool c_tma = have_tma && !(fg & 4) && !swap && splits == 1 && BN % 64 == 0 && a.N % 8 == 0 &&
+    bool c_tma = have_tma && !(fg & 4) && !swap && splits == 1 && out_cols % 64 == 0 && a.N % 8 == 0 &&
                  (reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc * 2) % 16 == 0 && a.M < (int64_t(1) << 32) &&
                  a.N < (int64_t(1) << 32) && (a.ldc * 2) < (int64_t(1) << 40) && (!c_bd || bs_ok(c_bs));
     if (c_tma)
@@ -609,7 +665,7 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     // operand is gathered (gathered tiles are slow, so balancing the last wave
     // pays for the fixup); otherwise the last partial wave is split along N.
     const int64_t sk_opt = opt(GEMM_F16_OPT_STREAMK);
-    const bool use_sk = splits == 1 && !quad && (sk_opt == 2 || (sk_opt == 0 && (!ca.tma || !cb.tma)));
+    const bool use_sk = splits == 1 && !quad && !gated && (sk_opt == 2 || (sk_opt == 0 && (!ca.tma || !cb.tma)));
     const bool may_cut = splits > 1 || use_sk;
     const int epi = (c_tma || may_cut) ? static_cast<int>(gemm_f16_dev::kEpiBytes) : 0;
     int stages = (kMaxDynSmem - kSmemAlignSlack - epi - static_cast<int>(gemm_f16_dev::kBarrierBytes)) /
@@ -641,8 +697,9 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     const int64_t unit_tiles = quad ? static_cast<int64_t>(unit_rows) * tiles_n : tiles;
     // Narrowest tail piece: the pair form keeps >= 64 B columns per CTA; a
     // TMA-stored C needs whole 64-column boxes; the four-CTA form never cuts.
+    // (gate/up tiles are never cut: the minimum piece is wider than the tile)
     const Schedule sch = make_schedule(unit_tiles, kblocks, splits, static_cast<int>(max_workers), BN,
-                                       quad ? 2 * BN : (pair ? 128 : 64), use_sk);
+                                       (quad || gated) ? 2 * BN : (pair ? 128 : 64), use_sk);
     const int grid = cluster_ctas * sch.workers;
     const int64_t panel = opt(GEMM_F16_OPT_PANEL);
 
@@ -676,6 +733,15 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
                  (b_3d ? gemm_f16_dev::kOpBox3d : 0u);
     kp.c_tma = c_tma ? 1u : 0u;
     kp.epi_smem = epi > 0 ? 1u : 0u;
+    pl->fused = a.fused;
+    if (a.fused) {
+        kp.bias = static_cast<const __half*>(a.bias);
+        kp.bias_up = static_cast<const __half*>(a.bias_up);
+        kp.bias_bs = a.sbias;
+        kp.act = a.act;
+        kp.gated = gated ? 1 : 0;
+        kp.bias_rows = swap ? 1 : 0;   // C^T: the bias runs along the kernel view's rows
+    }
     // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16
     // (bits 7-9, 10-12 = 0), A/B MN-major flags (bits 15, 16), N >> 3 (bits
     // 17-22), M >> 4 (bits 24-28); M is 256 for the pair form.
@@ -696,7 +762,9 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     pub.cluster_ctas = cluster_ctas;
     pub.a_tma = ca.tma, pub.a_mn_major = ca.mn, pub.b_tma = cb.tma, pub.b_mn_major = cb.mn, pub.c_tma = c_tma;
     pub.a_box3d = a_3d && ca.tma, pub.b_box3d = b_3d && cb.tma;
-    pub.tile_m = tile_rows, pub.tile_n = BN, pub.tiles_m = tiles_m, pub.tiles_n = tiles_n;
+    pub.tile_m = tile_rows, pub.tile_n = out_cols, pub.tiles_m = tiles_m, pub.tiles_n = tiles_n;
+    pub.fused = a.fused ? 1 : 0;
+    pub.gated = gated ? 1 : 0;
     pub.splits = splits, pub.kblocks = kblocks, pub.grid = grid;
     pub.units = static_cast<int>(quad ? unit_tiles : tiles * splits);
     pub.streamk_tiles = sch.sk_iters > 0 ? static_cast<int>(tiles - sch.sk_tile0) : 0;
@@ -718,7 +786,10 @@ gemm_f16_status launch(Plan& pl, DevInfo& dev, float* partials, int* counters, c
     if (!set_smem_attributes(dev)) return GEMM_F16_ERR_LAUNCH;
     const bool multi = kp.gmode != 0;
     if (!pl.pub.pair) {
-        if (multi)
+        if (pl.fused)
+            gemm_f16_dev::gemm_f16_persistent<false, false, true, true>
+                <<<pl.pub.grid, gemm_f16_dev::kNumThreads, pl.pub.smem_bytes, stream>>>(kp);
+        else if (multi)
             gemm_f16_dev::gemm_f16_persistent<false, false, true>
                 <<<pl.pub.grid, gemm_f16_dev::kNumThreads, pl.pub.smem_bytes, stream>>>(kp);
         else
@@ -739,8 +810,9 @@ gemm_f16_status launch(Plan& pl, DevInfo& dev, float* partials, int* counters, c
         cfg.numAttrs = 1;
         const cudaError_t e =
             pl.pub.cluster_ctas == 4 ? cudaLaunchKernelEx(&cfg, gemm_f16_dev::gemm_f16_persistent<true, true, false>, kp)
-            : multi                  ? cudaLaunchKernelEx(&cfg, gemm_f16_dev::gemm_f16_persistent<true, false, true>, kp)
-                                     : cudaLaunchKernelEx(&cfg, gemm_f16_dev::gemm_f16_persistent<true, false, false>, kp);
+            : pl.fused ? cudaLaunchKernelEx(&cfg, gemm_f16_dev::gemm_f16_persistent<true, false, true, true>, kp)
+            : multi    ? cudaLaunchKernelEx(&cfg, gemm_f16_dev::gemm_f16_persistent<true, false, true>, kp)
+                       : cudaLaunchKernelEx(&cfg, gemm_f16_dev::gemm_f16_persistent<true, false, false>, kp);
         if (e != cudaSuccess) {
             cudaGetLastError();
             return GEMM_F16_ERR_LAUNCH;
@@ -874,6 +946,27 @@ gemm_f16_status run_noalloc(const Args& a, cudaStream_t stream)
     return launch(pl, *dev, partials, counters, stream);
 }
 
+void set_fused(Args& a, const void* B_up, const void* bias, const void* bias_up, int64_t stride_bias, int act)
+{
+    a.fused = true;
+    a.Bu = B_up;
+    a.bias = bias;
+    a.bias_up = bias_up;
+    a.sbias = stride_bias;
+    a.act = act;
+}
+
+// Sum of the group rows (false if one is negative or the sum overflows).
+bool total_rows(const int64_t* group_rows, int64_t groups, int64_t* total)
+{
+    if (!group_rows || groups < 1 || groups > gemm_f16_dev::kMaxGroups) return false;
+    int64_t t = 0;
+    for (int64_t g = 0; g < groups; ++g)
+        if (group_rows[g] < 0 || __builtin_add_overflow(t, group_rows[g], &t)) return false;
+    *total = t;
+    return true;
+}
+
 }  // namespace
 
 extern "C" {
@@ -918,17 +1011,72 @@ gemm_f16_status gemm_f16_grouped(const void* A, int64_t stride_am, int64_t strid
                                  const int64_t* group_rows, int64_t groups, int64_t N, int64_t K,
                                  cudaStream_t stream)
 {
-    if (!group_rows || groups < 1 || groups > gemm_f16_dev::kMaxGroups) return GEMM_F16_ERR_INVALID_VALUE;
     int64_t total = 0;
-    for (int64_t g = 0; g < groups; ++g) {
-        if (group_rows[g] < 0 || __builtin_add_overflow(total, group_rows[g], &total)) return GEMM_F16_ERR_INVALID_VALUE;
-    }
+    if (!total_rows(group_rows, groups, &total)) return GEMM_F16_ERR_INVALID_VALUE;
     if (total == 0) return (A && B && C && N > 0 && K > 0) ? GEMM_F16_OK : GEMM_F16_ERR_INVALID_VALUE;
     Args a{A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, total, N, K};
     a.batch = groups;
     a.sbb = stride_bg;
     a.rows = group_rows;
     return run(a, nullptr, 0, true, stream);
+}
+
+gemm_f16_status gemm_f16_fused(const void* A, int64_t stride_am, int64_t stride_ak, const void* B, int64_t stride_bk,
+                               int64_t stride_bn, const void* B_up, const void* bias, const void* bias_up, int act,
+                               void* C, int64_t ldc, int64_t M, int64_t N, int64_t K, cudaStream_t stream)
+{
+    Args a{A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, M, N, K};
+    set_fused(a, B_up, bias, bias_up, 0, act);
+    return run(a, nullptr, 0, true, stream);
+}
+
+gemm_f16_status gemm_f16_batched_fused(const void* A, int64_t stride_ab, int64_t stride_am, int64_t stride_ak,
+                                       const void* B, int64_t stride_bb, int64_t stride_bk, int64_t stride_bn,
+                                       const void* B_up, const void* bias, const void* bias_up, int64_t stride_bias,
+                                       int act, void* C, int64_t stride_cb, int64_t ldc, int64_t M, int64_t N,
+                                       int64_t K, int64_t batch, cudaStream_t stream)
+{
+    Args a{A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, M, N, K};
+    a.batch = batch;
+    a.sab = stride_ab, a.sbb = stride_bb, a.scb = stride_cb;
+    set_fused(a, B_up, bias, bias_up, stride_bias, act);
+    return run(a, nullptr, 0, true, stream);
+}
+
+gemm_f16_status gemm_f16_grouped_fused(const void* A, int64_t stride_am, int64_t stride_ak, const void* B,
+                                       int64_t stride_bg, int64_t stride_bk, int64_t stride_bn, const void* B_up,
+                                       const void* bias, const void* bias_up, int64_t stride_bias, int act, void* C,
+                                       int64_t ldc, const int64_t* group_rows, int64_t groups, int64_t N, int64_t K,
+                                       cudaStream_t stream)
+{
+    int64_t total = 0;
+    if (!total_rows(group_rows, groups, &total)) return GEMM_F16_ERR_INVALID_VALUE;
+    if (act < GEMM_F16_ACT_NONE || act > GEMM_F16_ACT_GELU || stride_bias < 0 || (bias_up && !B_up))
+        return GEMM_F16_ERR_INVALID_VALUE;
+    if (total == 0) return (A && B && C && N > 0 && K > 0) ? GEMM_F16_OK : GEMM_F16_ERR_INVALID_VALUE;
+    Args a{A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, total, N, K};
+    a.batch = groups;
+    a.sbb = stride_bg;
+    a.rows = group_rows;
+    set_fused(a, B_up, bias, bias_up, stride_bias, act);
+    return run(a, nullptr, 0, true, stream);
+}
+
+gemm_f16_status gemm_f16_fused_get_plan(const void* A, int64_t stride_am, int64_t stride_ak, const void* B,
+                                        int64_t stride_bk, int64_t stride_bn, const void* B_up, const void* bias,
+                                        const void* bias_up, int act, void* C, int64_t ldc, int64_t M, int64_t N,
+                                        int64_t K, gemm_f16_plan* plan)
+{
+    if (!plan) return GEMM_F16_ERR_INVALID_VALUE;
+    Args a{A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, M, N, K};
+    set_fused(a, B_up, bias, bias_up, 0, act);
+    DevInfo* dev = nullptr;
+    gemm_f16_status st = validate(a, true, &dev);
+    if (st != GEMM_F16_OK) return st;
+    Plan pl;
+    st = make_plan(a, *dev, &pl);
+    if (st == GEMM_F16_OK) *plan = pl.pub;
+    return st;
 }
 
 gemm_f16_status gemm_f16_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes)

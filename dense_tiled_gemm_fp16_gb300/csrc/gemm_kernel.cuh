@@ -91,6 +91,7 @@ struct KernelParams {
     CUtensorMap tmB;   // B' (K-major: dims {K, N}; MN-major: dims {N, K})
     CUtensorMap tmB2;  // B' with the box of a tail piece (tail_split > 1): as narrow as the piece
     CUtensorMap tmC;   // C  (dims {N, M}, box 64 x 32)
+    CUtensorMap tmBu;  // gated fused stage: the up projection's B' (the geometry of tmB)
     const __half* A;   // A'[m,k] = A[m*a_sm + k*a_sk]
     int64_t a_sm, a_sk;
     const __half* B;   // B'[k,n] = B[k*b_sk + n*b_sn]
@@ -136,6 +137,18 @@ struct KernelParams {
     int g_tm[kMaxGroups];
     int64_t g_row0[kMaxGroups];
     int64_t g_rows[kMaxGroups];
+    // Fused output stage (kEpi kernels): out = act(acc + bias), or, gated,
+    // out = act(acc_gate + bias) * (acc_up + bias_up).  A gated tile's BN
+    // accumulator columns are BN/2 gate columns followed by the same BN/2
+    // columns of the up projection: both B' operands land in one stage, so one
+    // MMA stream computes both products of the shared A' rows.
+    const __half* Bu;         // up projection B' (the strides and batch stride of B')
+    const __half* bias;       // fp16 bias, or null
+    const __half* bias_up;    // fp16 bias of the up projection, or null
+    int64_t bias_bs;          // elements between the bias vectors of consecutive problems / groups
+    int act;                  // 0 identity, 1 ReLU, 2 SiLU, 3 GELU (exact, x * Phi(x))
+    int gated;
+    int bias_rows;            // 1: the bias runs along the kernel view's rows (the swapped form)
 };
 
 struct SmemLayout {
@@ -301,6 +314,7 @@ struct UnitGeom {
     int32_t az, bz, cz;
     const __half* A;
     const __half* B;
+    const __half* Bu;   // gated fused stage only
     __half* C;
 };
 
@@ -314,18 +328,21 @@ __device__ __forceinline__ UnitGeom unit_geom(const KernelParams& p, const Unit&
     u.az = u.bz = u.cz = 0;
     u.A = p.A;
     u.B = p.B;
+    u.Bu = p.Bu;
     u.C = p.C;
     if (!kMulti) {
     } else if (p.gmode == 1) {
         u.az = u.bz = u.cz = w.g;
         u.A = p.A + g * p.a_bs;
         u.B = p.B + g * p.b_bs;
+        u.Bu = p.Bu + g * p.b_bs;
         u.C = p.C + g * p.c_bs;
     } else if (p.gmode == 2) {
         u.a_row = p.g_row0[w.g];
         u.row_lim = p.g_row0[w.g] + p.g_rows[w.g];
         u.bz = w.g;
         u.B = p.B + g * p.b_bs;
+        u.Bu = p.Bu + g * p.b_bs;
     }
     return u;
 }
@@ -385,9 +402,9 @@ __device__ __forceinline__ void load_a_slot(const KernelParams& p, uint32_t sa, 
     }
 }
 
-// B' columns col .. col+bcols-1 of one slot: K-major one box (k, col) of the
-// map's width; MN-major one 3-D box (0, k, col/64) or one 2-D box (col, k) per
-// 64 columns.
+// B' columns col .. col+bcols-1 of one slot through map `tmb`: K-major one box
+// (k, col) of the map's width; MN-major one 3-D box (0, k, col/64) or one 2-D
+// box (col, k) per 64 columns.
 template <bool kPair>
 __device__ __forceinline__ void load_b_slot(const KernelParams& p, const CUtensorMap* tmb, uint32_t sb, int32_t k0,
                                             int64_t col, int32_t z, int bcols, bool b_mn, bool b_3d, bool bd,
@@ -407,9 +424,9 @@ __device__ __forceinline__ void load_b_slot(const KernelParams& p, const CUtenso
     } else {
         for (int j = 0; j < bcols / 64; ++j) {
             if (bd)
-                tma3<kPair>(sb + j * 8192, &p.tmB, c + 64 * j, k0, z, bar);
+                tma3<kPair>(sb + j * 8192, tmb, c + 64 * j, k0, z, bar);
             else
-                tma2<kPair>(sb + j * 8192, &p.tmB, c + 64 * j, k0, bar);
+                tma2<kPair>(sb + j * 8192, tmb, c + 64 * j, k0, bar);
         }
     }
 }
@@ -678,16 +695,183 @@ __device__ __forceinline__ void add_tmem16(uint32_t taddr, float* sacc)
     for (int i = 0; i < 16; ++i) sacc[i] += __uint_as_float(v[i]);
 }
 
+// ---------------------------------------------------------------------------
+// Fused output stage.  The pages name bias and activation fusion into the
+// GEMM's output stage (TileLang tutorial ch. 14, section 6.3, item 4; AI-infra
+// page, section 05) and a gate/up GEMM that fuses two projections with the
+// activation and the multiply (C500 review, section 17.3).  Everything runs in
+// fp32 on the accumulator values, with one rounding to fp16 at the store.
+
+// act(x): 1 ReLU (x < 0 -> 0, NaN kept), 2 SiLU x / (1 + e^-x),
+// 3 GELU x * Phi(x) with Phi(x) = erfc(-x / sqrt 2) / 2; otherwise identity.
+__device__ __forceinline__ float act_apply(int act, float x)
+{
+    switch (act) {
+    case 1: return x < 0.f ? 0.f : x;
+    case 2: return x / (1.f + expf(-x));
+    case 3: return x * (0.5f * erfcf(-x * 0.70710678118654752f));
+    default: return x;
+    }
+}
+
+__device__ __forceinline__ float half_lo(uint32_t w) { return __half2float(__ushort_as_half(static_cast<unsigned short>(w))); }
+__device__ __forceinline__ float half_hi(uint32_t w)
+{
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+
+// v[i] = b[n + i] for the 16 columns n .. n+15 (0 past N, or without a bias).
+__device__ __forceinline__ void load_bias16(const __half* b, int64_t n, int64_t N, float* v)
+{
+    if (b == nullptr) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        return;
+    }
+    const __half* q = b + n;
+    if (n + 16 <= N && (reinterpret_cast<uintptr_t>(q) & 15u) == 0) {
+        const uint4 x0 = __ldg(reinterpret_cast<const uint4*>(q));
+        const uint4 x1 = __ldg(reinterpret_cast<const uint4*>(q) + 1);
+        const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[2 * i] = half_lo(w[i]);
+            v[2 * i + 1] = half_hi(w[i]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = (n + i < N) ? __half2float(q[i]) : 0.f;
+    }
+}
+
+// v = act(v + bias) for 16 sums of kernel columns n .. n+15 of one row: the
+// bias along the columns, or (bias_rows) the row's own value `brow`.
+__device__ __forceinline__ void epi_finish16(const KernelParams& p, const __half* bias, float brow, int64_t n, float* v)
+{
+    float b[16];
+    if (p.bias_rows) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) b[i] = brow;
+    } else {
+        load_bias16(bias, n, p.N, b);
+    }
+    const int act = p.act;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = act_apply(act, v[i] + b[i]);
+}
+
+// Gated: g = act(g + bias) * (u + bias_up) for columns n .. n+15.
+__device__ __forceinline__ void epi_gated16(const KernelParams& p, const __half* bias, const __half* bias_up, int64_t n,
+                                            float* g, const float* u)
+{
+    float bg[16], bu[16];
+    load_bias16(bias, n, p.N, bg);
+    load_bias16(bias_up, n, p.N, bu);
+    const int act = p.act;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) g[i] = act_apply(act, g[i] + bg[i]) * (u[i] + bu[i]);
+}
+
+// One 16-column piece of a warp's 32 output rows (h: this lane's 8 packed
+// pairs): into the warp's swizzled staging buffer, written out by a TMA store
+// every four pieces (64 columns) and after the last one, or by masked stores.
+template <bool kMulti>
+__device__ __forceinline__ void emit_piece(const KernelParams& p, const SmemLayout& L, const UnitGeom& ug, int piece,
+                                           int npieces, const uint32_t* h, int64_t m0, int64_t n0, int64_t crow,
+                                           bool ctma, uint32_t& buf, uint32_t& group_count)
+{
+    const int lane = threadIdx.x & 31;
+    const int q = (threadIdx.x >> 5) & 3;
+    if (ctma) {
+        const int j0 = (piece & 3) * 2;   // 16-byte chunk inside the 128-byte row
+        if ((piece & 3) == 0) {
+            buf = L.epi + (q * 2 + (group_count & 1u)) * kEpiBufBytes;
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+        }
+        st_smem_v4(buf + lane * 128 + ((j0 ^ (lane & 7)) << 4), make_uint4(h[0], h[1], h[2], h[3]));
+        st_smem_v4(buf + lane * 128 + (((j0 + 1) ^ (lane & 7)) << 4), make_uint4(h[4], h[5], h[6], h[7]));
+        if ((piece & 3) == 3 || piece == npieces - 1) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                if (crow < ug.row_lim) {
+                    const int32_t xn = static_cast<int32_t>(n0 + 16 * (piece & ~3));
+                    if (kMulti && p.c_bdim)
+                        tma_store_3d(&p.tmC, buf, xn, static_cast<int32_t>(crow), ug.cz);
+                    else
+                        tma_store_2d(&p.tmC, buf, xn, static_cast<int32_t>(crow));
+                }
+                bulk_commit_group();
+            }
+            ++group_count;
+        }
+    } else {
+        store_piece_masked(p, ug.C, ug.row_lim, ug.a_row + m0 + 32 * q + lane, n0 + 16 * piece, h);
+    }
+}
+
+// Whole-tile epilogue with the fused output stage: `ow` output columns from
+// n0 (gated: the accumulator's first ow columns are the gate sums, the next
+// ow the up sums of the same output columns).
+template <bool kPair, bool kMulti>
+__device__ __forceinline__ void fused_tile_epilogue(const KernelParams& p, const SmemLayout& L, const UnitGeom& ug,
+                                                   const __half* bias, const __half* bias_up, float brow,
+                                                   uint32_t taddr, uint32_t tempty, int64_t m0, int64_t n0, int ow,
+                                                   bool gated, int64_t crow, bool ctma, uint32_t& group_count)
+{
+    const int lane = threadIdx.x & 31;
+    const int npieces = ow / 16;
+    uint32_t buf = 0;
+    auto release = [&]() {   // the accumulator is in registers: the MMA may reuse it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+            if (kPair)
+                mbar_arrive_cluster(tempty);
+            else
+                mbar_arrive(tempty);
+        }
+    };
+    // One output piece per TMEM wait: the activation's inlined math needs the
+    // registers that more accumulator columns in flight would hold.
+    for (int piece = 0; piece < npieces; ++piece) {
+        const int64_t n = n0 + 16 * piece;
+        uint32_t r[32];
+        tmem_ld_x16(taddr + 16 * piece, r);
+        if (gated) tmem_ld_x16(taddr + ow + 16 * piece, r + 16);
+        tmem_wait_ld();
+        if (piece == npieces - 1) release();
+        float g[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) g[i] = __uint_as_float(r[i]);
+        if (gated) {
+            float u[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) u[i] = __uint_as_float(r[16 + i]);
+            epi_gated16(p, bias, bias_up, n, g, u);
+        } else {
+            epi_finish16(p, bias, brow, n, g);
+        }
+        uint32_t h[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) h[i] = pack_half2(g[2 * i], g[2 * i + 1]);
+        emit_piece<kMulti>(p, L, ug, piece, npieces, h, m0, n0, crow, ctma, buf, group_count);
+    }
+}
+
 // Epilogue of a unit whose tile is cut along K (split-K or stream-K), run by
 // the 128 epilogue threads.  This unit's fp32 sum is a partial.  The last unit
 // of the tile to finish adds all partials in K order (deterministic) and stores
 // C; the others leave their partial in the workspace.  The accumulator stays in
 // TMEM until the decision, so the last one takes its own values from TMEM.
-template <bool kPair, bool kMulti>
+// kEpi: the complete sums go through the fused bias + activation stage
+// (`bias`, or the row's `brow`) before the store; gated tiles are never cut.
+template <bool kPair, bool kMulti, bool kEpi>
 __device__ __forceinline__ void cut_tile_epilogue(const KernelParams& p, const SmemLayout& L, const Unit& w,
                                                const UnitGeom& ug, uint32_t taddr, uint32_t tempty, int64_t m0, int64_t n0,
                                                volatile int* flag, volatile int* abort, uint32_t& fix_ph,
-                                               bool last_unit)
+                                               bool last_unit, const __half* bias, float brow)
 {
     const int lane = threadIdx.x & 31;
     const int row = 32 * ((threadIdx.x >> 5) & 3) + lane;
@@ -812,6 +996,7 @@ __device__ __forceinline__ void cut_tile_epilogue(const KernelParams& p, const S
                             for (int h1 = 0; h1 < 2; ++h1) {
                                 const int h2 = hp + h1;
                                 uint32_t h[8];
+                                float sv[16];
 #pragma unroll
                                 for (int i = 0; i < 8; ++i) {
                                     const float o0 = __uint_as_float(r[16 * h2 + 2 * i]);
@@ -820,10 +1005,12 @@ __device__ __forceinline__ void cut_tile_epilogue(const KernelParams& p, const S
                                     const float p0 = (i & 1) ? q4.z : q4.x;
                                     const float p1 = (i & 1) ? q4.w : q4.y;
                                     // K order: 0 + first + second, exactly as in the general loop
-                                    const float s0v = own_first ? (0.f + o0) + p0 : (0.f + p0) + o0;
-                                    const float s1v = own_first ? (0.f + o1) + p1 : (0.f + p1) + o1;
-                                    h[i] = pack_half2(s0v, s1v);
+                                    sv[2 * i] = own_first ? (0.f + o0) + p0 : (0.f + p0) + o0;
+                                    sv[2 * i + 1] = own_first ? (0.f + o1) + p1 : (0.f + p1) + o1;
                                 }
+                                if (kEpi) epi_finish16(p, bias, brow, n0 + (b0 + g0 + h2) * 16, sv);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) h[i] = pack_half2(sv[2 * i], sv[2 * i + 1]);
                                 if (stage_c) {
                                     const int j0 = h2 * 2;
                                     st_smem_v4(buf + lane * 128 + ((j0 ^ (lane & 7)) << 4),
@@ -870,6 +1057,7 @@ __device__ __forceinline__ void cut_tile_epilogue(const KernelParams& p, const S
 #pragma unroll
                                 for (int i = 0; i < 16; ++i) acc[i] += __uint_as_float(r[16 * h1 + i]);
                             }
+                            if (kEpi) epi_finish16(p, bias, brow, n0 + (b0 + c) * 16, acc);
                             uint32_t h[8];
 #pragma unroll
                             for (int i = 0; i < 8; ++i) h[i] = pack_half2(acc[2 * i], acc[2 * i + 1]);
@@ -953,6 +1141,7 @@ __device__ __forceinline__ void cut_tile_epilogue(const KernelParams& p, const S
                     }
                     if (j == others - 1) {
                         if (w.seg == others) add_tmem16(taddr + c * 16, sacc);   // own sum is the last in K order
+                        if (kEpi) epi_finish16(p, bias, brow, n0 + c * 16, sacc);
                         uint32_t h[8];
     #pragma unroll
                         for (int i = 0; i < 8; ++i) h[i] = pack_half2(sacc[2 * i], sacc[2 * i + 1]);
@@ -981,7 +1170,9 @@ __device__ __forceinline__ void cut_tile_epilogue(const KernelParams& p, const S
 // stage's empty barrier then waits for both pairs' MMAs (count 2).
 // kMulti: batched or grouped launches (gmode != 0); the one-GEMM launch is
 // compiled without that geometry.
-template <bool kPair, bool kQuad, bool kMulti>
+// kEpi: the fused output stage (bias, activation, gate/up product); built on
+// the kMulti geometry, which also runs one-GEMM launches (gmode 0).
+template <bool kPair, bool kQuad, bool kMulti, bool kEpi = false>
 __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __grid_constant__ KernelParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1001,6 +1192,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
     const bool a_3d = p.a_flags & kOpBox3d, b_3d = p.b_flags & kOpBox3d;
     const bool a_bd = kMulti && p.a_bdim != 0, b_bd = kMulti && p.b_bdim != 0;   // maps with a trailing batch dimension
     static_assert(kPair || !kQuad, "the four-CTA form is built on pairs");
+    static_assert(!kEpi || (kMulti && !kQuad), "the fused stage runs on the kMulti single and pair forms");
+    const bool gated = kEpi && p.gated != 0;
     const uint32_t crank = kPair ? cluster_ctarank() : 0u;   // rank in the cluster
     const uint32_t rank = crank & 1u;                         // rank in the pair
     const uint32_t pp = kQuad ? (crank >> 1) : 0u;            // pair index in the cluster
@@ -1029,6 +1222,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
         if (a_tma) tma_prefetch_desc(&p.tmA);
         if (b_tma) tma_prefetch_desc(&p.tmB);
         if (b_tma && p.tail_split > 1) tma_prefetch_desc(&p.tmB2);
+        if (b_tma && gated) tma_prefetch_desc(&p.tmBu);
         if (p.c_tma) tma_prefetch_desc(&p.tmC);
     }
     if (warp == kMmaWarp) {
@@ -1062,9 +1256,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
             for (int i = 0; i < nu && ok; ++i) {
                 const Unit w = unit_at<kMulti>(p, cid, i);
                 const UnitGeom ug = unit_geom<kMulti>(p, w);
-                const int bcols = kPair ? w.bn / 2 : w.bn;   // this CTA's share of the unit's B columns
+                // Columns of one B box: this CTA's share of the unit's B columns.  A
+                // gated unit's stage holds BN/2 gate then BN/2 up columns, both at B'
+                // column n0: the single form loads both boxes, the pair form's rank 0
+                // the gate box and rank 1 the up box.
+                const int bcols = (kPair || gated) ? w.bn / 2 : w.bn;
                 const int64_t m0 = static_cast<int64_t>(w.m_blk) * kUnitRows + pp * kTileRows + rank * kBM;
-                const int64_t n0 = static_cast<int64_t>(w.n_blk) * p.BN + w.n_off + rank * bcols;
+                const int64_t n0 = gated ? static_cast<int64_t>(w.n_blk) * (p.BN / 2)
+                                         : static_cast<int64_t>(w.n_blk) * p.BN + w.n_off + rank * bcols;
                 const int64_t arow = ug.a_row + m0;   // A' row of the slot boxes (rows of a group are concatenated)
                 // Bytes one stage of this unit brings in: MN-major B comes in
                 // 64-column boxes (or one 3-D box of the full stage width),
@@ -1072,9 +1271,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                 // narrower than the tile reads B through tmB2, whose box is the
                 // piece's width, so it brings only its own columns.
                 const bool narrow = w.bn < p.BN;
-                const CUtensorMap* tmb = narrow ? &p.tmB2 : &p.tmB;
+                const CUtensorMap* tmb = (narrow && !(b_mn && !b_3d)) ? &p.tmB2 : &p.tmB;
+                if (kPair && gated && rank == 1) tmb = &p.tmBu;
                 const uint32_t b_bytes =
-                    ((b_mn && !b_3d) || narrow) ? static_cast<uint32_t>(bcols) * 128u : p.stage_b_bytes;
+                    (!gated && ((b_mn && !b_3d) || narrow)) ? static_cast<uint32_t>(bcols) * 128u : p.stage_b_bytes;
                 const uint32_t tx = kPair ? 2u * (kStageABytes + b_bytes)
                                           : (a_tma ? kStageABytes : 0u) + (b_tma ? b_bytes : 0u);
                 for (int kb = w.kb0; kb < w.kb1; kb += kSlots) {
@@ -1116,13 +1316,21 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                         } else {
                             if (a_tma) load_a_slot<false>(p, sa, k0, arow, ug.az, a_mn, a_3d, a_bd, fb);
                             if (b_tma) load_b_slot<false>(p, tmb, sb, k0, n0, ug.bz, bcols, b_mn, b_3d, b_bd, fb);
+                            if (b_tma && gated)
+                                load_b_slot<false>(p, &p.tmBu, sb + bcols * 128, k0, n0, ug.bz, bcols, b_mn, b_3d, b_bd,
+                                                   fb);
                         }
                     }
                     if (!kPair && any_masked) {
                         if (!a_tma)
                             gather_tile(ug.A, p.a_sm, p.a_sk, ug.row_lim, p.K, ug.a_row + m0, k0, kBM, a_mn, sa, t);
-                        if (!b_tma)
-                            gather_tile(ug.B, p.b_sn, p.b_sk, p.N, p.K, n0, k0, w.bn, b_mn, sb, t);
+                        if (!b_tma) {
+                            // (one inlined gather body for both halves of a gated stage)
+#pragma unroll 1
+                            for (int hb = 0; hb < (gated ? 2 : 1); ++hb)
+                                gather_tile(hb ? ug.Bu : ug.B, p.b_sn, p.b_sk, p.N, p.K, n0, k0, bcols, b_mn,
+                                            sb + hb * bcols * 128, t);
+                        }
                     }
                     }
                     if (!kPair && any_masked) {
@@ -1241,7 +1449,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
         for (int ui = 0; ui < nu; ++ui) {
             const Unit w = unit_at<kMulti>(p, cid, ui);
             const int64_t m0 = static_cast<int64_t>(w.m_blk) * kUnitRows + pp * kTileRows + rank * kBM;
-            const int64_t n0 = static_cast<int64_t>(w.n_blk) * p.BN + w.n_off;
+            // first output column (a gated tile has BN/2 of them)
+            const int64_t n0 = gated ? static_cast<int64_t>(w.n_blk) * (p.BN / 2)
+                                     : static_cast<int64_t>(w.n_blk) * p.BN + w.n_off;
             const int npieces = w.bn / 16;          // 16 accumulator columns per piece
             // One thread waits for the accumulator and tells the other epilogue
             // threads, so that they all leave together on an abort (the named
@@ -1262,7 +1472,22 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
             // group must not spill into the next group's rows
             const int64_t crow = ug.a_row + m0 + 32 * q;
             const bool ctma = p.c_tma && (!kMulti || p.gmode != 2 || crow + 32 <= ug.row_lim);
-            if (w.slot < 0) {
+            // fused stage: this problem's bias vectors, and the row's own bias
+            // value when the bias runs along the kernel view's rows
+            const __half* bias = nullptr;
+            const __half* bias_up = nullptr;
+            float brow = 0.f;
+            if (kEpi) {
+                const int64_t bo = p.gmode != 0 ? static_cast<int64_t>(w.g) * p.bias_bs : 0;
+                if (p.bias) bias = p.bias + bo;
+                if (p.bias_up) bias_up = p.bias_up + bo;
+                const int64_t mr = ug.a_row + m0 + row;
+                if (bias && p.bias_rows && mr < ug.row_lim) brow = __half2float(bias[mr]);
+            }
+            if (kEpi && w.slot < 0) {
+                fused_tile_epilogue<kPair, kMulti>(p, L, ug, bias, bias_up, brow, taddr, tempty, m0, n0,
+                                                   gated ? w.bn / 2 : w.bn, gated, crow, ctma, group_count);
+            } else if (w.slot < 0) {
                 uint32_t buf = 0;
                 for (int pc = 0; pc < npieces; pc += 4) {
                     // up to four pieces (64 columns) in flight per TMEM wait
@@ -1321,7 +1546,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                     }
                 }
             } else {
-                cut_tile_epilogue<kPair, kMulti>(p, L, w, ug, taddr, tempty, m0, n0, flag, abort, fix_ph, ui == nu - 1);
+                cut_tile_epilogue<kPair, kMulti, kEpi>(p, L, w, ug, taddr, tempty, m0, n0, flag, abort, fix_ph, ui == nu - 1,
+                                                      bias, brow);
             }
             if (++acc == 2) {
                 acc = 0;

@@ -165,6 +165,74 @@ gemm_f16_status gemm_f16_grouped(const void* A, int64_t stride_am, int64_t strid
                                  void* C, int64_t ldc, const int64_t* group_rows, int64_t groups,
                                  int64_t N, int64_t K, cudaStream_t stream);
 
+/*
+ * Fused output stage.  The pages name bias and activation fused into the
+ * GEMM's output stage (TileLang tutorial ch. 14 "GEMM operators", section 6.3,
+ * item 4, the epilogue of the comparison checklist; AI-infra knowledge base
+ * "Matrix multiplication and memory-access optimisation", section 05) and, for
+ * MoE layers, a gate/up GEMM fusing the two projections, with the activation
+ * and the multiply ("C500 TileLang GEMM review", section 17.3).  They fix no
+ * arithmetic; the library's reading:
+ *
+ *   B_up == NULL:  C[m,n] = fp16( act( sum_k A[m,k] B[k,n] + bias[n] ) )
+ *   B_up != NULL:  C[m,n] = fp16( act( sum_k A[m,k] B[k,n] + bias[n] )
+ *                                 * ( sum_k A[m,k] B_up[k,n] + bias_up[n] ) )
+ *
+ * B is the gate projection.  B_up is read with B's strides (and B's batch or
+ * group stride): the two projections share a layout.  bias and bias_up are
+ * fp16 vectors of N elements (unit stride) or NULL for zero; bias_up needs
+ * B_up.  The sums accumulate in fp32; bias, activation and product are
+ * evaluated in fp32 on them and rounded once to fp16.
+ *
+ * act: GEMM_F16_ACT_NONE (identity), _RELU (x < 0 ? 0 : x), _SILU
+ * (x / (1 + e^-x)), _GELU (exact: x * Phi(x), Phi(x) = erfc(-x / sqrt 2) / 2).
+ *
+ * Execution: the gate/up form computes both products in one MMA stream per
+ * tile (each stage holds the A rows once and both projections' columns; the
+ * accumulator holds the gate columns, then the up columns of the same output
+ * columns), so A is read once for both and neither product is written to
+ * memory.  Its tiles are never cut along K and never swapped (small M runs
+ * unswapped).  The bias/activation form runs every plan gemm_f16() runs,
+ * including the swapped form (the bias then runs along the kernel view's
+ * rows) and split-K / stream-K, where the stage is applied after the last
+ * partial is added.
+ *
+ * Errors: those of gemm_f16(), plus GEMM_F16_ERR_INVALID_VALUE for an unknown
+ * act, bias_up without B_up, an odd B_up / bias address or a negative
+ * stride_bias, and GEMM_F16_ERR_ALIAS when C overlaps B_up, bias or bias_up.
+ * Ownership and asynchrony are those of gemm_f16().
+ */
+enum {
+    GEMM_F16_ACT_NONE = 0,
+    GEMM_F16_ACT_RELU = 1,
+    GEMM_F16_ACT_SILU = 2,
+    GEMM_F16_ACT_GELU = 3
+};
+
+gemm_f16_status gemm_f16_fused(const void* A, int64_t stride_am, int64_t stride_ak,
+                               const void* B, int64_t stride_bk, int64_t stride_bn,
+                               const void* B_up, const void* bias, const void* bias_up, int act,
+                               void* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                               cudaStream_t stream);
+
+/* gemm_f16_batched() with the fused output stage; problem b uses the bias
+ * vectors at bias + b*stride_bias and bias_up + b*stride_bias (0 shares one). */
+gemm_f16_status gemm_f16_batched_fused(const void* A, int64_t stride_ab, int64_t stride_am, int64_t stride_ak,
+                                       const void* B, int64_t stride_bb, int64_t stride_bk, int64_t stride_bn,
+                                       const void* B_up, const void* bias, const void* bias_up,
+                                       int64_t stride_bias, int act, void* C, int64_t stride_cb, int64_t ldc,
+                                       int64_t M, int64_t N, int64_t K, int64_t batch, cudaStream_t stream);
+
+/* gemm_f16_grouped() with the fused output stage (the MoE expert layer: group g
+ * multiplies its rows by B + g*stride_bg and B_up + g*stride_bg, with the bias
+ * vectors at bias + g*stride_bias and bias_up + g*stride_bias). */
+gemm_f16_status gemm_f16_grouped_fused(const void* A, int64_t stride_am, int64_t stride_ak,
+                                       const void* B, int64_t stride_bg, int64_t stride_bk, int64_t stride_bn,
+                                       const void* B_up, const void* bias, const void* bias_up,
+                                       int64_t stride_bias, int act, void* C, int64_t ldc,
+                                       const int64_t* group_rows, int64_t groups, int64_t N, int64_t K,
+                                       cudaStream_t stream);
+
 /* Size of the fixed scratch array behind gemm_f16_noalloc(). */
 #define GEMM_F16_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 
@@ -225,6 +293,8 @@ typedef struct {
     size_t workspace_bytes;
     int a_box3d, b_box3d;   /* MN-major TMA operand read as one 3-D box per stage */
     int cluster_ctas;       /* CTAs per cluster: 1, 2 (pair form) or 4 (two pairs sharing B by multicast) */
+    int fused;              /* the fused output stage runs (gemm_f16_fused_get_plan) */
+    int gated;              /* gate/up form: tile_n output columns, 2 * tile_n accumulator columns */
 } gemm_f16_plan;
 
 /* Fill *plan for the given arguments without launching anything.  Returns the
@@ -233,6 +303,13 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
                                   const void* B, int64_t stride_bk, int64_t stride_bn,
                                   void* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
                                   gemm_f16_plan* plan);
+
+/* The plan gemm_f16_fused() would run for these arguments (same validation). */
+gemm_f16_status gemm_f16_fused_get_plan(const void* A, int64_t stride_am, int64_t stride_ak,
+                                        const void* B, int64_t stride_bk, int64_t stride_bn,
+                                        const void* B_up, const void* bias, const void* bias_up, int act,
+                                        void* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                        gemm_f16_plan* plan);
 
 /*
  * Process-wide tuning and test knobs (not thread-safe with concurrent calls):

@@ -244,6 +244,22 @@ def _bias_row(bias, N):
     return b
 
 
+def epilogue(S, act: str = "none", bias=0.0, S_up=None, bias_up=0.0):
+    """The fused output stage on double sums: fp16 act(S + bias), or with the
+    up sums ``S_up`` fp16 act(S + bias) * (S_up + bias_up); bias values in
+    double, broadcast against S.  Returns (C, g, u): the fp16 result, the
+    pre-activation gate g = S + bias and u = S_up + bias_up (None without)."""
+    if act not in ACTIVATIONS:
+        raise ValueError(f"unknown activation {act!r}")
+    g = np.asarray(S, dtype=np.float64) + bias
+    out = activation(g, act)
+    u = None
+    if S_up is not None:
+        u = np.asarray(S_up, dtype=np.float64) + bias_up
+        out = out * u
+    return double_to_half(out), g, u
+
+
 def gemm_fused(A: np.ndarray, B: np.ndarray, B_up: np.ndarray | None = None, bias=None, bias_up=None,
                act: str = "none", threads: int = 1, parts: bool = False):
     """fp16 act(A @ B + bias), or with ``B_up`` the gate/up form
@@ -257,15 +273,13 @@ def gemm_fused(A: np.ndarray, B: np.ndarray, B_up: np.ndarray | None = None, bia
     if bias_up is not None and B_up is None:
         raise ValueError("bias_up needs B_up")
     N = B.shape[1]
-    g = gemm_exact(A, B, threads) + _bias_row(bias, N)[None, :]
-    out = activation(g, act)
-    u = None
+    S_up = None
     if B_up is not None:
         if B_up.shape != B.shape:
             raise ValueError("B_up must have B's shape")
-        u = gemm_exact(A, B_up, threads) + _bias_row(bias_up, N)[None, :]
-        out = out * u
-    C = double_to_half(out)
+        S_up = gemm_exact(A, B_up, threads)
+    C, g, u = epilogue(gemm_exact(A, B, threads), act, _bias_row(bias, N)[None, :], S_up,
+                       _bias_row(bias_up, N)[None, :])
     return (C, g, u) if parts else C
 
 

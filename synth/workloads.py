@@ -144,11 +144,15 @@ class MultiWorkload:
     B: Operand
     description: str = ""
     group_rows: tuple = ()
+    # fused output stage: a second (up) projection stacked like B, and the activation
+    B_up: Operand | None = None
+    act: str = "none"
 
     @property
     def flops(self) -> float:
         problems = self.count if self.kind == "batched" else 1
-        return 2.0 * problems * self.M * self.N * self.K
+        products = 2 if self.B_up is not None else 1
+        return 2.0 * problems * products * self.M * self.N * self.K
 
     @property
     def c_rows(self) -> int:
@@ -161,6 +165,12 @@ class MultiWorkload:
         return Workload(self.name + "[0]", m0, self.N, self.K, _op(m0, self.K, self.A.kind, self.A.seed),
                         _op(self.K, self.N, self.B.kind, self.B.seed), "first problem")
 
+    def first_up(self):
+        """Problem 0's up projection (K x N operand), or None."""
+        if self.B_up is None:
+            return None
+        return _op(self.K, self.N, self.B_up.kind, self.B_up.seed)
+
 
 BATCHED_32x1024 = MultiWorkload(
     "batched_32x1024x1024x1024", "batched", 1024, 1024, 1024, 32,
@@ -172,5 +182,12 @@ GROUPED_MOE = MultiWorkload(
     "grouped MoE layer: 131072 routed rows over 8 experts (seeded shares), each expert's [7168,2048] B",
     group_rows_for(131072, 8, 16))
 
-MULTI = [BATCHED_32x1024, GROUPED_MOE]
+GROUPED_GATEUP_SILU = MultiWorkload(
+    "grouped_gateup_silu_g8_131072x2048x7168", "grouped", 131072, 2048, 7168, 8,
+    _op(131072, 7168, "uniform", 14), _op(8 * 7168, 2048, "uniform", 15),
+    "MoE gate/up layer: the routed rows of the grouped MoE workload through 8 experts' gate and up "
+    "projections [7168,2048] each, out = silu(A Bg) * (A Bu)",
+    group_rows_for(131072, 8, 16), B_up=_op(8 * 7168, 2048, "uniform", 17), act="silu")
+
+MULTI = [BATCHED_32x1024, GROUPED_MOE, GROUPED_GATEUP_SILU]
 BY_NAME.update({w.name: w for w in MULTI})

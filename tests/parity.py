@@ -76,3 +76,37 @@ def block_reference(w, m0, m1, n0, n1):
     A_rows = np.ascontiguousarray(w.A.values_at(np.arange(m0, m1)[:, None], k[None, :]))
     B_cols = np.ascontiguousarray(w.B.values_at(k[None, :], np.arange(n0, n1)[:, None]))
     return oracle.gemm(A_rows, B_cols.T, threads=oracle_threads())
+
+
+# Largest slope of each activation: |act'(x)| <= L (ReLU 1; SiLU peaks at
+# about 1.0998 near x = 2.4; GELU at about 1.1289 near x = 1.41).
+ACT_SLOPE = {"none": 1.0, "relu": 1.0, "silu": 1.1, "gelu": 1.13}
+
+
+def assert_close_fused(got, ref, K, g, u=None, act="none", what=""):
+    """Fused output stage: the plain tolerance's absolute term e = 1e-4*sqrt(K)
+    bounds the error of each fp32 sum; carried through act (slope <= L) and,
+    gated, the product act(g) * u, it becomes e*(L*|u| + |act(g)|) + L*e^2.
+    Plus 2 fp16 ulps of the result, and a relative Frobenius error <= 1e-3."""
+    gv = np.asarray(got).astype(np.float64)
+    r = np.asarray(ref).astype(np.float64)
+    assert gv.shape == r.shape, what
+    assert np.all(np.isfinite(gv) == np.isfinite(r)), f"{what}: non-finite mismatch"
+    e = 1e-4 * np.sqrt(K)
+    L = ACT_SLOPE[act]
+    if u is None:
+        absb = L * e + np.zeros_like(r)
+    else:
+        absb = e * (L * np.abs(u) + np.abs(oracle.activation(g, act))) + L * e * e
+    fin = np.isfinite(r)
+    err = np.abs(gv[fin] - r[fin])
+    tol = 2 * ulp16(r[fin]) + absb[fin]
+    bad = err > tol
+    if bad.any():
+        i = np.argmax(err - tol)
+        raise AssertionError(f"{what}: {bad.sum()} elements out of tolerance; worst err {err[i]:.3e} "
+                             f"tol {tol[i]:.3e} ref {r[fin][i]:.6g} got {gv[fin][i]:.6g}")
+    nr = np.linalg.norm(r[fin])
+    if nr > 0:
+        rel = np.linalg.norm(gv[fin] - r[fin]) / nr
+        assert rel <= 1e-3, f"{what}: relative Frobenius error {rel:.3e}"

@@ -11,7 +11,7 @@ import torch
 import dense_tiled_gemm_fp16_gb300 as g
 import oracle
 from synth import workloads
-from tests.parity import assert_bits, assert_close, oracle_threads
+from tests.parity import assert_bits, assert_close, assert_close_fused, oracle_threads
 
 pytestmark = pytest.mark.gpu
 
@@ -190,10 +190,18 @@ def test_grouped_all_empty_does_nothing():
 
 
 # ------------------------------------------------------- full-size workloads
-def _launch_as_bench(w, A, B, C):
+def _launch_as_bench(w, A, B, C, U=None):
     """The call bench.py times for a multi-problem workload."""
     M, N, K, n = w.M, w.N, w.K, w.count
-    if w.kind == "batched":
+    if U is not None or w.act != "none":
+        up, act = (U.data_ptr() if U is not None else 0), g.ACTIVATIONS[w.act]
+        if w.kind == "batched":
+            g.gemm_f16_batched_fused(A.data_ptr(), M * K, K, 1, B.data_ptr(), K * N, N, 1, up, 0, 0, 0, act,
+                                     C.data_ptr(), M * N, N, M, N, K, n)
+        else:
+            g.gemm_f16_grouped_fused(A.data_ptr(), K, 1, B.data_ptr(), K * N, N, 1, up, 0, 0, 0, act, C.data_ptr(),
+                                     N, list(w.group_rows), N, K)
+    elif w.kind == "batched":
         g.gemm_f16_batched(A.data_ptr(), M * K, K, 1, B.data_ptr(), K * N, N, 1, C.data_ptr(), M * N, N,
                            M, N, K, n)
     else:
@@ -215,10 +223,11 @@ def test_full_size_workload_sampled(w):
     plus the first and last row of every problem, against the oracle's dot
     products over the regenerated rows of A and columns of B."""
     A, B = w.A.device_view(DEV), w.B.device_view(DEV)
+    U = w.B_up.device_view(DEV) if w.B_up is not None else None
     C = torch.full((w.c_rows, w.N), float("nan"), dtype=torch.float16, device=DEV)
-    _launch_as_bench(w, A, B, C)
+    _launch_as_bench(w, A, B, C, U)
     torch.cuda.synchronize()
-    del A, B
+    del A, B, U
     assert not torch.isnan(C).any(), "an output element was not written"
     K = w.K
     if w.kind == "batched":
@@ -237,7 +246,16 @@ def test_full_size_workload_sampled(w):
     A_rows = w.A.values_at(rows[:, None], k[None, :])                    # [S, K]
     B_cols = w.B.values_at(prob[:, None] * K + k[None, :], cols[:, None])  # [S, K]
     idx = np.arange(rows.size, dtype=np.int64) * K
-    ref, _ = oracle.dots(A_rows.reshape(-1), idx, 1, B_cols.reshape(-1), idx, 1, K, threads=oracle_threads())
+    ref, S = oracle.dots(A_rows.reshape(-1), idx, 1, B_cols.reshape(-1), idx, 1, K, threads=oracle_threads())
     got = C[torch.from_numpy(rows).to(DEV), torch.from_numpy(cols).to(DEV)].cpu().numpy()
-    assert_close(got, ref, K, f"{w.name} samples")
+    if w.B_up is None and w.act == "none":
+        assert_close(got, ref, K, f"{w.name} samples")
+    else:
+        S_up = None
+        if w.B_up is not None:
+            U_cols = w.B_up.values_at(prob[:, None] * K + k[None, :], cols[:, None])
+            _, S_up = oracle.dots(A_rows.reshape(-1), idx, 1, U_cols.reshape(-1), idx, 1, K,
+                                  threads=oracle_threads())
+        ref, gp, u = oracle.epilogue(S, w.act, 0.0, S_up, 0.0)
+        assert_close_fused(got, ref, K, gp, u, w.act, f"{w.name} samples")
     assert g.gemm_f16_device_status() == 0
