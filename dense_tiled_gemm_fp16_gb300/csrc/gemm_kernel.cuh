@@ -514,18 +514,54 @@ __device__ __forceinline__ int clamp64(int64_t remaining)
     return remaining >= 64 ? 64 : (remaining <= 0 ? 0 : static_cast<int>(remaining));
 }
 
+// Shift a row's 36 loaded words left by `sh` bytes (even, 0..14) and store its
+// 8 chunks: word o of the row is bytes [4o + sh, 4o + sh + 4) of the words,
+// i.e. a funnel shift of words o + sh/4 and o + sh/4 + 1 by 8*(sh%4) bits.
+// The word offset sh/4 is applied as two levels of selects (by 1 word, then
+// by 2), so lanes whose rows have different offsets take the same
+// instructions (no divergent branch per chunk).
+__device__ __forceinline__ void shift_store_row(const uint4* wv, uint32_t sh, int nv, uint32_t rowaddr, int rk)
+{
+    uint32_t w[36];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+        w[4 * i] = wv[i].x;
+        w[4 * i + 1] = wv[i].y;
+        w[4 * i + 2] = wv[i].z;
+        w[4 * i + 3] = wv[i].w;
+    }
+    const bool d1 = (sh & 4u) != 0, d2 = (sh & 8u) != 0;
+    const uint32_t s = (sh & 3u) * 8u;
+#pragma unroll
+    for (int k = 0; k < 35; ++k) w[k] = d1 ? w[k + 1] : w[k];
+#pragma unroll
+    for (int k = 0; k < 33; ++k) w[k] = d2 ? w[k + 2] : w[k];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint4 c = make_uint4(__funnelshift_r(w[4 * j], w[4 * j + 1], s), __funnelshift_r(w[4 * j + 1], w[4 * j + 2], s),
+                             __funnelshift_r(w[4 * j + 2], w[4 * j + 3], s),
+                             __funnelshift_r(w[4 * j + 3], w[4 * j + 4], s));
+        const int cv = clamp8(nv - 8 * j);
+        if (cv < 8) c = keep_first(c, cv);   // (cv <= 0 zeroes the chunk)
+        st_smem_v4(rowaddr + ((j ^ (rk & 7)) << 4), c);
+    }
+}
+
+// Rows each producer thread has in flight (9 loads each) in the unit-stride gather.
+constexpr int kGatherRows = 2;
+
 __device__ __forceinline__ void gather_rows_unit(const __half* base, int64_t s_mn, int64_t s_k, int64_t MN,
                                                  int64_t K, int64_t mn0, int64_t k0, int rows_tile, bool mn_major,
                                                  uint32_t dst, int t)
 {
     const int nrows = rows_tile;   // K-major: MN rows; MN-major: (rows_tile / 64) atoms x 64 K rows
     const uintptr_t b = reinterpret_cast<uintptr_t>(base);
-    for (int r0 = t; r0 < nrows; r0 += 2 * kProducerThreads) {
-        uint4 wv[2][9];
-        uint32_t sh[2], rowaddr[2];
-        int nv[2], rk[2];
+    for (int r0 = t; r0 < nrows; r0 += kGatherRows * kProducerThreads) {
+        uint4 wv[kGatherRows][9];
+        uint32_t sh[kGatherRows], rowaddr[kGatherRows];
+        int nv[kGatherRows], rk[kGatherRows];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
+        for (int q = 0; q < kGatherRows; ++q) {
             const int rr = r0 + q * kProducerThreads;
             nv[q] = 0;
             sh[q] = 0;
@@ -547,31 +583,21 @@ __device__ __forceinline__ void gather_rows_unit(const __half* base, int64_t s_m
                     rk[q] = r;
                     rowaddr[q] = dst + a * 8192 + r * 128;
                 }
-                if (nv[q] > 0) {
-                    const uintptr_t addr = b + 2 * static_cast<uintptr_t>(off);
-                    sh[q] = static_cast<uint32_t>(addr & 15u);
-                    const uintptr_t a0 = addr - sh[q];
-                    const int nw = static_cast<int>((sh[q] + 2u * static_cast<uint32_t>(nv[q]) + 15u) / 16u);
+                const uintptr_t addr = b + 2 * static_cast<uintptr_t>(off);
+                sh[q] = static_cast<uint32_t>(addr & 15u);
+                const uintptr_t a0 = addr - sh[q];
+                // words holding valid elements (none when the row is outside the view)
+                const int nw = nv[q] > 0 ? static_cast<int>((sh[q] + 2u * static_cast<uint32_t>(nv[q]) + 15u) / 16u) : 0;
 #pragma unroll
-                    for (int i = 0; i < 9; ++i)
-                        wv[q][i] = (i < nw) ? ld_nc_v4(reinterpret_cast<const void*>(a0 + 16u * i))
-                                            : make_uint4(0u, 0u, 0u, 0u);
-                }
+                for (int i = 0; i < 9; ++i)
+                    wv[q][i] = (i < nw) ? ld_nc_v4(reinterpret_cast<const void*>(a0 + 16u * i))
+                                        : make_uint4(0u, 0u, 0u, 0u);
             }
         }
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
+        for (int q = 0; q < kGatherRows; ++q) {
             if (r0 + q * kProducerThreads >= nrows) break;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                uint4 c = make_uint4(0u, 0u, 0u, 0u);
-                const int cv = clamp8(nv[q] - 8 * j);
-                if (cv > 0) {
-                    c = (sh[q] != 0) ? funnel16(wv[q][j], wv[q][j + 1], sh[q]) : wv[q][j];
-                    if (cv < 8) c = keep_first(c, cv);
-                }
-                st_smem_v4(rowaddr[q] + ((j ^ (rk[q] & 7)) << 4), c);
-            }
+            shift_store_row(wv[q], sh[q], nv[q], rowaddr[q], rk[q]);
         }
     }
 }
