@@ -575,12 +575,13 @@ def report(args, w, plan, peaks, bnd, flops, nbytes, ms_per_step, value, wall, c
                    "options": args.opt,
                    "plan": {k: plan[k] for k in ("swap_ab", "pair", "a_tma", "b_tma", "c_tma", "tile_n",
                                                  "splits", "streamk_tiles", "tail_split", "grid",
-                                                 "stages")}},
+                                                 "stages", "repack")}},
         "hbm_gbs_min_traffic": round(nbytes / (ms_per_step * 1e-3) / 1e9, 1),
         "wall_s_timed_region": round(wall, 4),
         "clocks": clk,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        # the GEMM kernel, plus one aligned-copy kernel per repacked operand
+        "gpu_launches": args.steps * (1 + bin(plan["repack"]).count("1")),
         "roofline": roof,
         "cpu_baseline": cpu,
         "device_status": status,

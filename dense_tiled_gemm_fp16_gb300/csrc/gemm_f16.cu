@@ -13,6 +13,7 @@
 
 #include "gemm_f16.h"
 #include "gemm_kernel.cuh"
+#include "repack.cuh"
 static_assert(GEMM_F16_MAX_GROUPS == gemm_f16_dev::kMaxGroups, "the header and the kernel agree on the group limit");
 
 using gemm_f16_dev::KernelParams;
@@ -49,10 +50,12 @@ struct Workspace {
     size_t partial_bytes = 0;
     int* counters = nullptr;
     size_t counter_bytes = 0;
+    void* repack = nullptr;   // aligned copies of operands TMA cannot address
+    size_t repack_bytes = 0;
 };
 Workspace g_ws[kMaxDevices];
 
-std::atomic<int64_t> g_opt[13];
+std::atomic<int64_t> g_opt[14];
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 PFN_cuMemGetAddressRange_v3020 g_addr_range = nullptr;
@@ -171,6 +174,10 @@ struct Args {
     const void* bias_up = nullptr;
     int64_t sbias = 0;
     int act = 0;
+    // The plan may copy an operand TMA cannot address into an aligned buffer
+    // of the library workspace (the entry points that own no caller workspace
+    // and may allocate).
+    bool repack = false;
 };
 
 // Elements spanned by `n` copies of a view of `e` elements placed `stride`
@@ -304,6 +311,8 @@ bool encode_3d_mn(CUtensorMap* tm, const void* ptr, uint64_t MN, uint64_t K, uin
 struct Plan {
     gemm_f16_plan pub;
     bool fused;   // launch the kernels with the fused output stage
+    int ncopies;  // repack copies to run before the GEMM (A', B', up projection)
+    gemm_f16_dev::RepackArgs copies[3];
     KernelParams kp;
     size_t counter_bytes;   // split-K counters: align256(4 * tiles)
     size_t partial_bytes;   // split-K partials: align256(4 * units * tile_m * tile_n)
@@ -503,7 +512,16 @@ size_t workspace_bytes_for(int64_t slots, int BN, int64_t tiles, int ranks, size
     return cb + pb;
 }
 
-gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
+// Device buffer of `bytes` for repacked operands: the library workspace's, or
+// (plan_only) a stand-in aligned address that is never dereferenced.
+void* repack_buffer(size_t bytes, bool plan_only, cudaStream_t stream);
+
+// Products below this many FLOPs gather unaligned operands in the kernel: the
+// copy's extra launch and traffic would not pay for itself.
+constexpr double kRepackMinFlops = 1e9;
+
+gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan_only = false,
+                          cudaStream_t stream = nullptr)
 {
     std::memset(pl, 0, sizeof(*pl));
     KernelParams& kp = pl->kp;
@@ -570,6 +588,77 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
         const OperandChoice cu = choose_operand(kp.Bu, kp.b_sn, kp.b_sk, Nv, a.K, out_cols,
                                                 have_tma && !(fg & 2) && (!b_bd || bs_ok(b_bs)));
         if (cu.tma != cb.tma || cu.mn != cb.mn) cb = choose_operand(kp.B, kp.b_sn, kp.b_sk, Nv, a.K, out_cols, false);
+    }
+
+    // Padding form of the boundary handling (AI-infra page, section 05): an
+    // operand TMA cannot address (unaligned base or pitch, no unit stride) is
+    // copied once into an aligned buffer whose rows run along its smaller
+    // stride, when the product is large enough; the gather stays for small
+    // products, forced gathers and the entry points that may not allocate.
+    pl->ncopies = 0;
+    int repacked = 0;
+    {
+        const int64_t rp = opt(GEMM_F16_OPT_REPACK);
+        const double work = 2.0 * static_cast<double>(Mv) * static_cast<double>(Nv) * static_cast<double>(a.K) *
+                            static_cast<double>(batched ? a.batch : 1);
+        const bool want_a = !ca.tma && !(fg & 1), want_b = !cb.tma && !(fg & 2);
+        if (a.repack && have_tma && rp != 1 && (rp == 2 || work >= kRepackMinFlops) && (want_a || want_b)) {
+            struct Layout {
+                bool mn;   // rows of the copy run along MN (MN-major result)
+                int64_t rows, cols, s_r, s_c, pitch, nb, s_b;
+            };
+            auto layout = [&](int64_t s_mn, int64_t s_k, int64_t MN, int64_t bs, bool bd) {
+                Layout l;
+                l.mn = s_mn == 1 || (s_k != 1 && s_mn <= s_k);
+                l.rows = l.mn ? a.K : MN;
+                l.cols = l.mn ? MN : a.K;
+                l.s_r = l.mn ? s_k : s_mn;
+                l.s_c = l.mn ? s_mn : s_k;
+                l.pitch = round_up(l.cols, 8);
+                l.nb = bd ? a.batch : 1;
+                l.s_b = bd ? bs : 0;
+                return l;
+            };
+            const Layout la = layout(kp.a_sm, kp.a_sk, Mv, a_bs, a_bd);
+            const Layout lb = layout(kp.b_sn, kp.b_sk, Nv, b_bs, b_bd);
+            const int tile_b = gated ? out_cols : BN;
+            // the copy must be TMA-addressable (an MN-major copy needs 64-wide tiles)
+            const bool do_a = want_a && (!la.mn || gemm_f16_dev::kBM % 64 == 0);
+            const bool do_b = want_b && (!lb.mn || tile_b % 64 == 0);
+            auto bytes_of = [](const Layout& l) {
+                return static_cast<size_t>(round_up(2 * l.nb * l.rows * l.pitch, 256));
+            };
+            const size_t need = (do_a ? bytes_of(la) : 0) + (do_b ? (gated ? 2 : 1) * bytes_of(lb) : 0);
+            char* buf = need ? static_cast<char*>(repack_buffer(need, plan_only, stream)) : nullptr;
+            if (need && !buf) return GEMM_F16_ERR_OUT_OF_MEMORY;
+            auto add_copy = [&](const Layout& l, const __half* src) {
+                gemm_f16_dev::RepackArgs& c = pl->copies[pl->ncopies++];
+                c.src = src, c.s_r = l.s_r, c.s_c = l.s_c, c.s_b = l.s_b;
+                c.dst = reinterpret_cast<__half*>(buf);
+                c.pitch = l.pitch, c.dst_bs = l.rows * l.pitch;
+                c.rows = l.rows, c.cols = l.cols, c.batch = l.nb;
+                buf += bytes_of(l);
+                return c.dst;
+            };
+            if (do_a) {
+                kp.A = add_copy(la, kp.A);
+                kp.a_sm = la.mn ? 1 : la.pitch;
+                kp.a_sk = la.mn ? la.pitch : 1;
+                if (a_bd) a_bs = la.rows * la.pitch;
+                ca = choose_operand(kp.A, kp.a_sm, kp.a_sk, Mv, a.K, gemm_f16_dev::kBM,
+                                    have_tma && (!a_bd || bs_ok(a_bs)));
+                repacked |= 1;
+            }
+            if (do_b) {
+                kp.B = add_copy(lb, kp.B);
+                if (gated) kp.Bu = add_copy(lb, kp.Bu);
+                kp.b_sn = lb.mn ? 1 : lb.pitch;
+                kp.b_sk = lb.mn ? lb.pitch : 1;
+                if (b_bd) b_bs = lb.rows * lb.pitch;
+                cb = choose_operand(kp.B, kp.b_sn, kp.b_sk, Nv, a.K, tile_b, have_tma && (!b_bd || bs_ok(b_bs)));
+                repacked |= 2;
+            }
+        }
     }
 
     // Pair form (two CTAs per 256 x BN tile): TMA operands, no split-K, and a
@@ -765,6 +854,7 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl)
     pub.tile_m = tile_rows, pub.tile_n = out_cols, pub.tiles_m = tiles_m, pub.tiles_n = tiles_n;
     pub.fused = a.fused ? 1 : 0;
     pub.gated = gated ? 1 : 0;
+    pub.repack = repacked;
     pub.splits = splits, pub.kblocks = kblocks, pub.grid = grid;
     pub.units = static_cast<int>(quad ? unit_tiles : tiles * splits);
     pub.streamk_tiles = sch.sk_iters > 0 ? static_cast<int>(tiles - sch.sk_tile0) : 0;
@@ -784,6 +874,12 @@ gemm_f16_status launch(Plan& pl, DevInfo& dev, float* partials, int* counters, c
     kp.counters = counters;
     if (pl.pub.grid == 0) return GEMM_F16_OK;   // no tile (every group empty)
     if (!set_smem_attributes(dev)) return GEMM_F16_ERR_LAUNCH;
+    for (int i = 0; i < pl.ncopies; ++i) {
+        const gemm_f16_dev::RepackArgs& c = pl.copies[i];
+        const int64_t warps = c.rows * c.batch;
+        const int64_t blocks = std::min<int64_t>((warps + 7) / 8, static_cast<int64_t>(dev.sms) * 8);
+        gemm_f16_dev::repack_rows<<<static_cast<unsigned>(blocks), gemm_f16_dev::kRepackThreads, 0, stream>>>(c);
+    }
     const bool multi = kp.gmode != 0;
     if (!pl.pub.pair) {
         if (pl.fused)
@@ -848,13 +944,29 @@ bool grow(void** buf, size_t* have, size_t need, bool zero, cudaStream_t stream)
     return true;
 }
 
-gemm_f16_status run(const Args& a, void* user_ws, size_t user_ws_bytes, bool use_library_ws, cudaStream_t stream)
+void* repack_buffer(size_t bytes, bool plan_only, cudaStream_t stream)
 {
+    if (plan_only) return reinterpret_cast<void*>(uintptr_t(1) << 21);
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(g_mutex);
+    Workspace& w = g_ws[d];
+    if (!grow(&w.repack, &w.repack_bytes, bytes, false, stream)) return nullptr;
+    return w.repack;
+}
+
+gemm_f16_status run(const Args& args, void* user_ws, size_t user_ws_bytes, bool use_library_ws, cudaStream_t stream)
+{
+    Args a = args;
+    a.repack = use_library_ws;
     DevInfo* dev = nullptr;
     gemm_f16_status st = validate(a, true, &dev);
     if (st != GEMM_F16_OK) return st;
     Plan pl;
-    st = make_plan(a, *dev, &pl);
+    st = make_plan(a, *dev, &pl, false, stream);
     if (st != GEMM_F16_OK) return st;
     float* partials = nullptr;
     int* counters = nullptr;
@@ -1070,11 +1182,12 @@ gemm_f16_status gemm_f16_fused_get_plan(const void* A, int64_t stride_am, int64_
     if (!plan) return GEMM_F16_ERR_INVALID_VALUE;
     Args a{A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, M, N, K};
     set_fused(a, B_up, bias, bias_up, 0, act);
+    a.repack = true;
     DevInfo* dev = nullptr;
     gemm_f16_status st = validate(a, true, &dev);
     if (st != GEMM_F16_OK) return st;
     Plan pl;
-    st = make_plan(a, *dev, &pl);
+    st = make_plan(a, *dev, &pl, true);
     if (st == GEMM_F16_OK) *plan = pl.pub;
     return st;
 }
@@ -1159,19 +1272,21 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
                                   int64_t K, gemm_f16_plan* plan)
 {
     if (!plan) return GEMM_F16_ERR_INVALID_VALUE;
-    const Args a{A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, M, N, K};
+    Args a{A, stride_am, stride_ak, B, stride_bk, stride_bn, C, ldc, M, N, K};
+    a.repack = true;   // as gemm_f16() would run it
     DevInfo* dev = nullptr;
     gemm_f16_status st = validate(a, true, &dev);
     if (st != GEMM_F16_OK) return st;
     Plan pl;
-    st = make_plan(a, *dev, &pl);
+    st = make_plan(a, *dev, &pl, true);
     if (st == GEMM_F16_OK) *plan = pl.pub;
     return st;
 }
 
 gemm_f16_status gemm_f16_set_option(int option, int64_t value)
 {
-    if (option < 1 || option > 12 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option < 1 || option > 13 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option == GEMM_F16_OPT_REPACK && value > 2) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_MULTICAST && value > 2) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_MAX_STAGES && value == 1) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_TAIL_SPLIT && value > 1) return GEMM_F16_ERR_INVALID_VALUE;

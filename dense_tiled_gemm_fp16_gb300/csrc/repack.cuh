@@ -1,0 +1,90 @@
+// Repack of an operand that TMA cannot address into a dense, 16-byte-aligned
+// copy, so that the GEMM can run its TMA path on the copy.
+//
+// The pages give two ways to meet a tile boundary that the data does not
+// respect: masks, or padding with the extra storage and traffic accounted for
+// (AI-infra knowledge base "Matrix multiplication and memory-access
+// optimisation", section 05; the mask side is the Triton GEMM page's
+// boundary handling).  The in-kernel gather is the mask form.  It re-reads and
+// re-aligns an operand once per tile that uses it, which costs more than one
+// aligned copy once the operand is reused across many tiles.  This kernel is
+// the padding form: it reads the view once, realigns every row, and writes rows
+// whose pitch is a multiple of 8 elements (16 bytes), zero-filling the padding.
+// It is HBM-bound: 2 bytes read and 2 written per element.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "gemm_kernel.cuh"
+
+namespace gemm_f16_dev {
+
+constexpr int kRepackThreads = 256;
+constexpr int kRepackUnroll = 4;   // 16-byte output chunks a lane has in flight
+
+struct RepackArgs {
+    const __half* src;   // element (b, r, c) at src + b*s_b + r*s_r + c*s_c
+    int64_t s_r, s_c, s_b;
+    __half* dst;         // element (b, r, c) at dst + b*dst_bs + r*pitch + c
+    int64_t pitch, dst_bs;
+    int64_t rows, cols, batch;
+};
+
+// 8 fp16 values of the 16 bytes at byte offset sh (even) of the 32-byte pair
+// w0:w1; the offset is the same for the whole row, so the branch is uniform
+// across the warp.
+__device__ __forceinline__ uint4 repack_shift(const uint4& w0, const uint4& w1, uint32_t sh)
+{
+    return sh == 0 ? w0 : funnel16(w0, w1, sh);
+}
+
+// One warp per row (grid-stride over batch * rows).  Unit column stride: the
+// lane loads the aligned 16-byte source words that hold its output chunk's
+// valid elements (never a word without one, so no load leaves the view's
+// pages), shifts them into place and stores the chunk.  Other strides: element
+// by element.
+__global__ void __launch_bounds__(kRepackThreads) repack_rows(const RepackArgs a)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (kRepackThreads / 32);
+    const int64_t total = a.rows * a.batch;
+    const int64_t chunks = a.pitch / 8;
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * (kRepackThreads / 32) + (threadIdx.x >> 5); q < total;
+         q += warps) {
+        const int64_t b = q / a.rows, r = q - b * a.rows;
+        const __half* srow = a.src + b * a.s_b + r * a.s_r;
+        uint4* drow = reinterpret_cast<uint4*>(a.dst + b * a.dst_bs + r * a.pitch);
+        if (a.s_c == 1) {
+            const uintptr_t addr = reinterpret_cast<uintptr_t>(srow);
+            const uint32_t sh = static_cast<uint32_t>(addr & 15u);
+            const uint4* w = reinterpret_cast<const uint4*>(addr - sh);
+            for (int64_t j0 = lane; j0 < chunks; j0 += 32 * kRepackUnroll) {
+                uint4 w0[kRepackUnroll], w1[kRepackUnroll];
+                int nv[kRepackUnroll];
+#pragma unroll
+                for (int u = 0; u < kRepackUnroll; ++u) {
+                    const int64_t j = j0 + 32 * u;
+                    const int64_t left = a.cols - 8 * j;
+                    nv[u] = j < chunks ? (left >= 8 ? 8 : (left <= 0 ? 0 : static_cast<int>(left))) : 0;
+                    w0[u] = w1[u] = make_uint4(0u, 0u, 0u, 0u);
+                    if (nv[u] > 0) w0[u] = ld_nc_v4(w + j);
+                    if (nv[u] > 0 && sh + 2u * static_cast<uint32_t>(nv[u]) > 16u) w1[u] = ld_nc_v4(w + j + 1);
+                }
+#pragma unroll
+                for (int u = 0; u < kRepackUnroll; ++u) {
+                    const int64_t j = j0 + 32 * u;
+                    if (j >= chunks) break;
+                    uint4 c = repack_shift(w0[u], w1[u], sh);
+                    if (nv[u] < 8) c = keep_first(c, nv[u]);
+                    drow[j] = c;
+                }
+            }
+        } else {
+            uint16_t* d = reinterpret_cast<uint16_t*>(drow);
+            const uint16_t* s = reinterpret_cast<const uint16_t*>(srow);
+            for (int64_t c = lane; c < a.pitch; c += 32) d[c] = c < a.cols ? ld_nc_u16(s + c * a.s_c) : uint16_t(0);
+        }
+    }
+}
+
+}  // namespace gemm_f16_dev

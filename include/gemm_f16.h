@@ -78,15 +78,20 @@ typedef enum {
  * Any positive strides are accepted (row-major, column-major / transposed
  * views, pitched slices, non-unit inner strides).  Alignment is not required:
  * operands whose base is 16-byte aligned with a unit inner stride and a
- * 16-byte-multiple pitch go through TMA; the others through a bounds-checked
- * gather path with identical results.
+ * 16-byte-multiple pitch go through TMA.  The others are either gathered by the
+ * kernel with bounds-checked loads (products under 1e9 FLOPs) or first copied
+ * once, by a separate HBM-bound kernel on `stream`, into an aligned buffer of
+ * the library workspace (rows along the operand's smaller stride, pitch a
+ * multiple of 8 elements) that the GEMM then reads through TMA: the padding
+ * form of boundary handling.  Results are identical either way.
  *
  * Ownership: the caller owns A, B and C; they must stay valid until the work
- * on `stream` completes.  For shapes that use split-K the library uses a
- * per-device workspace that it allocates on first need (cudaMalloc, which
- * synchronises the device), grows on demand and frees at process exit; split-K
- * calls that run concurrently on different streams must use gemm_f16_ws() with
- * separate workspaces.
+ * on `stream` completes.  For shapes that use split-K, and for the aligned
+ * operand copies, the library uses a per-device workspace that it allocates on
+ * first need (cudaMalloc, which synchronises the device), grows on demand and
+ * frees at process exit; such calls that run concurrently on different streams
+ * must use gemm_f16_ws() with separate workspaces (which never copies operands:
+ * it gathers them).
  *
  * Errors: argument errors are returned before any device work is queued;
  * launch errors after.  A device-side bounded-wait expiry does not show here:
@@ -295,6 +300,7 @@ typedef struct {
     int cluster_ctas;       /* CTAs per cluster: 1, 2 (pair form) or 4 (two pairs sharing B by multicast) */
     int fused;              /* the fused output stage runs (gemm_f16_fused_get_plan) */
     int gated;              /* gate/up form: tile_n output columns, 2 * tile_n accumulator columns */
+    int repack;             /* bit 0: A, bit 1: B (and B_up) copied to an aligned buffer before the GEMM */
 } gemm_f16_plan;
 
 /* Fill *plan for the given arguments without launching anything.  Returns the
@@ -334,6 +340,9 @@ gemm_f16_status gemm_f16_fused_get_plan(const void* A, int64_t stride_am, int64_
  *   GEMM_F16_OPT_MULTICAST     0 default / 1: pairs load their own B; 2: clusters of four
  *                              CTAs (two pairs on adjacent 256-row tiles) read each B tile
  *                              once and multicast it (whole 256x256 tiles only)
+ *   GEMM_F16_OPT_REPACK        0 default: operands TMA cannot address are copied to an
+ *                              aligned buffer for products of at least 1e9 FLOPs and
+ *                              gathered below; 1 always gather; 2 always copy
  * A value of 0 restores the default.  Returns GEMM_F16_ERR_INVALID_VALUE for an
  * unknown option or a value out of range.
  */
@@ -349,7 +358,8 @@ enum {
     GEMM_F16_OPT_STREAMK = 9,
     GEMM_F16_OPT_TAIL_SPLIT = 10,
     GEMM_F16_OPT_MAX_STAGES = 11,
-    GEMM_F16_OPT_MULTICAST = 12
+    GEMM_F16_OPT_MULTICAST = 12,
+    GEMM_F16_OPT_REPACK = 13
 };
 gemm_f16_status gemm_f16_set_option(int option, int64_t value);
 

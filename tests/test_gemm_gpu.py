@@ -25,7 +25,7 @@ DEV = torch.device("cuda:0")
 def _defaults():
     yield
     for o in (g.OPT_FORCE_GATHER, g.OPT_SPLITS, g.OPT_TILE_N, g.OPT_PANEL, g.OPT_SWAP,
-              g.OPT_TIMEOUT_MS, g.OPT_MAX_CTAS, g.OPT_PAIR, g.OPT_STREAMK, g.OPT_TAIL_SPLIT, g.OPT_MAX_STAGES, g.OPT_MULTICAST):
+              g.OPT_TIMEOUT_MS, g.OPT_MAX_CTAS, g.OPT_PAIR, g.OPT_STREAMK, g.OPT_TAIL_SPLIT, g.OPT_MAX_STAGES, g.OPT_MULTICAST, g.OPT_REPACK):
         g.gemm_f16_set_option(o, 0)
 
 
@@ -426,7 +426,10 @@ def test_tail_split_bit_exact(M, N, K, layout):
 @pytest.mark.parametrize("M,N,K,layout", [(1000, 1000, 1000, "pitch"), (3001, 1999, 200, "offset")])
 def test_gathered_operands_default_to_stream_k(M, N, K, layout):
     """Gathered (non-TMA) operands make tiles slow, so by default the last
-    partial wave is balanced by stream-K; integer inputs stay bit-exact."""
+    partial wave is balanced by stream-K; integer inputs stay bit-exact.  (The
+    aligned-copy path is switched off: these products are large enough that it
+    would replace the gather.)"""
+    g.gemm_f16_set_option(g.OPT_REPACK, 1)
     rng = np.random.default_rng(M + 5 * N + K)
     Ah = rng.integers(-3, 4, (M, K)).astype(np.float16)
     Bh = rng.integers(-3, 4, (K, N)).astype(np.float16)
