@@ -756,7 +756,10 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
     const int64_t sk_opt = opt(GEMM_F16_OPT_STREAMK);
     const bool use_sk = splits == 1 && !quad && !gated && (sk_opt == 2 || (sk_opt == 0 && (!ca.tma || !cb.tma)));
     const bool may_cut = splits > 1 || use_sk;
-    const int epi = (c_tma || may_cut) ? static_cast<int>(gemm_f16_dev::kEpiBytes) : 0;
+    // A C that TMA cannot store but whose columns are contiguous is staged in
+    // the same buffer and written row by row by the epilogue warps.
+    const bool c_stage = !c_tma && !swap;
+    const int epi = (c_tma || c_stage || may_cut) ? static_cast<int>(gemm_f16_dev::kEpiBytes) : 0;
     int stages = (kMaxDynSmem - kSmemAlignSlack - epi - static_cast<int>(gemm_f16_dev::kBarrierBytes)) /
                  static_cast<int>(stage_bytes);
     stages = std::min(stages, gemm_f16_dev::kMaxStages);
@@ -821,6 +824,7 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
     kp.b_flags = (cb.tma ? gemm_f16_dev::kOpTma : 0u) | (cb.mn ? gemm_f16_dev::kOpMnMajor : 0u) |
                  (b_3d ? gemm_f16_dev::kOpBox3d : 0u);
     kp.c_tma = c_tma ? 1u : 0u;
+    kp.c_stage = c_stage ? 1u : 0u;
     kp.epi_smem = epi > 0 ? 1u : 0u;
     pl->fused = a.fused;
     if (a.fused) {
@@ -876,8 +880,9 @@ gemm_f16_status launch(Plan& pl, DevInfo& dev, float* partials, int* counters, c
     if (!set_smem_attributes(dev)) return GEMM_F16_ERR_LAUNCH;
     for (int i = 0; i < pl.ncopies; ++i) {
         const gemm_f16_dev::RepackArgs& c = pl.copies[i];
-        const int64_t warps = c.rows * c.batch;
-        const int64_t blocks = std::min<int64_t>((warps + 7) / 8, static_cast<int64_t>(dev.sms) * 8);
+        const int64_t seg = 8 * 32 * gemm_f16_dev::kRepackUnroll;   // elements per work item
+        const int64_t items = c.rows * c.batch * ((c.pitch + seg - 1) / seg);
+        const int64_t blocks = std::min<int64_t>((items + 7) / 8, static_cast<int64_t>(dev.sms) * 4);
         gemm_f16_dev::repack_rows<<<static_cast<unsigned>(blocks), gemm_f16_dev::kRepackThreads, 0, stream>>>(c);
     }
     const bool multi = kp.gmode != 0;

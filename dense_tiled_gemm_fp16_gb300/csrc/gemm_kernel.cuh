@@ -105,6 +105,10 @@ struct KernelParams {
     uint64_t timeout_ns;
     int tiles_m, tiles_n, splits, kblocks, num_units, panel, BN, stages;
     uint32_t a_flags, b_flags, c_tma, idesc, tx_bytes, stage_b_bytes, full_count;
+    // C that TMA cannot store (unaligned base or pitch, N not a multiple of 8)
+    // but with a unit column stride: boxes are staged in shared memory as for
+    // TMA and written row by row by the warp (stores of contiguous columns).
+    uint32_t c_stage;
     uint32_t epi_smem;   // 1: reserve the 32 KB epilogue buffer (TMA-store staging, fixup landing zone)
     // Work decomposition.  `workers` persistent CTAs (single form) or clusters
     // (pair form).  Worker c first takes the whole-tile (or classic split-K)
@@ -669,6 +673,34 @@ __device__ __forceinline__ void gather_tile(const __half* base, int64_t s_mn, in
     }
 }
 
+// Write a warp's staged 32 x 64 box (swizzled like a TMA box; `ncols` of its
+// columns hold output) to C rows crow .. crow+31, columns n .. n+ncols-1, row by
+// row: lane l writes columns 2l and 2l+1, as one 4-byte store where the address
+// allows, so each store instruction covers 128 contiguous bytes of a row.
+// Rows at or past row_lim and columns at or past N are not written.
+__device__ __forceinline__ void store_box_rows(const KernelParams& p, __half* C, int64_t row_lim, uint32_t buf,
+                                               int64_t crow, int64_t n, int ncols)
+{
+    const int lane = threadIdx.x & 31;
+    const int c = 2 * lane;
+    const int64_t nn = n + c;
+    const bool in0 = c < ncols && nn < p.N, in1 = c + 1 < ncols && nn + 1 < p.N;
+    const int j = c >> 3;   // 16-byte chunk of the box row
+    uint16_t* base = reinterpret_cast<uint16_t*>(C) + nn;
+    for (int r = 0; r < 32; ++r) {
+        const int64_t m = crow + r;
+        if (m >= row_lim) break;
+        const uint32_t v = ld_smem_u32(buf + r * 128 + ((j ^ (r & 7)) << 4) + (c & 7) * 2);
+        uint16_t* q = base + m * p.c_sm;
+        if (in1 && (reinterpret_cast<uintptr_t>(q) & 3u) == 0) {
+            *reinterpret_cast<uint32_t*>(q) = v;
+        } else {
+            if (in0) q[0] = static_cast<uint16_t>(v);
+            if (in1) q[1] = static_cast<uint16_t>(v >> 16);
+        }
+    }
+}
+
 __device__ __forceinline__ uint16_t half_bits(const uint32_t* h, int c)
 {
     return static_cast<uint16_t>(h[c >> 1] >> ((c & 1) * 16));
@@ -808,7 +840,7 @@ __device__ __forceinline__ void emit_piece(const KernelParams& p, const SmemLayo
 {
     const int lane = threadIdx.x & 31;
     const int q = (threadIdx.x >> 5) & 3;
-    if (ctma) {
+    if (ctma || p.c_stage) {
         const int j0 = (piece & 3) * 2;   // 16-byte chunk inside the 128-byte row
         if ((piece & 3) == 0) {
             buf = L.epi + (q * 2 + (group_count & 1u)) * kEpiBufBytes;
@@ -817,7 +849,11 @@ __device__ __forceinline__ void emit_piece(const KernelParams& p, const SmemLayo
         }
         st_smem_v4(buf + lane * 128 + ((j0 ^ (lane & 7)) << 4), make_uint4(h[0], h[1], h[2], h[3]));
         st_smem_v4(buf + lane * 128 + (((j0 + 1) ^ (lane & 7)) << 4), make_uint4(h[4], h[5], h[6], h[7]));
-        if ((piece & 3) == 3 || piece == npieces - 1) {
+        if (!ctma && ((piece & 3) == 3 || piece == npieces - 1)) {
+            __syncwarp();
+            store_box_rows(p, ug.C, ug.row_lim, buf, crow, n0 + 16 * (piece & ~3), 16 * ((piece & 3) + 1));
+            __syncwarp();   // the box is read before the next piece overwrites it
+        } else if ((piece & 3) == 3 || piece == npieces - 1) {
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -1539,7 +1575,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                         const int piece = pc + h2;
                         uint32_t h[8];
                         convert16(r + 16 * h2, h);
-                        if (ctma) {
+                        if (ctma || p.c_stage) {
                             const int j0 = (piece & 3) * 2;        // 16-byte chunk inside the 128-byte row
                             if ((piece & 3) == 0) {
                                 buf = L.epi + (q * 2 + (group_count & 1u)) * kEpiBufBytes;
@@ -1549,7 +1585,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                             st_smem_v4(buf + lane * 128 + ((j0 ^ (lane & 7)) << 4), make_uint4(h[0], h[1], h[2], h[3]));
                             st_smem_v4(buf + lane * 128 + (((j0 + 1) ^ (lane & 7)) << 4),
                                        make_uint4(h[4], h[5], h[6], h[7]));
-                            if ((piece & 3) == 3 || piece == npieces - 1) {
+                            if (!ctma && ((piece & 3) == 3 || piece == npieces - 1)) {
+                                __syncwarp();
+                                store_box_rows(p, ug.C, ug.row_lim, buf, crow, n0 + 16 * (piece & ~3),
+                                               16 * ((piece & 3) + 1));
+                                __syncwarp();   // the box is read before the next piece overwrites it
+                            } else if ((piece & 3) == 3 || piece == npieces - 1) {
                                 fence_proxy_async_smem();
                                 __syncwarp();
                                 if (lane == 0) {

@@ -473,6 +473,13 @@ __device__ __forceinline__ void st_global_v4(float* p, float a, float b, float c
     asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
+__device__ __forceinline__ uint32_t ld_smem_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ float4 ld_smem_f4(uint32_t addr)
 {
     float4 v;

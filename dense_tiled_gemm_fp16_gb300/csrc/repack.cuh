@@ -38,7 +38,9 @@ __device__ __forceinline__ uint4 repack_shift(const uint4& w0, const uint4& w1, 
     return sh == 0 ? w0 : funnel16(w0, w1, sh);
 }
 
-// One warp per row (grid-stride over batch * rows).  Unit column stride: the
+// Work items are (row, segment of 32 * kRepackUnroll output chunks), one warp
+// each, grid-stride over batch * rows * segments, so that a long row does not
+// serialise one warp on several memory round trips.  Unit column stride: the
 // lane loads the aligned 16-byte source words that hold its output chunk's
 // valid elements (never a word without one, so no load leaves the view's
 // pages), shifts them into place and stores the chunk.  Other strides: element
@@ -47,42 +49,45 @@ __global__ void __launch_bounds__(kRepackThreads) repack_rows(const RepackArgs a
 {
     const int lane = threadIdx.x & 31;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (kRepackThreads / 32);
-    const int64_t total = a.rows * a.batch;
     const int64_t chunks = a.pitch / 8;
+    constexpr int64_t kSeg = 32 * kRepackUnroll;
+    const int64_t segs = (chunks + kSeg - 1) / kSeg;
+    const int64_t total = a.rows * a.batch * segs;
     for (int64_t q = static_cast<int64_t>(blockIdx.x) * (kRepackThreads / 32) + (threadIdx.x >> 5); q < total;
          q += warps) {
-        const int64_t b = q / a.rows, r = q - b * a.rows;
+        const int64_t row = q / segs, seg = q - row * segs;
+        const int64_t b = row / a.rows, r = row - b * a.rows;
         const __half* srow = a.src + b * a.s_b + r * a.s_r;
         uint4* drow = reinterpret_cast<uint4*>(a.dst + b * a.dst_bs + r * a.pitch);
+        const int64_t j0 = seg * kSeg + lane;
         if (a.s_c == 1) {
             const uintptr_t addr = reinterpret_cast<uintptr_t>(srow);
             const uint32_t sh = static_cast<uint32_t>(addr & 15u);
             const uint4* w = reinterpret_cast<const uint4*>(addr - sh);
-            for (int64_t j0 = lane; j0 < chunks; j0 += 32 * kRepackUnroll) {
-                uint4 w0[kRepackUnroll], w1[kRepackUnroll];
-                int nv[kRepackUnroll];
+            uint4 w0[kRepackUnroll], w1[kRepackUnroll];
+            int nv[kRepackUnroll];
 #pragma unroll
-                for (int u = 0; u < kRepackUnroll; ++u) {
-                    const int64_t j = j0 + 32 * u;
-                    const int64_t left = a.cols - 8 * j;
-                    nv[u] = j < chunks ? (left >= 8 ? 8 : (left <= 0 ? 0 : static_cast<int>(left))) : 0;
-                    w0[u] = w1[u] = make_uint4(0u, 0u, 0u, 0u);
-                    if (nv[u] > 0) w0[u] = ld_nc_v4(w + j);
-                    if (nv[u] > 0 && sh + 2u * static_cast<uint32_t>(nv[u]) > 16u) w1[u] = ld_nc_v4(w + j + 1);
-                }
+            for (int u = 0; u < kRepackUnroll; ++u) {
+                const int64_t j = j0 + 32 * u;
+                const int64_t left = a.cols - 8 * j;
+                nv[u] = j < chunks ? (left >= 8 ? 8 : (left <= 0 ? 0 : static_cast<int>(left))) : 0;
+                w0[u] = w1[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (nv[u] > 0) w0[u] = ld_nc_v4(w + j);
+                if (nv[u] > 0 && sh + 2u * static_cast<uint32_t>(nv[u]) > 16u) w1[u] = ld_nc_v4(w + j + 1);
+            }
 #pragma unroll
-                for (int u = 0; u < kRepackUnroll; ++u) {
-                    const int64_t j = j0 + 32 * u;
-                    if (j >= chunks) break;
-                    uint4 c = repack_shift(w0[u], w1[u], sh);
-                    if (nv[u] < 8) c = keep_first(c, nv[u]);
-                    drow[j] = c;
-                }
+            for (int u = 0; u < kRepackUnroll; ++u) {
+                const int64_t j = j0 + 32 * u;
+                if (j >= chunks) break;
+                uint4 c = repack_shift(w0[u], w1[u], sh);
+                if (nv[u] < 8) c = keep_first(c, nv[u]);
+                drow[j] = c;
             }
         } else {
             uint16_t* d = reinterpret_cast<uint16_t*>(drow);
             const uint16_t* s = reinterpret_cast<const uint16_t*>(srow);
-            for (int64_t c = lane; c < a.pitch; c += 32) d[c] = c < a.cols ? ld_nc_u16(s + c * a.s_c) : uint16_t(0);
+            for (int64_t c = 8 * (seg * kSeg) + lane; c < a.pitch && c < 8 * (seg + 1) * kSeg; c += 32)
+                d[c] = c < a.cols ? ld_nc_u16(s + c * a.s_c) : uint16_t(0);
         }
     }
 }
