@@ -580,8 +580,8 @@ def report(args, w, plan, peaks, bnd, flops, nbytes, ms_per_step, value, wall, c
         "wall_s_timed_region": round(wall, 4),
         "clocks": clk,
         "e2e": e2e,
-        # the GEMM kernel, plus one aligned-copy kernel per repacked operand
-        "gpu_launches": args.steps * (1 + bin(plan["repack"]).count("1")),
+        # the GEMM kernel, plus one aligned-copy kernel when an operand is repacked
+        "gpu_launches": args.steps * (2 if plan["repack"] else 1),
         "roofline": roof,
         "cpu_baseline": cpu,
         "device_status": status,

@@ -878,12 +878,16 @@ gemm_f16_status launch(Plan& pl, DevInfo& dev, float* partials, int* counters, c
     kp.counters = counters;
     if (pl.pub.grid == 0) return GEMM_F16_OK;   // no tile (every group empty)
     if (!set_smem_attributes(dev)) return GEMM_F16_ERR_LAUNCH;
-    for (int i = 0; i < pl.ncopies; ++i) {
-        const gemm_f16_dev::RepackArgs& c = pl.copies[i];
-        const int64_t seg = 8 * 32 * gemm_f16_dev::kRepackUnroll;   // elements per work item
-        const int64_t items = c.rows * c.batch * ((c.pitch + seg - 1) / seg);
+    if (pl.ncopies > 0) {   // every copy in one launch, before the GEMM on the same stream
+        gemm_f16_dev::RepackBatch rb;
+        rb.n = pl.ncopies;
+        int64_t items = 0;
+        for (int i = 0; i < pl.ncopies; ++i) {
+            rb.c[i] = pl.copies[i];
+            items += gemm_f16_dev::repack_items(pl.copies[i]);
+        }
         const int64_t blocks = std::min<int64_t>((items + 7) / 8, static_cast<int64_t>(dev.sms) * 4);
-        gemm_f16_dev::repack_rows<<<static_cast<unsigned>(blocks), gemm_f16_dev::kRepackThreads, 0, stream>>>(c);
+        gemm_f16_dev::repack_rows<<<static_cast<unsigned>(blocks), gemm_f16_dev::kRepackThreads, 0, stream>>>(rb);
     }
     const bool multi = kp.gmode != 0;
     if (!pl.pub.pair) {

@@ -30,6 +30,19 @@ struct RepackArgs {
     int64_t rows, cols, batch;
 };
 
+// Up to three copies (A', B', the up projection) in one launch: their work
+// items are numbered one copy after the other.
+struct RepackBatch {
+    RepackArgs c[3];
+    int n;
+};
+
+__host__ __device__ inline int64_t repack_items(const RepackArgs& a)
+{
+    const int64_t seg = 32 * kRepackUnroll;
+    return a.rows * a.batch * ((a.pitch / 8 + seg - 1) / seg);
+}
+
 // 8 fp16 values of the 16 bytes at byte offset sh (even) of the 32-byte pair
 // w0:w1; the offset is the same for the whole row, so the branch is uniform
 // across the warp.
@@ -45,16 +58,21 @@ __device__ __forceinline__ uint4 repack_shift(const uint4& w0, const uint4& w1, 
 // valid elements (never a word without one, so no load leaves the view's
 // pages), shifts them into place and stores the chunk.  Other strides: element
 // by element.
-__global__ void __launch_bounds__(kRepackThreads) repack_rows(const RepackArgs a)
+__global__ void __launch_bounds__(kRepackThreads) repack_rows(const __grid_constant__ RepackBatch batch)
 {
     const int lane = threadIdx.x & 31;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (kRepackThreads / 32);
-    const int64_t chunks = a.pitch / 8;
     constexpr int64_t kSeg = 32 * kRepackUnroll;
-    const int64_t segs = (chunks + kSeg - 1) / kSeg;
-    const int64_t total = a.rows * a.batch * segs;
-    for (int64_t q = static_cast<int64_t>(blockIdx.x) * (kRepackThreads / 32) + (threadIdx.x >> 5); q < total;
-         q += warps) {
+    const int64_t n0 = batch.n > 0 ? repack_items(batch.c[0]) : 0;
+    const int64_t n1 = batch.n > 1 ? repack_items(batch.c[1]) : 0;
+    const int64_t total = n0 + n1 + (batch.n > 2 ? repack_items(batch.c[2]) : 0);
+    for (int64_t qq = static_cast<int64_t>(blockIdx.x) * (kRepackThreads / 32) + (threadIdx.x >> 5); qq < total;
+         qq += warps) {
+        const int ci = qq < n0 ? 0 : (qq < n0 + n1 ? 1 : 2);
+        const RepackArgs& a = batch.c[ci];
+        const int64_t q = qq - (ci == 0 ? 0 : (ci == 1 ? n0 : n0 + n1));
+        const int64_t chunks = a.pitch / 8;
+        const int64_t segs = (chunks + kSeg - 1) / kSeg;
         const int64_t row = q / segs, seg = q - row * segs;
         const int64_t b = row / a.rows, r = row - b * a.rows;
         const __half* srow = a.src + b * a.s_b + r * a.s_r;
