@@ -55,7 +55,7 @@ struct Workspace {
 };
 Workspace g_ws[kMaxDevices];
 
-std::atomic<int64_t> g_opt[14];
+std::atomic<int64_t> g_opt[15];
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 PFN_cuMemGetAddressRange_v3020 g_addr_range = nullptr;
@@ -825,6 +825,7 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
                  (b_3d ? gemm_f16_dev::kOpBox3d : 0u);
     kp.c_tma = c_tma ? 1u : 0u;
     kp.c_stage = c_stage ? 1u : 0u;
+    kp.test_stall = opt(GEMM_F16_OPT_TEST_STALL) == 1 ? 1u : 0u;
     kp.epi_smem = epi > 0 ? 1u : 0u;
     pl->fused = a.fused;
     if (a.fused) {
@@ -1294,7 +1295,8 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
 
 gemm_f16_status gemm_f16_set_option(int option, int64_t value)
 {
-    if (option < 1 || option > 13 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option < 1 || option > 14 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option == GEMM_F16_OPT_TEST_STALL && value > 1) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_REPACK && value > 2) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_MULTICAST && value > 2) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_MAX_STAGES && value == 1) return GEMM_F16_ERR_INVALID_VALUE;

@@ -109,6 +109,11 @@ struct KernelParams {
     // but with a unit column stride: boxes are staged in shared memory as for
     // TMA and written row by row by the warp (stores of contiguous columns).
     uint32_t c_stage;
+    // Failure-detection test: the MMA issuer first waits on a barrier that
+    // nothing arrives on, so the bounded wait runs out, the CTA aborts and the
+    // status word reports the timeout (the host reads it; the context stays
+    // usable).  0 in every ordinary call.
+    uint32_t test_stall;
     uint32_t epi_smem;   // 1: reserve the 32 KB epilogue buffer (TMA-store staging, fixup landing zone)
     // Work decomposition.  `workers` persistent CTAs (single form) or clusters
     // (pair form).  Worker c first takes the whole-tile (or classic split-K)
@@ -177,7 +182,9 @@ __device__ __forceinline__ uint32_t bar_tfull(uint32_t bars, int a) { return bar
 __device__ __forceinline__ uint32_t bar_tempty(uint32_t bars, int a) { return bars + 8u * (2 * kMaxStages + 2 + a); }
 __device__ __forceinline__ uint32_t bar_drain(uint32_t bars) { return bars + 8u * (2 * kMaxStages + 4); }
 __device__ __forceinline__ uint32_t bar_fix(uint32_t bars) { return bars + 8u * (2 * kMaxStages + 5); }
-constexpr uint32_t kTmemSlotOff = 8u * (2 * kMaxStages + 6);
+// Failure-detection test only: a barrier nothing ever arrives on (see test_stall).
+__device__ __forceinline__ uint32_t bar_never(uint32_t bars) { return bars + 8u * (2 * kMaxStages + 6); }
+constexpr uint32_t kTmemSlotOff = 8u * (2 * kMaxStages + 7);
 constexpr uint32_t kAbortOff = kTmemSlotOff + 4;
 constexpr uint32_t kFlagOff = kTmemSlotOff + 8;
 constexpr uint32_t kOkOff = kTmemSlotOff + 12;   // two words, indexed by accumulator
@@ -1278,6 +1285,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
         }
         mbar_init(bar_drain(L.bars), 1);
         mbar_init(bar_fix(L.bars), 1);
+        mbar_init(bar_never(L.bars), 1);
         *abort = 0;
         *flag = 0;
         fence_mbarrier_init();
@@ -1430,6 +1438,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
             bool any = false;
             const uint32_t b_atom_rows = 8192;   // MN-major: one 64-wide atom column over 64 K rows
             const int nu = units_of_worker(p, cid);
+            if (p.test_stall && !wait_bar<kPair>(bar_never(L.bars), 0, abort, p.timeout_ns)) {
+                raise_abort(p, abort);
+                ok = false;
+            }
             for (int i = 0; i < nu && ok; ++i) {
                 const Unit w = unit_at<kMulti>(p, cid, i);
                 if (!wait_bar<kPair>(bar_tempty(L.bars, acc), acc_phase ^ 1u, abort, p.timeout_ns)) {

@@ -343,6 +343,11 @@ gemm_f16_status gemm_f16_fused_get_plan(const void* A, int64_t stride_am, int64_
  *   GEMM_F16_OPT_REPACK        0 default: operands TMA cannot address are copied to an
  *                              aligned buffer for products of at least 1e9 FLOPs and
  *                              gathered below; 1 always gather; 2 always copy
+ *   GEMM_F16_OPT_TEST_STALL    failure-detection test: 1 makes every CTA's MMA issuer wait
+ *                              first on a barrier that nothing arrives on, so the bounded
+ *                              wait runs out (after GEMM_F16_OPT_TIMEOUT_MS), the kernel
+ *                              aborts cleanly and gemm_f16_device_status() reports
+ *                              GEMM_F16_ERR_TIMEOUT; C is left undefined.  0 default
  * A value of 0 restores the default.  Returns GEMM_F16_ERR_INVALID_VALUE for an
  * unknown option or a value out of range.
  */
@@ -359,7 +364,8 @@ enum {
     GEMM_F16_OPT_TAIL_SPLIT = 10,
     GEMM_F16_OPT_MAX_STAGES = 11,
     GEMM_F16_OPT_MULTICAST = 12,
-    GEMM_F16_OPT_REPACK = 13
+    GEMM_F16_OPT_REPACK = 13,
+    GEMM_F16_OPT_TEST_STALL = 14
 };
 gemm_f16_status gemm_f16_set_option(int option, int64_t value);
 
