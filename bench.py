@@ -9,8 +9,10 @@ inputs, fp32 accumulation, fp16 output) on inputs already resident in device
 memory.  Each timed step is bracketed by CUDA events on the launching stream;
 L2 is flushed (a 512 MiB write) between steps, outside the events.  `value` is
 TFLOP/s of useful 2MNK work over all ranks.  `e2e` repeats the measurement
-through the same C ABI with pinned-host inputs copied in and the result copied
-out inside the timed region.  `roofline` rates the GEMM kernel against the
+through the torch-level API with every step's inputs copied in from pinned host
+memory and its result copied out inside the timed region, pipelined as a
+serving loop runs it (two device slots; the copy-in of step i+1 and the
+copy-out of step i-1 overlap the compute of step i on their own streams).  `roofline` rates the GEMM kernel against the
 measured peak of this machine; `cpu_baseline` times the CPU oracle on a bounded
 slab of output rows.
 
@@ -393,54 +395,43 @@ def run_ours_multi(args, w, dev, barrier, pg, rank, world):
         # torch-level wrappers a user calls
         A_h = torch.from_numpy(np.ascontiguousarray(w.A.host_buffer())).pin_memory()
         B_h = torch.from_numpy(np.ascontiguousarray(w.B.host_buffer())).pin_memory()
-        C_h = torch.empty(tuple(C.shape), dtype=torch.float16).pin_memory()
-        A_buf = torch.empty(w.A.numel, dtype=torch.float16, device=dev)
-        B_buf = torch.empty(w.B.numel, dtype=torch.float16, device=dev)
-        U_h = U_buf = U3 = None
-        if w.B_up is not None:
-            U_h = torch.from_numpy(np.ascontiguousarray(w.B_up.host_buffer())).pin_memory()
-            U_buf = torch.empty(w.B_up.numel, dtype=torch.float16, device=dev)
-            U3 = U_buf.view(n, K, N)
-        B3 = B_buf.view(n, K, N)
+        U_h = (torch.from_numpy(np.ascontiguousarray(w.B_up.host_buffer())).pin_memory()
+               if w.B_up is not None else None)
+        C_h = [torch.empty(tuple(C.shape), dtype=torch.float16).pin_memory() for _ in range(2)]
+        A_buf = [torch.empty(w.A.numel, dtype=torch.float16, device=dev) for _ in range(2)]
+        B_buf = [torch.empty(w.B.numel, dtype=torch.float16, device=dev) for _ in range(2)]
+        U_buf = [torch.empty(w.B_up.numel, dtype=torch.float16, device=dev) if U_h is not None else None
+                 for _ in range(2)]
+        Cs = [C, torch.empty_like(C)]
 
-        def copy_in():
-            A_buf.copy_(A_h, non_blocking=True)
-            B_buf.copy_(B_h, non_blocking=True)
-            if U_h is not None:
-                U_buf.copy_(U_h, non_blocking=True)
+        def copy_in(k, s):
+            with torch.cuda.stream(s):
+                A_buf[k].copy_(A_h, non_blocking=True)
+                B_buf[k].copy_(B_h, non_blocking=True)
+                if U_h is not None:
+                    U_buf[k].copy_(U_h, non_blocking=True)
 
-        if w.kind == "batched":
-            A3, C3 = A_buf.view(n, M, K), C.view(n, M, N)
-
-            def e2e_step():
-                copy_in()
+        def compute(k, s):
+            B3 = B_buf[k].view(n, K, N)
+            U3 = U_buf[k].view(n, K, N) if U_h is not None else None
+            if w.kind == "batched":
+                A3, C3 = A_buf[k].view(n, M, K), Cs[k].view(n, M, N)
                 if fused:
-                    g.fused_mm(A3, B3, act=w.act, b_up=U3, out=C3, stream=stream)
+                    g.fused_mm(A3, B3, act=w.act, b_up=U3, out=C3, stream=s)
                 else:
-                    g.bmm(A3, B3, out=C3, stream=stream)
-                C_h.copy_(C, non_blocking=True)
-        else:
-            A2 = A_buf.view(M, K)
+                    g.bmm(A3, B3, out=C3, stream=s)
+            elif fused:
+                g.grouped_fused_mm(A_buf[k].view(M, K), B3, list(w.group_rows), act=w.act, b_up=U3, out=Cs[k],
+                                   stream=s)
+            else:
+                g.grouped_mm(A_buf[k].view(M, K), B3, list(w.group_rows), out=Cs[k], stream=s)
 
-            def e2e_step():
-                copy_in()
-                if fused:
-                    g.grouped_fused_mm(A2, B3, list(w.group_rows), act=w.act, b_up=U3, out=C, stream=stream)
-                else:
-                    g.grouped_mm(A2, B3, list(w.group_rows), out=C, stream=stream)
-                C_h.copy_(C, non_blocking=True)
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
-        torch.cuda.synchronize(dev)
-        e2e_steps = max(3, min(args.steps, 10))
-        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier()
-        es.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        ee.record(stream)
-        torch.cuda.synchronize(dev)
-        e2e_ms = es.elapsed_time(ee) / e2e_steps
+        def copy_out(k, s):
+            with torch.cuda.stream(s):
+                C_h[k].copy_(Cs[k], non_blocking=True)
+
+        e2e_ms = pipelined_e2e(dev, stream, max(5, min(args.steps, 10)), args.warmup, copy_in, compute, copy_out,
+                               barrier, pg)
         e2e = {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(in_bytes),
                "d2h_bytes_per_step": int(2 * C.numel())}
@@ -487,6 +478,57 @@ def run_ours_multi(args, w, dev, barrier, pg, rank, world):
     }
 
 
+def pipelined_e2e(dev, stream, steps, warmup, copy_in, compute, copy_out, barrier, pg):
+    """End-to-end steps as a serving loop runs them: two device slots, the
+    host-to-device copy of step i+1 on one copy stream and the device-to-host
+    copy of step i-1 on another while step i computes on `stream`.  Every
+    step's copies and compute lie inside the timed region, which runs from
+    before the first copy-in to after the last copy-out; returns ms per step.
+
+    copy_in(slot, s), compute(slot, s), copy_out(slot, s) enqueue one step's
+    work for device slot `slot` on stream `s`."""
+    import torch
+
+    h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    # slot_free[k]: the compute that last read slot k's inputs is done (its
+    # inputs may be overwritten); out_free[k]: slot k's result has been copied out
+    slot_free = [torch.cuda.Event() for _ in range(2)]
+    out_free = [torch.cuda.Event() for _ in range(2)]
+    for k in range(2):
+        slot_free[k].record(stream)
+        out_free[k].record(stream)
+
+    def run(n):
+        for i in range(n):
+            k = i & 1
+            h2d.wait_event(slot_free[k])
+            copy_in(k, h2d)
+            ready = torch.cuda.Event()
+            ready.record(h2d)
+            stream.wait_event(ready)
+            stream.wait_event(out_free[k])
+            compute(k, stream)
+            slot_free[k].record(stream)
+            d2h.wait_event(slot_free[k])
+            copy_out(k, d2h)
+            out_free[k].record(d2h)
+
+    run(max(1, warmup))
+    torch.cuda.synchronize(dev)
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    es.record(h2d)
+    run(steps)
+    ee.record(d2h)
+    torch.cuda.synchronize(dev)
+    ms = es.elapsed_time(ee) / steps
+    if pg is not None:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms
+
+
 def run_e2e(args, w, dev, stream, C, barrier, pg):
     import numpy as np
     import torch
@@ -496,37 +538,31 @@ def run_e2e(args, w, dev, stream, C, barrier, pg):
     M, N = w.M, w.N
     A_h = torch.from_numpy(np.ascontiguousarray(w.A.host_buffer())).pin_memory()
     B_h = torch.from_numpy(np.ascontiguousarray(w.B.host_buffer())).pin_memory()
-    C_h = torch.empty((M, N), dtype=torch.float16).pin_memory()
-    A_buf = torch.empty(w.A.numel, dtype=torch.float16, device=dev)
-    B_buf = torch.empty(w.B.numel, dtype=torch.float16, device=dev)
-    A_v = A_buf.view(*w.A.buf_shape)
-    B_v = B_buf.view(*w.B.buf_shape)
-    A_v = A_v.t() if w.A.transposed else A_v
-    B_v = B_v.t() if w.B.transposed else B_v
+    C_h = [torch.empty((M, N), dtype=torch.float16).pin_memory() for _ in range(2)]
+    A_buf = [torch.empty(w.A.numel, dtype=torch.float16, device=dev) for _ in range(2)]
+    B_buf = [torch.empty(w.B.numel, dtype=torch.float16, device=dev) for _ in range(2)]
+    Cs = [C, torch.empty_like(C)]
 
-    def e2e_step():
-        A_buf.copy_(A_h, non_blocking=True)
-        B_buf.copy_(B_h, non_blocking=True)
-        g.matmul(A_v, B_v, out=C, stream=stream)
-        C_h.copy_(C, non_blocking=True)
+    def views(k):
+        A_v = A_buf[k].view(*w.A.buf_shape)
+        B_v = B_buf[k].view(*w.B.buf_shape)
+        return (A_v.t() if w.A.transposed else A_v), (B_v.t() if w.B.transposed else B_v)
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    e2e_steps = max(3, min(args.steps, 10))
-    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    es.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    ee.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = es.elapsed_time(ee) / e2e_steps
-    if pg is not None:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    return e2e_ms
+    def copy_in(k, s):
+        with torch.cuda.stream(s):
+            A_buf[k].copy_(A_h, non_blocking=True)
+            B_buf[k].copy_(B_h, non_blocking=True)
+
+    def compute(k, s):
+        A_v, B_v = views(k)
+        g.matmul(A_v, B_v, out=Cs[k], stream=s)
+
+    def copy_out(k, s):
+        with torch.cuda.stream(s):
+            C_h[k].copy_(Cs[k], non_blocking=True)
+
+    return pipelined_e2e(dev, stream, max(10, min(args.steps, 30)), args.warmup, copy_in, compute, copy_out,
+                         barrier, pg)
 
 
 def report(args, w, plan, peaks, bnd, flops, nbytes, ms_per_step, value, wall, clk, e2e_ms, world,
