@@ -149,6 +149,24 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
+def max_over_ranks(pg, x: float, device) -> float:
+    """x reduced with MAX over every rank of the process group (x itself when
+    there is no group): the slowest rank's time is the job's time."""
+    if pg is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_step: float, steps: int, world: int, total_ms: float) -> float:
+    """Units per second of the whole job: every rank's units over the slowest
+    rank's time (the replicas each process `units_per_step` per step)."""
+    return units_per_step * steps * world / (total_ms * 1e-3)
+
+
 def oracle_slab(w, rows: int, threads: int, fused=None):
     """(callable, FLOPs): the CPU oracle on the first `rows` output rows of the
     one-GEMM workload `w`; `fused` = (up projection operand or None, act) runs
@@ -276,13 +294,9 @@ def run_ours(args):
     ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     clk = clocks.stop()
 
-    total_ms = sum(ms)
-    if pg is not None:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(pg, sum(ms), dev)
     ms_per_step = total_ms / args.steps
-    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    value = whole_job_rate(flops, args.steps, world, total_ms) / 1e12
 
     # ---- end to end: pinned host inputs in, result out, inside the timed region
     if args.no_e2e:
@@ -381,13 +395,9 @@ def run_ours_multi(args, w, dev, barrier, pg, rank, world):
     barrier()
     wall = time.perf_counter() - t0
     clk = clocks.stop()
-    total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
-    if pg is not None:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(pg, sum(s.elapsed_time(e) for s, e in zip(starts, ends)), dev)
     ms_per_step = total_ms / args.steps
-    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    value = whole_job_rate(flops, args.steps, world, total_ms) / 1e12
 
     e2e = None
     if not args.no_e2e:
@@ -521,12 +531,7 @@ def pipelined_e2e(dev, stream, steps, warmup, copy_in, compute, copy_out, barrie
     run(steps)
     ee.record(d2h)
     torch.cuda.synchronize(dev)
-    ms = es.elapsed_time(ee) / steps
-    if pg is not None:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
-    return ms
+    return max_over_ranks(pg, es.elapsed_time(ee) / steps, dev)
 
 
 def run_e2e(args, w, dev, stream, C, barrier, pg):
