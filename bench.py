@@ -6,8 +6,10 @@
 
 A step is one C = A*B of the workload (default: the square 4096^3 case, fp16
 inputs, fp32 accumulation, fp16 output) on inputs already resident in device
-memory.  Each timed step is bracketed by CUDA events on the launching stream;
-L2 is flushed (a 512 MiB write) between steps, outside the events.  `value` is
+memory.  When the inputs fit in L2, L2 is flushed (a 512 MiB write) between
+steps and each timed step is bracketed by its own CUDA events on the launching
+stream, the flush outside them; when they do not, the K steps run back to back
+as one replay of a CUDA graph of K calls, timed by two events around it.  `value` is
 TFLOP/s of useful 2MNK work over all ranks.  `e2e` repeats the measurement
 through the torch-level API with every step's inputs copied in from pinned host
 memory and its result copied out inside the timed region, pipelined as a
@@ -149,6 +151,49 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
+def timed_steps(torch, dev, stream, steps, flush, step, graph_step, barrier):
+    """Device time of `steps` steps on `stream` (ms), bracketed by a barrier
+    and a synchronize on both sides; returns (total ms, wall seconds, timing note).
+
+    With an L2 flush (inputs that fit in L2) every step is bracketed by its own
+    CUDA events and the flush runs between them, outside.  Without one (inputs
+    larger than L2) the steps run back to back: they are captured once as a
+    CUDA graph of `steps` calls (graph_step(s) enqueues one step on stream s)
+    and timed by two events around its replay, as a serving loop would run
+    them."""
+    if flush is None:
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        with torch.cuda.graph(graph, stream=cap):
+            for _ in range(steps):
+                graph_step(cap)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        return e0.elapsed_time(e1), time.perf_counter() - t0, "CUDA graph of the steps, events around its replay"
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    wall = time.perf_counter() - t0
+    return sum(a.elapsed_time(b) for a, b in zip(starts, ends)), wall, "per-step CUDA events, L2 flushed between"
+
+
 def max_over_ranks(pg, x: float, device) -> float:
     """x reduced with MAX over every rank of the process group (x itself when
     there is no group): the slowest rank's time is the job's time."""
@@ -263,6 +308,9 @@ def run_ours(args):
     def step():
         g.gemm_f16(*call_args, stream=handle)
 
+    def graph_step(s):
+        g.gemm_f16(*call_args, stream=s.cuda_stream)
+
     for _ in range(args.warmup):
         if flush is not None:
             flush.zero_()
@@ -277,24 +325,11 @@ def run_ours(args):
     clocks.start()
     time.sleep(0.3)
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    barrier()
-    torch.cuda.synchronize(dev)
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        if flush is not None:
-            flush.zero_()
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    wall = time.perf_counter() - t0
-    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    local_ms, wall, timing = timed_steps(torch, dev, stream, args.steps, flush, step, graph_step, barrier)
     clk = clocks.stop()
+    l2_note += "; " + timing
 
-    total_ms = max_over_ranks(pg, sum(ms), dev)
+    total_ms = max_over_ranks(pg, local_ms, dev)
     ms_per_step = total_ms / args.steps
     value = whole_job_rate(flops, args.steps, world, total_ms) / 1e12
 
@@ -347,26 +382,26 @@ def run_ours_multi(args, w, dev, barrier, pg, rank, world):
     if w.kind == "batched" and not fused:
         call = (A.data_ptr(), M * K, K, 1, B.data_ptr(), K * N, N, 1, C.data_ptr(), M * N, N, M, N, K, n)
 
-        def step():
-            g.gemm_f16_batched(*call, stream=handle)
+        def step(h=handle):
+            g.gemm_f16_batched(*call, stream=h)
     elif w.kind == "batched":
         call = (A.data_ptr(), M * K, K, 1, B.data_ptr(), K * N, N, 1, up, 0, 0, 0, act, C.data_ptr(), M * N, N,
                 M, N, K, n)
 
-        def step():
-            g.gemm_f16_batched_fused(*call, stream=handle)
+        def step(h=handle):
+            g.gemm_f16_batched_fused(*call, stream=h)
     elif not fused:
         rows = list(w.group_rows)
         call = (A.data_ptr(), K, 1, B.data_ptr(), K * N, N, 1, C.data_ptr(), N, rows, N, K)
 
-        def step():
-            g.gemm_f16_grouped(*call, stream=handle)
+        def step(h=handle):
+            g.gemm_f16_grouped(*call, stream=h)
     else:
         rows = list(w.group_rows)
         call = (A.data_ptr(), K, 1, B.data_ptr(), K * N, N, 1, up, 0, 0, 0, act, C.data_ptr(), N, rows, N, K)
 
-        def step():
-            g.gemm_f16_grouped_fused(*call, stream=handle)
+        def step(h=handle):
+            g.gemm_f16_grouped_fused(*call, stream=h)
 
     for _ in range(args.warmup):
         if flush is not None:
@@ -380,22 +415,11 @@ def run_ours_multi(args, w, dev, barrier, pg, rank, world):
     clocks = ClockSampler(str(uuid) if uuid else None)
     clocks.start()
     time.sleep(0.3)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    barrier()
-    torch.cuda.synchronize(dev)
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        if flush is not None:
-            flush.zero_()
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    wall = time.perf_counter() - t0
+    local_ms, wall, timing = timed_steps(torch, dev, stream, args.steps, flush, step,
+                                         lambda s: step(s.cuda_stream), barrier)
     clk = clocks.stop()
-    total_ms = max_over_ranks(pg, sum(s.elapsed_time(e) for s, e in zip(starts, ends)), dev)
+    l2_note += "; " + timing
+    total_ms = max_over_ranks(pg, local_ms, dev)
     ms_per_step = total_ms / args.steps
     value = whole_job_rate(flops, args.steps, world, total_ms) / 1e12
 
