@@ -558,3 +558,21 @@ def test_large_sampled_plus_boundary_tile(w):
 
 def test_no_kernel_reported_a_timeout():
     assert g.gemm_f16_device_status(reset=True) == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 16, (1 << 20) + 3),       # 16385 K blocks, swapped form
+                                   ((1 << 20) + 5, 64, 64),       # 4097 pair tile rows
+                                   (64, (1 << 20) + 7, 64),       # swapped: 8193 tiles along N
+                                   (3, 3, (1 << 21) + 1)])         # long K through split-K / stream-K
+def test_long_dimensions(M, N, K):
+    """One very long dimension: tile and K-block counts in the thousands, int64
+    offsets well past 2^31 bytes.  Integer inputs in [-1, 1]: every partial sum
+    is an integer below 2^24, exact in fp32 in any order, so the one rounding to
+    fp16 matches the oracle's bit for bit."""
+    rng = np.random.default_rng(M + N + K)
+    Ah = rng.integers(-1, 2, (M, K)).astype(np.float16)
+    Bh = rng.integers(-1, 2, (K, N)).astype(np.float16)
+    out = torch.empty((M, N), dtype=torch.float16, device=DEV)
+    C = host(gpu(to_dev(Ah), to_dev(Bh), out=out))
+    assert_bits(C, oracle.gemm(Ah, Bh, threads=oracle_threads()), f"{M}x{N}x{K}")
+    assert g.gemm_f16_device_status() == 0
