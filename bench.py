@@ -50,13 +50,20 @@ def log(*a):
 
 
 def kernel_source_hash() -> str:
-    """First 16 hex digits of sha256 over the kernel sources (ptx, kernel, host)."""
+    """First 16 hex digits of sha256 over the kernel sources (ptx, kernel, host,
+    operand copy), with comments and blank space removed: a change of comment
+    does not change the code the counters were taken on."""
     import hashlib
+    import re
+
     csrc = os.path.join(ROOT, "dense_tiled_gemm_fp16_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ("ptx.cuh", "gemm_kernel.cuh", "gemm_f16.cu"):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+    for f in ("ptx.cuh", "gemm_kernel.cuh", "gemm_f16.cu", "repack.cuh"):
+        with open(os.path.join(csrc, f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,38 +1,52 @@
 // Persistent, warp-specialised fp16 GEMM for sm_103a: C = A * B with fp16
 // operands, fp32 accumulation in tensor memory (TMEM) and fp16 output.
 //
-// One CTA per SM walks a list of work units.  A unit is one output tile, or,
-// in split-K mode, one K-segment of a tile.  Two forms share this source:
+// One CTA (or CTA cluster) per SM (pair) walks a list of work units.  A unit
+// is a whole output tile, a narrower piece of a tile of the last partial wave
+// (tail split along N), or a K segment of a tile (classic split-K, or the
+// stream-K tail).  The kernel template gemm_f16_persistent<kPair, kQuad,
+// kMulti, kEpi> has three forms:
 //
 //   single (kPair = false)  a 128 x BN tile per CTA, cta_group::1 MMAs.  Any
-//                           operand layout (TMA or gather), split-K.
+//                           operand layout (TMA or gather), any unit kind.
 //   pair   (kPair = true)   clusters of two CTAs; a 256 x BN tile per pair,
 //                           one cta_group::2 MMA stream issued by the leader
 //                           (rank 0).  Each CTA loads its own 128 rows of A
-//                           and its own BN/2 columns of B (no multicast), so a
-//                           CTA moves 2/3 of the single form's operand bytes
-//                           per MMA cycle and fits deeper pipelines.  TMA
-//                           operands only, no split-K.
+//                           and its own BN/2 columns of B, so a CTA moves 2/3
+//                           of the single form's operand bytes per MMA cycle
+//                           and fits deeper pipelines.  TMA operands only.
+//   four-CTA (kQuad)        two pairs on vertically adjacent tiles with the
+//                           same B columns; each CTA loads a quarter of its
+//                           pair rank's B columns and multicasts it to both
+//                           pairs (whole tiles only).
+//
+// kMulti adds the geometry of batched and grouped launches (per-unit problem,
+// trailing batch coordinate of the TMA maps, group row limits); kEpi adds the
+// fused output stage (bias, activation, gate/up product).
 //
 // Roles (8 warps; 256 threads leave each thread up to 255 registers):
 //   warps 0-2  producers.  Operands that TMA can address are loaded by one
 //              thread with cp.async.bulk.tensor into 128-byte-swizzled shared
 //              memory (out-of-range box elements arrive as zeros).  Operands
 //              TMA cannot address (unaligned base or pitch, non-unit inner
-//              stride) are gathered by all 96 threads with bounds-checked
-//              loads, written in the same swizzled layout and published to the
-//              tensor core with fence.proxy.async.  Either way the K tail is
-//              zero-filled: an index past K is never wrapped back into range.
-//   warps 4-7  epilogue.  tcgen05.ld of the fp32 accumulator (warp w reads
-//              TMEM lanes 32*(w%4)..+31), convert to fp16, then either stage
-//              through swizzled shared memory and TMA-store (clipped to M x N)
-//              or store with per-element bounds checks.  In split-K mode the
-//              fp32 partial goes to a workspace and the last CTA to finish a
-//              tile sums the partials in split order (deterministic).
+//              stride) and that the host did not copy to an aligned buffer are
+//              gathered by all 96 threads with bounds-checked loads, written in
+//              the same swizzled layout and published to the tensor core with
+//              fence.proxy.async.  Either way the K tail is zero-filled: an
+//              index past K is never wrapped back into range.
 //   warp 3     TMEM allocation and the MMA issuer (one thread): 4 x
-//              tcgen05.mma (K = 16 each) per 64-wide K block into one of two
-//              TMEM accumulators, so the epilogue of a tile overlaps the main
-//              loop of the next.
+//              tcgen05.mma (K = 16 each) per 64-wide K block, two K blocks per
+//              barrier phase, into one of two TMEM accumulators, so the
+//              epilogue of a tile overlaps the main loop of the next.
+//   warps 4-7  epilogue.  tcgen05.ld of the fp32 accumulator (warp w reads
+//              TMEM lanes 32*(w%4)..+31), the fused stage if any, convert to
+//              fp16, then stage 32 x 64 boxes in swizzled shared memory and
+//              either TMA-store them (clipped to M x N) or, where TMA cannot
+//              store C, write them row by row; the swapped form's transposed C
+//              takes per-element bounds-checked stores.  A unit that is a K
+//              segment leaves an fp32 partial in the workspace, and the last
+//              unit of its tile to finish adds all partials in K order
+//              (deterministic) before the store.
 //
 // Stages form a ring guarded by full/empty mbarriers; accumulators by
 // tmem_full/tmem_empty mbarriers.  All waits are bounded (see ptx.cuh).
