@@ -5,9 +5,14 @@ built in-tree by ``build.py``).  The binding only marshals arguments: every
 step of the product runs in the library's sm_103a kernels.  If the library is
 missing, calls raise :class:`GemmF16Error`; there is no fallback.
 
-``gemm_f16`` mirrors the C entry point (device pointers as integers, element
-strides).  ``matmul`` is the torch-tensor convenience form: it reads pointers,
-strides and the current stream from the tensors and calls ``gemm_f16``.
+The ``gemm_f16*`` functions mirror the C entry points one to one (device
+pointers as integers, element strides): the single product (``gemm_f16``, with
+caller workspace ``gemm_f16_ws``, allocation-free ``gemm_f16_noalloc``), the
+batched and grouped forms, and the fused output stage (bias, activation,
+gate/up product) for each.  The torch-tensor forms read pointers, strides and
+the current stream from the tensors: ``matmul``, ``bmm``, ``grouped_mm``,
+``fused_mm`` (2-D or batched) and ``grouped_fused_mm``; ``plan_for`` and
+``fused_plan_for`` report the execution plan.
 """
 from __future__ import annotations
 
