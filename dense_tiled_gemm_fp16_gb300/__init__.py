@@ -50,6 +50,7 @@ OPT_MAX_STAGES = 11
 OPT_MULTICAST = 12
 OPT_REPACK = 13
 OPT_TEST_STALL = 14
+OPT_PDL = 15
 
 # Activations of the fused output stage (gemm_f16_fused and friends).
 ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU = range(4)

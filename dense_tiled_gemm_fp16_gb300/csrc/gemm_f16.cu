@@ -55,7 +55,7 @@ struct Workspace {
 };
 Workspace g_ws[kMaxDevices];
 
-std::atomic<int64_t> g_opt[15];
+std::atomic<int64_t> g_opt[16];
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 PFN_cuMemGetAddressRange_v3020 g_addr_range = nullptr;
@@ -879,6 +879,36 @@ gemm_f16_status launch(Plan& pl, DevInfo& dev, float* partials, int* counters, c
     kp.counters = counters;
     if (pl.pub.grid == 0) return GEMM_F16_OK;   // no tile (every group empty)
     if (!set_smem_attributes(dev)) return GEMM_F16_ERR_LAUNCH;
+    // Every launch is a programmatic dependent of the kernel before it on the
+    // stream (unless GEMM_F16_OPT_PDL = 1): its prologue may overlap that
+    // kernel's tail, and the kernels wait (griddepcontrol.wait) before their
+    // first global-memory access.
+    const bool pdl = opt(GEMM_F16_OPT_PDL) != 1;
+    auto config = [&](cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, unsigned grid, unsigned block, size_t smem,
+                      int cluster) {
+        cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(block);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        int n = 0;
+        if (cluster > 1) {
+            attr[n].id = cudaLaunchAttributeClusterDimension;
+            attr[n].val.clusterDim.x = cluster;
+            attr[n].val.clusterDim.y = 1;
+            attr[n].val.clusterDim.z = 1;
+            ++n;
+        }
+        if (pdl) {
+            attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[n].val.programmaticStreamSerializationAllowed = 1;
+            ++n;
+        }
+        cfg.attrs = attr;
+        cfg.numAttrs = n;
+    };
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
     if (pl.ncopies > 0) {   // every copy in one launch, before the GEMM on the same stream
         gemm_f16_dev::RepackBatch rb;
         rb.n = pl.ncopies;
@@ -888,41 +918,27 @@ gemm_f16_status launch(Plan& pl, DevInfo& dev, float* partials, int* counters, c
             items += gemm_f16_dev::repack_items(pl.copies[i]);
         }
         const int64_t blocks = std::min<int64_t>((items + 7) / 8, static_cast<int64_t>(dev.sms) * 4);
-        gemm_f16_dev::repack_rows<<<static_cast<unsigned>(blocks), gemm_f16_dev::kRepackThreads, 0, stream>>>(rb);
-    }
-    const bool multi = kp.gmode != 0;
-    if (!pl.pub.pair) {
-        if (pl.fused)
-            gemm_f16_dev::gemm_f16_persistent<false, false, true, true>
-                <<<pl.pub.grid, gemm_f16_dev::kNumThreads, pl.pub.smem_bytes, stream>>>(kp);
-        else if (multi)
-            gemm_f16_dev::gemm_f16_persistent<false, false, true>
-                <<<pl.pub.grid, gemm_f16_dev::kNumThreads, pl.pub.smem_bytes, stream>>>(kp);
-        else
-            gemm_f16_dev::gemm_f16_persistent<false, false, false>
-                <<<pl.pub.grid, gemm_f16_dev::kNumThreads, pl.pub.smem_bytes, stream>>>(kp);
-    } else {
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = pl.pub.cluster_ctas;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(pl.pub.grid);
-        cfg.blockDim = dim3(gemm_f16_dev::kNumThreads);
-        cfg.dynamicSmemBytes = pl.pub.smem_bytes;
-        cfg.stream = stream;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        const cudaError_t e =
-            pl.pub.cluster_ctas == 4 ? cudaLaunchKernelEx(&cfg, gemm_f16_dev::gemm_f16_persistent<true, true, false>, kp)
-            : pl.fused ? cudaLaunchKernelEx(&cfg, gemm_f16_dev::gemm_f16_persistent<true, false, true, true>, kp)
-            : multi    ? cudaLaunchKernelEx(&cfg, gemm_f16_dev::gemm_f16_persistent<true, false, true>, kp)
-                       : cudaLaunchKernelEx(&cfg, gemm_f16_dev::gemm_f16_persistent<true, false, false>, kp);
-        if (e != cudaSuccess) {
+        config(cfg, attr, static_cast<unsigned>(blocks), gemm_f16_dev::kRepackThreads, 0, 1);
+        if (cudaLaunchKernelEx(&cfg, gemm_f16_dev::repack_rows, rb) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_F16_ERR_LAUNCH;
         }
+    }
+    const bool multi = kp.gmode != 0;
+    config(cfg, attr, static_cast<unsigned>(pl.pub.grid), gemm_f16_dev::kNumThreads, pl.pub.smem_bytes,
+           pl.pub.pair ? pl.pub.cluster_ctas : 1);
+    using gemm_f16_dev::gemm_f16_persistent;
+    const cudaError_t e =
+        !pl.pub.pair ? (pl.fused ? cudaLaunchKernelEx(&cfg, gemm_f16_persistent<false, false, true, true>, kp)
+                        : multi  ? cudaLaunchKernelEx(&cfg, gemm_f16_persistent<false, false, true>, kp)
+                                 : cudaLaunchKernelEx(&cfg, gemm_f16_persistent<false, false, false>, kp))
+        : pl.pub.cluster_ctas == 4 ? cudaLaunchKernelEx(&cfg, gemm_f16_persistent<true, true, false>, kp)
+        : pl.fused                 ? cudaLaunchKernelEx(&cfg, gemm_f16_persistent<true, false, true, true>, kp)
+        : multi                    ? cudaLaunchKernelEx(&cfg, gemm_f16_persistent<true, false, true>, kp)
+                                   : cudaLaunchKernelEx(&cfg, gemm_f16_persistent<true, false, false>, kp);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_F16_ERR_LAUNCH;
     }
     if (cudaGetLastError() != cudaSuccess) return GEMM_F16_ERR_LAUNCH;
     return GEMM_F16_OK;
@@ -1295,7 +1311,8 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
 
 gemm_f16_status gemm_f16_set_option(int option, int64_t value)
 {
-    if (option < 1 || option > 14 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option < 1 || option > 15 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option == GEMM_F16_OPT_PDL && value > 1) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_TEST_STALL && value > 1) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_REPACK && value > 2) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_MULTICAST && value > 2) return GEMM_F16_ERR_INVALID_VALUE;

@@ -1325,6 +1325,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
         __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Everything above (barriers, TMEM, descriptor prefetch) may overlap the
+    // previous kernel on the stream when this grid was launched as its
+    // programmatic dependent; no global memory is touched before that kernel
+    // has completed.  The next kernel may then be scheduled as SMs free up (it
+    // waits the same way before reading C or the workspace).
+    griddep_wait();
+    griddep_launch_dependents();
 
     if (warp < kMmaWarp) {
         // ------------------------------------------------------------ producers

@@ -79,6 +79,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
     }
 }
 
+// --------------------------------------------- programmatic dependent launch
+// Wait until the kernels this grid depends on (the previous kernel on the
+// stream, when this one was launched as its programmatic dependent) have
+// completed and their memory is visible; a no-op otherwise.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next kernel on the stream (if launched as a programmatic
+// dependent) to be scheduled; it still waits for this grid with griddep_wait.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ------------------------------------------------------------- clusters
 // The pair kernel runs as clusters of two CTAs whose tensor cores cooperate on
 // one 256-row MMA (cta_group::2).  Rank 0 of the pair is the leader: it owns

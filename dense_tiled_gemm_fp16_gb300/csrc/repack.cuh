@@ -60,6 +60,10 @@ __device__ __forceinline__ uint4 repack_shift(const uint4& w0, const uint4& w1, 
 // by element.
 __global__ void __launch_bounds__(kRepackThreads) repack_rows(const __grid_constant__ RepackBatch batch)
 {
+    // (as a programmatic dependent: the previous kernel, which may still read
+    // this buffer or write the source, has completed)
+    griddep_wait();
+    griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (kRepackThreads / 32);
     constexpr int64_t kSeg = 32 * kRepackUnroll;

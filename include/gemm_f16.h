@@ -343,6 +343,10 @@ gemm_f16_status gemm_f16_fused_get_plan(const void* A, int64_t stride_am, int64_
  *   GEMM_F16_OPT_REPACK        0 default: operands TMA cannot address are copied to an
  *                              aligned buffer for products of at least 1e9 FLOPs and
  *                              gathered below; 1 always gather; 2 always copy
+ *   GEMM_F16_OPT_PDL           0 default: every kernel is launched as a programmatic dependent
+ *                              of the kernel before it on the stream (its set-up overlaps that
+ *                              kernel's tail; it reads and writes memory only after that kernel
+ *                              has completed); 1 plain stream order
  *   GEMM_F16_OPT_TEST_STALL    failure-detection test: 1 makes every CTA's MMA issuer wait
  *                              first on a barrier that nothing arrives on, so the bounded
  *                              wait runs out (after GEMM_F16_OPT_TIMEOUT_MS), the kernel
@@ -365,7 +369,8 @@ enum {
     GEMM_F16_OPT_MAX_STAGES = 11,
     GEMM_F16_OPT_MULTICAST = 12,
     GEMM_F16_OPT_REPACK = 13,
-    GEMM_F16_OPT_TEST_STALL = 14
+    GEMM_F16_OPT_TEST_STALL = 14,
+    GEMM_F16_OPT_PDL = 15
 };
 gemm_f16_status gemm_f16_set_option(int option, int64_t value);
 
