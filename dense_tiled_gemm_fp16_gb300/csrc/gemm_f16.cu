@@ -817,7 +817,11 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
                                          static_cast<uint32_t>(piece), nb_b, bst_b);
         if (!ok) return GEMM_F16_ERR_LAUNCH;
     }
-    kp.panel = static_cast<int>(panel > 0 ? panel : 8);
+    // Raster panel (tile rows whose tiles run side by side): 8 by default;
+    // launches of at most four waves of tiles take 2, which measured 2 % faster
+    // on 4096^3 (wider panels measured faster from 6144^3 up).
+    const int default_panel = unit_tiles <= 4 * static_cast<int64_t>(sch.workers) ? 2 : 8;
+    kp.panel = static_cast<int>(panel > 0 ? panel : default_panel);
     kp.BN = BN, kp.stages = stages;
     kp.a_flags = (ca.tma ? gemm_f16_dev::kOpTma : 0u) | (ca.mn ? gemm_f16_dev::kOpMnMajor : 0u) |
                  (a_3d ? gemm_f16_dev::kOpBox3d : 0u);

@@ -323,7 +323,8 @@ gemm_f16_status gemm_f16_fused_get_plan(const void* A, int64_t stride_am, int64_
  *   GEMM_F16_OPT_SPLITS        > 0: classic split-K, every tile cut into this many K
  *                              segments (clamped to the K blocks); replaces stream-K
  *   GEMM_F16_OPT_TILE_N        > 0: force the tile width (multiple of 64, <= 256)
- *   GEMM_F16_OPT_PANEL         > 0: tile-rows per rasterisation panel (default 8)
+ *   GEMM_F16_OPT_PANEL         > 0: tile-rows per rasterisation panel (default 8, or 2 when the
+ *                              launch has at most four waves of tiles)
  *   GEMM_F16_OPT_SWAP          0 auto, 1 never swap, 2 always swap
  *   GEMM_F16_OPT_TIMEOUT_MS    bounded-wait limit in ms (default 1000)
  *   GEMM_F16_OPT_MAX_CTAS      > 0: cap the persistent grid
