@@ -580,6 +580,21 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
     const bool have_tma = g_encode != nullptr;
     OperandChoice ca = choose_operand(kp.A, kp.a_sm, kp.a_sk, Mv, a.K, gemm_f16_dev::kBM,
                                       have_tma && !(fg & 1) && (!a_bd || bs_ok(a_bs)));
+    // Grouped: an MN-major A box starts at its group's first row (+ a multiple
+    // of 128), and that row is the box's innermost (x) coordinate, which TMA
+    // needs on a 16-byte boundary.  Unless every non-empty group starts on a
+    // multiple of 8 rows, A is not read MN-major through TMA (it is gathered, or
+    // copied K-major below).
+    bool a_mn_tma_ok = true;
+    if (grouped) {
+        int64_t r0 = 0;
+        for (int64_t g = 0; g < a.batch; ++g) {
+            if (a.rows[g] > 0 && r0 % 8 != 0) a_mn_tma_ok = false;
+            r0 += a.rows[g];
+        }
+    }
+    if (ca.tma && ca.mn && !a_mn_tma_ok)
+        ca = choose_operand(kp.A, kp.a_sm, kp.a_sk, Mv, a.K, gemm_f16_dev::kBM, false);
     OperandChoice cb = choose_operand(kp.B, kp.b_sn, kp.b_sk, Nv, a.K, gated ? out_cols : BN,
                                       have_tma && !(fg & 2) && (!b_bd || bs_ok(b_bs)));
     if (gated) {
@@ -619,7 +634,12 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
                 l.s_b = bd ? bs : 0;
                 return l;
             };
-            const Layout la = layout(kp.a_sm, kp.a_sk, Mv, a_bs, a_bd);
+            Layout la = layout(kp.a_sm, kp.a_sk, Mv, a_bs, a_bd);
+            if (la.mn && !a_mn_tma_ok) {   // copy A K-major: rows of K along the rows of C
+                la.mn = false;
+                la.rows = Mv, la.cols = a.K, la.s_r = kp.a_sm, la.s_c = kp.a_sk;
+                la.pitch = round_up(a.K, 8);
+            }
             const Layout lb = layout(kp.b_sn, kp.b_sk, Nv, b_bs, b_bd);
             const int tile_b = gated ? out_cols : BN;
             // the copy must be TMA-addressable (an MN-major copy needs 64-wide tiles)

@@ -259,3 +259,30 @@ def test_full_size_workload_sampled(w):
         ref, gp, u = oracle.epilogue(S, w.act, 0.0, S_up, 0.0)
         assert_close_fused(got, ref, K, gp, u, w.act, f"{w.name} samples")
     assert g.gemm_f16_device_status() == 0
+
+
+@pytest.mark.parametrize("rows,N,K,opts", [
+    ([194, 241, 0, 165, 273, 217, 64, 0], 206, 1, {}),          # K = 1: A [rows, 1] has unit strides both ways
+    ([215, 236], 28, 1, {g.OPT_PAIR: 1, g.OPT_TAIL_SPLIT: 1}),
+    ([130, 77, 301], 256, 96, {}),                              # A column-major, group starts 130, 207
+    ([130, 77, 301], 256, 96, {g.OPT_REPACK: 2}),               # ... through the aligned copy (K-major)
+    ([512, 384, 640], 512, 136, {}),                            # starts on multiples of 8: MN-major TMA A
+])
+def test_grouped_column_major_a(rows, N, K, opts):
+    """A whose rows are contiguous in memory (a transposed view, or K = 1): in a
+    grouped call each group's first row is the innermost TMA coordinate of an
+    MN-major A box, which must sit on a 16-byte boundary; groups that start
+    elsewhere take the gather or a K-major copy.  Bit-exact either way."""
+    for o, v in opts.items():
+        g.gemm_f16_set_option(o, v)
+    rng = np.random.default_rng(sum(rows) + N + K)
+    Ah, Bh = ints(rng, (sum(rows), K)), ints(rng, (len(rows), K, N))
+    A = torch.from_numpy(np.ascontiguousarray(Ah.T)).to(DEV).t()     # strides (1, rows)
+    C = g.grouped_mm(A, dev(Bh), rows)
+    torch.cuda.synchronize()
+    assert_bits(C.cpu().numpy(), oracle.gemm_grouped(Ah, Bh, rows), f"grouped, column-major A {rows}")
+    U = ints(rng, (len(rows), K, N))
+    C = g.grouped_fused_mm(A, dev(Bh), rows, act="relu", b_up=dev(U))
+    torch.cuda.synchronize()
+    assert_bits(C.cpu().numpy(), oracle.gemm_fused_grouped(Ah, Bh, rows, U, act="relu"), "fused, column-major A")
+    assert g.gemm_f16_device_status() == 0
