@@ -1025,7 +1025,10 @@ __device__ __forceinline__ void cut_tile_epilogue(const KernelParams& p, const S
             int per = cap / others;
             if (per >= 4) per &= ~3;
             const int64_t crow = ug.a_row + m0 + 32 * ((threadIdx.x >> 5) & 3);   // this warp's first C row
-            const bool stage_c = last_unit && p.c_tma && (!kMulti || p.gmode != 2 || crow + 32 <= ug.row_lim);
+            // (a TMA store writes a whole 64-column box, so only batches of whole
+            // boxes, per >= 4 chunks, may go that way)
+            const bool stage_c =
+                last_unit && p.c_tma && per >= 4 && (!kMulti || p.gmode != 2 || crow + 32 <= ug.row_lim);
             const int q = (threadIdx.x >> 5) & 3;
             uint32_t gc = 0;   // TMA-store groups this warp issued
             for (int b0 = 0; b0 < chunks; b0 += per) {

@@ -576,3 +576,29 @@ def test_long_dimensions(M, N, K):
     C = host(gpu(to_dev(Ah), to_dev(Bh), out=out))
     assert_bits(C, oracle.gemm(Ah, Bh, threads=oracle_threads()), f"{M}x{N}x{K}")
     assert g.gemm_f16_device_status() == 0
+
+
+@pytest.mark.parametrize("opts", [
+    {g.OPT_STREAMK: 2, g.OPT_MAX_STAGES: 2},                  # pair form, 2-slot ring: 8-piece landing zone
+    {g.OPT_STREAMK: 2, g.OPT_MAX_STAGES: 2, g.OPT_TAIL_SPLIT: 1},
+    {g.OPT_STREAMK: 2, g.OPT_MAX_STAGES: 4},
+    {g.OPT_SPLITS: 3, g.OPT_MAX_STAGES: 2, g.OPT_PAIR: 1},
+])
+def test_shallow_ring_with_k_cuts(opts):
+    """Tiles cut along K with a shallow ring: the last unit of a worker collects
+    the other partials in the (small) stage area, in batches narrower than a
+    64-column TMA-store box; those batches must not go out as whole boxes
+    (which would overwrite the next tile's columns)."""
+    for o, v in opts.items():
+        g.gemm_f16_set_option(o, v)
+    rng = np.random.default_rng(4486)
+    M, N, K = 1190, 1216, 2986
+    Ah = rng.integers(-2, 3, (M, K)).astype(np.float16)
+    Bh = rng.integers(-2, 3, (K, N)).astype(np.float16)
+    A, B = to_dev(Ah), to_dev(Bh)
+    out = torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV)
+    plan = g.plan_for(A, B, out)
+    assert plan["streamk_tiles"] > 0 or plan["splits"] > 1, plan
+    C = host(gpu(A, B, out=out))
+    assert_bits(C, oracle.gemm(Ah, Bh, threads=oracle_threads()), f"shallow ring {opts}")
+    assert g.gemm_f16_device_status() == 0
