@@ -80,8 +80,22 @@ def _plain(rng):
     Ah, Bh = _ints(rng, (M, K)), _ints(rng, (K, N))
     A = _view(rng, Ah, int(rng.integers(0, 5)))
     B = _view(rng, Bh, int(rng.integers(0, 5)))
-    C = g.matmul(A, B)
-    return C, oracle.gemm(Ah, Bh, threads=oracle_threads()), f"plain {M}x{N}x{K}"
+    ref = oracle.gemm(Ah, Bh, threads=oracle_threads())
+    ck = int(rng.integers(0, 3))
+    if ck == 0:
+        return g.matmul(A, B), ref, f"plain {M}x{N}x{K}"
+    # C inside a NaN buffer, pitched (ck 1) or 2 bytes off alignment (ck 2): nothing
+    # outside the M x N view may change
+    ldc = N + int(rng.integers(1, 17)) if ck == 1 else N
+    off = 0 if ck == 1 else 1
+    buf = torch.full((M * ldc + 8,), float("nan"), dtype=torch.float16, device=DEV)
+    C = buf[off:off + M * ldc].view(M, ldc)[:, :N]
+    g.matmul(A, B, out=C)
+    torch.cuda.synchronize()
+    outside = torch.ones(buf.numel(), dtype=torch.bool)
+    outside[(off + torch.arange(M)[:, None] * ldc + torch.arange(N)[None, :]).reshape(-1)] = False
+    assert torch.isnan(buf.cpu()[outside]).all(), f"plain {M}x{N}x{K}: wrote outside the C view"
+    return C, ref, f"plain {M}x{N}x{K}, C layout {ck}, ldc {ldc}"
 
 
 def _fused(rng):
