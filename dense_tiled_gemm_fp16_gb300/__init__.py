@@ -33,8 +33,10 @@ STATUS = {
     4: "GEMM_F16_ERR_OUT_OF_MEMORY",
     5: "GEMM_F16_ERR_LAUNCH",
     6: "GEMM_F16_ERR_TIMEOUT",
+    7: "GEMM_F16_ERR_BOUNDS",
 }
-OK, ERR_INVALID_VALUE, ERR_ALIAS, ERR_UNSUPPORTED_DEVICE, ERR_OUT_OF_MEMORY, ERR_LAUNCH, ERR_TIMEOUT = range(7)
+(OK, ERR_INVALID_VALUE, ERR_ALIAS, ERR_UNSUPPORTED_DEVICE, ERR_OUT_OF_MEMORY, ERR_LAUNCH, ERR_TIMEOUT,
+ ERR_BOUNDS) = range(8)
 
 OPT_FORCE_GATHER = 1
 OPT_SPLITS = 2
@@ -51,6 +53,7 @@ OPT_MULTICAST = 12
 OPT_REPACK = 13
 OPT_TEST_STALL = 14
 OPT_PDL = 15
+OPT_DEBUG_BOUNDS = 16
 
 # Activations of the fused output stage (gemm_f16_fused and friends).
 ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU = range(4)

@@ -55,7 +55,7 @@ struct Workspace {
 };
 Workspace g_ws[kMaxDevices];
 
-std::atomic<int64_t> g_opt[16];
+std::atomic<int64_t> g_opt[17];
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 PFN_cuMemGetAddressRange_v3020 g_addr_range = nullptr;
@@ -849,6 +849,27 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
                  (b_3d ? gemm_f16_dev::kOpBox3d : 0u);
     kp.c_tma = c_tma ? 1u : 0u;
     kp.c_stage = c_stage ? 1u : 0u;
+    // Debug bounds check: the byte range each kernel view spans, every problem or
+    // group included.  Value 2 is the checker's own test: each range ends 16
+    // bytes early, so accesses to the last 8 elements are reported (and skipped)
+    // although they are inside the real view.
+    const int64_t dbg = opt(GEMM_F16_OPT_DEBUG_BOUNDS);
+    kp.debug_bounds = dbg > 0 ? 1u : 0u;
+    if (dbg > 0) {
+        auto span = [&](int which, const void* ptr, int64_t rows, int64_t cols, int64_t s_r, int64_t s_c,
+                        int64_t nb, int64_t bs) {
+            int64_t e = 0;
+            if (!view_extent(rows, cols, s_r, s_c, &e)) e = 0;
+            if (nb > 1 && bs > 0 && !batch_extent(e, nb, bs, &e)) e = 0;
+            kp.span_lo[which] = reinterpret_cast<uintptr_t>(ptr);
+            kp.span_hi[which] = kp.span_lo[which] + static_cast<uintptr_t>(2 * e) - (dbg == 2 ? 16u : 0u);
+        };
+        const int64_t nb = (batched || grouped) ? a.batch : 1;
+        span(gemm_f16_dev::kSpanA, kp.A, Mv, a.K, kp.a_sm, kp.a_sk, batched ? nb : 1, a_bs);
+        span(gemm_f16_dev::kSpanB, kp.B, a.K, Nv, kp.b_sk, kp.b_sn, nb, b_bs);
+        if (gated) span(gemm_f16_dev::kSpanBu, kp.Bu, a.K, Nv, kp.b_sk, kp.b_sn, nb, b_bs);
+        span(gemm_f16_dev::kSpanC, kp.C, Mv, Nv, kp.c_sm, kp.c_sn, batched ? nb : 1, c_bs);
+    }
     kp.test_stall = opt(GEMM_F16_OPT_TEST_STALL) == 1 ? 1u : 0u;
     kp.epi_smem = epi > 0 ? 1u : 0u;
     pl->fused = a.fused;
@@ -1280,6 +1301,7 @@ const char* gemm_f16_status_string(int status)
     case GEMM_F16_ERR_OUT_OF_MEMORY: return "GEMM_F16_ERR_OUT_OF_MEMORY";
     case GEMM_F16_ERR_LAUNCH: return "GEMM_F16_ERR_LAUNCH";
     case GEMM_F16_ERR_TIMEOUT: return "GEMM_F16_ERR_TIMEOUT";
+    case GEMM_F16_ERR_BOUNDS: return "GEMM_F16_ERR_BOUNDS";
     default: return "GEMM_F16_UNKNOWN_STATUS";
     }
 }
@@ -1335,7 +1357,8 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
 
 gemm_f16_status gemm_f16_set_option(int option, int64_t value)
 {
-    if (option < 1 || option > 15 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option < 1 || option > 16 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option == GEMM_F16_OPT_DEBUG_BOUNDS && value > 2) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_PDL && value > 1) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_TEST_STALL && value > 1) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_REPACK && value > 2) return GEMM_F16_ERR_INVALID_VALUE;

@@ -93,6 +93,9 @@ constexpr uint32_t kEpiBufBytes = 32 * 64 * 2;           // one warp's 32 x 64 f
 constexpr uint32_t kEpiBytes = 4 * 2 * kEpiBufBytes;     // 4 warps, double-buffered
 constexpr uint32_t kBarrierBytes = 512;
 constexpr int kStatusTimeout = 6;
+constexpr int kStatusBounds = 7;   // debug bounds check: an access was skipped (GEMM_F16_ERR_BOUNDS)
+// Spans of the debug bounds check (KernelParams::span_lo / span_hi).
+enum : int { kSpanA = 0, kSpanB = 1, kSpanBu = 2, kSpanC = 3 };
 
 // Operand flags.  kOpBox3d: an MN-major TMA operand whose MN extent is a
 // multiple of 64 is described as a 3-D tensor (64 MN elements, K, MN / 64
@@ -123,6 +126,12 @@ struct KernelParams {
     // but with a unit column stride: boxes are staged in shared memory as for
     // TMA and written row by row by the warp (stores of contiguous columns).
     uint32_t c_stage;
+    // Debug bounds check (0 off): byte ranges [span_lo, span_hi) of the kernel
+    // views A', B', the up projection and C; every gathered load and every
+    // per-thread store of C is checked against its range, and one that would
+    // leave it is skipped and reported (kStatusBounds).
+    uint32_t debug_bounds;
+    uintptr_t span_lo[4], span_hi[4];
     // Failure-detection test: the MMA issuer first waits on a barrier that
     // nothing arrives on, so the bounded wait runs out, the CTA aborts and the
     // status word reports the timeout (the host reads it; the context stays
@@ -493,14 +502,31 @@ __device__ __forceinline__ uint4 keep_first(uint4 r, int nvalid)
     return make_uint4(k(r.x, 0), k(r.y, 1), k(r.z, 2), k(r.w, 3));
 }
 
+// Debug bounds check of one access of `bytes` at address a against span
+// `which`.  A gathered 16-byte word is read whole to reach the elements inside
+// it, so for a word (`word`) it is enough that it overlaps the span; every
+// other access must lie inside.  Off (the default) it is one uniform test.
+__device__ __forceinline__ bool bounds_ok(const KernelParams& p, int which, uintptr_t a, uint32_t bytes, bool word)
+{
+    if (!p.debug_bounds) return true;
+    const uintptr_t lo = p.span_lo[which], hi = p.span_hi[which];
+    const bool ok = word ? (a < hi && a + bytes > lo) : (a >= lo && a + bytes <= hi);
+    if (!ok && p.status) atomicExch(p.status, kStatusBounds);
+    return ok;
+}
+
 // Eight elements along a non-unit `step` from element offset `off`; the first
 // `nvalid` are loaded one by one, the rest are zero.
-__device__ __forceinline__ uint4 load8_strided(const __half* base, int64_t off, int64_t step, int nvalid)
+__device__ __forceinline__ uint4 load8_strided(const KernelParams& p, int which, const __half* base, int64_t off,
+                                               int64_t step, int nvalid)
 {
     const uint16_t* q = reinterpret_cast<const uint16_t*>(base) + off;
     uint32_t v[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = (e < nvalid) ? static_cast<uint32_t>(ld_nc_u16(q + e * step)) : 0u;
+    for (int e = 0; e < 8; ++e)
+        v[e] = (e < nvalid && bounds_ok(p, which, reinterpret_cast<uintptr_t>(q + e * step), 2, false))
+                   ? static_cast<uint32_t>(ld_nc_u16(q + e * step))
+                   : 0u;
     return make_uint4(v[0] | (v[1] << 16), v[2] | (v[3] << 16), v[4] | (v[5] << 16), v[6] | (v[7] << 16));
 }
 
@@ -575,7 +601,8 @@ __device__ __forceinline__ void shift_store_row(const uint4* wv, uint32_t sh, in
 // Rows each producer thread has in flight (9 loads each) in the unit-stride gather.
 constexpr int kGatherRows = 2;
 
-__device__ __forceinline__ void gather_rows_unit(const __half* base, int64_t s_mn, int64_t s_k, int64_t MN,
+__device__ __forceinline__ void gather_rows_unit(const KernelParams& p, int which, const __half* base,
+                                                 int64_t s_mn, int64_t s_k, int64_t MN,
                                                  int64_t K, int64_t mn0, int64_t k0, int rows_tile, bool mn_major,
                                                  uint32_t dst, int t)
 {
@@ -615,8 +642,9 @@ __device__ __forceinline__ void gather_rows_unit(const __half* base, int64_t s_m
                 const int nw = nv[q] > 0 ? static_cast<int>((sh[q] + 2u * static_cast<uint32_t>(nv[q]) + 15u) / 16u) : 0;
 #pragma unroll
                 for (int i = 0; i < 9; ++i)
-                    wv[q][i] = (i < nw) ? ld_nc_v4(reinterpret_cast<const void*>(a0 + 16u * i))
-                                        : make_uint4(0u, 0u, 0u, 0u);
+                    wv[q][i] = (i < nw && bounds_ok(p, which, a0 + 16u * i, 16, true))
+                                   ? ld_nc_v4(reinterpret_cast<const void*>(a0 + 16u * i))
+                                   : make_uint4(0u, 0u, 0u, 0u);
             }
         }
 #pragma unroll
@@ -627,12 +655,13 @@ __device__ __forceinline__ void gather_rows_unit(const __half* base, int64_t s_m
     }
 }
 
-__device__ __forceinline__ void gather_tile(const __half* base, int64_t s_mn, int64_t s_k,
+__device__ __forceinline__ void gather_tile(const KernelParams& p, int which, const __half* base, int64_t s_mn,
+                                            int64_t s_k,
                                             int64_t MN, int64_t K, int64_t mn0, int64_t k0,
                                             int rows_tile, bool mn_major, uint32_t dst, int t)
 {
     if ((mn_major ? s_mn : s_k) == 1) {
-        gather_rows_unit(base, s_mn, s_k, MN, K, mn0, k0, rows_tile, mn_major, dst, t);
+        gather_rows_unit(p, which, base, s_mn, s_k, MN, K, mn0, k0, rows_tile, mn_major, dst, t);
         return;
     }
     const int chunks = rows_tile * 8;   // 16-byte chunks in the tile
@@ -675,10 +704,11 @@ __device__ __forceinline__ void gather_tile(const __half* base, int64_t s_mn, in
                         sh[i] = static_cast<uint32_t>(a & 15u);
                         const uintptr_t a0 = a - sh[i];
                         const bool two = sh[i] != 0 && sh[i] + 2u * static_cast<uint32_t>(nv[i]) > 16u;
-                        w0[i] = ld_nc_v4(reinterpret_cast<const void*>(a0));
-                        w1[i] = ld_nc_v4(reinterpret_cast<const void*>(two ? a0 + 16 : a0));
+                        if (bounds_ok(p, which, a0, 16, true)) w0[i] = ld_nc_v4(reinterpret_cast<const void*>(a0));
+                        if (two && bounds_ok(p, which, a0 + 16, 16, true))
+                            w1[i] = ld_nc_v4(reinterpret_cast<const void*>(a0 + 16));
                     } else {
-                        w0[i] = load8_strided(base, off, step, nv[i]);
+                        w0[i] = load8_strided(p, which, base, off, step, nv[i]);
                     }
                 }
             }
@@ -713,11 +743,12 @@ __device__ __forceinline__ void store_box_rows(const KernelParams& p, __half* C,
         if (m >= row_lim) break;
         const uint32_t v = ld_smem_u32(buf + r * 128 + ((j ^ (r & 7)) << 4) + (c & 7) * 2);
         uint16_t* q = base + m * p.c_sm;
-        if (in1 && (reinterpret_cast<uintptr_t>(q) & 3u) == 0) {
-            *reinterpret_cast<uint32_t*>(q) = v;
+        const uintptr_t qa = reinterpret_cast<uintptr_t>(q);
+        if (in1 && (qa & 3u) == 0) {
+            if (bounds_ok(p, kSpanC, qa, 4, false)) *reinterpret_cast<uint32_t*>(q) = v;
         } else {
-            if (in0) q[0] = static_cast<uint16_t>(v);
-            if (in1) q[1] = static_cast<uint16_t>(v >> 16);
+            if (in0 && bounds_ok(p, kSpanC, qa, 2, false)) q[0] = static_cast<uint16_t>(v);
+            if (in1 && bounds_ok(p, kSpanC, qa + 2, 2, false)) q[1] = static_cast<uint16_t>(v >> 16);
         }
     }
 }
@@ -740,11 +771,13 @@ __device__ __forceinline__ void store_piece_masked(const KernelParams& p, __half
             const int64_t nn = n + 8 * j;
             uint16_t* q = row + nn;
             if (nn + 8 <= p.N && (reinterpret_cast<uintptr_t>(q) & 15u) == 0) {
-                *reinterpret_cast<uint4*>(q) = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+                if (bounds_ok(p, kSpanC, reinterpret_cast<uintptr_t>(q), 16, false))
+                    *reinterpret_cast<uint4*>(q) = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
             } else {
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
-                    if (nn + e < p.N) q[e] = half_bits(h, 8 * j + e);
+                    if (nn + e < p.N && bounds_ok(p, kSpanC, reinterpret_cast<uintptr_t>(q + e), 2, false))
+                        q[e] = half_bits(h, 8 * j + e);
             }
         }
     } else {
@@ -752,7 +785,7 @@ __device__ __forceinline__ void store_piece_masked(const KernelParams& p, __half
         const int64_t lim = p.N - n;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-            if (c < lim) *q = half_bits(h, c);
+            if (c < lim && bounds_ok(p, kSpanC, reinterpret_cast<uintptr_t>(q), 2, false)) *q = half_bits(h, c);
             q += p.c_sn;
         }
     }
@@ -1417,12 +1450,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                     }
                     if (!kPair && any_masked) {
                         if (!a_tma)
-                            gather_tile(ug.A, p.a_sm, p.a_sk, ug.row_lim, p.K, ug.a_row + m0, k0, kBM, a_mn, sa, t);
+                            gather_tile(p, kSpanA, ug.A, p.a_sm, p.a_sk, ug.row_lim, p.K, ug.a_row + m0, k0, kBM, a_mn,
+                                        sa, t);
                         if (!b_tma) {
                             // (one inlined gather body for both halves of a gated stage)
 #pragma unroll 1
                             for (int hb = 0; hb < (gated ? 2 : 1); ++hb)
-                                gather_tile(hb ? ug.Bu : ug.B, p.b_sn, p.b_sk, p.N, p.K, n0, k0, bcols, b_mn,
+                                gather_tile(p, hb ? kSpanBu : kSpanB, hb ? ug.Bu : ug.B, p.b_sn, p.b_sk, p.N, p.K, n0, k0,
+                                            bcols, b_mn,
                                             sb + hb * bcols * 128, t);
                         }
                     }

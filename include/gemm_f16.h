@@ -60,7 +60,11 @@ typedef enum {
     GEMM_F16_ERR_LAUNCH = 5,
     /* Reported through gemm_f16_device_status(): a kernel gave up on a bounded
        wait (a lost pipeline arrival) and returned early; C is undefined. */
-    GEMM_F16_ERR_TIMEOUT = 6
+    GEMM_F16_ERR_TIMEOUT = 6,
+    /* Reported through gemm_f16_device_status() with GEMM_F16_OPT_DEBUG_BOUNDS on: a
+       gathered load or a per-thread store of C would have left the byte range its
+       view spans and was skipped; C is undefined. */
+    GEMM_F16_ERR_BOUNDS = 7
 } gemm_f16_status;
 
 /*
@@ -348,6 +352,12 @@ gemm_f16_status gemm_f16_fused_get_plan(const void* A, int64_t stride_am, int64_
  *                              of the kernel before it on the stream (its set-up overlaps that
  *                              kernel's tail; it reads and writes memory only after that kernel
  *                              has completed); 1 plain stream order
+ *   GEMM_F16_OPT_DEBUG_BOUNDS  1: every gathered operand load and every per-thread store of C
+ *                              is checked against the byte range its view spans (TMA
+ *                              accesses are bounded by their tensor maps); one that would
+ *                              leave it is skipped and gemm_f16_device_status() reports
+ *                              GEMM_F16_ERR_BOUNDS.  2: the checker's own test, with each
+ *                              range ending 16 bytes early.  0 default (off)
  *   GEMM_F16_OPT_TEST_STALL    failure-detection test: 1 makes every CTA's MMA issuer wait
  *                              first on a barrier that nothing arrives on, so the bounded
  *                              wait runs out (after GEMM_F16_OPT_TIMEOUT_MS), the kernel
@@ -371,7 +381,8 @@ enum {
     GEMM_F16_OPT_MULTICAST = 12,
     GEMM_F16_OPT_REPACK = 13,
     GEMM_F16_OPT_TEST_STALL = 14,
-    GEMM_F16_OPT_PDL = 15
+    GEMM_F16_OPT_PDL = 15,
+    GEMM_F16_OPT_DEBUG_BOUNDS = 16
 };
 gemm_f16_status gemm_f16_set_option(int option, int64_t value);
 
