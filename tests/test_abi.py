@@ -100,3 +100,71 @@ def test_package_has_no_oracle_dependency():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "gemm_oracle" not in text, f
+
+
+# ------------------------------------------------ batched, grouped, fused
+def test_batched_and_grouped_argument_errors():
+    with pytest.raises(g.GemmF16Error) as e:   # batch 0
+        g.gemm_f16_batched(A, 16, 4, 1, B, 16, 4, 1, C, 16, 4, 4, 4, 4, 0)
+    assert e.value.status == g.ERR_INVALID_VALUE
+    with pytest.raises(g.GemmF16Error) as e:   # the problems' outputs overlap (C stride below one view)
+        g.gemm_f16_batched(A, 16, 4, 1, B, 16, 4, 1, C, 8, 4, 4, 4, 4, 2)
+    assert e.value.status == g.ERR_INVALID_VALUE
+    with pytest.raises(g.GemmF16Error) as e:   # a negative group
+        g.gemm_f16_grouped(A, 4, 1, B, 16, 4, 1, C, 4, [3, -1], 4, 4)
+    assert e.value.status == g.ERR_INVALID_VALUE
+    with pytest.raises(g.GemmF16Error) as e:   # more groups than the limit
+        g.gemm_f16_grouped(A, 4, 1, B, 16, 4, 1, C, 4, [1] * (g.MAX_GROUPS + 1), 4, 4)
+    assert e.value.status == g.ERR_INVALID_VALUE
+    # every group empty: nothing to do, no device touched
+    g.gemm_f16_grouped(A, 4, 1, B, 16, 4, 1, C, 4, [0, 0, 0], 4, 4)
+
+
+def test_fused_argument_errors_on_the_host():
+    base = (A, 4, 1, B, 4, 1)
+    with pytest.raises(g.GemmF16Error) as e:   # unknown activation
+        g.gemm_f16_fused(*base, 0, 0, 0, 9, C, 4, 4, 4, 4)
+    assert e.value.status == g.ERR_INVALID_VALUE
+    with pytest.raises(g.GemmF16Error) as e:   # bias_up without an up projection
+        g.gemm_f16_fused(*base, 0, 0, B + (1 << 12), 0, C, 4, 4, 4, 4)
+    assert e.value.status == g.ERR_INVALID_VALUE
+    with pytest.raises(g.GemmF16Error) as e:   # odd up-projection address
+        g.gemm_f16_fused(*base, B + (1 << 12) + 1, 0, 0, 0, C, 4, 4, 4, 4)
+    assert e.value.status == g.ERR_INVALID_VALUE
+    with pytest.raises(g.GemmF16Error) as e:   # C overlaps the bias
+        g.gemm_f16_fused(*base, 0, C + 2, 0, 1, C, 4, 4, 4, 4)
+    assert e.value.status == g.ERR_ALIAS
+    with pytest.raises(g.GemmF16Error) as e:   # C overlaps the up projection
+        g.gemm_f16_fused(*base, C, 0, 0, 1, C, 4, 4, 4, 4)
+    assert e.value.status == g.ERR_ALIAS
+    with pytest.raises(g.GemmF16Error) as e:   # grouped: negative bias stride
+        g.gemm_f16_grouped_fused(A, 4, 1, B, 16, 4, 1, 0, C + (1 << 12), 0, -1, 1, C, 4, [2, 2], 4, 4)
+    assert e.value.status == g.ERR_INVALID_VALUE
+
+
+@pytest.mark.parametrize("option,value", [(0, 0), (99, 0), (g.OPT_STREAMK, 3), (g.OPT_PAIR, 3), (g.OPT_SWAP, 3),
+                                          (g.OPT_TILE_N, 96), (g.OPT_TILE_N, 320), (g.OPT_MAX_STAGES, 1),
+                                          (g.OPT_MULTICAST, 3), (g.OPT_REPACK, 3), (g.OPT_PDL, 2),
+                                          (g.OPT_DEBUG_BOUNDS, 3), (g.OPT_TEST_STALL, 2), (g.OPT_SPLITS, -1)])
+def test_options_reject_values_out_of_range(option, value):
+    with pytest.raises(g.GemmF16Error) as e:
+        g.gemm_f16_set_option(option, value)
+    assert e.value.status == g.ERR_INVALID_VALUE
+
+
+def test_torch_wrappers_check_arguments_before_any_call():
+    import torch
+    a = torch.zeros((4, 8), dtype=torch.float16)
+    b = torch.zeros((8, 6), dtype=torch.float16)
+    with pytest.raises(ValueError):
+        g.fused_mm(a, b, act="tanh")
+    with pytest.raises(ValueError):                       # bias_up needs b_up
+        g.fused_mm(a, b, bias_up=torch.zeros(6, dtype=torch.float16))
+    with pytest.raises(ValueError):                       # b_up must have b's shape and strides
+        g.fused_mm(a, b, b_up=torch.zeros((6, 8), dtype=torch.float16).t())
+    with pytest.raises(ValueError):                       # a bias holds N values
+        g.fused_mm(a, b, bias=torch.zeros(5, dtype=torch.float16))
+    with pytest.raises(ValueError):                       # group rows must add up to a's rows
+        g.grouped_mm(a, torch.zeros((2, 8, 6), dtype=torch.float16), [1, 2])
+    with pytest.raises(ValueError):
+        g.bmm(torch.zeros((2, 4, 8), dtype=torch.float16), torch.zeros((3, 8, 6), dtype=torch.float16))
