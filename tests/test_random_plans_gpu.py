@@ -1,7 +1,8 @@
 """Randomised parity sweep: shapes, operand layouts, entry points (plain,
 fused, grouped, batched) and planner options drawn together from a fixed seed,
 integer inputs in [-2, 2] so every result is exact and compared bit for bit
-with the oracle.  Combinations that no hand-written case names are where plan
+with the oracle; and real-valued inputs, plain and fused, held to the
+tolerance.  Combinations that no hand-written case names are where plan
 interactions hide (a grouped call with K = 1 once reached an unaligned TMA box
 this way)."""
 import numpy as np
@@ -10,7 +11,7 @@ import torch
 
 import dense_tiled_gemm_fp16_gb300 as g
 import oracle
-from tests.parity import oracle_threads
+from tests.parity import assert_close, assert_close_fused, oracle_threads
 
 pytestmark = pytest.mark.gpu
 
@@ -151,3 +152,49 @@ def test_random_plans_bit_exact(seed):
             bad = np.argwhere(got.view(np.uint16) != ref.view(np.uint16))
             raise AssertionError(f"case {i}: {what}, options {opts}: {len(bad)} elements differ, first at "
                                  f"{bad[0].tolist()}")
+
+
+def _real(rng):
+    """Real-valued inputs, uniform [-1, 1] in fp16: every fp32 summation order is
+    a correct result, so the plain product is held to the stated tolerance and
+    the fused stage (every activation, plain and gated) to its propagated one."""
+    M, N, K = (int(x) for x in rng.integers(1, 700, 3))
+    if rng.random() < 0.3:
+        K = int(rng.integers(700, 4000))
+    Ah = rng.uniform(-1, 1, (M, K)).astype(np.float16)
+    Bh = rng.uniform(-1, 1, (K, N)).astype(np.float16)
+    A = _view(rng, Ah, int(rng.integers(0, 5)))
+    B = _view(rng, Bh, int(rng.integers(0, 5)))
+    if rng.random() < 0.4:
+        C = g.matmul(A, B)
+        torch.cuda.synchronize()
+        assert_close(C.cpu().numpy(), oracle.gemm(Ah, Bh, threads=oracle_threads()), K, f"real {M}x{N}x{K}")
+        return f"real {M}x{N}x{K}"
+    act = ("none", "relu", "silu", "gelu")[int(rng.integers(0, 4))]
+    gated = rng.random() < 0.5
+    Uh = rng.uniform(-1, 1, (K, N)).astype(np.float16) if gated else None
+    bh = rng.uniform(-1, 1, N).astype(np.float16) if rng.random() < 0.7 else None
+    buh = rng.uniform(-1, 1, N).astype(np.float16) if gated and rng.random() < 0.7 else None
+    t = lambda x: None if x is None else torch.from_numpy(x).to(DEV)  # noqa: E731
+    U = None
+    if gated:   # the up projection with B's strides
+        U = torch.empty_strided(B.shape, B.stride(), dtype=torch.float16, device=DEV)
+        U.copy_(torch.from_numpy(Uh))
+    C = g.fused_mm(A, B, bias=t(bh), act=act, b_up=U, bias_up=t(buh))
+    torch.cuda.synchronize()
+    ref, gp, u = oracle.gemm_fused(Ah, Bh, Uh, bh, buh, act, threads=oracle_threads(), parts=True)
+    what = f"real fused {M}x{N}x{K} gated={gated} {act}"
+    assert_close_fused(C.cpu().numpy(), ref, K, gp, u, act, what)
+    return what
+
+
+@pytest.mark.parametrize("seed", [201, 202])
+def test_random_plans_real_valued_within_tolerance(seed):
+    rng = np.random.default_rng(seed)
+    for i in range(60):
+        _reset()
+        opts = _options(rng)
+        for o, v in opts.items():
+            g.gemm_f16_set_option(o, v)
+        what = _real(rng)
+        assert g.gemm_f16_device_status() == 0, (i, what, opts)
