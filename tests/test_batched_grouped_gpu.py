@@ -36,7 +36,8 @@ def reals(rng, shape):
 
 
 def dev(x):
-    return torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
+    # (a writable copy: some operands are read-only broadcast views)
+    return torch.from_numpy(np.array(x, order="C", copy=True)).to(DEV)
 
 
 # ------------------------------------------------------------------ batched
