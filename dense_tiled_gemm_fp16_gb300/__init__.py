@@ -38,6 +38,9 @@ STATUS = {
 (OK, ERR_INVALID_VALUE, ERR_ALIAS, ERR_UNSUPPORTED_DEVICE, ERR_OUT_OF_MEMORY, ERR_LAUNCH, ERR_TIMEOUT,
  ERR_BOUNDS) = range(8)
 
+# Largest M, N or K of a call (GEMM_F16_MAX_DIM: 32-bit copy coordinates).
+MAX_DIM = 2**31 - 2**16
+
 OPT_FORCE_GATHER = 1
 OPT_SPLITS = 2
 OPT_TILE_N = 3

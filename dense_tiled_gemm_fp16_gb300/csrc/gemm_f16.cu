@@ -194,6 +194,10 @@ gemm_f16_status validate(const Args& a, bool check_memory, DevInfo** dev)
 {
     if (!a.A || !a.B || !a.C) return GEMM_F16_ERR_INVALID_VALUE;
     if (a.M <= 0 || a.N <= 0 || a.K <= 0) return GEMM_F16_ERR_INVALID_VALUE;
+    // TMA copy coordinates and the kernel's K-loop coordinates are 32-bit, so
+    // each dimension (a grouped call's total rows included) stays below 2^31
+    // with room for one tile past the end; element offsets stay 64-bit.
+    if (a.M > GEMM_F16_MAX_DIM || a.N > GEMM_F16_MAX_DIM || a.K > GEMM_F16_MAX_DIM) return GEMM_F16_ERR_INVALID_VALUE;
     if (a.sam <= 0 || a.sak <= 0 || a.sbk <= 0 || a.sbn <= 0 || a.ldc < a.N) return GEMM_F16_ERR_INVALID_VALUE;
     if ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.B) | reinterpret_cast<uintptr_t>(a.C)) & 1u)
         return GEMM_F16_ERR_INVALID_VALUE;

@@ -42,9 +42,14 @@ extern "C" {
 
 #define GEMM_F16_ABI_VERSION 1
 
+/* Largest M, N or K (and total rows of a grouped call): 2^31 - 2^16.  The
+   copies' tile coordinates are 32-bit; element offsets are 64-bit and may
+   exceed 2^32 freely. */
+#define GEMM_F16_MAX_DIM ((int64_t)2147418112)
+
 typedef enum {
     GEMM_F16_OK = 0,
-    /* A null pointer, M/N/K <= 0, a stride <= 0, ldc < N, an fp16 pointer that
+    /* A null pointer, M/N/K <= 0 or > GEMM_F16_MAX_DIM, a stride <= 0, ldc < N, an fp16 pointer that
        is not 2-byte aligned, a size whose extent overflows int64, a pointer
        that is not device (or managed) memory of the current device, or a view
        that runs past the end of the allocation it points into. */
@@ -77,7 +82,8 @@ typedef enum {
  *   C        device pointer; element (m,n) is written at C + m*ldc + n.
  *            Elements of C outside the M x N view (the pitch padding between
  *            N and ldc) are never written.
- *   M, N, K  sizes, all > 0.  Any value; nothing needs to be a tile multiple.
+ *   M, N, K  sizes, 0 < size <= GEMM_F16_MAX_DIM; nothing needs to be a tile
+ *            multiple.
  *
  * Any positive strides are accepted (row-major, column-major / transposed
  * views, pitched slices, non-unit inner strides).  Alignment is not required:

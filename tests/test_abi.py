@@ -50,10 +50,32 @@ A, B, C = 1 << 20, 1 << 24, 1 << 28
     (A, 4, 1, B, 4, 1, C, 3, 4, 4, 4),        # ldc < N
     (A + 1, 4, 1, B, 4, 1, C, 4, 4, 4, 4),    # fp16 pointer not 2-byte aligned
     (A, 1 << 62, 1, B, 4, 1, C, 4, 4, 4, 4),  # extent overflows int64
+    (A, 1 << 31, 1, B, 1, 1, C, 1, 1, 1, 1 << 31),            # K beyond the 32-bit copy coordinates
+    (A, 1, 1, B, 1, 1, C, 1, g.MAX_DIM + 1, 1, 1),            # M one past the limit
+    (A, 1, 1, B, 1, 1, C, g.MAX_DIM + 1, 1, g.MAX_DIM + 1, 1),  # N one past the limit
 ])
 def test_invalid_arguments(args):
     with pytest.raises(g.GemmF16Error) as e:
         g.gemm_f16(*args)
+    assert e.value.status == g.ERR_INVALID_VALUE
+
+
+def test_largest_dimension_passes_validation():
+    # M = N = 1, K at the limit: validation accepts it and, without a GB300,
+    # the call stops at the device check
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    a, b, c = 1 << 20, 1 << 40, 1 << 44   # fake pointers whose 4 GB views do not overlap
+    with pytest.raises(g.GemmF16Error) as e:
+        g.gemm_f16(a, g.MAX_DIM, 1, b, 1, 1, c, 1, 1, 1, g.MAX_DIM)
+    assert e.value.status == g.ERR_UNSUPPORTED_DEVICE
+
+
+def test_grouped_total_rows_beyond_the_limit():
+    half = g.MAX_DIM // 2 + 1
+    with pytest.raises(g.GemmF16Error) as e:
+        g.gemm_f16_grouped(A, 4, 1, B, 16, 4, 1, C, 4, [half, half], 4, 4)
     assert e.value.status == g.ERR_INVALID_VALUE
 
 
