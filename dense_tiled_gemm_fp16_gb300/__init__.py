@@ -262,6 +262,24 @@ def gemm_f16_abi_version() -> int:
 
 
 # ------------------------------------------------------------ torch helpers
+def _check_tensors(*ts):
+    """Every given tensor (None entries skipped) is float16 and all sit on one
+    CUDA device: the library reads raw fp16 device memory, so anything else
+    would be misread rather than refused."""
+    import torch
+
+    ts = [t for t in ts if t is not None]
+    if any(t.dtype != torch.float16 for t in ts):
+        raise TypeError("gemm_f16 takes float16 tensors")
+    if not all(t.is_cuda for t in ts) or len({t.device for t in ts}) > 1:
+        raise ValueError("tensors must share one CUDA device")
+
+
+def _check_out(out, shape, what):
+    if out is not None and (tuple(out.shape) != tuple(shape) or out.stride(-1) != 1):
+        raise ValueError(f"out must be {what} with a unit column stride")
+
+
 def _args(a, b, out):
     if a.dim() != 2 or b.dim() != 2:
         raise ValueError("expected two matrices")
@@ -279,10 +297,10 @@ def matmul(a, b, out=None, stream=None):
     """fp16 C = a @ b for CUDA torch tensors (any positive strides); returns C."""
     import torch
 
-    if a.dtype != torch.float16 or b.dtype != torch.float16:
-        raise TypeError("gemm_f16 takes float16 tensors")
-    if not a.is_cuda or not b.is_cuda or a.device != b.device:
-        raise ValueError("inputs must share one CUDA device")
+    if a.dim() != 2 or b.dim() != 2:
+        raise ValueError("expected two matrices")
+    _check_out(out, (a.shape[0], b.shape[1]), "[M, N]")
+    _check_tensors(a, b, out)
     if out is None:
         out = torch.empty((a.shape[0], b.shape[1]), dtype=torch.float16, device=a.device)
     args = _args(a, b, out)
@@ -299,10 +317,10 @@ def bmm(a, b, out=None, stream=None):
 
     if a.dim() != 3 or b.dim() != 3 or a.shape[0] != b.shape[0] or a.shape[2] != b.shape[1]:
         raise ValueError("bmm takes [batch, M, K] and [batch, K, N]")
+    _check_out(out, (a.shape[0], a.shape[1], b.shape[2]), "[batch, M, N]")
+    _check_tensors(a, b, out)
     if out is None:
         out = torch.empty((a.shape[0], a.shape[1], b.shape[2]), dtype=torch.float16, device=a.device)
-    if out.stride(2) != 1:
-        raise ValueError("out must have a unit column stride")
     with torch.cuda.device(a.device):
         s = stream if stream is not None else torch.cuda.current_stream(a.device)
         gemm_f16_batched(a.data_ptr(), a.stride(0), a.stride(1), a.stride(2), b.data_ptr(), b.stride(0),
@@ -320,10 +338,10 @@ def grouped_mm(a, b, group_rows, out=None, stream=None):
         raise ValueError("grouped_mm takes [rows, K], [G, K, N] and G row counts")
     if sum(int(r) for r in group_rows) != a.shape[0]:
         raise ValueError("group_rows must add up to a's rows")
+    _check_out(out, (a.shape[0], b.shape[2]), "[rows, N]")
+    _check_tensors(a, b, out)
     if out is None:
         out = torch.empty((a.shape[0], b.shape[2]), dtype=torch.float16, device=a.device)
-    if out.stride(1) != 1:
-        raise ValueError("out must have a unit column stride")
     with torch.cuda.device(a.device):
         s = stream if stream is not None else torch.cuda.current_stream(a.device)
         gemm_f16_grouped(a.data_ptr(), a.stride(0), a.stride(1), b.data_ptr(), b.stride(0), b.stride(1),
@@ -380,21 +398,23 @@ def fused_mm(a, b, bias=None, act="none", b_up=None, bias_up=None, out=None, str
         raise ValueError("fused_mm takes two matrices or two batches of matrices")
     code = _act(act)
     if a.dim() == 2:
+        _check_out(out, (a.shape[0], b.shape[1]), "[M, N]")
+        bu, bp, bup, _ = _epilogue_args(b, b_up, bias, bias_up, 1, b.shape[1])
+        _check_tensors(a, b, out, b_up, bias, bias_up)
         if out is None:
             out = torch.empty((a.shape[0], b.shape[1]), dtype=torch.float16, device=a.device)
         args = _args(a, b, out)
-        bu, bp, bup, _ = _epilogue_args(b, b_up, bias, bias_up, 1, b.shape[1])
         with torch.cuda.device(a.device):
             s = stream if stream is not None else torch.cuda.current_stream(a.device)
             gemm_f16_fused(*args[:6], bu, bp, bup, code, *args[6:], stream=s.cuda_stream)
         return out
     if a.shape[0] != b.shape[0] or a.shape[2] != b.shape[1]:
         raise ValueError("fused_mm takes [batch, M, K] and [batch, K, N]")
+    _check_out(out, (a.shape[0], a.shape[1], b.shape[2]), "[batch, M, N]")
+    bu, bp, bup, sbias = _epilogue_args(b, b_up, bias, bias_up, a.shape[0], b.shape[2])
+    _check_tensors(a, b, out, b_up, bias, bias_up)
     if out is None:
         out = torch.empty((a.shape[0], a.shape[1], b.shape[2]), dtype=torch.float16, device=a.device)
-    if out.stride(2) != 1:
-        raise ValueError("out must have a unit column stride")
-    bu, bp, bup, sbias = _epilogue_args(b, b_up, bias, bias_up, a.shape[0], b.shape[2])
     with torch.cuda.device(a.device):
         s = stream if stream is not None else torch.cuda.current_stream(a.device)
         gemm_f16_batched_fused(a.data_ptr(), a.stride(0), a.stride(1), a.stride(2), b.data_ptr(), b.stride(0),
@@ -414,15 +434,16 @@ def grouped_fused_mm(a, b, group_rows, bias=None, act="none", b_up=None, bias_up
         raise ValueError("grouped_fused_mm takes [rows, K], [G, K, N] and G row counts")
     if sum(int(r) for r in group_rows) != a.shape[0]:
         raise ValueError("group_rows must add up to a's rows")
+    code = _act(act)
+    _check_out(out, (a.shape[0], b.shape[2]), "[rows, N]")
+    bu, bp, bup, sbias = _epilogue_args(b, b_up, bias, bias_up, b.shape[0], b.shape[2])
+    _check_tensors(a, b, out, b_up, bias, bias_up)
     if out is None:
         out = torch.empty((a.shape[0], b.shape[2]), dtype=torch.float16, device=a.device)
-    if out.stride(1) != 1:
-        raise ValueError("out must have a unit column stride")
-    bu, bp, bup, sbias = _epilogue_args(b, b_up, bias, bias_up, b.shape[0], b.shape[2])
     with torch.cuda.device(a.device):
         s = stream if stream is not None else torch.cuda.current_stream(a.device)
         gemm_f16_grouped_fused(a.data_ptr(), a.stride(0), a.stride(1), b.data_ptr(), b.stride(0), b.stride(1),
-                               b.stride(2), bu, bp, bup, sbias, _act(act), out.data_ptr(), out.stride(0), group_rows,
+                               b.stride(2), bu, bp, bup, sbias, code, out.data_ptr(), out.stride(0), group_rows,
                                b.shape[2], a.shape[1], stream=s.cuda_stream)
     return out
 
@@ -431,9 +452,12 @@ def fused_plan_for(a, b, out, bias=None, act="none", b_up=None, bias_up=None) ->
     """The execution plan fused_mm would use for these 2-D torch tensors."""
     args = _args(a, b, out)
     bu, bp, bup, _ = _epilogue_args(b, b_up, bias, bias_up, 1, b.shape[1])
+    _check_tensors(a, b, out, b_up, bias, bias_up)
     return gemm_f16_fused_get_plan(*args[:6], bu, bp, bup, _act(act), *args[6:])
 
 
 def plan_for(a, b, out) -> dict:
     """The execution plan gemm_f16 would use for these torch tensors."""
-    return gemm_f16_get_plan(*_args(a, b, out))
+    args = _args(a, b, out)
+    _check_tensors(a, b, out)
+    return gemm_f16_get_plan(*args)

@@ -190,3 +190,39 @@ def test_torch_wrappers_check_arguments_before_any_call():
         g.grouped_mm(a, torch.zeros((2, 8, 6), dtype=torch.float16), [1, 2])
     with pytest.raises(ValueError):
         g.bmm(torch.zeros((2, 4, 8), dtype=torch.float16), torch.zeros((3, 8, 6), dtype=torch.float16))
+
+
+def test_torch_wrappers_refuse_other_dtypes_shapes_and_devices():
+    # The library reads raw fp16 device memory: a float32 tensor, an output of
+    # the wrong shape or a host tensor is refused before any call.
+    import torch
+    h = torch.float16
+    a, b = torch.zeros((4, 8), dtype=h), torch.zeros((8, 6), dtype=h)
+    with pytest.raises(TypeError):
+        g.matmul(a.float(), b)
+    with pytest.raises(TypeError):                        # out of another dtype
+        g.matmul(a, b, out=torch.zeros((4, 6)))
+    with pytest.raises(ValueError):                       # out of another shape
+        g.matmul(a, b, out=torch.zeros((4, 7), dtype=h))
+    with pytest.raises(ValueError):                       # host tensors
+        g.matmul(a, b)
+    a3, b3 = torch.zeros((2, 4, 8), dtype=h), torch.zeros((2, 8, 6), dtype=h)
+    with pytest.raises(ValueError):
+        g.bmm(a3, b3, out=torch.zeros((2, 4, 5), dtype=h))
+    with pytest.raises(TypeError):
+        g.bmm(a3, b3.float())
+    with pytest.raises(ValueError):
+        g.fused_mm(a3, b3, out=torch.zeros((1, 4, 6), dtype=h))
+    with pytest.raises(TypeError):
+        g.fused_mm(a, b, out=torch.zeros((4, 6)))
+    bg = torch.zeros((2, 8, 6), dtype=h)
+    with pytest.raises(ValueError):
+        g.grouped_mm(a, bg, [1, 3], out=torch.zeros((4, 7), dtype=h))
+    with pytest.raises(TypeError):
+        g.grouped_mm(a.float(), bg, [1, 3])
+    with pytest.raises(ValueError):
+        g.grouped_fused_mm(a, bg, [1, 3], act="tanh")
+    with pytest.raises(ValueError):
+        g.grouped_fused_mm(a, bg, [1, 3], out=torch.zeros((3, 6), dtype=h))
+    with pytest.raises(ValueError):                       # host tensors
+        g.grouped_fused_mm(a, bg, [1, 3])
