@@ -103,6 +103,14 @@ typedef enum {
  * must use gemm_f16_ws() with separate workspaces (which never copies operands:
  * it gathers them).
  *
+ * Stream capture: a captured call records the workspace buffers current at
+ * capture time.  Growing a buffer synchronises the device and cannot happen
+ * inside a capture, so make one uncaptured call of the same shape first; and
+ * since growth frees the old buffer, a later uncaptured call that needs more
+ * workspace invalidates graphs that hold the old one.  Captured calls that
+ * must stay replayable regardless should use gemm_f16_ws() (caller-owned
+ * workspace) or gemm_f16_noalloc().
+ *
  * Errors: argument errors are returned before any device work is queued;
  * launch errors after.  A device-side bounded-wait expiry does not show here:
  * see gemm_f16_device_status().
