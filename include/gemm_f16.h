@@ -59,7 +59,8 @@ typedef enum {
     /* The current device is not compute capability 10.3 (GB300). */
     GEMM_F16_ERR_UNSUPPORTED_DEVICE = 3,
     /* The split-K workspace could not be allocated, or the caller-supplied
-       workspace is smaller than gemm_f16_workspace_size() reports. */
+       workspace is smaller than gemm_f16_workspace_size() reports or not
+       256-byte aligned. */
     GEMM_F16_ERR_OUT_OF_MEMORY = 4,
     /* A CUDA runtime/driver call failed while setting up or launching. */
     GEMM_F16_ERR_LAUNCH = 5,
@@ -122,7 +123,8 @@ gemm_f16_status gemm_f16(const void* A, int64_t stride_am, int64_t stride_ak,
 
 /*
  * Same as gemm_f16() with a caller-owned workspace: device memory of at least
- * gemm_f16_workspace_size() bytes, 256-byte aligned, any contents.  When the
+ * gemm_f16_workspace_size() bytes, 256-byte aligned (else
+ * GEMM_F16_ERR_OUT_OF_MEMORY), any contents.  When the
  * call uses split-K it first clears the workspace's counter block with
  * cudaMemsetAsync on `stream`, then the kernel writes fp32 partial sums into
  * the rest.  `workspace` may be NULL when the size query returns 0.  Calls
