@@ -26,6 +26,36 @@ def test_library_exports_every_declared_symbol():
         assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
 
 
+def header_constants():
+    """NAME -> value for every enum member and integer #define of the header."""
+    src = open(os.path.join(ROOT, "include", "gemm_f16.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    out = {}
+    for body in re.findall(r"enum\s*\{(.*?)\}", src, flags=re.S):
+        for name, val in re.findall(r"(GEMM_F16_\w+)\s*=\s*(\d+)", body):
+            out[name] = int(val)
+    for name, expr in re.findall(r"#define\s+(GEMM_F16_\w+)\s+(.+)", src):
+        expr = re.sub(r"\((?:int64_t|size_t)\)", "", expr).strip()
+        if re.fullmatch(r"[\d\s()<]+", expr):
+            out[name] = eval(expr)   # digits, parentheses and shifts only
+    return out
+
+
+def test_binding_constants_match_the_header():
+    h = header_constants()
+    prefix = "GEMM_F16_"
+    for name, value in h.items():
+        short = name[len(prefix):]
+        if short.startswith(("OPT_", "ACT_", "ERR_")) or short == "OK":
+            assert getattr(g, short) == value, name
+    assert {v: k for k, v in h.items() if k.startswith(prefix + "ERR_") or k == prefix + "OK"} == g.STATUS
+    assert g.MAX_DIM == h["GEMM_F16_MAX_DIM"]
+    assert g.MAX_GROUPS == h["GEMM_F16_MAX_GROUPS"]
+    assert g.NOALLOC_SCRATCH_BYTES == h["GEMM_F16_NOALLOC_SCRATCH_BYTES"]
+    assert g.gemm_f16_abi_version() == h["GEMM_F16_ABI_VERSION"]
+    assert len([k for k in h if k.startswith(prefix + "OPT_")]) == 16
+
+
 def test_status_strings_and_version():
     assert g.gemm_f16_abi_version() == 1
     for code, name in g.STATUS.items():
