@@ -1,0 +1,102 @@
+"""Host-side checks of the measurement plumbing in bench.py: the source hash
+that ties a committed ncu summary to the kernel it was taken on, the traffic
+lookup, the clock-sample parser and the peak table fallback."""
+import os
+import shutil
+
+import pytest
+
+import bench
+
+SOURCES = ("ptx.cuh", "gemm_kernel.cuh", "gemm_f16.cu", "repack.cuh")
+
+
+@pytest.fixture
+def tree(tmp_path, monkeypatch):
+    """A copy of the kernel sources under a scratch root that bench.py reads."""
+    src = os.path.join(bench.ROOT, "dense_tiled_gemm_fp16_gb300", "csrc")
+    dst = tmp_path / "dense_tiled_gemm_fp16_gb300" / "csrc"
+    dst.mkdir(parents=True)
+    for f in SOURCES:
+        shutil.copy(os.path.join(src, f), dst / f)
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    return tmp_path
+
+
+def test_source_hash_ignores_comments_and_spacing(tree):
+    h0 = bench.kernel_source_hash()
+    k = tree / "dense_tiled_gemm_fp16_gb300" / "csrc" / "gemm_kernel.cuh"
+    text = k.read_text()
+    k.write_text("// a new comment\n/* and a\n block */\n" + text.replace("\n", "\n\n", 3))
+    assert bench.kernel_source_hash() == h0
+    k.write_text(text.replace("kBK = 64", "kBK = 32", 1))
+    assert bench.kernel_source_hash() != h0
+
+
+def _summary(tree, workload, digest, nbytes):
+    (tree / "profiles" / f"gemm_f16_persistent__{workload}.md").write_text(
+        f"# summary\n\n```\nkernel: gemm_f16_persistent\nworkload: {workload}\n"
+        f"kernel_source_sha256_16: {digest}\ndram_bytes_per_launch: {nbytes}\n```\n")
+
+
+def test_traffic_only_from_a_summary_of_the_same_sources(tree):
+    assert bench.profiled_traffic("square_4096") is None            # no summary
+    _summary(tree, "square_4096", bench.kernel_source_hash(), 123456)
+    assert bench.profiled_traffic("square_4096") == 123456
+    _summary(tree, "square_4096", "0" * 16, 123456)                 # other sources
+    assert bench.profiled_traffic("square_4096") is None
+
+
+def test_committed_summaries_are_well_formed():
+    # every committed summary names its kernel and workload, the sources' hash
+    # and a positive byte count, and gives the ncu command that made it, with
+    # the clocks left alone
+    import re
+    d = os.path.join(bench.ROOT, "profiles")
+    names = [f for f in os.listdir(d) if f.startswith("gemm_f16_persistent__")]
+    assert names
+    for f in names:
+        text = open(os.path.join(d, f)).read()
+        workload = f[len("gemm_f16_persistent__"):-len(".md")]
+        assert f"workload: {workload}" in text, f
+        assert re.search(r"kernel_source_sha256_16: [0-9a-f]{16}\b", text), f
+        assert int(re.search(r"dram_bytes_per_launch: (\d+)", text).group(1)) > 0, f
+        cmds = [line for line in text.splitlines() if line.startswith("ncu ")]
+        assert cmds and all("--clock-control none" in c for c in cmds), f
+
+
+class _Done:
+    def terminate(self):
+        pass
+
+    def wait(self, timeout=None):
+        return 0
+
+
+def test_clock_samples_are_parsed_per_gpu(tmp_path):
+    rows = [
+        "0, GPU-a, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, GPU-a, 1950, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, GPU-a, 300, 2070, 90.0, 0x0, Not Active, Not Active, Not Active, Not Active",   # idle sample
+        "1, GPU-b, 1000, 2070, 1400.0, 0x40, Active, Not Active, Not Active, Not Active",   # another GPU
+        "garbage line",
+    ]
+    path = tmp_path / "clocks.csv"
+    path.write_text("\n".join(rows) + "\n")
+    s = bench.ClockSampler("GPU-a")
+    s.proc, s.path = _Done(), str(path)
+    c = s.stop()
+    assert c["samples"] == 3
+    assert c["sm_max_mhz"] == 2070.0
+    assert c["sm_mhz"] == pytest.approx((2070 + 1950) / 2)      # median of the loaded samples
+    assert c["reasons"] == ["sw_power_cap"]                        # GPU-b's hw_slowdown is not ours
+    assert not path.exists()
+
+
+def test_peaks_fall_back_when_no_measurement_is_present(tree):
+    p = bench.load_peaks()
+    assert p["source"] == "fallback" and p["tflops"] > 0 and p["hbm_gbs"] > 0
+    (tree / "MEASURED_PEAKS.json").write_text('{"hbm_gbs": 6782.8, "bf16_tflops": 1905.4}')
+    p = bench.load_peaks()
+    assert p["source"] == "measured" and p["tflops"] == 1905.4 and p["tflops_sustained"] == 1905.4
