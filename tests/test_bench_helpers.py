@@ -100,3 +100,27 @@ def test_peaks_fall_back_when_no_measurement_is_present(tree):
     (tree / "MEASURED_PEAKS.json").write_text('{"hbm_gbs": 6782.8, "bf16_tflops": 1905.4}')
     p = bench.load_peaks()
     assert p["source"] == "measured" and p["tflops"] == 1905.4 and p["tflops_sustained"] == 1905.4
+
+
+def test_whole_job_rate_counts_every_replica():
+    # 3 steps of 2e9 FLOPs on each of 4 replicas in 6 ms (the slowest rank)
+    assert bench.whole_job_rate(2e9, 3, 4, 6.0) == pytest.approx(2e9 * 3 * 4 / 6e-3)
+
+
+def test_cpu_baseline_runs_the_oracle_on_the_workload_itself():
+    # the slab the CPU baseline times is the workload's own product: on the
+    # small tail case the slab covers every row and equals the oracle's C
+    import numpy as np
+
+    import oracle
+    from synth import workloads
+
+    oracle.build()
+    for name in ("tail_130x70x65_b_rowmajor", "tail_130x70x65_b_transposed"):
+        w = workloads.BY_NAME[name]
+        run, flops = bench.oracle_slab(w, w.M, threads=1)
+        assert flops == 2.0 * w.M * w.N * w.K
+        want = oracle.gemm(np.ascontiguousarray(w.A.host_view()), w.B.host_view())
+        assert np.array_equal(run().view(np.uint16), want.view(np.uint16)), name
+        rate, rows, dt, reps = bench.cpu_oracle_rate(w, 0.05, threads=1)
+        assert rows == w.M and reps >= 1 and dt > 0 and rate > 0
