@@ -256,3 +256,13 @@ def test_torch_wrappers_refuse_other_dtypes_shapes_and_devices():
         g.grouped_fused_mm(a, bg, [1, 3], out=torch.zeros((3, 6), dtype=h))
     with pytest.raises(ValueError):                       # host tensors
         g.grouped_fused_mm(a, bg, [1, 3])
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    # no fallback of any kind: without the built library every call raises
+    monkeypatch.setattr(g, "_lib", None)
+    monkeypatch.setattr(g, "LIB_PATH", str(tmp_path / "libgemm_f16.so"))
+    with pytest.raises(g.GemmF16Error, match="not built"):
+        g.lib()
+    with pytest.raises(g.GemmF16Error):
+        g.gemm_f16(A, 4, 1, B, 4, 1, C, 4, 4, 4, 4)
