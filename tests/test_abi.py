@@ -266,3 +266,34 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
         g.lib()
     with pytest.raises(g.GemmF16Error):
         g.gemm_f16(A, 4, 1, B, 4, 1, C, 4, 4, 4, 4)
+
+
+def test_plain_c_program_links_and_calls_the_library(tmp_path):
+    # The boundary is a C ABI: a C11 program that includes the header, takes
+    # the address of every declared function and calls the host-only ones
+    # compiles, links against the library and runs without a GPU.
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    if cc is None or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
+        pytest.skip("no C compiler or CUDA headers")
+    g.lib()   # built
+    names = header_functions()
+    src = tmp_path / "use.c"
+    src.write_text(
+        "#include <stdio.h>\n#include \"gemm_f16.h\"\n"
+        "int main(void) {\n"
+        "    const void* fns[] = {" + ", ".join(f"(const void*){n}" for n in names) + "};\n"
+        "    size_t i, live = 0;\n"
+        "    for (i = 0; i < sizeof fns / sizeof fns[0]; ++i) live += fns[i] != 0;\n"
+        "    printf(\"%zu %d %s\\n\", live, gemm_f16_abi_version(), gemm_f16_status_string(GEMM_F16_ERR_ALIAS));\n"
+        "    return 0;\n}\n")
+    exe = tmp_path / "use"
+    libdir = os.path.dirname(g.LIB_PATH)
+    subprocess.run([cc, "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    "-I", cuda_inc, str(src), "-L", libdir, "-lgemm_f16",
+                    "-Wl,-rpath," + libdir, "-o", str(exe)], check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    assert out == [str(len(names)), "1", "GEMM_F16_ERR_ALIAS"]
