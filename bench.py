@@ -2,15 +2,16 @@
 """Benchmark of the sm_103a fp16 GEMM (one JSON line on stdout).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--no-cpu-baseline]
+                  [--workload NAME] [--no-cpu-baseline] [--cpu-threads T]
 
-A step is one C = A*B of the workload (default: the square 4096^3 case, fp16
-inputs, fp32 accumulation, fp16 output) on inputs already resident in device
-memory.  When the inputs fit in L2, L2 is flushed (a 512 MiB write) between
-steps and each timed step is bracketed by its own CUDA events on the launching
-stream, the flush outside them; when they do not, the K steps run back to back
-as one replay of a CUDA graph of K calls, timed by two events around it.  `value` is
-TFLOP/s of useful 2MNK work over all ranks.  `e2e` repeats the measurement
+A step is one C = A*B of the workload (default: the MoE-flattened
+131072 x 2048 x 7168 case of the C500 review, fp16 inputs, fp32 accumulation,
+fp16 output) on inputs already resident in device memory.  L2 is flushed (a
+512 MiB write) before every timed step and each step is bracketed by its own
+CUDA events on the launching stream, the flush outside them.  `value` is
+TFLOP/s of useful 2MNK work over all ranks.  `back_to_back` repeats the timing
+with the steps run back to back (one replay of a CUDA graph of K calls, two
+events around it, no flush): the warm figure of a serving loop.  `e2e` repeats the measurement
 through the torch-level API with every step's inputs copied in from pinned host
 memory and its result copied out inside the timed region, pipelined as a
 serving loop runs it (two device slots; the copy-in of step i+1 and the
@@ -162,12 +163,11 @@ def timed_steps(torch, dev, stream, steps, flush, step, graph_step, barrier):
     """Device time of `steps` steps on `stream` (ms), bracketed by a barrier
     and a synchronize on both sides; returns (total ms, wall seconds, timing note).
 
-    With an L2 flush (inputs that fit in L2) every step is bracketed by its own
-    CUDA events and the flush runs between them, outside.  Without one (inputs
-    larger than L2) the steps run back to back: they are captured once as a
-    CUDA graph of `steps` calls (graph_step(s) enqueues one step on stream s)
-    and timed by two events around its replay, as a serving loop would run
-    them."""
+    With an L2 flush buffer every step is bracketed by its own CUDA events and
+    the flush runs between them, outside.  Without one the steps run back to
+    back: they are captured once as a CUDA graph of `steps` calls (graph_step(s)
+    enqueues one step on stream s) and timed by two events around its replay,
+    as a serving loop would run them."""
     if flush is None:
         graph = torch.cuda.CUDAGraph()
         cap = torch.cuda.Stream(dev)
@@ -242,7 +242,8 @@ def oracle_slab(w, rows: int, threads: int, fused=None):
 
 def cpu_oracle_rate(w, target_s: float, threads: int, fused=None):
     """Time the CPU oracle on a slab of output rows (repeated when the whole
-    problem takes less than the target); returns (TFLOP/s, rows, seconds, reps)."""
+    problem takes less than the target); returns (TFLOP/s, rows, seconds, reps).
+    The whole problem's time follows by linear extrapolation over the rows."""
     def slab(rows, reps=1):
         run, flops = oracle_slab(w, rows, threads, fused)
         t = time.perf_counter()
@@ -260,6 +261,66 @@ def cpu_oracle_rate(w, target_s: float, threads: int, fused=None):
     reps = max(1, min(100, int(target_s * rate / rows))) if rows == w.M else 1
     dt, flops = slab(rows, reps)
     return flops / dt / 1e12, rows, dt, reps
+
+
+def back_to_back(torch, dev, stream, steps, step, graph_step, barrier, pg, flops, nbytes, world):
+    """The warm figure: the same steps run back to back without a flush, as
+    one replay of a CUDA graph of `steps` calls timed by two events."""
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(dev)
+    local_ms, _, note = timed_steps(torch, dev, stream, steps, None, step, graph_step, barrier)
+    total_ms = max_over_ranks(pg, local_ms, dev)
+    ms = total_ms / steps
+    return {"value": round(whole_job_rate(flops, steps, world, total_ms) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 5), "hbm_gbs_min_traffic": round(nbytes / (ms * 1e-3) / 1e9, 1),
+            "timing": note + ", no flush (L2 warm)"}
+
+
+def roofline(bnd, flops, nbytes, ms_per_step, peaks, workload):
+    """The dominant kernel against the measured peak: tensor-bound shapes in
+    TFLOP/s against the bf16 burst peak (the kernel is timed alone, one call
+    per step; the fraction of the sustained peak is given beside it),
+    HBM-bound shapes in GB/s of algorithmic bytes against the copy bandwidth."""
+    if bnd == "tensor":
+        achieved = flops / (ms_per_step * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["tflops"], 4), "peak_kind": "burst",
+                "frac_of_sustained": round(achieved / peaks["tflops_sustained"], 4),
+                "peak_sustained": peaks["tflops_sustained"]}
+    else:
+        achieved = nbytes / (ms_per_step * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_kind": "copy bandwidth"}
+    roof["traffic"] = profiled_traffic(workload)
+    roof["peak_source"] = (f"{peaks['source']} (MEASURED_PEAKS.json: bf16 burst and sustained GEMM, "
+                           "copy bandwidth)")
+    roof["kernel"] = "gemm_f16_persistent"
+    return roof
+
+
+# Workloads small enough that a single-thread oracle run is also reported.
+SINGLE_THREAD_CPU = ("tail_130x70x65_b_rowmajor", "tail_130x70x65_b_transposed", "decode_m16_n16384_k8192")
+
+
+def cpu_baseline(w, seconds, threads, fused=None, label="oracle", name=None):
+    """The CPU oracle, as it stands, on a slab of output rows with `threads`
+    threads; the whole workload's time is extrapolated linearly over its rows.
+    For the small workloads a single-thread run is reported beside it."""
+    rate, r, dt, reps = cpu_oracle_rate(w, seconds, threads, fused)
+    full_flops = 2.0 * w.M * w.N * w.K * (2 if fused is not None and fused[0] is not None else 1)
+    out = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+           "sample": f"{label}: {r} of {w.M} output rows x all {w.N} columns, K={w.K}"
+                     f"{f', {reps} times' if reps > 1 else ''} ({dt:.1f} s)",
+           "full_workload_s": round(full_flops / (rate * 1e12), 3),
+           "full_workload_s_kind": "measured" if r == w.M else "extrapolated from the slab"}
+    if (name or w.name) in SINGLE_THREAD_CPU and threads != 1:
+        rate1, r1, dt1, reps1 = cpu_oracle_rate(w, min(seconds, 5.0), 1, fused)
+        out["single_thread"] = {
+            "value": round(rate1, 6), "unit": "TFLOP/s", "cores": 1,
+            "sample": f"{r1} of {w.M} output rows{f', {reps1} times' if reps1 > 1 else ''} ({dt1:.1f} s)",
+            "full_workload_s": round(full_flops / (rate1 * 1e12), 4)}
+    return out
 
 
 # -------------------------------------------------------------- our arm
@@ -296,14 +357,10 @@ def run_ours(args):
     A = w.A.device_view(dev)
     B = w.B.device_view(dev)
     C = torch.empty((M, N), dtype=torch.float16, device=dev)
-    # Between timed steps the L2 must not hold the inputs: either the inputs
-    # are larger than L2 (their own streaming evicts them), or a 512 MiB buffer
-    # is written between steps.
-    in_bytes = 2 * (w.A.numel + w.B.numel)
-    flush_needed = in_bytes <= L2_BYTES
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if flush_needed else None
-    l2_note = ("flushed between steps (512 MiB write)" if flush_needed else
-               f"not flushed: inputs ({in_bytes / 1e6:.0f} MB) exceed L2 ({L2_BYTES / 1e6:.0f} MB)")
+    # Before every timed step a 512 MiB buffer is written, so no step finds
+    # the previous step's inputs in L2.
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    l2_note = "flushed before every step (512 MiB write)"
     stream = torch.cuda.current_stream(dev)
     plan = g.plan_for(A, B, C)
     # The C-ABI call with its arguments marshalled once (device pointers and
@@ -319,8 +376,7 @@ def run_ours(args):
         g.gemm_f16(*call_args, stream=s.cuda_stream)
 
     for _ in range(args.warmup):
-        if flush is not None:
-            flush.zero_()
+        flush.zero_()
         step()
     torch.cuda.synchronize(dev)
     assert g.gemm_f16_device_status() == 0
@@ -339,6 +395,7 @@ def run_ours(args):
     total_ms = max_over_ranks(pg, local_ms, dev)
     ms_per_step = total_ms / args.steps
     value = whole_job_rate(flops, args.steps, world, total_ms) / 1e12
+    b2b = back_to_back(torch, dev, stream, args.steps, step, graph_step, barrier, pg, flops, nbytes, world)
 
     # ---- end to end: pinned host inputs in, result out, inside the timed region
     if args.no_e2e:
@@ -350,6 +407,7 @@ def run_ours(args):
     if rank == 0:
         result = report(args, w, plan, peaks, bnd, flops, nbytes, ms_per_step, value, wall, clk, e2e_ms,
                         world, status, A, B, l2_note)
+        result["back_to_back"] = b2b
     if pg is not None:
         pg.destroy_process_group()
     return result
@@ -378,10 +436,8 @@ def run_ours_multi(args, w, dev, barrier, pg, rank, world):
     U = w.B_up.device_view(dev) if w.B_up is not None else None
     C = torch.empty((w.c_rows, N), dtype=torch.float16, device=dev)
     in_bytes = 2 * (w.A.numel + w.B.numel + (w.B_up.numel if w.B_up is not None else 0))
-    flush_needed = in_bytes <= L2_BYTES
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if flush_needed else None
-    l2_note = ("flushed between steps (512 MiB write)" if flush_needed else
-               f"not flushed: inputs ({in_bytes / 1e6:.0f} MB) exceed L2 ({L2_BYTES / 1e6:.0f} MB)")
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    l2_note = "flushed before every step (512 MiB write)"
     stream = torch.cuda.current_stream(dev)
     handle = stream.cuda_stream
     act = g.ACTIVATIONS[w.act]
@@ -411,8 +467,7 @@ def run_ours_multi(args, w, dev, barrier, pg, rank, world):
             g.gemm_f16_grouped_fused(*call, stream=h)
 
     for _ in range(args.warmup):
-        if flush is not None:
-            flush.zero_()
+        flush.zero_()
         step()
     torch.cuda.synchronize(dev)
     assert g.gemm_f16_device_status() == 0
@@ -429,6 +484,8 @@ def run_ours_multi(args, w, dev, barrier, pg, rank, world):
     total_ms = max_over_ranks(pg, local_ms, dev)
     ms_per_step = total_ms / args.steps
     value = whole_job_rate(flops, args.steps, world, total_ms) / 1e12
+    b2b = back_to_back(torch, dev, stream, args.steps, step, lambda s: step(s.cuda_stream), barrier, pg, flops,
+                       nbytes, world)
 
     e2e = None
     if not args.no_e2e:
@@ -481,27 +538,17 @@ def run_ours_multi(args, w, dev, barrier, pg, rank, world):
         pg.destroy_process_group()
     if rank != 0:
         return None
-    if bnd == "tensor":
-        achieved = flops / (ms_per_step * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["tflops"], "unit": "TFLOP/s",
-                "frac": round(achieved / peaks["tflops"], 4)}
-    else:
-        achieved = nbytes / (ms_per_step * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4)}
-    roof["traffic"] = profiled_traffic(w.name)
-    roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json bf16 burst / copy bandwidth)"
-    roof["kernel"] = "gemm_f16_persistent"
+    roof = roofline(bnd, flops, nbytes, ms_per_step, peaks, w.name)
     cpu = None
     if not args.no_cpu_baseline:
-        threads = os.cpu_count() or 1
+        threads = args.cpu_threads or os.cpu_count() or 1
         first = w.first_problem()
         fused = (w.first_up(), w.act) if (w.B_up is not None or w.act != "none") else None
-        rate, r, dt, reps = cpu_oracle_rate(first, args.cpu_seconds, threads, fused)
-        what = "fused-stage oracle" if fused else "oracle"
-        cpu = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": f"{what}: {r} of {first.M} output rows of problem 0 x all {N} columns, K={K}"
-                         f"{f', {reps} times' if reps > 1 else ''} ({dt:.1f} s)"}
+        cpu = cpu_baseline(first, args.cpu_seconds, threads, fused,
+                           ("fused-stage oracle" if fused else "oracle") + ", problem 0", name=w.name)
+        # the whole launch's time, extrapolated from problem 0's rate
+        cpu["full_workload_s"] = round(flops / (cpu["value"] * 1e12), 3)
+        cpu["full_workload_s_kind"] = "extrapolated from problem 0's slab"
     config = {"workload": w.name, "kind": w.kind, "M": M, "N": N, "K": K, "problems": n,
               "fused_stage": ({"act": w.act, "gate_up": w.B_up is not None} if fused else None),
               "distribution": w.A.kind, "l2": l2_note,
@@ -515,7 +562,7 @@ def run_ours_multi(args, w, dev, barrier, pg, rank, world):
         "data": "synthetic (seeded SplitMix64 fill)", "config": config,
         "hbm_gbs_min_traffic": round(nbytes / (ms_per_step * 1e-3) / 1e9, 1),
         "wall_s_timed_region": round(wall, 4), "clocks": clk, "e2e": e2e, "gpu_launches": args.steps,
-        "roofline": roof, "cpu_baseline": cpu, "device_status": status,
+        "roofline": roof, "cpu_baseline": cpu, "device_status": status, "back_to_back": b2b,
     }
 
 
@@ -604,23 +651,11 @@ def run_e2e(args, w, dev, stream, C, barrier, pg):
 def report(args, w, plan, peaks, bnd, flops, nbytes, ms_per_step, value, wall, clk, e2e_ms, world,
            status, A, B, l2_note):
     M, N, K = w.M, w.N, w.K
-    if bnd == "tensor":
-        achieved = flops / (ms_per_step * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["tflops"],
-                "unit": "TFLOP/s", "frac": round(achieved / peaks["tflops"], 4)}
-    else:
-        achieved = nbytes / (ms_per_step * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
-    roof["traffic"] = profiled_traffic(w.name)
-    roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json bf16 burst / copy bandwidth)"
-    roof["kernel"] = "gemm_f16_persistent"
+    roof = roofline(bnd, flops, nbytes, ms_per_step, peaks, w.name)
     cpu = None
     if not args.no_cpu_baseline:
-        threads = os.cpu_count() or 1
-        rate, rows, dt, _ = cpu_oracle_rate(w, args.cpu_seconds, threads)
-        cpu = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": f"{rows} of {M} output rows x all {N} columns, K={K} ({dt:.1f} s)"}
+        threads = args.cpu_threads or os.cpu_count() or 1
+        cpu = cpu_baseline(w, args.cpu_seconds, threads)
     e2e = None
     if e2e_ms == e2e_ms:   # not NaN
         e2e = {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
@@ -673,7 +708,7 @@ def run_reference(args):
         if w.B_up is not None or w.act != "none":
             fused = (w.first_up(), w.act)
         w = w.first_problem()
-    threads = os.cpu_count() or 1
+    threads = args.cpu_threads or os.cpu_count() or 1
     per_step = min(5.0, 150.0 / max(1, args.steps + args.warmup))
     # size one slab, then time warmup + steps slabs of that size
     _, rows, _, _ = cpu_oracle_rate(w, per_step, threads, fused)
@@ -708,12 +743,14 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="square_4096")
+    ap.add_argument("--workload", default="moe_131072x2048x7168")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--shape", default=None,
                     help="M,N,K: an ad-hoc row-major uniform[-1,1] workload instead of --workload")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-threads", type=int, default=0,
+                    help="threads of the CPU oracle baseline (default: every host core)")
     ap.add_argument("--opt", action="append", default=[],
                     help="library tuning knob NAME=VALUE (force_gather, splits, tile_n, panel, swap, max_ctas)")
     args = ap.parse_args()

@@ -52,7 +52,6 @@ OPT_PAIR = 8
 OPT_STREAMK = 9
 OPT_TAIL_SPLIT = 10
 OPT_MAX_STAGES = 11
-OPT_MULTICAST = 12
 OPT_REPACK = 13
 OPT_TEST_STALL = 14
 OPT_PDL = 15

@@ -33,10 +33,8 @@ struct DevInfo {
     int sms = 0;
     int* status_ptr = nullptr;
     bool smem_attr_set = false;
-    int pair_smem = -1;       // cached max_clusters() results for this smem size
+    int pair_smem = -1;       // cached max_clusters() result for this smem size
     int pair_clusters = 0;
-    int quad_smem = -1;
-    int quad_clusters = 0;
 };
 
 std::mutex g_mutex;
@@ -59,6 +57,7 @@ std::atomic<int64_t> g_opt[17];
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 PFN_cuMemGetAddressRange_v3020 g_addr_range = nullptr;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
 std::once_flag g_entry_once;
 
 void load_entry_points()
@@ -75,6 +74,10 @@ void load_entry_points()
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
             g_addr_range = reinterpret_cast<PFN_cuMemGetAddressRange_v3020>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
         cudaGetLastError();
     });
 }
@@ -126,16 +129,23 @@ bool overlaps(uintptr_t a, int64_t a_bytes, uintptr_t b, int64_t b_bytes)
     return a < b + static_cast<uintptr_t>(b_bytes) && b < a + static_cast<uintptr_t>(a_bytes);
 }
 
-// The pointer must be device or managed memory, and [p, p+bytes) must lie
-// inside the allocation it points into.
+// The pointer must be device or managed memory of the current device (a peer
+// GPU's memory or host memory, pinned or not, is refused), and [p, p+bytes)
+// must lie inside the allocation it points into.
 bool device_range_ok(const void* p, int64_t bytes)
 {
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
     cudaPointerAttributes at;
     if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
     if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) return false;
+    if (at.device != cur) return false;
     if (g_addr_range) {
         CUdeviceptr base = 0;
         size_t size = 0;
@@ -327,13 +337,12 @@ bool set_smem_attributes(DevInfo& dev)
     std::lock_guard<std::mutex> lk(g_mutex);
     if (dev.smem_attr_set) return true;
     using namespace gemm_f16_dev;
-    const void* kernels[] = {reinterpret_cast<const void*>(gemm_f16_persistent<false, false, false>),
-                             reinterpret_cast<const void*>(gemm_f16_persistent<true, false, false>),
-                             reinterpret_cast<const void*>(gemm_f16_persistent<true, true, false>),
-                             reinterpret_cast<const void*>(gemm_f16_persistent<false, false, true>),
-                             reinterpret_cast<const void*>(gemm_f16_persistent<true, false, true>),
-                             reinterpret_cast<const void*>(gemm_f16_persistent<false, false, true, true>),
-                             reinterpret_cast<const void*>(gemm_f16_persistent<true, false, true, true>)};
+    const void* kernels[] = {reinterpret_cast<const void*>(gemm_f16_persistent<false, false>),
+                             reinterpret_cast<const void*>(gemm_f16_persistent<true, false>),
+                             reinterpret_cast<const void*>(gemm_f16_persistent<false, true>),
+                             reinterpret_cast<const void*>(gemm_f16_persistent<true, true>),
+                             reinterpret_cast<const void*>(gemm_f16_persistent<false, true, true>),
+                             reinterpret_cast<const void*>(gemm_f16_persistent<true, true, true>)};
     bool ok = true;
     for (const void* k : kernels)
         ok = ok && cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) == cudaSuccess;
@@ -345,16 +354,15 @@ bool set_smem_attributes(DevInfo& dev)
     return true;
 }
 
-// How many clusters of `size` CTAs (2: pair form, 4: four-CTA multicast form)
-// can be resident at once.  Clusters must fit inside a GPC, so this can be less
-// than the SM count divided by the size.
-int max_clusters(DevInfo& dev, int smem, int size)
+// How many clusters of two CTAs (the pair form) can be resident at once.
+// Clusters must fit inside a GPC, so this can be less than half the SM count.
+int max_clusters(DevInfo& dev, int smem)
 {
+    constexpr int size = 2;
     if (!set_smem_attributes(dev)) return 0;
     {
         std::lock_guard<std::mutex> lk(g_mutex);
-        if (size == 2 && dev.pair_smem == smem) return dev.pair_clusters;
-        if (size == 4 && dev.quad_smem == smem) return dev.quad_clusters;
+        if (dev.pair_smem == smem) return dev.pair_clusters;
     }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -368,21 +376,14 @@ int max_clusters(DevInfo& dev, int smem, int size)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    const cudaError_t e =
-        size == 4 ? cudaOccupancyMaxActiveClusters(&n, gemm_f16_dev::gemm_f16_persistent<true, true, false>, &cfg)
-                  : cudaOccupancyMaxActiveClusters(&n, gemm_f16_dev::gemm_f16_persistent<true, false, false>, &cfg);
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, gemm_f16_dev::gemm_f16_persistent<true, false>, &cfg);
     if (e != cudaSuccess) {
         cudaGetLastError();
         n = 0;
     }
     std::lock_guard<std::mutex> lk(g_mutex);
-    if (size == 4) {
-        dev.quad_smem = smem;
-        dev.quad_clusters = n;
-    } else {
-        dev.pair_smem = smem;
-        dev.pair_clusters = n;
-    }
+    dev.pair_smem = smem;
+    dev.pair_clusters = n;
     return n;
 }
 
@@ -713,11 +714,6 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
     kp.gmode = grouped ? 2 : (batched ? 1 : 0);
     kp.groups = static_cast<int>(a.batch);
     kp.a_bs = a_bs, kp.b_bs = b_bs, kp.c_bs = c_bs;
-    // Four-CTA multicast form: two pairs on vertically adjacent tiles share each
-    // B tile (whole tiles only: no K cut, no tail split).
-    const int64_t mc_opt = opt(GEMM_F16_OPT_MULTICAST);
-    bool quad = pair && mc_opt == 2 && BN == 256 && splits == 1 && opt(GEMM_F16_OPT_STREAMK) != 2 && tiles_m >= 2 &&
-                !batched && !grouped && !a.fused;
 
     bool a_3d = false, b_3d = false;
     // trailing batch dimensions (0: none)
@@ -736,11 +732,10 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
             ca = choose_operand(kp.A, kp.a_sm, kp.a_sk, Mv, a.K, gemm_f16_dev::kBM, false);
         }
     }
-    // B's box: a CTA's whole share of the tile's columns, or in the four-CTA form
-    // the 64-column quarter it multicasts.
-    // The gate/up form reads boxes of its output width from both projections.
-    auto encode_b = [&](bool quarter) {
-        const int cols = gated ? out_cols : (quarter ? bcols / 2 : bcols);
+    // B's box: a CTA's whole share of the tile's columns.  The gate/up form
+    // reads boxes of its output width from both projections.
+    auto encode_b = [&]() {
+        const int cols = gated ? out_cols : bcols;
         auto enc = [&](CUtensorMap* tm, const __half* ptr) {
             b_3d = cb.mn && encode_3d_mn(tm, ptr, Nv, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk,
                                          static_cast<uint32_t>(cols / 64), nb_b, bst_b);
@@ -753,7 +748,7 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
         return enc(&kp.tmB, kp.B) && (!gated || enc(&kp.tmBu, kp.Bu));
     };
     if (cb.tma) {
-        if (!encode_b(quad)) {
+        if (!encode_b()) {
             if (pair) return GEMM_F16_ERR_LAUNCH;
             cb = choose_operand(kp.B, kp.b_sn, kp.b_sk, Nv, a.K, gated ? out_cols : BN, false);
         }
@@ -778,7 +773,7 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
     // operand is gathered (gathered tiles are slow, so balancing the last wave
     // pays for the fixup); otherwise the last partial wave is split along N.
     const int64_t sk_opt = opt(GEMM_F16_OPT_STREAMK);
-    const bool use_sk = splits == 1 && !quad && !gated && (sk_opt == 2 || (sk_opt == 0 && (!ca.tma || !cb.tma)));
+    const bool use_sk = splits == 1 && !gated && (sk_opt == 2 || (sk_opt == 0 && (!ca.tma || !cb.tma)));
     const bool may_cut = splits > 1 || use_sk;
     // A C that TMA cannot store but whose columns are contiguous is staged in
     // the same buffer and written row by row by the epilogue warps.
@@ -793,36 +788,25 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
     const int smem = kSmemAlignSlack + stages * static_cast<int>(stage_bytes) + epi +
                      static_cast<int>(gemm_f16_dev::kBarrierBytes);
 
-    // Persistent workers: CTAs, or clusters (of 2 CTAs in the pair form, of 4 in
-    // the four-CTA form).
+    // Persistent workers: CTAs, or clusters of 2 CTAs in the pair form.
     const int64_t cap = opt(GEMM_F16_OPT_MAX_CTAS);
     int64_t max_workers = dev.sms;
-    if (quad) {
-        max_workers = max_clusters(const_cast<DevInfo&>(dev), smem, 4);
-        if (max_workers < 1) {   // no four-CTA cluster fits: plain pairs
-            quad = false;
-            if (!encode_b(false)) return GEMM_F16_ERR_LAUNCH;
-        }
-    }
-    const int cluster_ctas = quad ? 4 : (pair ? 2 : 1);
-    if (pair && !quad) max_workers = max_clusters(const_cast<DevInfo&>(dev), smem, 2);
+    const int cluster_ctas = pair ? 2 : 1;
+    if (pair) max_workers = max_clusters(const_cast<DevInfo&>(dev), smem);
     if (cap > 0) max_workers = std::min<int64_t>(max_workers, std::max<int64_t>(1, cap / cluster_ctas));
     if (max_workers < 1) return GEMM_F16_ERR_LAUNCH;
-    // Units of the four-CTA form cover two tile rows.
-    const int unit_rows = quad ? (tiles_m + 1) / 2 : tiles_m;
-    const int64_t unit_tiles = quad ? static_cast<int64_t>(unit_rows) * tiles_n : tiles;
     // Narrowest tail piece: the pair form keeps >= 64 B columns per CTA; a
-    // TMA-stored C needs whole 64-column boxes; the four-CTA form never cuts.
-    // (gate/up tiles are never cut: the minimum piece is wider than the tile)
-    const Schedule sch = make_schedule(unit_tiles, kblocks, splits, static_cast<int>(max_workers), BN,
-                                       (quad || gated) ? 2 * BN : (pair ? 128 : 64), use_sk);
+    // TMA-stored C needs whole 64-column boxes.  (gate/up tiles are never cut:
+    // the minimum piece is wider than the tile)
+    const Schedule sch = make_schedule(tiles, kblocks, splits, static_cast<int>(max_workers), BN,
+                                       gated ? 2 * BN : (pair ? 128 : 64), use_sk);
     const int grid = cluster_ctas * sch.workers;
     const int64_t panel = opt(GEMM_F16_OPT_PANEL);
 
     kp.status = dev.status_ptr;
     const int64_t tmo = opt(GEMM_F16_OPT_TIMEOUT_MS);
     kp.timeout_ns = static_cast<uint64_t>(tmo > 0 ? tmo : 1000) * 1000000ull;
-    kp.tiles_m = unit_rows, kp.tiles_n = tiles_n, kp.splits = splits, kp.kblocks = kblocks;
+    kp.tiles_m = tiles_m, kp.tiles_n = tiles_n, kp.splits = splits, kp.kblocks = kblocks;
     kp.num_units = sch.num_units;
     kp.workers = sch.workers;
     kp.sk_tile0 = sch.sk_tile0;
@@ -844,7 +828,7 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
     // Raster panel (tile rows whose tiles run side by side): 8 by default;
     // launches of at most four waves of tiles take 2, which measured 2 % faster
     // on 4096^3 (wider panels measured faster from 6144^3 up).
-    const int default_panel = unit_tiles <= 4 * static_cast<int64_t>(sch.workers) ? 2 : 8;
+    const int default_panel = tiles <= 4 * static_cast<int64_t>(sch.workers) ? 2 : 8;
     kp.panel = static_cast<int>(panel > 0 ? panel : default_panel);
     kp.BN = BN, kp.stages = stages;
     kp.a_flags = (ca.tma ? gemm_f16_dev::kOpTma : 0u) | (ca.mn ? gemm_f16_dev::kOpMnMajor : 0u) |
@@ -910,7 +894,7 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
     pub.gated = gated ? 1 : 0;
     pub.repack = repacked;
     pub.splits = splits, pub.kblocks = kblocks, pub.grid = grid;
-    pub.units = static_cast<int>(quad ? unit_tiles : tiles * splits);
+    pub.units = static_cast<int>(tiles * splits);
     pub.streamk_tiles = sch.sk_iters > 0 ? static_cast<int>(tiles - sch.sk_tile0) : 0;
     pub.tail_split = sch.tail_split;
     pub.stages = stages, pub.smem_bytes = smem;
@@ -978,13 +962,12 @@ gemm_f16_status launch(Plan& pl, DevInfo& dev, float* partials, int* counters, c
            pl.pub.pair ? pl.pub.cluster_ctas : 1);
     using gemm_f16_dev::gemm_f16_persistent;
     const cudaError_t e =
-        !pl.pub.pair ? (pl.fused ? cudaLaunchKernelEx(&cfg, gemm_f16_persistent<false, false, true, true>, kp)
-                        : multi  ? cudaLaunchKernelEx(&cfg, gemm_f16_persistent<false, false, true>, kp)
-                                 : cudaLaunchKernelEx(&cfg, gemm_f16_persistent<false, false, false>, kp))
-        : pl.pub.cluster_ctas == 4 ? cudaLaunchKernelEx(&cfg, gemm_f16_persistent<true, true, false>, kp)
-        : pl.fused                 ? cudaLaunchKernelEx(&cfg, gemm_f16_persistent<true, false, true, true>, kp)
-        : multi                    ? cudaLaunchKernelEx(&cfg, gemm_f16_persistent<true, false, true>, kp)
-                                   : cudaLaunchKernelEx(&cfg, gemm_f16_persistent<true, false, false>, kp);
+        !pl.pub.pair ? (pl.fused ? cudaLaunchKernelEx(&cfg, gemm_f16_persistent<false, true, true>, kp)
+                        : multi  ? cudaLaunchKernelEx(&cfg, gemm_f16_persistent<false, true>, kp)
+                                 : cudaLaunchKernelEx(&cfg, gemm_f16_persistent<false, false>, kp))
+        : pl.fused ? cudaLaunchKernelEx(&cfg, gemm_f16_persistent<true, true, true>, kp)
+        : multi    ? cudaLaunchKernelEx(&cfg, gemm_f16_persistent<true, true>, kp)
+                   : cudaLaunchKernelEx(&cfg, gemm_f16_persistent<true, false>, kp);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return GEMM_F16_ERR_LAUNCH;
@@ -1084,7 +1067,15 @@ gemm_f16_status run(const Args& args, void* user_ws, size_t user_ws_bytes, bool 
 constexpr size_t kNoAllocScratchBytes = GEMM_F16_NOALLOC_SCRATCH_BYTES;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-void* g_noalloc_ptr[kMaxDevices] = {};
+// The address is cached per device together with the context it was taken in:
+// after cudaDeviceReset (or anything else that replaces the device's primary
+// context) the module is loaded again at another address, so a call in a new
+// context looks the address up again instead of using a stale one.
+struct NoAllocScratch {
+    void* ptr = nullptr;
+    CUcontext ctx = nullptr;
+};
+NoAllocScratch g_noalloc[kMaxDevices];
 
 // Device address of the scratch array on the current device (nullptr if the
 // runtime could not provide it).
@@ -1095,16 +1086,23 @@ void* noalloc_scratch()
         cudaGetLastError();
         return nullptr;
     }
+    load_entry_points();
+    CUcontext ctx = nullptr;
+    if (!g_ctx_current || g_ctx_current(&ctx) != CUDA_SUCCESS) ctx = nullptr;
     std::lock_guard<std::mutex> lk(g_mutex);
-    if (!g_noalloc_ptr[d]) {
+    NoAllocScratch& e = g_noalloc[d];
+    if (!e.ptr || !ctx || e.ctx != ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
             cudaGetLastError();
             return nullptr;
         }
-        g_noalloc_ptr[d] = p;
+        // (the lookup makes the primary context current if it was not yet)
+        if (!g_ctx_current || g_ctx_current(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+        e.ptr = p;
+        e.ctx = ctx;
     }
-    return g_noalloc_ptr[d];
+    return e.ptr;
 }
 
 gemm_f16_status run_noalloc(const Args& a, cudaStream_t stream)
@@ -1361,12 +1359,12 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
 
 gemm_f16_status gemm_f16_set_option(int option, int64_t value)
 {
-    if (option < 1 || option > 16 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    // (12 is not an option: that number is left unused)
+    if (option < 1 || option > 16 || option == 12 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_DEBUG_BOUNDS && value > 2) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_PDL && value > 1) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_TEST_STALL && value > 1) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_REPACK && value > 2) return GEMM_F16_ERR_INVALID_VALUE;
-    if (option == GEMM_F16_OPT_MULTICAST && value > 2) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_MAX_STAGES && value == 1) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_TAIL_SPLIT && value > 1) return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_STREAMK && value > 2) return GEMM_F16_ERR_INVALID_VALUE;

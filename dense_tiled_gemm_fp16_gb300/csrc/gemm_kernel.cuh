@@ -4,21 +4,18 @@
 // One CTA (or CTA cluster) per SM (pair) walks a list of work units.  A unit
 // is a whole output tile, a narrower piece of a tile of the last partial wave
 // (tail split along N), or a K segment of a tile (classic split-K, or the
-// stream-K tail).  The kernel template gemm_f16_persistent<kPair, kQuad,
-// kMulti, kEpi> has three forms:
+// stream-K tail).  The kernel template gemm_f16_persistent<kPair, kMulti,
+// kEpi> has two forms:
 //
 //   single (kPair = false)  a 128 x BN tile per CTA, cta_group::1 MMAs.  Any
 //                           operand layout (TMA or gather), any unit kind.
 //   pair   (kPair = true)   clusters of two CTAs; a 256 x BN tile per pair,
 //                           one cta_group::2 MMA stream issued by the leader
 //                           (rank 0).  Each CTA loads its own 128 rows of A
-//                           and its own BN/2 columns of B, so a CTA moves 2/3
-//                           of the single form's operand bytes per MMA cycle
-//                           and fits deeper pipelines.  TMA operands only.
-//   four-CTA (kQuad)        two pairs on vertically adjacent tiles with the
-//                           same B columns; each CTA loads a quarter of its
-//                           pair rank's B columns and multicasts it to both
-//                           pairs (whole tiles only).
+//                           and its own BN/2 columns of B into its own shared
+//                           memory (no multicast), so a CTA moves 2/3 of the
+//                           single form's operand bytes per MMA cycle and
+//                           fits deeper pipelines.  TMA operands only.
 //
 // kMulti adds the geometry of batched and grouped launches (per-unit problem,
 // trailing batch coordinate of the TMA maps, group row limits); kEpi adds the
@@ -1281,17 +1278,11 @@ __device__ __forceinline__ void cut_tile_epilogue(const KernelParams& p, const S
     }
 }
 
-// kQuad (with kPair): clusters of four CTAs, two pairs on vertically adjacent
-// 256-row tiles with the same B columns.  Cluster ranks 0,1 form pair 0 and
-// 2,3 pair 1.  Each CTA loads its own 128 A rows and one 64-column quarter of
-// the pair's B columns, multicast to the CTA with the same pair rank in both
-// pairs, so B is read from L2 once per cluster instead of once per pair.  The
-// stage's empty barrier then waits for both pairs' MMAs (count 2).
 // kMulti: batched or grouped launches (gmode != 0); the one-GEMM launch is
 // compiled without that geometry.
 // kEpi: the fused output stage (bias, activation, gate/up product); built on
 // the kMulti geometry, which also runs one-GEMM launches (gmode 0).
-template <bool kPair, bool kQuad, bool kMulti, bool kEpi = false>
+template <bool kPair, bool kMulti, bool kEpi = false>
 __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __grid_constant__ KernelParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1310,24 +1301,20 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
     const bool a_mn = p.a_flags & kOpMnMajor, b_mn = p.b_flags & kOpMnMajor;
     const bool a_3d = p.a_flags & kOpBox3d, b_3d = p.b_flags & kOpBox3d;
     const bool a_bd = kMulti && p.a_bdim != 0, b_bd = kMulti && p.b_bdim != 0;   // maps with a trailing batch dimension
-    static_assert(kPair || !kQuad, "the four-CTA form is built on pairs");
-    static_assert(!kEpi || (kMulti && !kQuad), "the fused stage runs on the kMulti single and pair forms");
+    static_assert(!kEpi || kMulti, "the fused stage runs on the kMulti single and pair forms");
     const bool gated = kEpi && p.gated != 0;
     const uint32_t crank = kPair ? cluster_ctarank() : 0u;   // rank in the cluster
     const uint32_t rank = crank & 1u;                         // rank in the pair
-    const uint32_t pp = kQuad ? (crank >> 1) : 0u;            // pair index in the cluster
     const uint32_t lead_rank = crank & ~1u;                   // cluster rank of this pair's leader
     const bool leader = (rank == 0);
-    const int cid = static_cast<int>(blockIdx.x >> (kQuad ? 2 : (kPair ? 1 : 0)));
+    const int cid = static_cast<int>(blockIdx.x >> (kPair ? 1 : 0));
     constexpr int kTileRows = kPair ? 2 * kBM : kBM;
-    // Tile rows handled per unit by the cluster (two pair tiles in the four-CTA form).
-    constexpr int kUnitRows = kQuad ? 2 * kTileRows : kTileRows;
     const int nps = p.stages / kSlots;   // barrier phases in the slot ring
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(bar_full(L.bars, s), p.full_count);
-            mbar_init(bar_empty(L.bars, s), kQuad ? 2 : 1);
+            mbar_init(bar_empty(L.bars, s), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar_tfull(L.bars, a), 1);
@@ -1388,7 +1375,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                 // column n0: the single form loads both boxes, the pair form's rank 0
                 // the gate box and rank 1 the up box.
                 const int bcols = (kPair || gated) ? w.bn / 2 : w.bn;
-                const int64_t m0 = static_cast<int64_t>(w.m_blk) * kUnitRows + pp * kTileRows + rank * kBM;
+                const int64_t m0 = static_cast<int64_t>(w.m_blk) * kTileRows + rank * kBM;
                 const int64_t n0 = gated ? static_cast<int64_t>(w.n_blk) * (p.BN / 2)
                                          : static_cast<int64_t>(w.n_blk) * p.BN + w.n_off + rank * bcols;
                 const int64_t arow = ug.a_row + m0;   // A' row of the slot boxes (rows of a group are concatenated)
@@ -1425,21 +1412,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                         if (kPair) {
                             const uint32_t fbc = mapa_shared(fb, lead_rank);
                             load_a_slot<true>(p, sa, k0, arow, ug.az, a_mn, a_3d, a_bd, fbc);
-                            if (kQuad) {
-                                // This CTA's quarter: B columns n0 + 64*pp .. +64 of its pair
-                                // rank's half, into both pairs' CTAs of that rank.
-                                const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (2u + rank)));
-                                const int32_t nq = static_cast<int32_t>(n0 + 64 * pp);
-                                const uint32_t sq = sb + pp * 8192u;
-                                if (!b_mn)
-                                    tma_load_2d_pair_mc(sq, &p.tmB, k0, nq, fbc, mask);
-                                else if (b_3d)
-                                    tma_load_3d_pair_mc(sq, &p.tmB, 0, k0, nq >> 6, fbc, mask);
-                                else
-                                    tma_load_2d_pair_mc(sq, &p.tmB, nq, k0, fbc, mask);
-                            } else {
-                                load_b_slot<true>(p, tmb, sb, k0, n0, ug.bz, bcols, b_mn, b_3d, b_bd, fbc);
-                            }
+                            load_b_slot<true>(p, tmb, sb, k0, n0, ug.bz, bcols, b_mn, b_3d, b_bd, fbc);
                         } else {
                             if (a_tma) load_a_slot<false>(p, sa, k0, arow, ug.az, a_mn, a_3d, a_bd, fb);
                             if (b_tma) load_b_slot<false>(p, tmb, sb, k0, n0, ug.bz, bcols, b_mn, b_3d, b_bd, fb);
@@ -1541,7 +1514,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                     }
                     any = true;
                     if (kPair)
-                        umma_commit_pair_mc(bar_empty(L.bars, stage), kQuad ? 0xF : 0x3);
+                        umma_commit_pair_mc(bar_empty(L.bars, stage), 0x3);
                     else
                         umma_commit(bar_empty(L.bars, stage));
                     if (++stage == nps) {
@@ -1581,7 +1554,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
         const int nu = units_of_worker(p, cid);
         for (int ui = 0; ui < nu; ++ui) {
             const Unit w = unit_at<kMulti>(p, cid, ui);
-            const int64_t m0 = static_cast<int64_t>(w.m_blk) * kUnitRows + pp * kTileRows + rank * kBM;
+            const int64_t m0 = static_cast<int64_t>(w.m_blk) * kTileRows + rank * kBM;
             // first output column (a gated tile has BN/2 of them)
             const int64_t n0 = gated ? static_cast<int64_t>(w.n_blk) * (p.BN / 2)
                                      : static_cast<int64_t>(w.n_blk) * p.BN + w.n_off;
@@ -1665,8 +1638,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                                 fence_proxy_async_smem();
                                 __syncwarp();
                                 if (lane == 0) {
-                                    // (a box wholly below row M, e.g. the second pair tile of a
-                                    // four-CTA unit on the last row, is not stored)
+                                    // (a box wholly below row M, e.g. the second CTA's rows of a
+                                    // pair tile on the last row, is not stored)
                                     if (crow < ug.row_lim) {
                                         const int32_t xn = static_cast<int32_t>(n0 + 16 * (piece & ~3));
                                         if (kMulti && p.c_bdim)

@@ -234,30 +234,6 @@ __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const void* tmap,
         : "memory");
 }
 
-// Pair form with cluster multicast: the box lands at the same shared-memory
-// offset in every CTA of `cta_mask`, and the transaction bytes are signalled on
-// the barrier at `bar_cluster`'s offset in the leader CTA of each destination's
-// pair.
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const void* tmap, int32_t x, int32_t y,
-                                                    uint32_t bar_cluster, uint16_t cta_mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar_cluster), "h"(cta_mask)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
-                                                    uint32_t bar_cluster, uint16_t cta_mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster), "h"(cta_mask)
-        : "memory");
-}
-
 // Contiguous global -> shared copy of `bytes` (multiple of 16, both addresses
 // 16-byte aligned), completion signalled as transaction bytes on `bar`.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)

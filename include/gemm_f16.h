@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define GEMM_F16_ABI_VERSION 1
+#define GEMM_F16_ABI_VERSION 2
 
 /* Largest M, N or K (and total rows of a grouped call): 2^31 - 2^16.  The
    copies' tile coordinates are 32-bit; element offsets are 64-bit and may
@@ -51,7 +51,8 @@ typedef enum {
     GEMM_F16_OK = 0,
     /* A null pointer, M/N/K <= 0 or > GEMM_F16_MAX_DIM, a stride <= 0, ldc < N, an fp16 pointer that
        is not 2-byte aligned, a size whose extent overflows int64, a pointer
-       that is not device (or managed) memory of the current device, or a view
+       that is not device (or managed) memory of the current device (host
+       memory, pinned or not, and another GPU's memory are refused), or a view
        that runs past the end of the allocation it points into. */
     GEMM_F16_ERR_INVALID_VALUE = 1,
     /* The bytes C's M x N view spans overlap the bytes spanned by A or B. */
@@ -276,11 +277,18 @@ gemm_f16_status gemm_f16_grouped_fused(const void* A, int64_t stride_am, int64_t
  * holds until the process exits.  The caller still passes A, B and C.
  *
  * - Set-up: the first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress, with that device current) and caches it; make that
- *   first call before any stream capture on the device.
+ *   (cudaGetSymbolAddress, with that device current) and caches it with the
+ *   device's current context; make that first call before any stream capture
+ *   on the device.  A call made in a different context (after
+ *   cudaDeviceReset(), for instance) looks the address up again.
+ * - Operands TMA cannot address are always gathered by the kernel, never
+ *   copied to an aligned buffer (gemm_f16() copies them for large products).
+ *   The plan this entry point runs is therefore the one gemm_f16_get_plan()
+ *   reports while GEMM_F16_OPT_REPACK is 1; for aligned operands it is the
+ *   plan of gemm_f16() whatever that option says.
  * - A call whose plan needs more than GEMM_F16_NOALLOC_SCRATCH_BYTES of
  *   workspace is rejected with GEMM_F16_ERR_OUT_OF_MEMORY before anything is
- *   queued (gemm_f16_get_plan() reports the need as workspace_bytes).
+ *   queued (that plan's workspace_bytes, as above).
  * - Every call on a device shares the one array and finds the previous call's
  *   contents there: the call first clears the counter block with
  *   cudaMemsetAsync on `stream`.  Calls that overlap on the GPU (different
@@ -317,7 +325,7 @@ typedef struct {
     int smem_bytes;
     size_t workspace_bytes;
     int a_box3d, b_box3d;   /* MN-major TMA operand read as one 3-D box per stage */
-    int cluster_ctas;       /* CTAs per cluster: 1, 2 (pair form) or 4 (two pairs sharing B by multicast) */
+    int cluster_ctas;       /* CTAs per cluster: 1, or 2 (pair form) */
     int fused;              /* the fused output stage runs (gemm_f16_fused_get_plan) */
     int gated;              /* gate/up form: tile_n output columns, 2 * tile_n accumulator columns */
     int repack;             /* bit 0: A, bit 1: B (and B_up) copied to an aligned buffer before the GEMM */
@@ -358,9 +366,6 @@ gemm_f16_status gemm_f16_fused_get_plan(const void* A, int64_t stride_am, int64_
  *   GEMM_F16_OPT_MAX_STAGES    >= 2: cap the pipeline depth in 64-wide K slots, rounded
  *                              down to an even count (default: as many as shared memory
  *                              holds, at most 16)
- *   GEMM_F16_OPT_MULTICAST     0 default / 1: pairs load their own B; 2: clusters of four
- *                              CTAs (two pairs on adjacent 256-row tiles) read each B tile
- *                              once and multicast it (whole 256x256 tiles only)
  *   GEMM_F16_OPT_REPACK        0 default: operands TMA cannot address are copied to an
  *                              aligned buffer for products of at least 1e9 FLOPs and
  *                              gathered below; 1 always gather; 2 always copy
@@ -394,7 +399,7 @@ enum {
     GEMM_F16_OPT_STREAMK = 9,
     GEMM_F16_OPT_TAIL_SPLIT = 10,
     GEMM_F16_OPT_MAX_STAGES = 11,
-    GEMM_F16_OPT_MULTICAST = 12,
+    /* 12 is not an option (gemm_f16_set_option() refuses it) */
     GEMM_F16_OPT_REPACK = 13,
     GEMM_F16_OPT_TEST_STALL = 14,
     GEMM_F16_OPT_PDL = 15,

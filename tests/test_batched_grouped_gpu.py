@@ -23,7 +23,7 @@ def _defaults():
     yield
     for o in (g.OPT_FORCE_GATHER, g.OPT_SPLITS, g.OPT_TILE_N, g.OPT_PANEL, g.OPT_SWAP,
               g.OPT_TIMEOUT_MS, g.OPT_MAX_CTAS, g.OPT_PAIR, g.OPT_STREAMK, g.OPT_TAIL_SPLIT, g.OPT_MAX_STAGES,
-              g.OPT_MULTICAST, g.OPT_REPACK):
+              g.OPT_REPACK):
         g.gemm_f16_set_option(o, 0)
 
 

@@ -124,3 +124,31 @@ def test_cpu_baseline_runs_the_oracle_on_the_workload_itself():
         assert np.array_equal(run().view(np.uint16), want.view(np.uint16)), name
         rate, rows, dt, reps = bench.cpu_oracle_rate(w, 0.05, threads=1)
         assert rows == w.M and reps >= 1 and dt > 0 and rate > 0
+
+
+def test_roofline_rates_against_burst_and_sustained_peaks():
+    peaks = {"tflops": 2000.0, "tflops_sustained": 1600.0, "hbm_gbs": 8000.0, "source": "measured"}
+    # 2e12 FLOPs in 1.25 ms: 1600 TFLOP/s, 0.8 of the burst peak, 1.0 of the sustained one
+    r = bench.roofline("tensor", 2e12, 1e9, 1.25, peaks, "no_such_workload")
+    assert r["unit"] == "TFLOP/s" and r["peak_kind"] == "burst"
+    assert r["achieved"] == pytest.approx(1600.0) and r["frac"] == pytest.approx(0.8)
+    assert r["frac_of_sustained"] == pytest.approx(1.0) and r["traffic"] is None
+    # 4e8 bytes in 0.1 ms: 4000 GB/s, half of the copy bandwidth
+    r = bench.roofline("hbm", 1e9, 4e8, 0.1, peaks, "no_such_workload")
+    assert r["unit"] == "GB/s" and r["achieved"] == pytest.approx(4000.0) and r["frac"] == pytest.approx(0.5)
+
+
+def test_cpu_baseline_labels_its_sample_and_adds_a_single_thread_run():
+    import oracle
+    from synth import workloads
+
+    oracle.build()
+    w = workloads.BY_NAME["tail_130x70x65_b_rowmajor"]
+    cpu = bench.cpu_baseline(w, 0.05, 2)
+    assert cpu["kind"] == "oracle" and cpu["cores"] == 2 and cpu["value"] > 0
+    assert cpu["full_workload_s_kind"] == "measured"       # the slab is the whole product
+    assert cpu["single_thread"]["cores"] == 1 and cpu["single_thread"]["value"] > 0
+    big = workloads.BY_NAME["square_4096"]                   # not a single-thread workload
+    cpu = bench.cpu_baseline(big, 0.05, 1)
+    assert "single_thread" not in cpu and cpu["full_workload_s_kind"].startswith("extrapolated")
+    assert cpu["full_workload_s"] > 0

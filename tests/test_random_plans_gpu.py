@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 
 DEV = torch.device("cuda:0")
 OPTIONS = (g.OPT_FORCE_GATHER, g.OPT_SPLITS, g.OPT_TILE_N, g.OPT_PANEL, g.OPT_SWAP, g.OPT_PAIR, g.OPT_STREAMK,
-           g.OPT_TAIL_SPLIT, g.OPT_MAX_STAGES, g.OPT_MULTICAST, g.OPT_REPACK, g.OPT_PDL)
+           g.OPT_TAIL_SPLIT, g.OPT_MAX_STAGES, g.OPT_REPACK, g.OPT_PDL)
 
 
 def _reset():
@@ -66,7 +66,6 @@ def _options(rng):
              (0.2, g.OPT_STREAMK, lambda: int(rng.integers(1, 3))),
              (0.1, g.OPT_TAIL_SPLIT, lambda: 1),
              (0.1, g.OPT_MAX_STAGES, lambda: int(rng.choice([2, 4, 6]))),
-             (0.1, g.OPT_MULTICAST, lambda: 2),
              (0.2, g.OPT_REPACK, lambda: int(rng.integers(1, 3))),
              (0.1, g.OPT_PDL, lambda: 1))
     return {o: f() for p, o, f in draws if rng.random() < p}

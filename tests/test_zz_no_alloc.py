@@ -23,7 +23,7 @@ DEV = torch.device("cuda:0")
 @pytest.fixture(autouse=True)
 def _defaults():
     for o in (g.OPT_FORCE_GATHER, g.OPT_SPLITS, g.OPT_TILE_N, g.OPT_PANEL, g.OPT_SWAP,
-              g.OPT_TIMEOUT_MS, g.OPT_MAX_CTAS, g.OPT_PAIR, g.OPT_STREAMK, g.OPT_TAIL_SPLIT, g.OPT_MAX_STAGES, g.OPT_MULTICAST):
+              g.OPT_TIMEOUT_MS, g.OPT_MAX_CTAS, g.OPT_PAIR, g.OPT_STREAMK, g.OPT_TAIL_SPLIT, g.OPT_MAX_STAGES):
         g.gemm_f16_set_option(o, 0)
     yield
     for o in (g.OPT_STREAMK, g.OPT_SPLITS):
@@ -78,3 +78,45 @@ def test_no_alloc_rejects_a_plan_beyond_its_scratch():
     with pytest.raises(g.GemmF16Error) as e:
         g.gemm_f16_noalloc(*_args(A, B, out))
     assert e.value.status == g.ERR_OUT_OF_MEMORY
+
+
+def test_no_alloc_gathers_unaligned_views_and_allocates_nothing():
+    """An operand TMA cannot address (a transposed view whose pitch, 17
+    elements, is not a multiple of 16 bytes) is gathered by this entry point
+    (gemm_f16 would copy it into its workspace for a large product), and the
+    tiles are cut along K, so the partial sums go to the fixed array.  Integer
+    inputs make every order of the fp32 sums exact: the result must equal the
+    oracle bit for bit.  Device memory in use must not change across the calls,
+    which come before any gemm_f16 call of this shape."""
+    torch.cuda.set_device(DEV)
+    rng = np.random.default_rng(37)
+    M, N, K = 16, 4096, 8192
+    buf = rng.integers(-3, 4, (K, M + 1)).astype(np.float16)   # A = buf[:, :M].T, strides (1, M + 1)
+    Bh = rng.integers(-3, 4, (K, N)).astype(np.float16)
+    A = torch.from_numpy(buf).to(DEV)[:, :M].t()
+    B = torch.from_numpy(Bh).to(DEV)
+    assert A.stride() == (1, M + 1)
+    outs = [torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV) for _ in range(2)]
+    g.gemm_f16_set_option(g.OPT_REPACK, 1)        # the plan this entry point runs
+    try:
+        plan = g.gemm_f16_get_plan(*_args(A, B, outs[0]))
+    finally:
+        g.gemm_f16_set_option(g.OPT_REPACK, 0)
+    assert plan["repack"] == 0 and not (plan["a_tma"] and plan["b_tma"]), plan
+    assert plan["streamk_tiles"] > 0 or plan["splits"] > 1, plan
+    assert 0 < plan["workspace_bytes"] <= g.NOALLOC_SCRATCH_BYTES, plan
+    stream = torch.cuda.current_stream(DEV).cuda_stream
+    # warm-up on another shape that also cuts tiles along K: loads the module
+    # and looks up the array's address, which are set-up, not allocations
+    g.gemm_f16_noalloc(*_args(A[:, :4096], B[:4096, :2048], outs[1][:, :2048]), stream=stream)
+    torch.cuda.synchronize(DEV)
+    free0 = torch.cuda.mem_get_info(DEV)[0]
+    for out in outs:                              # two calls in a row on the shared array
+        g.gemm_f16_noalloc(*_args(A, B, out), stream=stream)
+    torch.cuda.synchronize(DEV)
+    assert torch.cuda.mem_get_info(DEV)[0] == free0
+    ref = oracle.gemm(A.cpu().numpy(), Bh, threads=oracle_threads())
+    for call, out in enumerate(outs):
+        got = out.cpu().numpy()
+        assert np.array_equal(got.view(np.uint16), ref.view(np.uint16)), f"noalloc call {call} vs oracle"
+    assert g.gemm_f16_device_status() == 0
