@@ -6,9 +6,11 @@
 
 A step is one C = A*B of the workload (default: the MoE-flattened
 131072 x 2048 x 7168 case of the C500 review, fp16 inputs, fp32 accumulation,
-fp16 output) on inputs already resident in device memory.  L2 is flushed (a
-512 MiB write) before every timed step and each step is bracketed by its own
-CUDA events on the launching stream, the flush outside them.  `value` is
+fp16 output) on inputs already resident in device memory.  L2 is flushed
+before every timed step (a 512 MiB buffer written, then a second 512 MiB
+buffer read, so the step finds neither its inputs nor dirty lines in L2) and
+each step is bracketed by its own CUDA events on the launching stream, the
+flush outside them.  `value` is
 TFLOP/s of useful 2MNK work over all ranks.  `back_to_back` repeats the timing
 with the steps run back to back (one replay of a CUDA graph of K calls, two
 events around it, no flush): the warm figure of a serving loop.  `e2e` repeats the measurement
@@ -43,7 +45,25 @@ if ROOT not in sys.path:
 
 METRIC = "fp16 GEMM TFLOP/s (fp32 acc) and % of GB300 roofline; HBM GB/s at small M"
 L2_FLUSH_BYTES = 512 << 20
-L2_BYTES = 129e6      # GB300 L2 capacity
+L2_NOTE = ("flushed before every step (a 512 MiB buffer written, then another 512 MiB buffer read: "
+           "no input lines and no dirty lines left in L2)")
+
+
+class L2Flush:
+    """Evicts L2 between timed steps: writing a buffer four times the L2's
+    129 MB pushes every line of the previous step out; reading a second one
+    then replaces the written (dirty) lines with clean ones, so the next step
+    does not pay for writing the flush buffer back to HBM."""
+
+    def __init__(self, torch, dev):
+        self.torch = torch
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.out = torch.empty((), dtype=torch.float32, device=dev)
+
+    def zero_(self):
+        self.w.zero_()
+        self.torch.sum(self.r, dim=0, out=self.out)
 
 
 def log(*a):
@@ -357,10 +377,10 @@ def run_ours(args):
     A = w.A.device_view(dev)
     B = w.B.device_view(dev)
     C = torch.empty((M, N), dtype=torch.float16, device=dev)
-    # Before every timed step a 512 MiB buffer is written, so no step finds
-    # the previous step's inputs in L2.
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    l2_note = "flushed before every step (512 MiB write)"
+    # L2 is flushed before every timed step, so no step finds the previous
+    # step's inputs (or the flush's dirty lines) in L2.
+    flush = L2Flush(torch, dev)
+    l2_note = L2_NOTE
     stream = torch.cuda.current_stream(dev)
     plan = g.plan_for(A, B, C)
     # The C-ABI call with its arguments marshalled once (device pointers and
@@ -436,8 +456,8 @@ def run_ours_multi(args, w, dev, barrier, pg, rank, world):
     U = w.B_up.device_view(dev) if w.B_up is not None else None
     C = torch.empty((w.c_rows, N), dtype=torch.float16, device=dev)
     in_bytes = 2 * (w.A.numel + w.B.numel + (w.B_up.numel if w.B_up is not None else 0))
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    l2_note = "flushed before every step (512 MiB write)"
+    flush = L2Flush(torch, dev)
+    l2_note = L2_NOTE
     stream = torch.cuda.current_stream(dev)
     handle = stream.cuda_stream
     act = g.ACTIVATIONS[w.act]
@@ -747,7 +767,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--shape", default=None,
-                    help="M,N,K: an ad-hoc row-major uniform[-1,1] workload instead of --workload")
+                    help="M,N,K[,at][,bt]: an ad-hoc uniform[-1,1] workload instead of --workload (row-major; "
+                         "at / bt make A / B transposed views of row-major buffers)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-threads", type=int, default=0,
                     help="threads of the CPU oracle baseline (default: every host core)")
@@ -761,11 +782,14 @@ def main():
             g.gemm_f16_set_option(getattr(g, "OPT_" + k.upper()), int(v))
     if args.shape:
         from synth import workloads
-        M, N, K = (int(x) for x in args.shape.split(","))
-        name = f"rowmajor_{M}x{N}x{K}"
+        parts = args.shape.split(",")
+        M, N, K = (int(x) for x in parts[:3])
+        at, bt = "at" in parts[3:], "bt" in parts[3:]
+        name = f"rowmajor_{M}x{N}x{K}" + ("_at" if at else "") + ("_bt" if bt else "")
         workloads.BY_NAME[name] = workloads.Workload(
-            name, M, N, K, workloads.Operand(M, K, "uniform", 21), workloads.Operand(K, N, "uniform", 22),
-            "ad-hoc row-major uniform[-1,1] shape")
+            name, M, N, K, workloads.Operand(M, K, "uniform", 21, transposed=at),
+            workloads.Operand(K, N, "uniform", 22, transposed=bt),
+            "ad-hoc uniform[-1,1] shape (row-major, or transposed views with at / bt)")
         args.workload = name
     if args.warmup < 3 and args.impl == "ours":
         log("note: fewer than 3 warm-up steps")

@@ -56,6 +56,9 @@ OPT_REPACK = 13
 OPT_TEST_STALL = 14
 OPT_PDL = 15
 OPT_DEBUG_BOUNDS = 16
+OPT_L2_A = 17
+OPT_L2_B = 18
+OPT_L2_C = 19
 
 # Activations of the fused output stage (gemm_f16_fused and friends).
 ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU = range(4)

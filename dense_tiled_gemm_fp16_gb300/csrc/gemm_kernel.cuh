@@ -135,6 +135,9 @@ struct KernelParams {
     // usable).  0 in every ordinary call.
     uint32_t test_stall;
     uint32_t epi_smem;   // 1: reserve the 32 KB epilogue buffer (TMA-store staging, fixup landing zone)
+    // L2 eviction policy of the TMA loads of A' and B' and of the TMA stores
+    // of C: 0 none, 1 evict first, 2 evict last (see l2_policy).
+    uint32_t l2_a, l2_b, l2_c;
     // Work decomposition.  `workers` persistent CTAs (single form) or clusters
     // (pair form).  Worker c first takes the whole-tile (or classic split-K)
     // units c, c+workers, ... < num_units; then, if sk_iters > 0, the
@@ -379,31 +382,51 @@ __device__ __forceinline__ UnitGeom unit_geom(const KernelParams& p, const Unit&
 }
 
 // TMA loads of one slot, single or pair form, with the map's trailing batch
-// coordinate z when it has one.
+// coordinate z when it has one; `hk` is the L2 eviction policy kind of the
+// operand (0: none; see l2_policy).
 template <bool kPair>
-__device__ __forceinline__ void tma2(uint32_t d, const void* m, int32_t x, int32_t y, uint32_t bar)
+__device__ __forceinline__ void tma2(uint32_t d, const void* m, int32_t x, int32_t y, uint32_t bar, uint32_t hk)
 {
-    if (kPair)
+    if (hk) {
+        if (kPair)
+            tma_load_2d_pair_hint(d, m, x, y, bar, l2_policy(hk));
+        else
+            tma_load_2d_hint(d, m, x, y, bar, l2_policy(hk));
+    } else if (kPair) {
         tma_load_2d_pair(d, m, x, y, bar);
-    else
+    } else {
         tma_load_2d(d, m, x, y, bar);
+    }
 }
 template <bool kPair>
-__device__ __forceinline__ void tma3(uint32_t d, const void* m, int32_t x, int32_t y, int32_t z, uint32_t bar)
+__device__ __forceinline__ void tma3(uint32_t d, const void* m, int32_t x, int32_t y, int32_t z, uint32_t bar,
+                                     uint32_t hk)
 {
-    if (kPair)
+    if (hk) {
+        if (kPair)
+            tma_load_3d_pair_hint(d, m, x, y, z, bar, l2_policy(hk));
+        else
+            tma_load_3d_hint(d, m, x, y, z, bar, l2_policy(hk));
+    } else if (kPair) {
         tma_load_3d_pair(d, m, x, y, z, bar);
-    else
+    } else {
         tma_load_3d(d, m, x, y, z, bar);
+    }
 }
 template <bool kPair>
 __device__ __forceinline__ void tma4(uint32_t d, const void* m, int32_t x, int32_t y, int32_t z, int32_t v,
-                                     uint32_t bar)
+                                     uint32_t bar, uint32_t hk)
 {
-    if (kPair)
+    if (hk) {
+        if (kPair)
+            tma_load_4d_pair_hint(d, m, x, y, z, v, bar, l2_policy(hk));
+        else
+            tma_load_4d_hint(d, m, x, y, z, v, bar, l2_policy(hk));
+    } else if (kPair) {
         tma_load_4d_pair(d, m, x, y, z, v, bar);
-    else
+    } else {
         tma_load_4d(d, m, x, y, z, v, bar);
+    }
 }
 
 // A' rows row .. row+127 of one 64-wide K slot: K-major one box (k, row);
@@ -415,20 +438,20 @@ __device__ __forceinline__ void load_a_slot(const KernelParams& p, uint32_t sa, 
     const int32_t r = static_cast<int32_t>(row);
     if (!a_mn) {
         if (bd)
-            tma3<kPair>(sa, &p.tmA, k0, r, z, bar);
+            tma3<kPair>(sa, &p.tmA, k0, r, z, bar, p.l2_a);
         else
-            tma2<kPair>(sa, &p.tmA, k0, r, bar);
+            tma2<kPair>(sa, &p.tmA, k0, r, bar, p.l2_a);
     } else if (a_3d) {
         if (bd)
-            tma4<kPair>(sa, &p.tmA, 0, k0, r >> 6, z, bar);
+            tma4<kPair>(sa, &p.tmA, 0, k0, r >> 6, z, bar, p.l2_a);
         else
-            tma3<kPair>(sa, &p.tmA, 0, k0, r >> 6, bar);
+            tma3<kPair>(sa, &p.tmA, 0, k0, r >> 6, bar, p.l2_a);
     } else {
         for (int j = 0; j < 2; ++j) {
             if (bd)
-                tma3<kPair>(sa + j * 8192, &p.tmA, r + 64 * j, k0, z, bar);
+                tma3<kPair>(sa + j * 8192, &p.tmA, r + 64 * j, k0, z, bar, p.l2_a);
             else
-                tma2<kPair>(sa + j * 8192, &p.tmA, r + 64 * j, k0, bar);
+                tma2<kPair>(sa + j * 8192, &p.tmA, r + 64 * j, k0, bar, p.l2_a);
         }
     }
 }
@@ -444,20 +467,20 @@ __device__ __forceinline__ void load_b_slot(const KernelParams& p, const CUtenso
     const int32_t c = static_cast<int32_t>(col);
     if (!b_mn) {
         if (bd)
-            tma3<kPair>(sb, tmb, k0, c, z, bar);
+            tma3<kPair>(sb, tmb, k0, c, z, bar, p.l2_b);
         else
-            tma2<kPair>(sb, tmb, k0, c, bar);
+            tma2<kPair>(sb, tmb, k0, c, bar, p.l2_b);
     } else if (b_3d) {
         if (bd)
-            tma4<kPair>(sb, tmb, 0, k0, c >> 6, z, bar);
+            tma4<kPair>(sb, tmb, 0, k0, c >> 6, z, bar, p.l2_b);
         else
-            tma3<kPair>(sb, tmb, 0, k0, c >> 6, bar);
+            tma3<kPair>(sb, tmb, 0, k0, c >> 6, bar, p.l2_b);
     } else {
         for (int j = 0; j < bcols / 64; ++j) {
             if (bd)
-                tma3<kPair>(sb + j * 8192, tmb, c + 64 * j, k0, z, bar);
+                tma3<kPair>(sb + j * 8192, tmb, c + 64 * j, k0, z, bar, p.l2_b);
             else
-                tma2<kPair>(sb + j * 8192, tmb, c + 64 * j, k0, bar);
+                tma2<kPair>(sb + j * 8192, tmb, c + 64 * j, k0, bar, p.l2_b);
         }
     }
 }
@@ -911,9 +934,9 @@ __device__ __forceinline__ void emit_piece(const KernelParams& p, const SmemLayo
                 if (crow < ug.row_lim) {
                     const int32_t xn = static_cast<int32_t>(n0 + 16 * (piece & ~3));
                     if (kMulti && p.c_bdim)
-                        tma_store_3d(&p.tmC, buf, xn, static_cast<int32_t>(crow), ug.cz);
+                        tma_store_3d_l2(&p.tmC, buf, xn, static_cast<int32_t>(crow), ug.cz, p.l2_c);
                     else
-                        tma_store_2d(&p.tmC, buf, xn, static_cast<int32_t>(crow));
+                        tma_store_2d_l2(&p.tmC, buf, xn, static_cast<int32_t>(crow), p.l2_c);
                 }
                 bulk_commit_group();
             }
@@ -1195,9 +1218,9 @@ __device__ __forceinline__ void cut_tile_epilogue(const KernelParams& p, const S
                             if (crow < ug.row_lim) {
                                 const int32_t xn = static_cast<int32_t>(n0 + 16 * (b0 + g0));
                                 if (kMulti && p.c_bdim)
-                                    tma_store_3d(&p.tmC, buf, xn, static_cast<int32_t>(crow), ug.cz);
+                                    tma_store_3d_l2(&p.tmC, buf, xn, static_cast<int32_t>(crow), ug.cz, p.l2_c);
                                 else
-                                    tma_store_2d(&p.tmC, buf, xn, static_cast<int32_t>(crow));
+                                    tma_store_2d_l2(&p.tmC, buf, xn, static_cast<int32_t>(crow), p.l2_c);
                             }
                             bulk_commit_group();
                         }
@@ -1643,9 +1666,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                                     if (crow < ug.row_lim) {
                                         const int32_t xn = static_cast<int32_t>(n0 + 16 * (piece & ~3));
                                         if (kMulti && p.c_bdim)
-                                            tma_store_3d(&p.tmC, buf, xn, static_cast<int32_t>(crow), ug.cz);
+                                            tma_store_3d_l2(&p.tmC, buf, xn, static_cast<int32_t>(crow), ug.cz, p.l2_c);
                                         else
-                                            tma_store_2d(&p.tmC, buf, xn, static_cast<int32_t>(crow));
+                                            tma_store_2d_l2(&p.tmC, buf, xn, static_cast<int32_t>(crow), p.l2_c);
                                     }
                                     bulk_commit_group();
                                 }

@@ -234,6 +234,82 @@ __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const void* tmap,
         : "memory");
 }
 
+// ------------------------------------------------------ L2 eviction policy
+// An L2 cache policy for the copies below: kind 1 marks the lines a copy
+// brings into L2 as first to evict, kind 2 as last to evict (data that many
+// CTAs will read again soon).  Kind 0 means no policy: the plain forms are
+// used instead.
+__device__ __forceinline__ uint64_t l2_policy(uint32_t kind)
+{
+    uint64_t pol;
+    if (kind == 2)
+        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    else
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// The tiled loads above with an L2 cache policy (single and pair form).
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* tmap, int32_t x, int32_t y, uint32_t bar,
+                                                 uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void* tmap, int32_t x, int32_t y,
+                                                      uint32_t bar_cluster, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar_cluster), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                                 uint32_t bar, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                                      uint32_t bar_cluster, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                                 int32_t w, uint32_t bar, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_pair_hint(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                                      int32_t w, uint32_t bar_cluster, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar_cluster), "l"(pol)
+        : "memory");
+}
+
 // Contiguous global -> shared copy of `bytes` (multiple of 16, both addresses
 // 16-byte aligned), completion signalled as transaction bytes on `bar`.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
@@ -259,6 +335,32 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int
     asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
                      reinterpret_cast<uint64_t>(tmap)),
                  "r"(x), "r"(y), "r"(z), "r"(src)
+                 : "memory");
+}
+
+// The tiled stores with an L2 cache policy: kind 0 plain, else l2_policy(kind).
+__device__ __forceinline__ void tma_store_2d_l2(const void* tmap, uint32_t src, int32_t x, int32_t y, uint32_t kind)
+{
+    if (kind == 0) {
+        tma_store_2d(tmap, src, x, y);
+        return;
+    }
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y), "r"(src), "l"(l2_policy(kind))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_store_3d_l2(const void* tmap, uint32_t src, int32_t x, int32_t y, int32_t z,
+                                                uint32_t kind)
+{
+    if (kind == 0) {
+        tma_store_3d(tmap, src, x, y, z);
+        return;
+    }
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2, %3}], [%4], %5;" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y), "r"(z), "r"(src), "l"(l2_policy(kind))
                  : "memory");
 }
 

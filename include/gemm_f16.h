@@ -359,8 +359,10 @@ gemm_f16_status gemm_f16_fused_get_plan(const void* A, int64_t stride_am, int64_
  *   GEMM_F16_OPT_PAIR          0 default (2-CTA pair tiles for 256-wide tiles of TMA
  *                              operands without split-K), 1 never, 2 also for 128-wide tiles
  *   GEMM_F16_OPT_STREAMK       0 default: stream-K tail when an operand is gathered (not
- *                              TMA-addressable), whole tiles otherwise; 1: whole tiles only;
- *                              2: stream-K tail whenever the tiles do not divide evenly
+ *                              TMA-addressable) or when a swapped (small-M) plan has fewer
+ *                              tiles than the device has SMs, whole tiles otherwise; 1: whole
+ *                              tiles only; 2: stream-K tail whenever the tiles do not divide
+ *                              evenly
  *   GEMM_F16_OPT_TAIL_SPLIT    0 default: cut the last partial wave of tiles along N
  *                              into narrower tiles; 1 never
  *   GEMM_F16_OPT_MAX_STAGES    >= 2: cap the pipeline depth in 64-wide K slots, rounded
@@ -379,6 +381,11 @@ gemm_f16_status gemm_f16_fused_get_plan(const void* A, int64_t stride_am, int64_
  *                              leave it is skipped and gemm_f16_device_status() reports
  *                              GEMM_F16_ERR_BOUNDS.  2: the checker's own test, with each
  *                              range ending 16 bytes early.  0 default (off)
+ *   GEMM_F16_OPT_L2_A, _L2_B   L2 eviction policy of the TMA loads of the kernel's A and B
+ *   GEMM_F16_OPT_L2_C          operands and of the TMA stores of C (the kernel computes
+ *                              C^T = B^T A^T when the plan swaps, so its A is then the
+ *                              caller's B): 1 none, 2 evict first, 3 evict last; 0 default
+ *                              (none)
  *   GEMM_F16_OPT_TEST_STALL    failure-detection test: 1 makes every CTA's MMA issuer wait
  *                              first on a barrier that nothing arrives on, so the bounded
  *                              wait runs out (after GEMM_F16_OPT_TIMEOUT_MS), the kernel
@@ -403,7 +410,10 @@ enum {
     GEMM_F16_OPT_REPACK = 13,
     GEMM_F16_OPT_TEST_STALL = 14,
     GEMM_F16_OPT_PDL = 15,
-    GEMM_F16_OPT_DEBUG_BOUNDS = 16
+    GEMM_F16_OPT_DEBUG_BOUNDS = 16,
+    GEMM_F16_OPT_L2_A = 17,
+    GEMM_F16_OPT_L2_B = 18,
+    GEMM_F16_OPT_L2_C = 19
 };
 gemm_f16_status gemm_f16_set_option(int option, int64_t value);
 

@@ -25,7 +25,8 @@ DEV = torch.device("cuda:0")
 def _defaults():
     yield
     for o in (g.OPT_FORCE_GATHER, g.OPT_SPLITS, g.OPT_TILE_N, g.OPT_PANEL, g.OPT_SWAP,
-              g.OPT_TIMEOUT_MS, g.OPT_MAX_CTAS, g.OPT_PAIR, g.OPT_STREAMK, g.OPT_TAIL_SPLIT, g.OPT_MAX_STAGES, g.OPT_REPACK):
+              g.OPT_TIMEOUT_MS, g.OPT_MAX_CTAS, g.OPT_PAIR, g.OPT_STREAMK, g.OPT_TAIL_SPLIT, g.OPT_MAX_STAGES, g.OPT_REPACK,
+              g.OPT_L2_A, g.OPT_L2_B, g.OPT_L2_C):
         g.gemm_f16_set_option(o, 0)
 
 
@@ -573,4 +574,29 @@ def test_shallow_ring_with_k_cuts(opts):
     assert plan["streamk_tiles"] > 0 or plan["splits"] > 1, plan
     C = host(gpu(A, B, out=out))
     assert_bits(C, oracle.gemm(Ah, Bh, threads=oracle_threads()), f"shallow ring {opts}")
+    assert g.gemm_f16_device_status() == 0
+
+
+# ------------------------------------------------------ L2 eviction policies
+@pytest.mark.parametrize("a,b,c", [(2, 3, 1), (3, 2, 2), (2, 2, 3), (1, 3, 2)])
+@pytest.mark.parametrize("case", [(1100, 1288, 896, "row", "row", {}),            # pair form, 3-D B boxes
+                                  (704, 520, 296, "col", "col", {g.OPT_PAIR: 1}),  # single form, MN-major A
+                                  (1190, 1216, 2984, "row", "row", {g.OPT_STREAMK: 2})])
+def test_l2_policies_do_not_change_results(case, a, b, c):
+    """Eviction policies on the operand copies and the C stores only steer L2
+    replacement: every combination gives the oracle's result bit for bit."""
+    M, N, K, la, lb, opts = case
+    for o, v in opts.items():
+        g.gemm_f16_set_option(o, v)
+    g.gemm_f16_set_option(g.OPT_L2_A, a)
+    g.gemm_f16_set_option(g.OPT_L2_B, b)
+    g.gemm_f16_set_option(g.OPT_L2_C, c)
+    rng = np.random.default_rng(M + 7 * N + K + a)
+    Ah = rng.integers(-3, 4, (M, K)).astype(np.float16)
+    Bh = rng.integers(-3, 4, (K, N)).astype(np.float16)
+    A, B = make_view(Ah, la), make_view(Bh, lb)
+    out = torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV)
+    plan = g.plan_for(A, B, out)
+    assert plan["a_tma"] and plan["b_tma"] and plan["c_tma"] and not plan["repack"], plan
+    assert_bits(host(gpu(A, B, out=out)), oracle.gemm(Ah, Bh, threads=oracle_threads()), f"L2 {a}{b}{c} {case[:5]}")
     assert g.gemm_f16_device_status() == 0

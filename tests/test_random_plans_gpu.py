@@ -17,7 +17,8 @@ pytestmark = pytest.mark.gpu
 
 DEV = torch.device("cuda:0")
 OPTIONS = (g.OPT_FORCE_GATHER, g.OPT_SPLITS, g.OPT_TILE_N, g.OPT_PANEL, g.OPT_SWAP, g.OPT_PAIR, g.OPT_STREAMK,
-           g.OPT_TAIL_SPLIT, g.OPT_MAX_STAGES, g.OPT_REPACK, g.OPT_PDL)
+           g.OPT_TAIL_SPLIT, g.OPT_MAX_STAGES, g.OPT_REPACK, g.OPT_PDL,
+           g.OPT_L2_A, g.OPT_L2_B, g.OPT_L2_C)
 
 
 def _reset():
@@ -67,7 +68,10 @@ def _options(rng):
              (0.1, g.OPT_TAIL_SPLIT, lambda: 1),
              (0.1, g.OPT_MAX_STAGES, lambda: int(rng.choice([2, 4, 6]))),
              (0.2, g.OPT_REPACK, lambda: int(rng.integers(1, 3))),
-             (0.1, g.OPT_PDL, lambda: 1))
+             (0.1, g.OPT_PDL, lambda: 1),
+             (0.15, g.OPT_L2_A, lambda: int(rng.integers(1, 4))),
+             (0.15, g.OPT_L2_B, lambda: int(rng.integers(1, 4))),
+             (0.15, g.OPT_L2_C, lambda: int(rng.integers(1, 4))))
     return {o: f() for p, o, f in draws if rng.random() < p}
 
 
