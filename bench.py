@@ -707,8 +707,9 @@ def report(args, w, plan, peaks, bnd, flops, nbytes, ms_per_step, value, wall, c
         "wall_s_timed_region": round(wall, 4),
         "clocks": clk,
         "e2e": e2e,
-        # the GEMM kernel, plus one aligned-copy kernel when an operand is repacked
-        "gpu_launches": args.steps * (2 if plan["repack"] else 1),
+        # the GEMM kernel, plus the copy of operands TMA cannot address into an
+        # aligned buffer (repack bits 0-1) and the copy of C out of one (bit 2)
+        "gpu_launches": args.steps * (1 + (1 if plan["repack"] & 3 else 0) + (1 if plan["repack"] & 4 else 0)),
         "roofline": roof,
         "cpu_baseline": cpu,
         "device_status": status,

@@ -327,6 +327,8 @@ struct Plan {
     bool fused;   // launch the kernels with the fused output stage
     int ncopies;  // repack copies to run before the GEMM (A', B', up projection)
     gemm_f16_dev::RepackArgs copies[3];
+    bool unpack;  // C goes through an aligned buffer, then this copy moves it into place
+    gemm_f16_dev::UnpackArgs out;
     KernelParams kp;
     size_t counter_bytes;   // split-K counters: align256(4 * tiles)
     size_t partial_bytes;   // split-K partials: align256(4 * units * tile_m * tile_n)
@@ -591,10 +593,14 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
     // multiple of 8 rows, A is not read MN-major through TMA (it is gathered, or
     // copied K-major below).
     bool a_mn_tma_ok = true;
+    // (the one-copy 3-D box of an MN-major A addresses whole 64-row swizzle
+    // atoms, so a grouped A takes it only when every group starts on one)
+    bool a_3d_groups_ok = true;
     if (grouped) {
         int64_t r0 = 0;
         for (int64_t g = 0; g < a.batch; ++g) {
             if (a.rows[g] > 0 && r0 % 8 != 0) a_mn_tma_ok = false;
+            if (a.rows[g] > 0 && r0 % 64 != 0) a_3d_groups_ok = false;
             r0 += a.rows[g];
         }
     }
@@ -617,12 +623,24 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
     // products, forced gathers and the entry points that may not allocate.
     pl->ncopies = 0;
     int repacked = 0;
+    // MN extent the 3-D box maps see: the operand's, or for an MN-major copy
+    // its rows rounded up to whole 64-element atoms (the copy's pitch covers
+    // them and the copy zero-fills them), so that the copy always takes the
+    // one-box-per-stage form.
+    int64_t a_mn_ext = Mv, b_mn_ext = Nv;
     {
         const int64_t rp = opt(GEMM_F16_OPT_REPACK);
         const double work = 2.0 * static_cast<double>(Mv) * static_cast<double>(Nv) * static_cast<double>(a.K) *
                             static_cast<double>(batched ? a.batch : 1);
         const bool want_a = !ca.tma && !(fg & 1), want_b = !cb.tma && !(fg & 2);
-        if (a.repack && have_tma && rp != 1 && (rp == 2 || work >= kRepackMinFlops) && (want_a || want_b)) {
+        // C that TMA cannot store in place (unaligned base or pitch, or N not a
+        // multiple of 8) but whose tiles could go out by TMA: stored into an
+        // aligned buffer and moved into place by the unpack copy.
+        const bool c_in_place = a.N % 8 == 0 && (reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 &&
+                                (a.ldc * 2) % 16 == 0 && (a.ldc * 2) < (int64_t(1) << 40) && (!c_bd || bs_ok(c_bs));
+        const bool want_c = !c_in_place && !(fg & 4) && !swap && splits == 1 && out_cols % 64 == 0 &&
+                            a.M < (int64_t(1) << 32) && a.N < (int64_t(1) << 32);
+        if (a.repack && have_tma && rp != 1 && (rp == 2 || work >= kRepackMinFlops) && (want_a || want_b || want_c)) {
             struct Layout {
                 bool mn;   // rows of the copy run along MN (MN-major result)
                 int64_t rows, cols, s_r, s_c, pitch, nb, s_b;
@@ -634,7 +652,8 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
                 l.cols = l.mn ? MN : a.K;
                 l.s_r = l.mn ? s_k : s_mn;
                 l.s_c = l.mn ? s_mn : s_k;
-                l.pitch = round_up(l.cols, 8);
+                // (MN-major copies: whole 64-element swizzle atoms per row)
+                l.pitch = round_up(l.cols, l.mn ? 64 : 8);
                 l.nb = bd ? a.batch : 1;
                 l.s_b = bd ? bs : 0;
                 return l;
@@ -653,7 +672,11 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
             auto bytes_of = [](const Layout& l) {
                 return static_cast<size_t>(round_up(2 * l.nb * l.rows * l.pitch, 256));
             };
-            const size_t need = (do_a ? bytes_of(la) : 0) + (do_b ? (gated ? 2 : 1) * bytes_of(lb) : 0);
+            // the aligned C buffer: rows of C, pitch N rounded up to 8 elements
+            const int64_t c_pitch = round_up(a.N, 8), c_nb = c_bd ? a.batch : 1;
+            const size_t c_bytes = want_c ? static_cast<size_t>(round_up(2 * c_nb * a.M * c_pitch, 256)) : 0;
+            const size_t need =
+                (do_a ? bytes_of(la) : 0) + (do_b ? (gated ? 2 : 1) * bytes_of(lb) : 0) + c_bytes;
             char* buf = need ? static_cast<char*>(repack_buffer(need, plan_only, stream)) : nullptr;
             if (need && !buf) return GEMM_F16_ERR_OUT_OF_MEMORY;
             auto add_copy = [&](const Layout& l, const __half* src) {
@@ -672,6 +695,7 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
                 if (a_bd) a_bs = la.rows * la.pitch;
                 ca = choose_operand(kp.A, kp.a_sm, kp.a_sk, Mv, a.K, gemm_f16_dev::kBM,
                                     have_tma && (!a_bd || bs_ok(a_bs)));
+                if (la.mn) a_mn_ext = round_up(Mv, 64);
                 repacked |= 1;
             }
             if (do_b) {
@@ -681,7 +705,22 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
                 kp.b_sk = lb.mn ? lb.pitch : 1;
                 if (b_bd) b_bs = lb.rows * lb.pitch;
                 cb = choose_operand(kp.B, kp.b_sn, kp.b_sk, Nv, a.K, tile_b, have_tma && (!b_bd || bs_ok(b_bs)));
+                if (lb.mn) b_mn_ext = round_up(Nv, 64);
                 repacked |= 2;
+            }
+            if (want_c) {
+                // the kernel writes C' into the aligned buffer (by TMA, and the
+                // few per-thread stores a grouped tile may take); the unpack copy
+                // then writes only the M x N view of the caller's C
+                __half* cs = reinterpret_cast<__half*>(buf);
+                gemm_f16_dev::UnpackArgs& u = pl->out;
+                u.src = cs, u.spitch = c_pitch, u.sbs = a.M * c_pitch;
+                u.dst = static_cast<__half*>(a.C), u.ldc = a.ldc, u.dbs = c_bd ? a.scb : 0;
+                u.rows = a.M, u.cols = a.N, u.batch = c_nb;
+                pl->unpack = true;
+                kp.C = cs, kp.c_sm = c_pitch, kp.c_sn = 1;
+                if (c_bd) c_bs = a.M * c_pitch;
+                repacked |= 4;
             }
         }
     }
@@ -720,7 +759,8 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
     const uint64_t nb_a = a_bd ? a.batch : 0, bst_a = a_bd ? 2 * a_bs : 0;
     const uint64_t nb_b = b_bd ? a.batch : 0, bst_b = b_bd ? 2 * b_bs : 0;
     if (ca.tma) {
-        a_3d = ca.mn && encode_3d_mn(&kp.tmA, kp.A, Mv, a.K, a.K == 1 ? round_up(2 * Mv, 16) : 2 * kp.a_sk,
+        a_3d = ca.mn && (!grouped || a_3d_groups_ok) &&
+               encode_3d_mn(&kp.tmA, kp.A, a_mn_ext, a.K, a.K == 1 ? round_up(2 * Mv, 16) : 2 * kp.a_sk,
                                      gemm_f16_dev::kBM / 64, nb_a, bst_a);
         const bool ok = a_3d ? true
                         : ca.mn ? encode_2d(&kp.tmA, kp.A, Mv, a.K, a.K == 1 ? round_up(2 * Mv, 16) : 2 * kp.a_sk, 64, 64,
@@ -737,7 +777,7 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
     auto encode_b = [&]() {
         const int cols = gated ? out_cols : bcols;
         auto enc = [&](CUtensorMap* tm, const __half* ptr) {
-            b_3d = cb.mn && encode_3d_mn(tm, ptr, Nv, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk,
+            b_3d = cb.mn && encode_3d_mn(tm, ptr, b_mn_ext, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk,
                                          static_cast<uint32_t>(cols / 64), nb_b, bst_b);
             return b_3d ? true
                    : cb.mn ? encode_2d(tm, ptr, Nv, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk, 64, 64, nb_b,
@@ -756,11 +796,13 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
     // TMA stores write whole 16-byte chunks at the N edge, so a C row whose
     // width is not a multiple of 8 elements would get its pitch padding
     // overwritten: such a C goes through the masked stores.
-    bool c_tma = have_tma && !(fg & 4) && !swap && splits == 1 && out_cols % 64 == 0 && a.N % 8 == 0 &&
-                 (reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc * 2) % 16 == 0 && a.M < (int64_t(1) << 32) &&
-                 a.N < (int64_t(1) << 32) && (a.ldc * 2) < (int64_t(1) << 40) && (!c_bd || bs_ok(c_bs));
-    if (c_tma)
-        c_tma = encode_2d(&kp.tmC, a.C, a.N, a.M, 2 * a.ldc, 64, 32, c_bd ? a.batch : 0, c_bd ? 2 * c_bs : 0);
+    bool c_tma = pl->unpack ||
+                 (have_tma && !(fg & 4) && !swap && splits == 1 && out_cols % 64 == 0 && a.N % 8 == 0 &&
+                  (reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc * 2) % 16 == 0 && a.M < (int64_t(1) << 32) &&
+                  a.N < (int64_t(1) << 32) && (a.ldc * 2) < (int64_t(1) << 40) && (!c_bd || bs_ok(c_bs)));
+    if (c_tma)   // (kp.C / kp.c_sm: the caller's C, or the aligned buffer)
+        c_tma = encode_2d(&kp.tmC, kp.C, a.N, a.M, 2 * kp.c_sm, 64, 32, c_bd ? a.batch : 0, c_bd ? 2 * c_bs : 0);
+    if (pl->unpack && !c_tma) return GEMM_F16_ERR_LAUNCH;
     kp.a_bdim = (ca.tma && a_bd) ? 1u : 0u;
     kp.b_bdim = (cb.tma && b_bd) ? 1u : 0u;
     kp.c_bdim = (c_tma && c_bd) ? 1u : 0u;
@@ -824,7 +866,7 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
         // Tail pieces read B through a box of their own width (the 2-D N-major
         // form already reads one 64-column box per atom column).
         const int piece = bcols / sch.tail_split;
-        const bool ok = b_3d ? encode_3d_mn(&kp.tmB2, kp.B, Nv, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk,
+        const bool ok = b_3d ? encode_3d_mn(&kp.tmB2, kp.B, b_mn_ext, a.K, a.K == 1 ? round_up(2 * Nv, 16) : 2 * kp.b_sk,
                                             static_cast<uint32_t>(piece / 64), nb_b, bst_b)
                              : encode_2d(&kp.tmB2, kp.B, a.K, Nv, Nv == 1 ? round_up(2 * a.K, 16) : 2 * kp.b_sn, 64,
                                          static_cast<uint32_t>(piece), nb_b, bst_b);
@@ -832,8 +874,13 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
     }
     // Raster panel (tile rows whose tiles run side by side): 8 by default;
     // launches of at most four waves of tiles take 2, which measured 2 % faster
-    // on 4096^3 (wider panels measured faster from 6144^3 up).
-    const int default_panel = tiles <= 4 * static_cast<int64_t>(sch.workers) ? 2 : 8;
+    // on 4096^3 (wider panels measured faster from 6144^3 up).  So do launches
+    // with at most 16 tile columns (e.g. the MoE shape's 8): there a panel of 8
+    // tile rows spreads each A row panel's tiles over two waves, and the second
+    // wave re-reads it from HBM (131072 x 2048 x 7168: 4.71 GB of DRAM reads
+    // with panels of 8, 3.65 GB with panels of 2, the same time).
+    const int default_panel =
+        (tiles <= 4 * static_cast<int64_t>(sch.workers) || tiles_n <= 16) ? 2 : 8;
     kp.panel = static_cast<int>(panel > 0 ? panel : default_panel);
     kp.BN = BN, kp.stages = stages;
     kp.a_flags = (ca.tma ? gemm_f16_dev::kOpTma : 0u) | (ca.mn ? gemm_f16_dev::kOpMnMajor : 0u) |
@@ -982,6 +1029,16 @@ gemm_f16_status launch(Plan& pl, DevInfo& dev, float* partials, int* counters, c
     if (e != cudaSuccess) {
         cudaGetLastError();
         return GEMM_F16_ERR_LAUNCH;
+    }
+    if (pl.unpack) {   // C from the aligned buffer into place, after the GEMM on the same stream
+        const int64_t items = gemm_f16_dev::unpack_items(pl.out);
+        const int64_t per_block = 8 * gemm_f16_dev::kUnpackUnroll;   // 8 warps, each kUnpackUnroll items a pass
+        const int64_t blocks = std::min<int64_t>((items + per_block - 1) / per_block, static_cast<int64_t>(dev.sms) * 8);
+        config(cfg, attr, static_cast<unsigned>(std::max<int64_t>(blocks, 1)), gemm_f16_dev::kRepackThreads, 0, 1);
+        if (cudaLaunchKernelEx(&cfg, gemm_f16_dev::unpack_rows, pl.out) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_F16_ERR_LAUNCH;
+        }
     }
     if (cudaGetLastError() != cudaSuccess) return GEMM_F16_ERR_LAUNCH;
     return GEMM_F16_OK;

@@ -94,8 +94,13 @@ typedef enum {
  * kernel with bounds-checked loads (products under 1e9 FLOPs) or first copied
  * once, by a separate HBM-bound kernel on `stream`, into an aligned buffer of
  * the library workspace (rows along the operand's smaller stride, pitch a
- * multiple of 8 elements) that the GEMM then reads through TMA: the padding
- * form of boundary handling.  Results are identical either way.
+ * multiple of 8 elements, of 64 when the rows run along M or N) that the GEMM
+ * then reads through TMA: the padding
+ * form of boundary handling.  Likewise a C that TMA cannot store in place (an
+ * unaligned base, a pitch or N that is not a multiple of 8 elements) is, for
+ * such products, stored by TMA into an aligned buffer of the workspace and
+ * then copied into the M x N view by a second HBM-bound kernel, which writes
+ * no element outside the view.  Results are identical either way.
  *
  * Ownership: the caller owns A, B and C; they must stay valid until the work
  * on `stream` completes.  For shapes that use split-K, and for the aligned
@@ -328,7 +333,8 @@ typedef struct {
     int cluster_ctas;       /* CTAs per cluster: 1, or 2 (pair form) */
     int fused;              /* the fused output stage runs (gemm_f16_fused_get_plan) */
     int gated;              /* gate/up form: tile_n output columns, 2 * tile_n accumulator columns */
-    int repack;             /* bit 0: A, bit 1: B (and B_up) copied to an aligned buffer before the GEMM */
+    int repack;             /* bit 0: A, bit 1: B (and B_up) copied to an aligned buffer before the GEMM;
+                               bit 2: C written to an aligned buffer, then copied into place */
 } gemm_f16_plan;
 
 /* Fill *plan for the given arguments without launching anything.  Returns the
@@ -352,7 +358,7 @@ gemm_f16_status gemm_f16_fused_get_plan(const void* A, int64_t stride_am, int64_
  *                              segments (clamped to the K blocks); replaces stream-K
  *   GEMM_F16_OPT_TILE_N        > 0: force the tile width (multiple of 64, <= 256)
  *   GEMM_F16_OPT_PANEL         > 0: tile-rows per rasterisation panel (default 8, or 2 when the
- *                              launch has at most four waves of tiles)
+ *                              launch has at most four waves of tiles or at most 16 tile columns)
  *   GEMM_F16_OPT_SWAP          0 auto, 1 never swap, 2 always swap
  *   GEMM_F16_OPT_TIMEOUT_MS    bounded-wait limit in ms (default 1000)
  *   GEMM_F16_OPT_MAX_CTAS      > 0: cap the persistent grid

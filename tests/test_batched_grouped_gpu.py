@@ -268,6 +268,8 @@ def test_full_size_workload_sampled(w):
     ([130, 77, 301], 256, 96, {}),                              # A column-major, group starts 130, 207
     ([130, 77, 301], 256, 96, {g.OPT_REPACK: 2}),               # ... through the aligned copy (K-major)
     ([512, 384, 640], 512, 136, {}),                            # starts on multiples of 8: MN-major TMA A
+    ([8, 120, 64, 64], 256, 136, {}),                           # starts 0, 8, 128, 192: MN-major TMA A in
+    ([200, 56, 256], 256, 96, {}),                              # 64-row boxes only where a group starts on one
 ])
 def test_grouped_column_major_a(rows, N, K, opts):
     """A whose rows are contiguous in memory (a transposed view, or K = 1): in a
@@ -286,4 +288,22 @@ def test_grouped_column_major_a(rows, N, K, opts):
     C = g.grouped_fused_mm(A, dev(Bh), rows, act="relu", b_up=dev(U))
     torch.cuda.synchronize()
     assert_bits(C.cpu().numpy(), oracle.gemm_fused_grouped(Ah, Bh, rows, U, act="relu"), "fused, column-major A")
+    assert g.gemm_f16_device_status() == 0
+
+
+@pytest.mark.parametrize("rows,K", [([8, 120, 64, 64], 136), ([200, 56, 259], 96), ([64, 1000], 72)])
+def test_grouped_column_major_a_through_the_aligned_copy(rows, K):
+    """A column-major A whose pitch (total rows + 3) TMA cannot take, copied to
+    an aligned MN-major buffer whose rows are padded to whole 64-row atoms and
+    read with the one-box-per-stage form where the group starts allow it."""
+    g.gemm_f16_set_option(g.OPT_REPACK, 2)
+    N = 256
+    rng = np.random.default_rng(sum(rows) * 7 + K)
+    Ah, Bh = ints(rng, (sum(rows), K)), ints(rng, (len(rows), K, N))
+    buf = torch.full((K, sum(rows) + 3), float("nan"), dtype=torch.float16)
+    buf[:, :sum(rows)] = torch.from_numpy(np.ascontiguousarray(Ah.T))
+    A = buf.to(DEV)[:, :sum(rows)].t()                                # strides (1, rows + 3)
+    C = g.grouped_mm(A, dev(Bh), rows)
+    torch.cuda.synchronize()
+    assert_bits(C.cpu().numpy(), oracle.gemm_grouped(Ah, Bh, rows), f"grouped, copied column-major A {rows}")
     assert g.gemm_f16_device_status() == 0
