@@ -104,7 +104,8 @@ struct KernelParams {
     CUtensorMap tmA;   // A' (K-major: dims {K, M}; MN-major: dims {M, K})
     CUtensorMap tmB;   // B' (K-major: dims {K, N}; MN-major: dims {N, K})
     CUtensorMap tmB2;  // B' with the box of a tail piece (tail_split > 1): as narrow as the piece
-    CUtensorMap tmC;   // C  (dims {N, M}, box 64 x 32)
+    CUtensorMap tmC;   // C  (dims {N, M}, box 64 x 32): one epilogue warp's rows
+    CUtensorMap tmC4;  // C  with a box of 64 x 128: the four epilogue warps' rows in one store
     CUtensorMap tmBu;  // gated fused stage: the up projection's B' (the geometry of tmB)
     const __half* A;   // A'[m,k] = A[m*a_sm + k*a_sk]
     int64_t a_sm, a_sk;
@@ -1353,7 +1354,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
         if (b_tma) tma_prefetch_desc(&p.tmB);
         if (b_tma && p.tail_split > 1) tma_prefetch_desc(&p.tmB2);
         if (b_tma && gated) tma_prefetch_desc(&p.tmBu);
-        if (p.c_tma) tma_prefetch_desc(&p.tmC);
+        if (p.c_tma) {
+            tma_prefetch_desc(&p.tmC);
+            tma_prefetch_desc(&p.tmC4);
+        }
     }
     if (warp == kMmaWarp) {
         if (kPair) {
@@ -1601,6 +1605,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
             // group must not spill into the next group's rows
             const int64_t crow = ug.a_row + m0 + 32 * q;
             const bool ctma = p.c_tma && (!kMulti || p.gmode != 2 || crow + 32 <= ug.row_lim);
+            // Whole tiles whose 128 rows all go out by TMA store take one
+            // 64 x 128 box per 64 columns for the CTA (four times fewer stores
+            // than a box per warp; measured 4-5 % faster on the batched 32 x
+            // 1024^3 launch, the same elsewhere).  The same for all four
+            // epilogue warps.
+            const bool cta_store = p.c_tma && (!kMulti || p.gmode != 2 || ug.a_row + m0 + kBM <= ug.row_lim);
             // fused stage: this problem's bias vectors, and the row's own bias
             // value when the bias runs along the kernel view's rows
             const __half* bias = nullptr;
@@ -1618,6 +1628,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                                                    gated ? w.bn / 2 : w.bn, gated, crow, ctma, group_count);
             } else if (w.slot < 0) {
                 uint32_t buf = 0;
+                // Stores of the previous unit may still read the epilogue buffer:
+                // the whole-CTA boxes (issued by one thread) cover every warp's part
+                // of it, so before this unit stages anything that thread's stores
+                // are done reading (each warp tracks its own per-warp boxes).
+                if (threadIdx.x == kEpiLead) bulk_wait_group_read<0>();
+                if (cta_store && lane == 0) bulk_wait_group_read<0>();
+                named_bar_sync(1, 128);
                 for (int pc = 0; pc < npieces; pc += 4) {
                     // up to four pieces (64 columns) in flight per TMEM wait
                     const int cnt = min(4, npieces - pc);
@@ -1636,47 +1653,67 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                                 mbar_arrive(tempty);
                         }
                     }
+                    if (cta_store) {
+                        // the CTA's staging box for these 64 columns: 128 rows, this
+                        // warp's 32 of them; one thread stores it once all are staged
+                        buf = L.epi + (group_count & 1u) * (4u * kEpiBufBytes) + q * kEpiBufBytes;
+                        if (threadIdx.x == kEpiLead) bulk_wait_group_read<1>();   // box free (two stores back)
+                        named_bar_sync(1, 128);
+                    } else if (ctma || p.c_stage) {
+                        buf = L.epi + (q * 2 + (group_count & 1u)) * kEpiBufBytes;
+                        if (lane == 0) bulk_wait_group_read<1>();
+                        __syncwarp();
+                    }
 #pragma unroll
                     for (int h2 = 0; h2 < 4; ++h2) {
                         if (h2 >= cnt) break;
                         const int piece = pc + h2;
                         uint32_t h[8];
                         convert16(r + 16 * h2, h);
-                        if (ctma || p.c_stage) {
-                            const int j0 = (piece & 3) * 2;        // 16-byte chunk inside the 128-byte row
-                            if ((piece & 3) == 0) {
-                                buf = L.epi + (q * 2 + (group_count & 1u)) * kEpiBufBytes;
-                                if (lane == 0) bulk_wait_group_read<1>();
-                                __syncwarp();
-                            }
+                        if (cta_store || ctma || p.c_stage) {
+                            const int j0 = h2 * 2;        // 16-byte chunk inside the 128-byte row
                             st_smem_v4(buf + lane * 128 + ((j0 ^ (lane & 7)) << 4), make_uint4(h[0], h[1], h[2], h[3]));
                             st_smem_v4(buf + lane * 128 + (((j0 + 1) ^ (lane & 7)) << 4),
                                        make_uint4(h[4], h[5], h[6], h[7]));
-                            if (!ctma && ((piece & 3) == 3 || piece == npieces - 1)) {
-                                __syncwarp();
-                                store_box_rows(p, ug.C, ug.row_lim, buf, crow, n0 + 16 * (piece & ~3),
-                                               16 * ((piece & 3) + 1));
-                                __syncwarp();   // the box is read before the next piece overwrites it
-                            } else if ((piece & 3) == 3 || piece == npieces - 1) {
-                                fence_proxy_async_smem();
-                                __syncwarp();
-                                if (lane == 0) {
-                                    // (a box wholly below row M, e.g. the second CTA's rows of a
-                                    // pair tile on the last row, is not stored)
-                                    if (crow < ug.row_lim) {
-                                        const int32_t xn = static_cast<int32_t>(n0 + 16 * (piece & ~3));
-                                        if (kMulti && p.c_bdim)
-                                            tma_store_3d_l2(&p.tmC, buf, xn, static_cast<int32_t>(crow), ug.cz, p.l2_c);
-                                        else
-                                            tma_store_2d_l2(&p.tmC, buf, xn, static_cast<int32_t>(crow), p.l2_c);
-                                    }
-                                    bulk_commit_group();
-                                }
-                                ++group_count;
-                            }
                         } else {
                             store_piece_masked(p, ug.C, ug.row_lim, ug.a_row + m0 + row, n0 + 16 * piece, h);
                         }
+                    }
+                    const int32_t xn = static_cast<int32_t>(n0 + 16 * pc);
+                    if (cta_store) {
+                        fence_proxy_async_smem();
+                        named_bar_sync(1, 128);
+                        if (threadIdx.x == kEpiLead) {
+                            const int64_t crow0 = ug.a_row + m0;   // (rows past M are clipped by the map)
+                            const uint32_t box = L.epi + (group_count & 1u) * (4u * kEpiBufBytes);
+                            if (crow0 < ug.row_lim) {
+                                if (kMulti && p.c_bdim)
+                                    tma_store_3d_l2(&p.tmC4, box, xn, static_cast<int32_t>(crow0), ug.cz, p.l2_c);
+                                else
+                                    tma_store_2d_l2(&p.tmC4, box, xn, static_cast<int32_t>(crow0), p.l2_c);
+                            }
+                            bulk_commit_group();
+                        }
+                        ++group_count;
+                    } else if (ctma) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            // (a box wholly below row M, e.g. the second CTA's rows of a
+                            // pair tile on the last row, is not stored)
+                            if (crow < ug.row_lim) {
+                                if (kMulti && p.c_bdim)
+                                    tma_store_3d_l2(&p.tmC, buf, xn, static_cast<int32_t>(crow), ug.cz, p.l2_c);
+                                else
+                                    tma_store_2d_l2(&p.tmC, buf, xn, static_cast<int32_t>(crow), p.l2_c);
+                            }
+                            bulk_commit_group();
+                        }
+                        ++group_count;
+                    } else if (p.c_stage) {
+                        __syncwarp();
+                        store_box_rows(p, ug.C, ug.row_lim, buf, crow, n0 + 16 * pc, 16 * cnt);
+                        __syncwarp();   // the box is read before the next piece overwrites it
                     }
                 }
             } else {

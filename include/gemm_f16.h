@@ -390,8 +390,12 @@ gemm_f16_status gemm_f16_fused_get_plan(const void* A, int64_t stride_am, int64_
  *   GEMM_F16_OPT_L2_A, _L2_B   L2 eviction policy of the TMA loads of the kernel's A and B
  *   GEMM_F16_OPT_L2_C          operands and of the TMA stores of C (the kernel computes
  *                              C^T = B^T A^T when the plan swaps, so its A is then the
- *                              caller's B): 1 none, 2 evict first, 3 evict last; 0 default
- *                              (none)
+ *                              caller's B): 1 none, 2 evict first, 3 evict last; 0 default:
+ *                              A evict first, B evict last and C evict first for one-problem,
+ *                              non-gated launches of several waves whose A is at least 256 MB,
+ *                              whose B is at most 48 MB and whose raster keeps each A row
+ *                              panel within one wave (at most 16 tile columns, raster panels
+ *                              of at most 2 rows); none otherwise
  *   GEMM_F16_OPT_TEST_STALL    failure-detection test: 1 makes every CTA's MMA issuer wait
  *                              first on a barrier that nothing arrives on, so the bounded
  *                              wait runs out (after GEMM_F16_OPT_TIMEOUT_MS), the kernel
