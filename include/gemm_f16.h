@@ -375,8 +375,9 @@ gemm_f16_status gemm_f16_fused_get_plan(const void* A, int64_t stride_am, int64_
  *                              down to an even count (default: as many as shared memory
  *                              holds, at most 16)
  *   GEMM_F16_OPT_REPACK        0 default: operands TMA cannot address are copied to an
- *                              aligned buffer for products of at least 1e9 FLOPs and
- *                              gathered below; 1 always gather; 2 always copy
+ *                              aligned buffer, and a C TMA cannot store in place goes out
+ *                              through one, for products of at least 1e9 FLOPs (gathered
+ *                              operands and row-wise C stores below); 1 never; 2 always
  *   GEMM_F16_OPT_PDL           0 default: every kernel is launched as a programmatic dependent
  *                              of the kernel before it on the stream (its set-up overlaps that
  *                              kernel's tail; it reads and writes memory only after that kernel
