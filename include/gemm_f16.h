@@ -363,7 +363,9 @@ gemm_f16_status gemm_f16_fused_get_plan(const void* A, int64_t stride_am, int64_
  *   GEMM_F16_OPT_TIMEOUT_MS    bounded-wait limit in ms (default 1000)
  *   GEMM_F16_OPT_MAX_CTAS      > 0: cap the persistent grid
  *   GEMM_F16_OPT_PAIR          0 default (2-CTA pair tiles for 256-wide tiles of TMA
- *                              operands without split-K), 1 never, 2 also for 128-wide tiles
+ *                              operands without split-K, and for swapped small-M plans whose
+ *                              B, the caller's A, is K-major), 1 never, 2 also for 128-wide
+ *                              tiles
  *   GEMM_F16_OPT_STREAMK       0 default: stream-K tail when an operand is gathered (not
  *                              TMA-addressable) or when a swapped (small-M) plan has fewer
  *                              tiles than the device has SMs, whole tiles otherwise; 1: whole

@@ -600,3 +600,21 @@ def test_l2_policies_do_not_change_results(case, a, b, c):
     assert plan["a_tma"] and plan["b_tma"] and plan["c_tma"] and not plan["repack"], plan
     assert_bits(host(gpu(A, B, out=out)), oracle.gemm(Ah, Bh, threads=oracle_threads()), f"L2 {a}{b}{c} {case[:5]}")
     assert g.gemm_f16_device_status() == 0
+
+
+# ---------------------------------------------- swapped form on CTA pairs
+@pytest.mark.parametrize("M,N,K", [(16, 4096, 1024), (48, 2048, 520), (8, 3000, 640), (40, 16384, 2048)])
+def test_swapped_small_m_on_pairs(M, N, K):
+    """Small M computed as C^T = B^T A^T on 2-CTA pairs (M = 256 per MMA, each
+    CTA loading half of the BN activation rows): the default for a row-major A."""
+    rng = np.random.default_rng(M * 31 + N + K)
+    Ah = rng.integers(-3, 4, (M, K)).astype(np.float16)
+    Bh = rng.integers(-3, 4, (K, N)).astype(np.float16)
+    A, B = to_dev(Ah), to_dev(Bh)
+    out = torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV)
+    plan = g.plan_for(A, B, out)
+    assert plan["swap_ab"] and plan["pair"] and plan["tile_m"] == 256, plan
+    C = host(gpu(A, B, out=out))
+    assert_bits(C, oracle.gemm(Ah, Bh, threads=oracle_threads()), f"swapped pairs {M}x{N}x{K}")
+    assert_bits(host(gpu(A, B, out=out)), C, "repeatable")
+    assert g.gemm_f16_device_status() == 0
