@@ -152,3 +152,11 @@ def test_cpu_baseline_labels_its_sample_and_adds_a_single_thread_run():
     cpu = bench.cpu_baseline(big, 0.05, 1)
     assert "single_thread" not in cpu and cpu["full_workload_s_kind"].startswith("extrapolated")
     assert cpu["full_workload_s"] > 0
+
+
+def test_vs_baseline_only_for_the_pages_own_workload():
+    # the pages measured only the MoE-flattened shape (117.25 TFLOPS on a C500)
+    v, ref = bench.vs_pages("moe_131072x2048x7168", 1800.0, "TFLOP/s")
+    assert v == pytest.approx(1800.0 / 117.25, abs=1e-3) and "C500" in ref
+    assert bench.vs_pages("square_4096", 1500.0, "TFLOP/s") == (None, None)
+    assert bench.vs_pages("moe_131072x2048x7168", 1800.0, "GB/s") == (None, None)
