@@ -227,3 +227,26 @@ def test_c_through_the_aligned_buffer_batched_grouped_fused():
     torch.cuda.synchronize()
     _check_view_and_padding(buf, C, oracle.gemm_fused(Ah, Bh, act="relu", bias=bias), "fused via buffer")
     assert g.gemm_f16_device_status() == 0
+
+
+@pytest.mark.parametrize("N", [1, 9, 255, 256, 257, 511, 513, 1000])
+def test_c_copy_every_alignment_offset(N):
+    """The C copy for every 2-byte offset of the view's base inside a 16-byte
+    word (offsets 0..7 elements) and ragged segment ends: the view bit for bit,
+    nothing outside it written."""
+    g.gemm_f16_set_option(g.OPT_REPACK, 2)
+    rng = np.random.default_rng(N)
+    M, K = 200, 64   # (M > 64: no swapped plan)
+    Ah = rng.integers(-3, 4, (M, K)).astype(np.float16)
+    Bh = rng.integers(-3, 4, (K, N)).astype(np.float16)
+    A, B = torch.from_numpy(Ah).to(DEV), torch.from_numpy(Bh).to(DEV)
+    ref = oracle.gemm(Ah, Bh)
+    for off in range(8):
+        ldc = N + 3 + off   # a pitch that is not a multiple of 8 for most offsets
+        buf, C = _padded_out(M, N, ldc, off)
+        plan = g.plan_for(A, B, C)
+        assert plan["repack"] & 4 and not plan["swap_ab"], plan
+        g.matmul(A, B, out=C)
+        torch.cuda.synchronize()
+        _check_view_and_padding(buf, C, ref, f"N={N} offset={off}")
+    assert g.gemm_f16_device_status() == 0
