@@ -793,7 +793,8 @@ def main():
     ap.add_argument("--cpu-threads", type=int, default=0,
                     help="threads of the CPU oracle baseline (default: every host core)")
     ap.add_argument("--opt", action="append", default=[],
-                    help="library tuning knob NAME=VALUE (force_gather, splits, tile_n, panel, swap, max_ctas)")
+                    help="library tuning knob NAME=VALUE, NAME an option of the library without its OPT_ prefix "
+                         "(force_gather, splits, tile_n, panel, swap, max_ctas, l2_a, two_k_loads, ...)")
     args = ap.parse_args()
     if args.opt and args.impl == "ours":
         import dense_tiled_gemm_fp16_gb300 as g

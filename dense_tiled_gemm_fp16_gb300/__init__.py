@@ -59,6 +59,7 @@ OPT_DEBUG_BOUNDS = 16
 OPT_L2_A = 17
 OPT_L2_B = 18
 OPT_L2_C = 19
+OPT_TWO_K_LOADS = 20
 
 # Activations of the fused output stage (gemm_f16_fused and friends).
 ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU = range(4)
@@ -88,7 +89,7 @@ class Plan(ctypes.Structure):
         "swap_ab", "pair", "a_tma", "a_mn_major", "b_tma", "b_mn_major", "c_tma",
         "tile_m", "tile_n", "tiles_m", "tiles_n", "splits", "kblocks", "units", "grid",
         "stages", "streamk_tiles", "tail_split", "smem_bytes")] + [("workspace_bytes", ctypes.c_size_t)] + [
-        (n, ctypes.c_int) for n in ("a_box3d", "b_box3d", "cluster_ctas", "fused", "gated", "repack")]
+        (n, ctypes.c_int) for n in ("a_box3d", "b_box3d", "cluster_ctas", "fused", "gated", "repack", "two_k_loads")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

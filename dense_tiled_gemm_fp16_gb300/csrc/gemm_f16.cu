@@ -53,7 +53,7 @@ struct Workspace {
 };
 Workspace g_ws[kMaxDevices];
 
-std::atomic<int64_t> g_opt[20];
+std::atomic<int64_t> g_opt[21];
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 PFN_cuMemGetAddressRange_v3020 g_addr_range = nullptr;
@@ -318,6 +318,40 @@ bool encode_3d_mn(CUtensorMap* tm, const void* ptr, uint64_t MN, uint64_t K, uin
     CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, nb > 0 ? 4 : 3, const_cast<void*>(ptr), dims, strides,
                           box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Operand X' (MN extent mn, K extent K, rows or K rows pitch_bytes apart)
+// with the 64-wide K block as an outer dimension, so that one box of two
+// blocks lands in two consecutive pipeline slots, each laid out as the
+// one-block box would lay it out.  K-major: {64 K, mn, K / 64}, box
+// {64, box_mn, 2}; MN-major (mn a multiple of 64): {64 MN, 64 K, mn / 64,
+// K / 64}, box {64, 64, box_mn / 64, 2}; then the batch dimension, if any.
+// Only whole K blocks are addressable: a ragged last block, whose missing
+// columns a box must zero-fill, is read through the one-block map.
+bool encode_two_k(CUtensorMap* tm, const void* ptr, bool mn_major, uint64_t mn, uint64_t K, uint64_t pitch_bytes,
+                  uint32_t box_mn, uint64_t nb, uint64_t bstride_bytes)
+{
+    if (!g_encode || K < 128 || (mn_major && mn % 64 != 0)) return false;
+    cuuint64_t dims[5] = {64, mn, K / 64, 0, 0};
+    cuuint64_t strides[4] = {pitch_bytes, 128, 0, 0};
+    cuuint32_t box[5] = {64, box_mn, 2, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    int rank = 3;
+    if (mn_major) {
+        dims[1] = 64, dims[2] = mn / 64, dims[3] = K / 64;
+        strides[2] = 64 * pitch_bytes;
+        box[1] = 64, box[2] = box_mn / 64, box[3] = 2;
+        rank = 4;
+    }
+    if (nb > 0) {
+        dims[rank] = nb;
+        strides[rank - 1] = bstride_bytes;
+        ++rank;
+    }
+    CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, static_cast<cuuint32_t>(rank), const_cast<void*>(ptr),
+                          dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -813,6 +847,21 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
     kp.a_bdim = (ca.tma && a_bd) ? 1u : 0u;
     kp.b_bdim = (cb.tma && b_bd) ? 1u : 0u;
     kp.c_bdim = (c_tma && c_bd) ? 1u : 0u;
+    // Two K blocks per copy: both operands by TMA in a layout the one-block
+    // maps read with a single box per slot (K-major, or MN-major as 3-D boxes).
+    kp.k2 = 0;
+    kp.kfull = static_cast<int>(a.K / 64);
+    if (opt(GEMM_F16_OPT_TWO_K_LOADS) != 1 && !gated && ca.tma && cb.tma && (!ca.mn || a_3d) && (!cb.mn || b_3d) &&
+        a.K >= 128) {
+        const bool ok =
+            encode_two_k(&kp.tmA2k, kp.A, ca.mn, ca.mn ? a_mn_ext : Mv, a.K,
+                         ca.mn ? 2 * kp.a_sk : (Mv == 1 ? round_up(2 * a.K, 16) : 2 * kp.a_sm), gemm_f16_dev::kBM, nb_a,
+                         bst_a) &&
+            encode_two_k(&kp.tmB2k, kp.B, cb.mn, cb.mn ? b_mn_ext : Nv, a.K,
+                         cb.mn ? 2 * kp.b_sk : (Nv == 1 ? round_up(2 * a.K, 16) : 2 * kp.b_sn),
+                         static_cast<uint32_t>(bcols), nb_b, bst_b);
+        kp.k2 = ok ? 1u : 0u;
+    }
 
     const uint32_t stage_b = static_cast<uint32_t>(bcols) * gemm_f16_dev::kBK * 2;
     const uint32_t stage_bytes = gemm_f16_dev::kStageABytes + stage_b;
@@ -974,6 +1023,7 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
     pub.fused = a.fused ? 1 : 0;
     pub.gated = gated ? 1 : 0;
     pub.repack = repacked;
+    pub.two_k_loads = static_cast<int>(kp.k2);
     pub.splits = splits, pub.kblocks = kblocks, pub.grid = grid;
     pub.units = static_cast<int>(tiles * splits);
     pub.streamk_tiles = sch.sk_iters > 0 ? static_cast<int>(tiles - sch.sk_tile0) : 0;
@@ -1452,7 +1502,8 @@ gemm_f16_status gemm_f16_get_plan(const void* A, int64_t stride_am, int64_t stri
 gemm_f16_status gemm_f16_set_option(int option, int64_t value)
 {
     // (12 is not an option: that number is left unused)
-    if (option < 1 || option > 19 || option == 12 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option < 1 || option > 20 || option == 12 || value < 0) return GEMM_F16_ERR_INVALID_VALUE;
+    if (option == GEMM_F16_OPT_TWO_K_LOADS && value > 1) return GEMM_F16_ERR_INVALID_VALUE;
     if ((option == GEMM_F16_OPT_L2_A || option == GEMM_F16_OPT_L2_B || option == GEMM_F16_OPT_L2_C) && value > 3)
         return GEMM_F16_ERR_INVALID_VALUE;
     if (option == GEMM_F16_OPT_DEBUG_BOUNDS && value > 2) return GEMM_F16_ERR_INVALID_VALUE;

@@ -107,6 +107,15 @@ struct KernelParams {
     CUtensorMap tmC;   // C  (dims {N, M}, box 64 x 32): one epilogue warp's rows
     CUtensorMap tmC4;  // C  with a box of 64 x 128: the four epilogue warps' rows in one store
     CUtensorMap tmBu;  // gated fused stage: the up projection's B' (the geometry of tmB)
+    // A' and B' with the 64-wide K block as an outer dimension (k2 != 0): one
+    // copy brings an operand's boxes of both K blocks of a barrier phase into
+    // its two consecutive slots (K-major: dims {64 K, MN, K blocks}; MN-major:
+    // {64 MN, 64 K, atom columns, K blocks}; a trailing batch dimension as in
+    // tmA / tmB).  Only whole K blocks (kfull = K / 64) are addressed.
+    CUtensorMap tmA2k;
+    CUtensorMap tmB2k;
+    uint32_t k2;
+    int kfull;
     const __half* A;   // A'[m,k] = A[m*a_sm + k*a_sk]
     int64_t a_sm, a_sk;
     const __half* B;   // B'[k,n] = B[k*b_sk + n*b_sn]
@@ -183,6 +192,9 @@ struct KernelParams {
     int gated;
     int bias_rows;            // 1: the bias runs along the kernel view's rows (the swapped form)
 };
+// (a __grid_constant__ parameter block: at most 4 KB keeps it within every
+// launch path's limit)
+static_assert(sizeof(KernelParams) <= 4096, "kernel parameters exceed 4 KB");
 
 struct SmemLayout {
     uint32_t a, b, epi, bars;
@@ -415,6 +427,21 @@ __device__ __forceinline__ void tma3(uint32_t d, const void* m, int32_t x, int32
     }
 }
 template <bool kPair>
+__device__ __forceinline__ void tma5(uint32_t d, const void* m, int32_t x, int32_t y, int32_t z, int32_t v, int32_t u,
+                                     uint32_t bar, uint32_t hk)
+{
+    if (hk) {
+        if (kPair)
+            tma_load_5d_pair_hint(d, m, x, y, z, v, u, bar, l2_policy(hk));
+        else
+            tma_load_5d_hint(d, m, x, y, z, v, u, bar, l2_policy(hk));
+    } else if (kPair) {
+        tma_load_5d_pair(d, m, x, y, z, v, u, bar);
+    } else {
+        tma_load_5d(d, m, x, y, z, v, u, bar);
+    }
+}
+template <bool kPair>
 __device__ __forceinline__ void tma4(uint32_t d, const void* m, int32_t x, int32_t y, int32_t z, int32_t v,
                                      uint32_t bar, uint32_t hk)
 {
@@ -483,6 +510,37 @@ __device__ __forceinline__ void load_b_slot(const KernelParams& p, const CUtenso
             else
                 tma2<kPair>(sb + j * 8192, tmb, c + 64 * j, k0, bar, p.l2_b);
         }
+    }
+}
+
+// Both K blocks kb, kb+1 of a barrier phase in one copy per operand, into the
+// phase's two consecutive slots (sa, sb: the first slot's A' and B' bases).
+// A' rows row .. row+127; B' columns col .. col + (the map's box width).
+template <bool kPair>
+__device__ __forceinline__ void load_two_k_blocks(const KernelParams& p, uint32_t sa, uint32_t sb, int32_t kb,
+                                                  int64_t row, int64_t col, int32_t az, int32_t bz, bool a_mn,
+                                                  bool b_mn, bool a_bd, bool b_bd, uint32_t bar)
+{
+    const int32_t r = static_cast<int32_t>(row), c = static_cast<int32_t>(col);
+    if (!a_mn) {
+        if (a_bd)
+            tma4<kPair>(sa, &p.tmA2k, 0, r, kb, az, bar, p.l2_a);
+        else
+            tma3<kPair>(sa, &p.tmA2k, 0, r, kb, bar, p.l2_a);
+    } else if (a_bd) {
+        tma5<kPair>(sa, &p.tmA2k, 0, 0, r >> 6, kb, az, bar, p.l2_a);
+    } else {
+        tma4<kPair>(sa, &p.tmA2k, 0, 0, r >> 6, kb, bar, p.l2_a);
+    }
+    if (!b_mn) {
+        if (b_bd)
+            tma4<kPair>(sb, &p.tmB2k, 0, c, kb, bz, bar, p.l2_b);
+        else
+            tma3<kPair>(sb, &p.tmB2k, 0, c, kb, bar, p.l2_b);
+    } else if (b_bd) {
+        tma5<kPair>(sb, &p.tmB2k, 0, 0, c >> 6, kb, bz, bar, p.l2_b);
+    } else {
+        tma4<kPair>(sb, &p.tmB2k, 0, 0, c >> 6, kb, bar, p.l2_b);
     }
 }
 
@@ -1358,6 +1416,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
             tma_prefetch_desc(&p.tmC);
             tma_prefetch_desc(&p.tmC4);
         }
+        if (p.k2) {
+            tma_prefetch_desc(&p.tmA2k);
+            tma_prefetch_desc(&p.tmB2k);
+        }
     }
     if (warp == kMmaWarp) {
         if (kPair) {
@@ -1430,7 +1492,15 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                     // the phase on its own barrier; the peer's copies complete there.
                     if (t == tiss && (a_tma || b_tma) && (!kPair || leader))
                         mbar_arrive_expect_tx(fb, tx * static_cast<uint32_t>(nk));
-                    for (int h = 0; h < nk; ++h) {
+                    // Both K blocks of the phase in one copy per operand (whole K
+                    // blocks of a full-width unit): half the TMA instructions, which
+                    // the operand feed is sensitive to (131072 x 2048 x 7168: +2.6 %).
+                    const bool two = p.k2 && nk == 2 && !narrow && kb + 2 <= p.kfull;
+                    if (two && t == tiss)
+                        load_two_k_blocks<kPair>(p, L.a + stage * kSlots * kStageABytes,
+                                                 L.b + stage * kSlots * p.stage_b_bytes, kb, arow, n0, ug.az, ug.bz,
+                                                 a_mn, b_mn, a_bd, b_bd, kPair ? mapa_shared(fb, lead_rank) : fb);
+                    for (int h = 0; h < (two ? 0 : nk); ++h) {
                     const int slot = stage * kSlots + h;
                     const uint32_t sa = L.a + slot * kStageABytes;
                     const uint32_t sb = L.b + slot * p.stage_b_bytes;

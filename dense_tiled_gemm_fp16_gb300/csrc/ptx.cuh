@@ -234,6 +234,27 @@ __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const void* tmap,
         : "memory");
 }
 
+// Five-dimensional boxes (a batch dimension after a 4-D box), single and pair form.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                            int32_t w, int32_t v, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d_pair(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                                 int32_t w, int32_t v, uint32_t bar_cluster)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v), "r"(bar_cluster)
+        : "memory");
+}
+
 // ------------------------------------------------------ L2 eviction policy
 // An L2 cache policy for the copies below: kind 1 marks the lines a copy
 // brings into L2 as first to evict, kind 2 as last to evict (data that many
@@ -307,6 +328,26 @@ __device__ __forceinline__ void tma_load_4d_pair_hint(uint32_t dst, const void* 
         "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar_cluster), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d_hint(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                                 int32_t w, int32_t v, uint32_t bar, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v), "r"(bar), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d_pair_hint(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                                      int32_t w, int32_t v, uint32_t bar_cluster, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v), "r"(bar_cluster), "l"(pol)
         : "memory");
 }
 

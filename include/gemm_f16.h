@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define GEMM_F16_ABI_VERSION 2
+#define GEMM_F16_ABI_VERSION 3
 
 /* Largest M, N or K (and total rows of a grouped call): 2^31 - 2^16.  The
    copies' tile coordinates are 32-bit; element offsets are 64-bit and may
@@ -335,6 +335,8 @@ typedef struct {
     int gated;              /* gate/up form: tile_n output columns, 2 * tile_n accumulator columns */
     int repack;             /* bit 0: A, bit 1: B (and B_up) copied to an aligned buffer before the GEMM;
                                bit 2: C written to an aligned buffer, then copied into place */
+    int two_k_loads;        /* both 64-wide K blocks of a pipeline phase come in one TMA copy per
+                               operand (whole K blocks of full-width tiles; see GEMM_F16_OPT_TWO_K_LOADS) */
 } gemm_f16_plan;
 
 /* Fill *plan for the given arguments without launching anything.  Returns the
@@ -399,6 +401,13 @@ gemm_f16_status gemm_f16_fused_get_plan(const void* A, int64_t stride_am, int64_
  *                              whose B is at most 48 MB and whose raster keeps each A row
  *                              panel within one wave (at most 16 tile columns, raster panels
  *                              of at most 2 rows); none otherwise
+ *   GEMM_F16_OPT_TWO_K_LOADS   0 default: when both operands are TMA-addressable (K-major, or
+ *                              MN-major read as 3-D boxes), not gate/up, and K holds at least two
+ *                              whole 64-wide blocks, each pipeline phase of a full-width tile
+ *                              loads its two K blocks with one copy per operand (a map with the
+ *                              K block as an outer dimension), half the copies of one per K
+ *                              block; a ragged last K block and narrow tail pieces keep one copy
+ *                              per block.  1 one copy per K block always
  *   GEMM_F16_OPT_TEST_STALL    failure-detection test: 1 makes every CTA's MMA issuer wait
  *                              first on a barrier that nothing arrives on, so the bounded
  *                              wait runs out (after GEMM_F16_OPT_TIMEOUT_MS), the kernel
@@ -426,7 +435,8 @@ enum {
     GEMM_F16_OPT_DEBUG_BOUNDS = 16,
     GEMM_F16_OPT_L2_A = 17,
     GEMM_F16_OPT_L2_B = 18,
-    GEMM_F16_OPT_L2_C = 19
+    GEMM_F16_OPT_L2_C = 19,
+    GEMM_F16_OPT_TWO_K_LOADS = 20
 };
 gemm_f16_status gemm_f16_set_option(int option, int64_t value);
 

@@ -53,11 +53,11 @@ def test_binding_constants_match_the_header():
     assert g.MAX_GROUPS == h["GEMM_F16_MAX_GROUPS"]
     assert g.NOALLOC_SCRATCH_BYTES == h["GEMM_F16_NOALLOC_SCRATCH_BYTES"]
     assert g.gemm_f16_abi_version() == h["GEMM_F16_ABI_VERSION"]
-    assert len([k for k in h if k.startswith(prefix + "OPT_")]) == 18   # (12 is left unused)
+    assert len([k for k in h if k.startswith(prefix + "OPT_")]) == 19   # (12 is left unused)
 
 
 def test_status_strings_and_version():
-    assert g.gemm_f16_abi_version() == 2
+    assert g.gemm_f16_abi_version() == 3
     for code, name in g.STATUS.items():
         assert g.gemm_f16_status_string(code) == name
     assert g.gemm_f16_status_string(99) == "GEMM_F16_UNKNOWN_STATUS"
@@ -196,7 +196,7 @@ def test_fused_argument_errors_on_the_host():
 
 @pytest.mark.parametrize("option,value", [(0, 0), (99, 0), (g.OPT_STREAMK, 3), (g.OPT_PAIR, 3), (g.OPT_SWAP, 3),
                                           (g.OPT_TILE_N, 96), (g.OPT_TILE_N, 320), (g.OPT_MAX_STAGES, 1),
-                                          (12, 0), (12, 2), (g.OPT_L2_A, 4), (g.OPT_L2_C, 9), (20, 0), (g.OPT_REPACK, 3), (g.OPT_PDL, 2),
+                                          (12, 0), (12, 2), (g.OPT_L2_A, 4), (g.OPT_L2_C, 9), (g.OPT_TWO_K_LOADS, 2), (21, 0), (g.OPT_REPACK, 3), (g.OPT_PDL, 2),
                                           (g.OPT_DEBUG_BOUNDS, 3), (g.OPT_TEST_STALL, 2), (g.OPT_SPLITS, -1)])
 def test_options_reject_values_out_of_range(option, value):
     with pytest.raises(g.GemmF16Error) as e:
@@ -296,4 +296,4 @@ def test_plain_c_program_links_and_calls_the_library(tmp_path):
                     "-I", cuda_inc, str(src), "-L", libdir, "-lgemm_f16",
                     "-Wl,-rpath," + libdir, "-o", str(exe)], check=True, capture_output=True)
     out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
-    assert out == [str(len(names)), "2", "GEMM_F16_ERR_ALIAS"]
+    assert out == [str(len(names)), "3", "GEMM_F16_ERR_ALIAS"]

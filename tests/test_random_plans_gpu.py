@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 OPTIONS = (g.OPT_FORCE_GATHER, g.OPT_SPLITS, g.OPT_TILE_N, g.OPT_PANEL, g.OPT_SWAP, g.OPT_PAIR, g.OPT_STREAMK,
            g.OPT_TAIL_SPLIT, g.OPT_MAX_STAGES, g.OPT_REPACK, g.OPT_PDL,
-           g.OPT_L2_A, g.OPT_L2_B, g.OPT_L2_C)
+           g.OPT_L2_A, g.OPT_L2_B, g.OPT_L2_C, g.OPT_TWO_K_LOADS)
 
 
 def _reset():
@@ -71,7 +71,8 @@ def _options(rng):
              (0.1, g.OPT_PDL, lambda: 1),
              (0.15, g.OPT_L2_A, lambda: int(rng.integers(1, 4))),
              (0.15, g.OPT_L2_B, lambda: int(rng.integers(1, 4))),
-             (0.15, g.OPT_L2_C, lambda: int(rng.integers(1, 4))))
+             (0.15, g.OPT_L2_C, lambda: int(rng.integers(1, 4))),
+             (0.2, g.OPT_TWO_K_LOADS, lambda: 1))
     return {o: f() for p, o, f in draws if rng.random() < p}
 
 
