@@ -851,15 +851,19 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
     // maps read with a single box per slot (K-major, or MN-major as 3-D boxes).
     kp.k2 = 0;
     kp.kfull = static_cast<int>(a.K / 64);
-    if (opt(GEMM_F16_OPT_TWO_K_LOADS) != 1 && !gated && ca.tma && cb.tma && (!ca.mn || a_3d) && (!cb.mn || b_3d) &&
-        a.K >= 128) {
+    // (The single-CTA gate/up stage interleaves gate and up boxes per slot, a
+    // layout one two-block box cannot write; its pair form splits them over
+    // the two CTAs.)
+    if (opt(GEMM_F16_OPT_TWO_K_LOADS) != 1 && (!gated || pair) && ca.tma && cb.tma && (!ca.mn || a_3d) &&
+        (!cb.mn || b_3d) && a.K >= 128) {
+        const uint64_t pitch_b = cb.mn ? 2 * kp.b_sk : (Nv == 1 ? round_up(2 * a.K, 16) : 2 * kp.b_sn);
+        const uint32_t box_b = static_cast<uint32_t>(gated ? out_cols : bcols);
         const bool ok =
             encode_two_k(&kp.tmA2k, kp.A, ca.mn, ca.mn ? a_mn_ext : Mv, a.K,
                          ca.mn ? 2 * kp.a_sk : (Mv == 1 ? round_up(2 * a.K, 16) : 2 * kp.a_sm), gemm_f16_dev::kBM, nb_a,
                          bst_a) &&
-            encode_two_k(&kp.tmB2k, kp.B, cb.mn, cb.mn ? b_mn_ext : Nv, a.K,
-                         cb.mn ? 2 * kp.b_sk : (Nv == 1 ? round_up(2 * a.K, 16) : 2 * kp.b_sn),
-                         static_cast<uint32_t>(bcols), nb_b, bst_b);
+            encode_two_k(&kp.tmB2k, kp.B, cb.mn, cb.mn ? b_mn_ext : Nv, a.K, pitch_b, box_b, nb_b, bst_b) &&
+            (!gated || encode_two_k(&kp.tmBu2k, kp.Bu, cb.mn, cb.mn ? b_mn_ext : Nv, a.K, pitch_b, box_b, nb_b, bst_b));
         kp.k2 = ok ? 1u : 0u;
     }
 

@@ -111,9 +111,11 @@ struct KernelParams {
     // copy brings an operand's boxes of both K blocks of a barrier phase into
     // its two consecutive slots (K-major: dims {64 K, MN, K blocks}; MN-major:
     // {64 MN, 64 K, atom columns, K blocks}; a trailing batch dimension as in
-    // tmA / tmB).  Only whole K blocks (kfull = K / 64) are addressed.
+    // tmA / tmB).  Only whole K blocks (kfull = K / 64) are addressed.  The
+    // gate/up pair form's rank 1 reads the up projection through tmBu2k.
     CUtensorMap tmA2k;
     CUtensorMap tmB2k;
+    CUtensorMap tmBu2k;
     uint32_t k2;
     int kfull;
     const __half* A;   // A'[m,k] = A[m*a_sm + k*a_sk]
@@ -515,9 +517,10 @@ __device__ __forceinline__ void load_b_slot(const KernelParams& p, const CUtenso
 
 // Both K blocks kb, kb+1 of a barrier phase in one copy per operand, into the
 // phase's two consecutive slots (sa, sb: the first slot's A' and B' bases).
-// A' rows row .. row+127; B' columns col .. col + (the map's box width).
+// A' rows row .. row+127; B' columns col .. col + (the box width of tmb).
 template <bool kPair>
-__device__ __forceinline__ void load_two_k_blocks(const KernelParams& p, uint32_t sa, uint32_t sb, int32_t kb,
+__device__ __forceinline__ void load_two_k_blocks(const KernelParams& p, const CUtensorMap* tmb, uint32_t sa,
+                                                  uint32_t sb, int32_t kb,
                                                   int64_t row, int64_t col, int32_t az, int32_t bz, bool a_mn,
                                                   bool b_mn, bool a_bd, bool b_bd, uint32_t bar)
 {
@@ -534,13 +537,13 @@ __device__ __forceinline__ void load_two_k_blocks(const KernelParams& p, uint32_
     }
     if (!b_mn) {
         if (b_bd)
-            tma4<kPair>(sb, &p.tmB2k, 0, c, kb, bz, bar, p.l2_b);
+            tma4<kPair>(sb, tmb, 0, c, kb, bz, bar, p.l2_b);
         else
-            tma3<kPair>(sb, &p.tmB2k, 0, c, kb, bar, p.l2_b);
+            tma3<kPair>(sb, tmb, 0, c, kb, bar, p.l2_b);
     } else if (b_bd) {
-        tma5<kPair>(sb, &p.tmB2k, 0, 0, c >> 6, kb, bz, bar, p.l2_b);
+        tma5<kPair>(sb, tmb, 0, 0, c >> 6, kb, bz, bar, p.l2_b);
     } else {
-        tma4<kPair>(sb, &p.tmB2k, 0, 0, c >> 6, kb, bar, p.l2_b);
+        tma4<kPair>(sb, tmb, 0, 0, c >> 6, kb, bar, p.l2_b);
     }
 }
 
@@ -1419,6 +1422,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
         if (p.k2) {
             tma_prefetch_desc(&p.tmA2k);
             tma_prefetch_desc(&p.tmB2k);
+            if (gated) tma_prefetch_desc(&p.tmBu2k);
         }
     }
     if (warp == kMmaWarp) {
@@ -1494,10 +1498,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                         mbar_arrive_expect_tx(fb, tx * static_cast<uint32_t>(nk));
                     // Both K blocks of the phase in one copy per operand (whole K
                     // blocks of a full-width unit): half the TMA instructions, which
-                    // the operand feed is sensitive to (131072 x 2048 x 7168: +2.6 %).
+                    // the operand feed is sensitive to (131072 x 2048 x 7168: +3 %).
+                    // (A gated stage qualifies only in the pair form, where each
+                    // CTA's B slot holds one box: the gate or the up columns.)
                     const bool two = p.k2 && nk == 2 && !narrow && kb + 2 <= p.kfull;
                     if (two && t == tiss)
-                        load_two_k_blocks<kPair>(p, L.a + stage * kSlots * kStageABytes,
+                        load_two_k_blocks<kPair>(p, (kPair && gated && rank == 1) ? &p.tmBu2k : &p.tmB2k,
+                                                 L.a + stage * kSlots * kStageABytes,
                                                  L.b + stage * kSlots * p.stage_b_bytes, kb, arow, n0, ug.az, ug.bz,
                                                  a_mn, b_mn, a_bd, b_bd, kPair ? mapa_shared(fb, lead_rank) : fb);
                     for (int h = 0; h < (two ? 0 : nk); ++h) {

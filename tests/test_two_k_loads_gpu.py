@@ -119,3 +119,43 @@ def test_grouped_two_k_block_copies(rows, N, K):
     assert_bits(c2, oracle.gemm_grouped(Ah, Bh, rows, threads=oracle_threads()), "grouped two-block copies")
     assert_bits(c2, c1, "one copy per block")
     assert g.gemm_f16_device_status() == 0
+
+
+# (M, N, K, B layout, options, does the plan take two-block copies?)
+GATED = [
+    (1000, 512, 448, "row", {}, 1),                 # pair form: rank 0 the gate box, rank 1 the up box
+    (600, 384, 200, "col", {}, 1),                  # K-major B and B_up, ragged K
+    (1000, 512, 448, "row", {g.OPT_PAIR: 1}, 0),    # single CTA: gate and up boxes interleave in each slot
+]
+
+
+@pytest.mark.parametrize("case", GATED, ids=lambda c: f"{c[0]}x{c[1]}x{c[2]}-{c[3]}-{c[4]}")
+def test_gate_up_two_k_block_copies(case):
+    M, N, K, lb, opts, expect = case
+    for o, v in opts.items():
+        g.gemm_f16_set_option(o, v)
+    rng = np.random.default_rng(M + 5 * N + 3 * K)
+    Ah, Bh, Uh = ints(rng, (M, K)), ints(rng, (K, N)), ints(rng, (K, N))
+    bh, buh = ints(rng, (N,)), ints(rng, (N,))
+    A, B, U = view(Ah, "row"), view(Bh, lb), view(Uh, lb)
+    bias, bias_up = torch.from_numpy(bh).to(DEV), torch.from_numpy(buh).to(DEV)
+    out = torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV)
+    plan = g.fused_plan_for(A, B, out, bias=bias, act="relu", b_up=U, bias_up=bias_up)
+    assert plan["gated"] == 1 and plan["two_k_loads"] == expect, plan
+    c2, c1 = run_both(lambda: g.fused_mm(A, B, bias=bias, act="relu", b_up=U, bias_up=bias_up, out=out))
+    # integer sums are exact, relu(g) * u below 2^24 is exact in fp32: one rounding on both sides
+    assert_bits(c2, oracle.gemm_fused(Ah, Bh, Uh, bh, buh, "relu", threads=oracle_threads()), f"gate/up {case[:4]}")
+    assert_bits(c2, c1, "one copy per block")
+    assert g.gemm_f16_device_status() == 0
+
+
+def test_grouped_gate_up_two_k_block_copies():
+    rows, N, K = [512, 384, 640], 256, 448
+    rng = np.random.default_rng(77)
+    Ah, Bh, Uh = ints(rng, (sum(rows), K)), ints(rng, (len(rows), K, N)), ints(rng, (len(rows), K, N))
+    A, B, U = (torch.from_numpy(x).to(DEV) for x in (Ah, Bh, Uh))
+    c2, c1 = run_both(lambda: g.grouped_fused_mm(A, B, rows, act="relu", b_up=U))
+    ref = oracle.gemm_fused_grouped(Ah, Bh, rows, B_up=Uh, act="relu", threads=oracle_threads())
+    assert_bits(c2, ref, "grouped gate/up two-block copies")
+    assert_bits(c2, c1, "one copy per block")
+    assert g.gemm_f16_device_status() == 0
