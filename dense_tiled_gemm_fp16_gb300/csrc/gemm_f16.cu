@@ -368,6 +368,13 @@ struct Plan {
     size_t partial_bytes;   // split-K partials: align256(4 * units * tile_m * tile_n)
 };
 
+// Blocks of 8 warps for a copy of `items` work items (one item per warp and
+// pass): at most the resident blocks of every SM, one wave.
+unsigned copy_blocks(int64_t items, int sms, int per_sm)
+{
+    return static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>((items + 7) / 8, static_cast<int64_t>(sms) * per_sm)));
+}
+
 bool set_smem_attributes(DevInfo& dev)
 {
     std::lock_guard<std::mutex> lk(g_mutex);
@@ -1085,8 +1092,8 @@ gemm_f16_status launch(Plan& pl, DevInfo& dev, float* partials, int* counters, c
             rb.c[i] = pl.copies[i];
             items += gemm_f16_dev::repack_items(pl.copies[i]);
         }
-        const int64_t blocks = std::min<int64_t>((items + 7) / 8, static_cast<int64_t>(dev.sms) * 4);
-        config(cfg, attr, static_cast<unsigned>(blocks), gemm_f16_dev::kRepackThreads, 0, 1);
+        config(cfg, attr, copy_blocks(items, dev.sms, gemm_f16_dev::kRepackBlocksPerSm), gemm_f16_dev::kRepackThreads, 0,
+               1);
         if (cudaLaunchKernelEx(&cfg, gemm_f16_dev::repack_rows, rb) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_F16_ERR_LAUNCH;
@@ -1108,10 +1115,8 @@ gemm_f16_status launch(Plan& pl, DevInfo& dev, float* partials, int* counters, c
         return GEMM_F16_ERR_LAUNCH;
     }
     if (pl.unpack) {   // C from the aligned buffer into place, after the GEMM on the same stream
-        const int64_t items = gemm_f16_dev::unpack_items(pl.out);
-        const int64_t per_block = 8 * gemm_f16_dev::kUnpackUnroll;   // 8 warps, each kUnpackUnroll items a pass
-        const int64_t blocks = std::min<int64_t>((items + per_block - 1) / per_block, static_cast<int64_t>(dev.sms) * 8);
-        config(cfg, attr, static_cast<unsigned>(std::max<int64_t>(blocks, 1)), gemm_f16_dev::kRepackThreads, 0, 1);
+        config(cfg, attr, copy_blocks(gemm_f16_dev::unpack_items(pl.out), dev.sms, gemm_f16_dev::kUnpackBlocksPerSm),
+               gemm_f16_dev::kRepackThreads, 0, 1);
         if (cudaLaunchKernelEx(&cfg, gemm_f16_dev::unpack_rows, pl.out) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_F16_ERR_LAUNCH;

@@ -20,7 +20,10 @@
 namespace gemm_f16_dev {
 
 constexpr int kRepackThreads = 256;
-constexpr int kRepackUnroll = 4;   // 16-byte output chunks a lane has in flight
+constexpr int kCopyUnroll = 4;                   // 16-byte destination chunks a lane has in flight per item
+constexpr int kCopySeg = 32 * kCopyUnroll;       // destination chunks of one work item (2 KB)
+constexpr int kRepackBlocksPerSm = 4;            // resident blocks (the register budget of __launch_bounds__)
+constexpr int kUnpackBlocksPerSm = 4;
 
 struct RepackArgs {
     const __half* src;   // element (b, r, c) at src + b*s_b + r*s_r + c*s_c
@@ -37,80 +40,132 @@ struct RepackBatch {
     int n;
 };
 
-__host__ __device__ inline int64_t repack_items(const RepackArgs& a)
+// Work items of a copy: (row, segment of kCopySeg destination chunks).
+__host__ __device__ inline int64_t repack_segs(const RepackArgs& a) { return (a.pitch / 8 + kCopySeg - 1) / kCopySeg; }
+__host__ __device__ inline int64_t repack_items(const RepackArgs& a) { return a.rows * a.batch * repack_segs(a); }
+
+// One work item of a row copy with realignment: destination bytes [od, od +
+// wlen) relative to the aligned chunk base of the row's destination (od = its
+// offset in a 16-byte chunk) receive the row's source bytes [0, len) and,
+// past them, zeros (kZero; wlen = len otherwise).  The lane handles the
+// destination chunks k = seg * kCopySeg + 32 u + lane.  Destination chunk k
+// holds the bytes of two consecutive aligned source chunks, k and its
+// neighbour (k + 1 when the source's offset in its chunk is at least the
+// destination's, k - 1 otherwise), from a byte offset that is the same for the
+// whole row.  The lane loads source chunk k (only chunks with at least one
+// byte of the row, so no load leaves the row's pages) and takes the neighbour
+// from the next or previous lane with one shuffle per word; at the item's
+// edge the lane on the wrap-around side takes it from its own extra load.  It
+// shifts the pair into place and stores whole chunks with one 16-byte store;
+// only a ragged first or last chunk of a row takes 2-byte stores.  Every load
+// is issued before the first store.
+template <bool kZero>
+__device__ __forceinline__ void copy_row_segment(const __half* src, __half* dst, int64_t len, int64_t wlen,
+                                                 int64_t seg, int lane)
 {
-    const int64_t seg = 32 * kRepackUnroll;
-    return a.rows * a.batch * ((a.pitch / 8 + seg - 1) / seg);
+    const uintptr_t sa = reinterpret_cast<uintptr_t>(src), da = reinterpret_cast<uintptr_t>(dst);
+    const int os = static_cast<int>(sa & 15u), od = static_cast<int>(da & 15u);
+    const uint4* S = reinterpret_cast<const uint4*>(sa - os);
+    uint4* D = reinterpret_cast<uint4*>(da - od);
+    // destination chunk k = source bytes [16k + t, 16k + t + 16) relative to S
+    const int t = os - od;
+    const bool up = t >= 0;   // pair (k, k + 1) from byte t; else (k - 1, k) from byte 16 + t
+    const uint32_t sh = static_cast<uint32_t>(up ? t : 16 + t);
+    // (chunk counts of a row fit 32 bits: a row holds fewer than 2^31 elements)
+    const int64_t vend = od + len, wend = od + wlen;   // copied / written bytes end, relative to D
+    const uint32_t nsrc = static_cast<uint32_t>((os + len + 15) >> 4);   // source chunks holding bytes of the row
+    const uint32_t nch = static_cast<uint32_t>((wend + 15) >> 4);        // destination chunks written
+    const uint32_t kw1 = static_cast<uint32_t>(wend >> 4);               // end of the whole destination chunks
+    const uint32_t kv = static_cast<uint32_t>(vend >> 4);                // chunk holding the end of the copied bytes
+    const int vrem = static_cast<int>(vend & 15);
+    const uint32_t kb = static_cast<uint32_t>(seg) * kCopySeg, k0 = kb + static_cast<uint32_t>(lane);
+    uint4 w[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+        const uint32_t k = k0 + 32u * u;
+        w[u] = k < nsrc ? ld_nc_v4(S + k) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    // the neighbour beyond the item: chunk kb + kCopySeg for lane 31 (up), kb - 1 for lane 0
+    uint4 extra = make_uint4(0u, 0u, 0u, 0u);
+    if (sh != 0 && lane == (up ? 31 : 0)) {
+        const uint32_t kx = up ? kb + kCopySeg : kb - 1u;   // (kb - 1 wraps to 2^32 - 1 for kb = 0: not < nsrc)
+        if (kx < nsrc) extra = ld_nc_v4(S + kx);
+    }
+    const int from = up ? ((lane + 1) & 31) : ((lane + 31) & 31);
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+        const uint32_t k = k0 + 32u * u;
+        uint4 c = w[u];
+        if (sh != 0) {
+            // the wrap-around lane reads the chunk 32 lanes on: the first lane's
+            // next chunk (up) or the last lane's previous one
+            uint4 give = w[u];
+            if (up && lane == 0 && u + 1 < kCopyUnroll) give = w[u + 1];
+            if (!up && lane == 31 && u > 0) give = w[u - 1];
+            uint4 nb;
+            nb.x = __shfl_sync(0xffffffffu, give.x, from);
+            nb.y = __shfl_sync(0xffffffffu, give.y, from);
+            nb.z = __shfl_sync(0xffffffffu, give.z, from);
+            nb.w = __shfl_sync(0xffffffffu, give.w, from);
+            if (up && lane == 31 && u + 1 == kCopyUnroll) nb = extra;
+            if (!up && lane == 0 && u == 0) nb = extra;
+            c = up ? funnel16(w[u], nb, sh) : funnel16(nb, w[u], sh);
+        }
+        if (k >= nch) continue;
+        if (kZero && k >= kv) c = keep_first(c, k == kv ? vrem / 2 : 0);
+        if ((k > 0 || od == 0) && k < kw1) {
+            D[k] = c;
+        } else {   // the row's ragged first or last chunk: bytes [od, 16) of chunk 0, [0, wend - 16k) of the last
+            const uint32_t wd[4] = {c.x, c.y, c.z, c.w};
+            uint16_t* cp = reinterpret_cast<uint16_t*>(D + k);
+            const int b0 = k == 0 ? od : 0, b1 = k < kw1 ? 16 : static_cast<int>(wend & 15);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (2 * i >= b0 && 2 * i < b1) cp[i] = static_cast<uint16_t>(wd[i >> 1] >> ((i & 1) * 16));
+        }
+    }
 }
 
-// 8 fp16 values of the 16 bytes at byte offset sh (even) of the 32-byte pair
-// w0:w1; the offset is the same for the whole row, so the branch is uniform
-// across the warp.
-__device__ __forceinline__ uint4 repack_shift(const uint4& w0, const uint4& w1, uint32_t sh)
+// Work items go to the warps round-robin (item q to warp q mod warps), so
+// the warps in flight at any time cover one contiguous stretch of the rows.
+__device__ __forceinline__ int64_t warp_index() { return static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5); }
+__device__ __forceinline__ int64_t warp_count() { return static_cast<int64_t>(gridDim.x) * (blockDim.x / 32); }
+
+// Item q of one copy.  Unit column stride: copy_row_segment (destination
+// rows aligned, zero-filled from the view's columns to the pitch); other
+// column strides element by element.
+__device__ __forceinline__ void repack_item(const RepackArgs& a, int64_t q, int lane)
 {
-    return sh == 0 ? w0 : funnel16(w0, w1, sh);
+    const int64_t segs = repack_segs(a);
+    const int64_t row = q / segs, seg = q - row * segs;
+    const int64_t b = row / a.rows, r = row - b * a.rows;
+    const __half* srow = a.src + b * a.s_b + r * a.s_r;
+    __half* drow = a.dst + b * a.dst_bs + r * a.pitch;
+    if (a.s_c == 1) {
+        copy_row_segment<true>(srow, drow, 2 * a.cols, 2 * a.pitch, seg, lane);
+    } else {
+        uint16_t* d = reinterpret_cast<uint16_t*>(drow);
+        const uint16_t* sp = reinterpret_cast<const uint16_t*>(srow);
+        const int64_t c1 = 8 * (seg + 1) * kCopySeg < a.pitch ? 8 * (seg + 1) * kCopySeg : a.pitch;
+        for (int64_t c = 8 * seg * kCopySeg + lane; c < c1; c += 32)
+            d[c] = c < a.cols ? ld_nc_u16(sp + c * a.s_c) : uint16_t(0);
+    }
 }
 
-// Work items are (row, segment of 32 * kRepackUnroll output chunks), one warp
-// each, grid-stride over batch * rows * segments, so that a long row does not
-// serialise one warp on several memory round trips.  Unit column stride: the
-// lane loads the aligned 16-byte source words that hold its output chunk's
-// valid elements (never a word without one, so no load leaves the view's
-// pages), shifts them into place and stores the chunk.  Other strides: element
-// by element.
-__global__ void __launch_bounds__(kRepackThreads) repack_rows(const __grid_constant__ RepackBatch batch)
+__global__ void __launch_bounds__(kRepackThreads, kRepackBlocksPerSm) repack_rows(const __grid_constant__ RepackBatch batch)
 {
     // (as a programmatic dependent: the previous kernel, which may still read
     // this buffer or write the source, has completed)
     griddep_wait();
     griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
-    const int64_t warps = static_cast<int64_t>(gridDim.x) * (kRepackThreads / 32);
-    constexpr int64_t kSeg = 32 * kRepackUnroll;
     const int64_t n0 = batch.n > 0 ? repack_items(batch.c[0]) : 0;
     const int64_t n1 = batch.n > 1 ? repack_items(batch.c[1]) : 0;
     const int64_t total = n0 + n1 + (batch.n > 2 ? repack_items(batch.c[2]) : 0);
-    for (int64_t qq = static_cast<int64_t>(blockIdx.x) * (kRepackThreads / 32) + (threadIdx.x >> 5); qq < total;
-         qq += warps) {
-        const int ci = qq < n0 ? 0 : (qq < n0 + n1 ? 1 : 2);
-        const RepackArgs& a = batch.c[ci];
-        const int64_t q = qq - (ci == 0 ? 0 : (ci == 1 ? n0 : n0 + n1));
-        const int64_t chunks = a.pitch / 8;
-        const int64_t segs = (chunks + kSeg - 1) / kSeg;
-        const int64_t row = q / segs, seg = q - row * segs;
-        const int64_t b = row / a.rows, r = row - b * a.rows;
-        const __half* srow = a.src + b * a.s_b + r * a.s_r;
-        uint4* drow = reinterpret_cast<uint4*>(a.dst + b * a.dst_bs + r * a.pitch);
-        const int64_t j0 = seg * kSeg + lane;
-        if (a.s_c == 1) {
-            const uintptr_t addr = reinterpret_cast<uintptr_t>(srow);
-            const uint32_t sh = static_cast<uint32_t>(addr & 15u);
-            const uint4* w = reinterpret_cast<const uint4*>(addr - sh);
-            uint4 w0[kRepackUnroll], w1[kRepackUnroll];
-            int nv[kRepackUnroll];
-#pragma unroll
-            for (int u = 0; u < kRepackUnroll; ++u) {
-                const int64_t j = j0 + 32 * u;
-                const int64_t left = a.cols - 8 * j;
-                nv[u] = j < chunks ? (left >= 8 ? 8 : (left <= 0 ? 0 : static_cast<int>(left))) : 0;
-                w0[u] = w1[u] = make_uint4(0u, 0u, 0u, 0u);
-                if (nv[u] > 0) w0[u] = ld_nc_v4(w + j);
-                if (nv[u] > 0 && sh + 2u * static_cast<uint32_t>(nv[u]) > 16u) w1[u] = ld_nc_v4(w + j + 1);
-            }
-#pragma unroll
-            for (int u = 0; u < kRepackUnroll; ++u) {
-                const int64_t j = j0 + 32 * u;
-                if (j >= chunks) break;
-                uint4 c = repack_shift(w0[u], w1[u], sh);
-                if (nv[u] < 8) c = keep_first(c, nv[u]);
-                drow[j] = c;
-            }
-        } else {
-            uint16_t* d = reinterpret_cast<uint16_t*>(drow);
-            const uint16_t* s = reinterpret_cast<const uint16_t*>(srow);
-            for (int64_t c = 8 * (seg * kSeg) + lane; c < a.pitch && c < 8 * (seg + 1) * kSeg; c += 32)
-                d[c] = c < a.cols ? ld_nc_u16(s + c * a.s_c) : uint16_t(0);
-        }
+    // (the copies' items are numbered one copy after the other)
+    for (int64_t q = warp_index(); q < total; q += warp_count()) {
+        const int ci = q < n0 ? 0 : (q < n0 + n1 ? 1 : 2);
+        repack_item(batch.c[ci], q - (ci == 0 ? 0 : (ci == 1 ? n0 : n0 + n1)), lane);
     }
 }
 
@@ -122,11 +177,9 @@ namespace gemm_f16_dev {
 // multiple of 8 elements, or an unaligned base): the GEMM stores its tiles by
 // TMA into an aligned buffer (rows `spitch` elements apart, a multiple of 8),
 // and this kernel moves the M x N view into C.  Only the view's elements are
-// written: C's pitch padding is never touched.  Aligned 16-byte loads; each
-// lane then assembles the aligned 16-byte chunk of the destination row that
-// its data falls in (a funnel shift of its own and the previous lane's
-// bytes), so whole chunks go out as 16-byte stores and only the two ragged
-// ends of a row segment take 2-byte stores.  HBM-bound: 2 bytes read and 2
+// written: C's pitch padding is never touched.  copy_row_segment with aligned
+// source rows: whole destination chunks go out as 16-byte stores and only the
+// two ragged ends of a row take 2-byte stores.  HBM-bound: 2 bytes read and 2
 // written per element.
 struct UnpackArgs {
     const __half* src;   // element (b, r, c) at src + b*sbs + r*spitch + c; 16-byte-aligned rows
@@ -136,94 +189,28 @@ struct UnpackArgs {
     int64_t rows, cols, batch;
 };
 
-constexpr int kUnpackSeg = 256;   // elements of a row one warp moves per work item
-constexpr int kUnpackUnroll = 4;  // work items a warp has in flight (their loads issued together)
-
-__host__ __device__ inline int64_t unpack_items(const UnpackArgs& a)
+// Work items: (row, segment of kCopySeg destination chunks); a destination
+// row touches at most (2 cols + 14) / 16 + 1 chunks.
+__host__ __device__ inline int64_t unpack_segs(const UnpackArgs& a)
 {
-    return a.batch * a.rows * ((a.cols + kUnpackSeg - 1) / kUnpackSeg);
+    return ((2 * a.cols + 29) / 16 + kCopySeg - 1) / kCopySeg;
 }
+__host__ __device__ inline int64_t unpack_items(const UnpackArgs& a) { return a.batch * a.rows * unpack_segs(a); }
 
-// Store the halfwords [lo, hi) of a 16-byte chunk (byte offsets lo, hi even).
-__device__ __forceinline__ void store_chunk_part(uint16_t* chunk, const uint4& v, uint32_t lo, uint32_t hi)
-{
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (uint32_t i = 0; i < 8; ++i)
-        if (2 * i >= lo && 2 * i < hi) chunk[i] = static_cast<uint16_t>(w[i >> 1] >> ((i & 1) * 16));
-}
-
-// One work item (a segment of up to 256 elements of one row) whose source
-// chunk `cur` this lane has already loaded: realign and store.
-__device__ __forceinline__ void unpack_store(uint16_t* d, int64_t nvalid, const uint4& cur, int lane)
-{
-    const uintptr_t D = reinterpret_cast<uintptr_t>(d);
-    const uint32_t o = static_cast<uint32_t>(D & 15u);      // even
-    uint16_t* A = reinterpret_cast<uint16_t*>(D - o);       // aligned chunk 0
-    const uint32_t vbytes = 2u * static_cast<uint32_t>(nvalid);   // valid bytes from D
-    uint4 prev;
-    prev.x = __shfl_up_sync(0xffffffffu, cur.x, 1);
-    prev.y = __shfl_up_sync(0xffffffffu, cur.y, 1);
-    prev.z = __shfl_up_sync(0xffffffffu, cur.z, 1);
-    prev.w = __shfl_up_sync(0xffffffffu, cur.w, 1);
-    // chunk `lane`: destination bytes [16*lane, 16*lane + 16) from A, i.e.
-    // bytes [16 - o, 32 - o) of prev:cur (o = 0: cur itself)
-    const uint4 chunk = o == 0 ? cur : funnel16(prev, cur, 16u - o);
-    // valid bytes of this chunk, relative to A: [o, o + vbytes)
-    const uint32_t lo = 16u * lane, hi = lo + 16u;
-    const uint32_t vlo = o > lo ? o : lo, vhi = (o + vbytes) < hi ? (o + vbytes) : hi;
-    if (vlo < vhi) {
-        uint16_t* cp = A + 8 * lane;
-        if (vlo == lo && vhi == hi)
-            *reinterpret_cast<uint4*>(cp) = chunk;
-        else
-            store_chunk_part(cp, chunk, vlo - lo, vhi - lo);
-    }
-    // chunk 32: the last lane's final o bytes when the segment is full
-    const uint4 last = make_uint4(__shfl_sync(0xffffffffu, cur.x, 31), __shfl_sync(0xffffffffu, cur.y, 31),
-                                  __shfl_sync(0xffffffffu, cur.z, 31), __shfl_sync(0xffffffffu, cur.w, 31));
-    if (lane == 0 && o != 0 && o + vbytes > 512u) {
-        const uint4 tail = funnel16(last, make_uint4(0u, 0u, 0u, 0u), 16u - o);
-        store_chunk_part(A + 8 * 32, tail, 0u, o + vbytes - 512u);
-    }
-}
-
-__global__ void __launch_bounds__(kRepackThreads) unpack_rows(const __grid_constant__ UnpackArgs a)
+__global__ void __launch_bounds__(kRepackThreads, kUnpackBlocksPerSm) unpack_rows(const __grid_constant__ UnpackArgs a)
 {
     // (as a programmatic dependent of the GEMM: its TMA stores are complete
     // and visible once this returns)
     griddep_wait();
     griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
-    const int64_t warps = static_cast<int64_t>(gridDim.x) * (kRepackThreads / 32);
-    const int64_t segs = (a.cols + kUnpackSeg - 1) / kUnpackSeg;
+    const int64_t segs = unpack_segs(a);
     const int64_t total = unpack_items(a);
-    // A warp takes kUnpackUnroll consecutive items per pass: every load first,
-    // then the realigned stores, so several loads are in flight per lane.
-    for (int64_t q0 = (static_cast<int64_t>(blockIdx.x) * (kRepackThreads / 32) + (threadIdx.x >> 5)) * kUnpackUnroll;
-         q0 < total; q0 += warps * kUnpackUnroll) {
-        uint4 cur[kUnpackUnroll];
-        uint16_t* d[kUnpackUnroll];
-        int64_t nv[kUnpackUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnpackUnroll; ++u) {
-            const int64_t qq = q0 + u;
-            nv[u] = 0;
-            d[u] = nullptr;
-            cur[u] = make_uint4(0u, 0u, 0u, 0u);
-            if (qq < total) {
-                const int64_t row = qq / segs, seg = qq - row * segs;
-                const int64_t b = row / a.rows, r = row - b * a.rows;
-                const int64_t c0 = seg * kUnpackSeg;
-                nv[u] = a.cols - c0 < kUnpackSeg ? a.cols - c0 : kUnpackSeg;
-                d[u] = reinterpret_cast<uint16_t*>(a.dst + b * a.dbs + r * a.ldc + c0);
-                // (the load stays inside the source row's padded pitch)
-                if (8 * lane < nv[u]) cur[u] = ld_nc_v4(a.src + b * a.sbs + r * a.spitch + c0 + 8 * lane);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kUnpackUnroll; ++u)
-            if (q0 + u < total) unpack_store(d[u], nv[u], cur[u], lane);   // (uniform across the warp)
+    for (int64_t q = warp_index(); q < total; q += warp_count()) {
+        const int64_t row = q / segs, seg = q - row * segs;
+        const int64_t b = row / a.rows, r = row - b * a.rows;
+        copy_row_segment<false>(a.src + b * a.sbs + r * a.spitch, a.dst + b * a.dbs + r * a.ldc, 2 * a.cols,
+                                2 * a.cols, seg, lane);
     }
 }
 
