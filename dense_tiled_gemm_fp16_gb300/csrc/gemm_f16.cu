@@ -1016,9 +1016,13 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
     kp.idesc = (1u << 4) | ((ca.mn ? 1u : 0u) << 15) | ((cb.mn ? 1u : 0u) << 16) |
                ((static_cast<uint32_t>(BN) >> 3) << 17) | ((static_cast<uint32_t>(tile_rows) >> 4) << 24);
     kp.stage_b_bytes = stage_b;
+    // (with both operands by TMA, the A' and B' issuers each arrive on the full barrier)
     if (pair) {
         kp.tx_bytes = 2u * stage_bytes;   // both CTAs' boxes complete on the leader's barrier
-        kp.full_count = 1u;
+        kp.full_count = 2u;
+    } else if (ca.tma && cb.tma) {
+        kp.tx_bytes = gemm_f16_dev::kStageABytes + stage_b;
+        kp.full_count = 2u;
     } else {
         kp.tx_bytes = (ca.tma ? gemm_f16_dev::kStageABytes : 0u) + (cb.tma ? stage_b : 0u);
         kp.full_count = ((ca.tma || cb.tma) ? 1u : 0u) +

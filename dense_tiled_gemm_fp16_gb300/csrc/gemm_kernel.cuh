@@ -516,16 +516,18 @@ __device__ __forceinline__ void load_b_slot(const KernelParams& p, const CUtenso
 }
 
 // Both K blocks kb, kb+1 of a barrier phase in one copy per operand, into the
-// phase's two consecutive slots (sa, sb: the first slot's A' and B' bases).
+// phase's two consecutive slots (sa, sb: the first slot's A' and B' bases);
+// the A' copy when do_a, the B' copy when do_b.
 // A' rows row .. row+127; B' columns col .. col + (the box width of tmb).
 template <bool kPair>
 __device__ __forceinline__ void load_two_k_blocks(const KernelParams& p, const CUtensorMap* tmb, uint32_t sa,
                                                   uint32_t sb, int32_t kb,
                                                   int64_t row, int64_t col, int32_t az, int32_t bz, bool a_mn,
-                                                  bool b_mn, bool a_bd, bool b_bd, uint32_t bar)
+                                                  bool b_mn, bool a_bd, bool b_bd, uint32_t bar, bool do_a, bool do_b)
 {
     const int32_t r = static_cast<int32_t>(row), c = static_cast<int32_t>(col);
-    if (!a_mn) {
+    if (!do_a) {
+    } else if (!a_mn) {
         if (a_bd)
             tma4<kPair>(sa, &p.tmA2k, 0, r, kb, az, bar, p.l2_a);
         else
@@ -535,7 +537,8 @@ __device__ __forceinline__ void load_two_k_blocks(const KernelParams& p, const C
     } else {
         tma4<kPair>(sa, &p.tmA2k, 0, 0, r >> 6, kb, bar, p.l2_a);
     }
-    if (!b_mn) {
+    if (!do_b) {
+    } else if (!b_mn) {
         if (b_bd)
             tma4<kPair>(sb, tmb, 0, c, kb, bz, bar, p.l2_b);
         else
@@ -1453,8 +1456,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
         // ------------------------------------------------------------ producers
         const int t = threadIdx.x;
         const bool any_masked = !a_tma || !b_tma;
-        const int tiss = any_masked ? 0 : kTmaThread;   // the thread that issues TMA copies
-        if (t == tiss || any_masked) {
+        // The threads that issue TMA copies: with both operands by TMA, one for
+        // A' (warp 1) and one for B' (warp 2), so that each copy's issue overlaps
+        // the other's (0.3-1 % on the large shapes, e.g. 4096^3 and the
+        // 32 x 1024^3 batch); each announces its own bytes on the full barrier,
+        // which then expects two arrivals.  With a gathered operand thread 0
+        // issues the TMA operand's copies and the producer warps gather the other.
+        const int tiss = any_masked ? 0 : kTmaThread;
+        const int tiss_b = any_masked ? 0 : kTmaThread + 32;
+        const bool do_a = t == tiss, do_b = t == tiss_b;
+        if (do_a || do_b || any_masked) {
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -1494,33 +1505,41 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                     const uint32_t fb = bar_full(L.bars, stage);
                     // The leader (pair form) expects both CTAs' bytes of every slot of
                     // the phase on its own barrier; the peer's copies complete there.
-                    if (t == tiss && (a_tma || b_tma) && (!kPair || leader))
-                        mbar_arrive_expect_tx(fb, tx * static_cast<uint32_t>(nk));
+                    if ((a_tma || b_tma) && (!kPair || leader)) {
+                        const uint32_t nkb = static_cast<uint32_t>(nk) * (kPair ? 2u : 1u);
+                        if (any_masked) {
+                            if (do_a) mbar_arrive_expect_tx(fb, tx * static_cast<uint32_t>(nk));
+                        } else {
+                            if (do_a) mbar_arrive_expect_tx(fb, kStageABytes * nkb);
+                            if (do_b) mbar_arrive_expect_tx(fb, b_bytes * nkb);
+                        }
+                    }
                     // Both K blocks of the phase in one copy per operand (whole K
                     // blocks of a full-width unit): half the TMA instructions, which
                     // the operand feed is sensitive to (131072 x 2048 x 7168: +3 %).
                     // (A gated stage qualifies only in the pair form, where each
                     // CTA's B slot holds one box: the gate or the up columns.)
                     const bool two = p.k2 && nk == 2 && !narrow && kb + 2 <= p.kfull;
-                    if (two && t == tiss)
+                    if (two && (do_a || do_b))
                         load_two_k_blocks<kPair>(p, (kPair && gated && rank == 1) ? &p.tmBu2k : &p.tmB2k,
                                                  L.a + stage * kSlots * kStageABytes,
                                                  L.b + stage * kSlots * p.stage_b_bytes, kb, arow, n0, ug.az, ug.bz,
-                                                 a_mn, b_mn, a_bd, b_bd, kPair ? mapa_shared(fb, lead_rank) : fb);
+                                                 a_mn, b_mn, a_bd, b_bd, kPair ? mapa_shared(fb, lead_rank) : fb, do_a,
+                                                 do_b);
                     for (int h = 0; h < (two ? 0 : nk); ++h) {
                     const int slot = stage * kSlots + h;
                     const uint32_t sa = L.a + slot * kStageABytes;
                     const uint32_t sb = L.b + slot * p.stage_b_bytes;
                     const int32_t k0 = (kb + h) * kBK;
-                    if (t == tiss && (a_tma || b_tma)) {
+                    if ((do_a || do_b) && (a_tma || b_tma)) {
                         if (kPair) {
                             const uint32_t fbc = mapa_shared(fb, lead_rank);
-                            load_a_slot<true>(p, sa, k0, arow, ug.az, a_mn, a_3d, a_bd, fbc);
-                            load_b_slot<true>(p, tmb, sb, k0, n0, ug.bz, bcols, b_mn, b_3d, b_bd, fbc);
+                            if (do_a) load_a_slot<true>(p, sa, k0, arow, ug.az, a_mn, a_3d, a_bd, fbc);
+                            if (do_b) load_b_slot<true>(p, tmb, sb, k0, n0, ug.bz, bcols, b_mn, b_3d, b_bd, fbc);
                         } else {
-                            if (a_tma) load_a_slot<false>(p, sa, k0, arow, ug.az, a_mn, a_3d, a_bd, fb);
-                            if (b_tma) load_b_slot<false>(p, tmb, sb, k0, n0, ug.bz, bcols, b_mn, b_3d, b_bd, fb);
-                            if (b_tma && gated)
+                            if (a_tma && do_a) load_a_slot<false>(p, sa, k0, arow, ug.az, a_mn, a_3d, a_bd, fb);
+                            if (b_tma && do_b) load_b_slot<false>(p, tmb, sb, k0, n0, ug.bz, bcols, b_mn, b_3d, b_bd, fb);
+                            if (b_tma && gated && do_b)
                                 load_b_slot<false>(p, &p.tmBu, sb + bcols * 128, k0, n0, ug.bz, bcols, b_mn, b_3d, b_bd,
                                                    fb);
                         }
@@ -1550,9 +1569,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_f16_persistent(const __gr
                     }
                 }
             }
-            if (!ok && t == tiss && (a_tma || b_tma) && (!kPair || leader)) {
+            if (!ok && (do_a || do_b) && (a_tma || b_tma) && (!kPair || leader)) {
                 // Let TMA copies already in flight land before the CTA exits:
-                // wait (bounded) on the full barrier of each recently issued phase.
+                // wait (bounded) on the full barrier of each phase this thread
+                // issued recently (one whose other issuer never arrived runs
+                // out its bound, by when this thread's own copies have landed).
                 const int n = issued < nps ? issued : nps;
                 for (int i = 0; i < n; ++i) {
                     if (--stage < 0) {
