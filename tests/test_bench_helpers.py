@@ -129,10 +129,14 @@ def test_cpu_baseline_runs_the_oracle_on_the_workload_itself():
 def test_roofline_rates_against_burst_and_sustained_peaks():
     peaks = {"tflops": 2000.0, "tflops_sustained": 1600.0, "hbm_gbs": 8000.0, "source": "measured"}
     # 2e12 FLOPs in 1.25 ms: 1600 TFLOP/s, 0.8 of the burst peak, 1.0 of the sustained one
-    r = bench.roofline("tensor", 2e12, 1e9, 1.25, peaks, "no_such_workload")
-    assert r["unit"] == "TFLOP/s" and r["peak_kind"] == "burst"
+    r = bench.roofline("tensor", 2e12, 1e9, 1.25, peaks, "no_such_workload", busy_ms=25.0)
+    assert r["unit"] == "TFLOP/s" and r["peak_kind"] == "burst" and r["peak"] == 2000.0
     assert r["achieved"] == pytest.approx(1600.0) and r["frac"] == pytest.approx(0.8)
     assert r["frac_of_sustained"] == pytest.approx(1.0) and r["traffic"] is None
+    # a timed region long enough to run under the power limit: the sustained peak
+    r = bench.roofline("tensor", 2e12, 1e9, 1.25, peaks, "no_such_workload", busy_ms=250.0)
+    assert r["peak_kind"] == "sustained" and r["peak"] == 1600.0 and r["frac"] == pytest.approx(1.0)
+    assert r["frac_of_burst"] == pytest.approx(0.8)
     # 4e8 bytes in 0.1 ms: 4000 GB/s, half of the copy bandwidth
     r = bench.roofline("hbm", 1e9, 4e8, 0.1, peaks, "no_such_workload")
     assert r["unit"] == "GB/s" and r["achieved"] == pytest.approx(4000.0) and r["frac"] == pytest.approx(0.5)
