@@ -439,6 +439,36 @@ int choose_splits(int kblocks)
     return forced > 0 ? static_cast<int>(std::min<int64_t>(forced, kblocks)) : 1;
 }
 
+// K segments per tile that a swapped small-M pair plan runs by default (1:
+// none).  With fewer tiles T than clusters W (sms / 2) but at least half as
+// many, S in {2, 3, 4} segments make S*T units in ceil(S*T / W) waves; the S
+// that fills its waves best (ties: the smaller S) is taken when it fills them
+// to at least 80 % and leaves each segment 8 K blocks or more; neither
+// split-K nor stream-K may be forced.  16 x N x 8192, L2 flushed, us per call
+// for the best S against stream-K: 40 tiles 43.7 (S 3) vs 43.0, 48 tiles
+// 45.9 (S 3) vs 47.2, 56 tiles 50.6 (S 4) vs 52.8, 64 tiles 52.8 (S 2) vs
+// 56.2; the unit order, K segment first, is what pays (64 tiles, S 2,
+// tile-major order: 56.3).
+int kseg_default(bool swap, bool pair, bool gated, int64_t tiles, int kblocks, int sms)
+{
+    const int64_t W = sms / 2;
+    if (!swap || !pair || gated || opt(GEMM_F16_OPT_SPLITS) != 0 || opt(GEMM_F16_OPT_STREAMK) != 0 || tiles >= W ||
+        2 * tiles < W)
+        return 1;
+    int best = 1;
+    double best_fill = 0.8 - 1e-9;
+    for (int S = 2; S <= 4; ++S) {
+        if (kblocks < 8 * S) break;
+        const int64_t units = S * tiles, waves = (units + W - 1) / W;
+        const double fill = static_cast<double>(units) / static_cast<double>(waves * W);
+        if (fill > best_fill + 1e-9) {
+            best_fill = fill;
+            best = S;
+        }
+    }
+    return best;
+}
+
 // How the tiles are spread over the persistent workers (CTAs, or 2-CTA
 // clusters in the pair form).  With W workers and T tiles of KB K blocks:
 //  - classic split-K (forced): T*splits equal units, round-robin;
@@ -878,13 +908,17 @@ gemm_f16_status make_plan(const Args& a, const DevInfo& dev, Plan* pl, bool plan
     const uint32_t stage_bytes = gemm_f16_dev::kStageABytes + stage_b;
     // The 32 KB epilogue buffer stages TMA stores of C, and is where the last
     // unit of a tile cut along K collects the other units' partials.
+    // K segments for a swapped small-M pair plan whose tiles are fewer than the
+    // clusters but at least half as many (kseg_default): every cluster then
+    // streams a segment of the large operand, and the segment-major unit order
+    // has the clusters read the same rows of it at the same time.
+    if (splits == 1) splits = kseg_default(swap, pair, gated, tiles, kblocks, dev.sms);
     // Stream-K: forced by GEMM_F16_OPT_STREAMK = 2, and the default when an
     // operand is gathered (gathered tiles are slow, so balancing the last wave
-    // pays for the fixup) and for the swapped small-M form when its tiles are
-    // fewer than the SMs (the product streams the large operand from HBM, and
-    // stream-K lets every SM stream a share: 16 x 16384 x 8192 measured 56.9
-    // instead of 59.1 us per call with L2 flushed); otherwise the last partial
-    // wave is split along N.
+    // pays for the fixup) and for other swapped small-M plans with fewer tiles
+    // than SMs (the product streams the large operand from HBM, and stream-K
+    // lets every SM stream a share); otherwise the last partial wave is split
+    // along N.
     const int64_t sk_opt = opt(GEMM_F16_OPT_STREAMK);
     const bool sk_default = !ca.tma || !cb.tma || (swap && tiles < dev.sms);
     const bool use_sk = splits == 1 && !gated && (sk_opt == 2 || (sk_opt == 0 && sk_default));
@@ -1439,8 +1473,9 @@ gemm_f16_status gemm_f16_workspace_size(int64_t M, int64_t N, int64_t K, size_t*
         // the single form may gather an operand, and the swapped form (single or
         // pair) has fewer tiles than SMs: both turn stream-K on by default
         const int64_t sk = opt(GEMM_F16_OPT_STREAMK);
-        const bool streamk = splits == 1 && (sk == 2 || (sk == 0 && (!pair || swap)));
-        const Schedule s = make_schedule(tiles, kblocks, splits, workers, BN, pair ? 128 : 64, streamk);
+        const int sp = splits == 1 ? kseg_default(swap, pair != 0, false, tiles, kblocks, dev->sms) : splits;
+        const bool streamk = sp == 1 && (sk == 2 || (sk == 0 && (!pair || swap)));
+        const Schedule s = make_schedule(tiles, kblocks, sp, workers, BN, pair ? 128 : 64, streamk);
         if (s.partial_slots > 0)
             need = std::max(need, workspace_bytes_for(s.partial_slots, BN, tiles, pair ? 2 : 1, nullptr, nullptr));
     }

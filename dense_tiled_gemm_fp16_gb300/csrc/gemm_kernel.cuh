@@ -324,13 +324,19 @@ __device__ __forceinline__ Unit unit_at(const KernelParams& p, int cid, int i)
             w.kb0 = 0;
             w.kb1 = p.kblocks;
         } else {
-            w.tile = u / p.splits;
-            const int split = u - w.tile * p.splits;
+            // Classic split-K units are numbered K segment first (unit u: tile
+            // u mod tiles, segment u / tiles), so the units in flight at once
+            // cover the same K range of neighbouring tiles and read the same
+            // operand rows together (16 x 16384 x 8192, 2 segments: 53.2
+            // against 56.3 us per call with the tile-major order).
+            const int ntl = p.num_units / p.splits;   // (classic split-K: units = tiles * splits)
+            w.tile = u % ntl;
+            const int split = u / ntl;
             w.kb0 = static_cast<int>(static_cast<int64_t>(split) * p.kblocks / p.splits);
             w.kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * p.kblocks / p.splits);
             if (p.splits > 1) {
                 w.slot0 = w.tile * p.splits;
-                w.slot = u;
+                w.slot = w.slot0 + split;
                 w.expected = p.splits;
                 w.seg = split;
             }

@@ -357,7 +357,14 @@ gemm_f16_status gemm_f16_fused_get_plan(const void* A, int64_t stride_am, int64_
  * Process-wide tuning and test knobs (not thread-safe with concurrent calls):
  *   GEMM_F16_OPT_FORCE_GATHER  bit 0: A, bit 1: B, bit 2: C never use TMA
  *   GEMM_F16_OPT_SPLITS        > 0: classic split-K, every tile cut into this many K
- *                              segments (clamped to the K blocks); replaces stream-K
+ *                              segments (clamped to the K blocks); replaces stream-K.
+ *                              Units are numbered segment-major (all tiles' first
+ *                              segments, then the second ones, ...).  0 default: none,
+ *                              except for a swapped small-M pair plan whose tiles are
+ *                              fewer than half the SMs but at least a quarter of them:
+ *                              2, 3 or 4 segments, whichever fills the waves of units
+ *                              best, when that fill is at least 80 % and each segment
+ *                              keeps 8 or more K blocks
  *   GEMM_F16_OPT_TILE_N        > 0: force the tile width (multiple of 64, <= 256)
  *   GEMM_F16_OPT_PANEL         > 0: tile-rows per rasterisation panel (default 8, or 2 when the
  *                              launch has at most four waves of tiles or at most 16 tile columns)
@@ -370,7 +377,8 @@ gemm_f16_status gemm_f16_fused_get_plan(const void* A, int64_t stride_am, int64_
  *                              tiles
  *   GEMM_F16_OPT_STREAMK       0 default: stream-K tail when an operand is gathered (not
  *                              TMA-addressable) or when a swapped (small-M) plan has fewer
- *                              tiles than the device has SMs, whole tiles otherwise; 1: whole
+ *                              tiles than the device has SMs and does not take the K
+ *                              segments above, whole tiles otherwise; 1: whole
  *                              tiles only; 2: stream-K tail whenever the tiles do not divide
  *                              evenly
  *   GEMM_F16_OPT_TAIL_SPLIT    0 default: cut the last partial wave of tiles along N

@@ -602,6 +602,45 @@ def test_l2_policies_do_not_change_results(case, a, b, c):
     assert g.gemm_f16_device_status() == 0
 
 
+# ----------------------------------- K segments for swapped small-M pairs
+# (M, N, K, B transposed, segments: 64 pair tiles take 2, 48 take 3, 56 take 4
+# when each segment keeps 8 K blocks, 40 keep stream-K)
+@pytest.mark.parametrize("M,N,K,bt,S", [(16, 16384, 1024, False, 2), (40, 12288, 1600, False, 3),
+                                        (16, 14336, 2048, True, 4), (16, 14336, 1024, False, 1),
+                                        (16, 10240, 2048, True, 1)])
+def test_swapped_pairs_take_k_segments(M, N, K, bt, S):
+    """A swapped pair plan whose tiles are fewer than the clusters but at least
+    half as many runs S K segments per tile (classic split-K, units numbered
+    segment-major) when S fills the waves of units; the last of a tile's units
+    adds the others' partials.  Bit for bit on integers, the same bits through a
+    caller workspace of the size gemm_f16_workspace_size reports, and the same
+    as stream-K."""
+    rng = np.random.default_rng(M * 7 + N + K)
+    Ah = rng.integers(-3, 4, (M, K)).astype(np.float16)
+    Bh = rng.integers(-3, 4, (K, N)).astype(np.float16)
+    A = to_dev(Ah)
+    B = make_view(Bh, "col" if bt else "row")
+    out = torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV)
+    plan = g.plan_for(A, B, out)
+    assert plan["swap_ab"] and plan["pair"] and plan["splits"] == S, plan
+    assert (plan["streamk_tiles"] > 0) == (S == 1) and plan["workspace_bytes"] > 0, plan
+    C = host(gpu(A, B, out=out))
+    assert_bits(C, oracle.gemm(Ah, Bh, threads=oracle_threads()), f"{S} K segments {M}x{N}x{K}")
+    nbytes = g.gemm_f16_workspace_size(M, N, K)
+    assert nbytes >= plan["workspace_bytes"]
+    ws = torch.zeros(nbytes // 4 + 64, dtype=torch.int32, device=DEV)
+    out2 = torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV)
+    g.gemm_f16_ws(A.data_ptr(), A.stride(0), A.stride(1), B.data_ptr(), B.stride(0), B.stride(1), out2.data_ptr(), N,
+                  M, N, K, ws.data_ptr(), nbytes, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert_bits(host(out2), C, "caller workspace")
+    g.gemm_f16_set_option(g.OPT_STREAMK, 2)   # a forced stream-K keeps stream-K
+    p2 = g.plan_for(A, B, out)
+    assert p2["splits"] == 1 and p2["streamk_tiles"] > 0, p2
+    assert_bits(host(gpu(A, B, out=out)), C, "stream-K")
+    assert g.gemm_f16_device_status() == 0
+
+
 # ---------------------------------------------- swapped form on CTA pairs
 @pytest.mark.parametrize("M,N,K", [(16, 4096, 1024), (48, 2048, 520), (8, 3000, 640), (40, 16384, 2048)])
 def test_swapped_small_m_on_pairs(M, N, K):
