@@ -527,32 +527,34 @@ __device__ __forceinline__ void load_b_slot(const KernelParams& p, const CUtenso
 // A' rows row .. row+127; B' columns col .. col + (the box width of tmb).
 template <bool kPair>
 __device__ __forceinline__ void load_two_k_blocks(const KernelParams& p, const CUtensorMap* tmb, uint32_t sa,
-                                                  uint32_t sb, int32_t kb,
-                                                  int64_t row, int64_t col, int32_t az, int32_t bz, bool a_mn,
-                                                  bool b_mn, bool a_bd, bool b_bd, uint32_t bar, bool do_a, bool do_b)
+                                                  uint32_t sb, int32_t kb, int64_t row, int64_t col, int32_t az,
+                                                  int32_t bz, bool a_mn, bool b_mn, bool a_bd, bool b_bd, uint32_t bar,
+                                                  bool do_a, bool do_b)
 {
     const int32_t r = static_cast<int32_t>(row), c = static_cast<int32_t>(col);
-    if (!do_a) {
-    } else if (!a_mn) {
-        if (a_bd)
-            tma4<kPair>(sa, &p.tmA2k, 0, r, kb, az, bar, p.l2_a);
-        else
-            tma3<kPair>(sa, &p.tmA2k, 0, r, kb, bar, p.l2_a);
-    } else if (a_bd) {
-        tma5<kPair>(sa, &p.tmA2k, 0, 0, r >> 6, kb, az, bar, p.l2_a);
-    } else {
-        tma4<kPair>(sa, &p.tmA2k, 0, 0, r >> 6, kb, bar, p.l2_a);
+    if (do_a) {
+        if (!a_mn) {
+            if (a_bd)
+                tma4<kPair>(sa, &p.tmA2k, 0, r, kb, az, bar, p.l2_a);
+            else
+                tma3<kPair>(sa, &p.tmA2k, 0, r, kb, bar, p.l2_a);
+        } else if (a_bd) {
+            tma5<kPair>(sa, &p.tmA2k, 0, 0, r >> 6, kb, az, bar, p.l2_a);
+        } else {
+            tma4<kPair>(sa, &p.tmA2k, 0, 0, r >> 6, kb, bar, p.l2_a);
+        }
     }
-    if (!do_b) {
-    } else if (!b_mn) {
-        if (b_bd)
-            tma4<kPair>(sb, tmb, 0, c, kb, bz, bar, p.l2_b);
-        else
-            tma3<kPair>(sb, tmb, 0, c, kb, bar, p.l2_b);
-    } else if (b_bd) {
-        tma5<kPair>(sb, tmb, 0, 0, c >> 6, kb, bz, bar, p.l2_b);
-    } else {
-        tma4<kPair>(sb, tmb, 0, 0, c >> 6, kb, bar, p.l2_b);
+    if (do_b) {
+        if (!b_mn) {
+            if (b_bd)
+                tma4<kPair>(sb, tmb, 0, c, kb, bz, bar, p.l2_b);
+            else
+                tma3<kPair>(sb, tmb, 0, c, kb, bar, p.l2_b);
+        } else if (b_bd) {
+            tma5<kPair>(sb, tmb, 0, 0, c >> 6, kb, bz, bar, p.l2_b);
+        } else {
+            tma4<kPair>(sb, tmb, 0, 0, c >> 6, kb, bar, p.l2_b);
+        }
     }
 }
 
