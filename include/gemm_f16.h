@@ -410,8 +410,9 @@ gemm_f16_status gemm_f16_fused_get_plan(const void* A, int64_t stride_am, int64_
  *                              panel within one wave (at most 16 tile columns, raster panels
  *                              of at most 2 rows); none otherwise
  *   GEMM_F16_OPT_TWO_K_LOADS   0 default: when both operands are TMA-addressable (K-major, or
- *                              MN-major read as 3-D boxes), not gate/up, and K holds at least two
- *                              whole 64-wide blocks, each pipeline phase of a full-width tile
+ *                              MN-major read as 3-D boxes), the plan is not the single-CTA gate/up
+ *                              form, and K holds at least two whole 64-wide blocks, each pipeline
+ *                              phase of a full-width tile
  *                              loads its two K blocks with one copy per operand (a map with the
  *                              K block as an outer dimension), half the copies of one per K
  *                              block; a ragged last K block and narrow tail pieces keep one copy
