@@ -120,3 +120,31 @@ def test_no_alloc_gathers_unaligned_views_and_allocates_nothing():
         got = out.cpu().numpy()
         assert np.array_equal(got.view(np.uint16), ref.view(np.uint16)), f"noalloc call {call} vs oracle"
     assert g.gemm_f16_device_status() == 0
+
+
+def test_no_alloc_with_the_default_k_segments():
+    """A swapped small-M pair plan that takes K segments by default (16 x
+    16384 x 1024: 64 pair tiles, 2 segments) keeps its partials in the fixed
+    array: bit for bit against gemm_f16 and the oracle on integers."""
+    torch.cuda.set_device(DEV)
+    rng = np.random.default_rng(37)
+    M, N, K = 16, 16384, 1024
+    Ah = rng.integers(-3, 4, (M, K)).astype(np.float16)
+    Bh = rng.integers(-3, 4, (K, N)).astype(np.float16)
+    A = torch.from_numpy(Ah).to(DEV)
+    B = torch.from_numpy(Bh).to(DEV)
+    out = torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV)
+    plan = g.gemm_f16_get_plan(*_args(A, B, out))
+    assert plan["splits"] == 2 and plan["pair"] and plan["swap_ab"], plan
+    assert 0 < plan["workspace_bytes"] <= g.NOALLOC_SCRATCH_BYTES, plan
+    stream = torch.cuda.current_stream(DEV).cuda_stream
+    g.gemm_f16_noalloc(*_args(A, B, out), stream=stream)
+    torch.cuda.synchronize(DEV)
+    got = out.cpu().numpy()
+    ref = oracle.gemm(Ah, Bh, threads=oracle_threads())
+    assert np.array_equal(got.view(np.uint16), ref.view(np.uint16))
+    out2 = torch.empty_like(out)
+    g.gemm_f16(*_args(A, B, out2), stream=stream)
+    torch.cuda.synchronize(DEV)
+    assert np.array_equal(out2.cpu().numpy().view(np.uint16), got.view(np.uint16))
+    assert g.gemm_f16_device_status() == 0
