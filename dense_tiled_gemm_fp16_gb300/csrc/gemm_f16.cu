@@ -445,10 +445,10 @@ int choose_splits(int kblocks)
 // that fills its waves best (ties: the smaller S) is taken when it fills them
 // to at least 80 % and leaves each segment 8 K blocks or more; neither
 // split-K nor stream-K may be forced.  16 x N x 8192, L2 flushed, us per call
-// for the best S against stream-K: 40 tiles 43.7 (S 3) vs 43.0, 48 tiles
-// 45.9 (S 3) vs 47.2, 56 tiles 50.6 (S 4) vs 52.8, 64 tiles 52.8 (S 2) vs
-// 56.2; the unit order, K segment first, is what pays (64 tiles, S 2,
-// tile-major order: 56.3).
+// for the best S against stream-K: 48 tiles 45.9 (S 3) vs 47.2, 56 tiles
+// 50.6 (S 4) vs 52.8, 64 tiles 52.8 (S 2) vs 56.2; at 40 tiles the best fill
+// is 0.79 (S 3: 43.7) and stream-K (43.0) stays.  The unit order, K segment
+// first, is what pays (64 tiles, S 2, tile-major order: 56.3).
 int kseg_default(bool swap, bool pair, bool gated, int64_t tiles, int kblocks, int sms)
 {
     const int64_t W = sms / 2;
